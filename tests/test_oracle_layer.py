@@ -1,0 +1,157 @@
+"""Pins for the oracle's whole-layer evaluations (CPU only).
+
+The layer is the MoE expert FFN of the page "A 35B Hybrid-Attention
+Mixture-of-Experts Model on a 6GB 2011 GPU" (Methodology 1: grouped 4-bit GEMM
+over routed experts in prefill, W4A8 integer kernel in decode; Methodology 2:
+Q4_0-family weights, 8-bit decode activations), read as: router top-k with
+softmax weights, SwiGLU expert FFN (gate, up, down), weighted combine plus
+residual.  The hand-computed case below fixes signs, the q - 8 offset, which
+projection goes through silu, the block-to-scale mapping and the residual.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+import workloads
+
+
+def _bits(v):
+    return workloads.f32_to_bf16_bits(np.asarray(v, np.float32))
+
+
+def _hand_layer(x_val, k=1):
+    """H = 64, I = 32, E = 2.  Expert 0: gate codes 9 (q-8 = 1) with block
+    scales 1/32 and 1/64; up codes 12 (q-8 = 4), scales 1/64; down rows
+    alternate codes 7 (q-8 = -1) and 10 (q-8 = 2), scale 1/2.  Expert 1 has
+    zero scales.  Router: expert 0 weights 1/64 (exact in fp32), expert 1 weights 0."""
+    H, I, E = 64, 32, 2
+    x = _bits(np.full((1, H), x_val))
+    wr = np.zeros((E, H), np.float32)
+    wr[0] = 1 / 64
+    gu_codes = np.zeros((E, 2 * I, H), np.uint8)
+    gu_scales = np.zeros((E, 2 * I, H // 32), np.float16)
+    gu_codes[0, :I] = 9
+    gu_scales[0, :I, 0] = 1 / 32
+    gu_scales[0, :I, 1] = 1 / 64
+    gu_codes[0, I:] = 12
+    gu_scales[0, I:] = 1 / 64
+    d_codes = np.zeros((E, H, I), np.uint8)
+    d_scales = np.zeros((E, H, I // 32), np.float16)
+    d_codes[0, 0::2] = 7
+    d_codes[0, 1::2] = 10
+    d_scales[0] = 0.5
+    return x, wr, gu_codes, gu_scales, d_codes, d_scales
+
+
+def test_prefill_hand_computed_layer():
+    x, wr, gc, gs, dc, ds = _hand_layer(1.0)
+    out, r = O.moe_prefill(x, wr, gc, gs, dc, ds, k=1)
+    assert r["idx"].tolist() == [[0]] and r["w"].tolist() == [[1.0]]
+    # g = 32*1*(1/32) + 32*1*(1/64) = 1.5 ; u = 64*4*(1/64) = 4
+    # h = silu(1.5) * 4 = 6 / (1 + e^-1.5)
+    h = 6.0 / (1.0 + math.exp(-1.5))
+    assert abs(h - 4.905446857161862) < 1e-12
+    # even rows: 0.5 * (-1) * 32 h = -16 h ; odd rows: 0.5 * 2 * 32 h = 32 h ; plus x = 1
+    expect = np.where(np.arange(64) % 2 == 0, 1.0 - 16 * h, 1.0 + 32 * h)
+    assert np.allclose(out[0], expect, rtol=0, atol=1e-10)
+    # with k = 2 the zero-scale expert adds nothing and expert 0 is weighted by
+    # softmax(64 * 1/64, 0)[0] = 1 / (1 + e^-1)
+    out2, r2 = O.moe_prefill(x, wr, gc, gs, dc, ds, k=2)
+    w0 = 1.0 / (1.0 + math.exp(-1.0))
+    assert abs(w0 - 0.7310585786300049) < 1e-15
+    assert abs(r2["w"][0, 0] - w0) < 1e-14
+    expect2 = 1.0 + w0 * np.where(np.arange(64) % 2 == 0, -16 * h, 32 * h)
+    assert np.allclose(out2[0], expect2, rtol=0, atol=1e-10)
+
+
+def test_decode_hand_computed_layer_exact_integers():
+    # x = 127 everywhere: d_x = fp16(127/127) = 1, q_x = 127.
+    x, wr, gc, gs, dc, ds = _hand_layer(127.0)
+    out, st = O.moe_decode(x, wr, gc, gs, dc, ds, k=1, keep_dots=True)
+    assert np.all(st["qx"] == 127) and np.all(st["dx"].astype(np.float64) == 1.0)
+    G = st["dots_gu"][(0, 0)]
+    assert np.all(G[:32] == 32 * 127)           # gate: (9-8)*127 per element
+    assert np.all(G[32:] == 4 * 32 * 127)       # up:   (12-8)*127
+    # g = 4064/32 + 4064/64 = 190.5 ; u = 2 * 16256/64 = 508 ; h = silu(190.5)*508 = 96774
+    assert np.all(st["h"][0, 0] == 96774.0)
+    # h quantises exactly: 96774 / 127 = 762 -> d_h = 762, q_h = 127
+    assert np.all(st["qh"] == 127) and np.all(st["dh"].astype(np.float64) == 762.0)
+    D = st["dots_d"][(0, 0)]
+    assert np.all(D[0::2] == -32 * 127) and np.all(D[1::2] == 2 * 32 * 127)
+    # y = 0.5 * 762 * D ; out = 127 + y
+    expect = np.where(np.arange(64) % 2 == 0, 127.0 - 1548384.0, 127.0 + 3096768.0)
+    assert np.array_equal(out[0], expect)
+    # the prefill evaluation of the same exactly-representable case agrees
+    outp, _ = O.moe_prefill(x, wr, gc, gs, dc, ds, k=1)
+    assert np.array_equal(outp[0], expect)
+
+
+@pytest.mark.parametrize("evaluate", ["prefill", "decode"])
+def test_zero_scales_give_identity(evaluate):
+    li = workloads.tiny()
+    zs = np.zeros_like(li.gu_scales)
+    fn = O.moe_prefill if evaluate == "prefill" else O.moe_decode
+    out, _ = fn(li.x, li.wr, li.gu_codes, zs, li.d_codes, li.d_scales, li.k)
+    assert np.array_equal(out, O.bf16_bits_to_f64(li.x))
+    out, _ = fn(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, np.zeros_like(li.d_scales), li.k)
+    assert np.array_equal(out, O.bf16_bits_to_f64(li.x))
+
+
+def test_bucketed_equals_dense_bruteforce():
+    li = workloads.make_layer("small", 12, 64, 32, 5, 2, seed=11, wr_std=0.1)
+    out, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    dense = O.moe_dense_bruteforce(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    assert np.allclose(out, dense, rtol=0, atol=1e-12 * max(1.0, np.abs(dense).max()))
+
+
+def test_token_subset_matches_full_rows():
+    li = workloads.tiny()
+    full, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    sub, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k,
+                           tokens=[3, 17, 40])
+    assert np.allclose(sub, full[[3, 17, 40]], rtol=0, atol=1e-12)
+
+
+def test_down_scale_doubling_doubles_the_moe_term():
+    li = workloads.tiny()
+    X = O.bf16_bits_to_f64(li.x)
+    a, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    b, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes,
+                         (li.d_scales.astype(np.float32) * 2).astype(np.float16), li.k)
+    assert np.allclose(b - X, 2 * (a - X), rtol=0, atol=1e-12)
+    # doubling the up scales doubles h, hence the MoE term, too
+    gs = li.gu_scales.copy()
+    gs[:, li.I:] = (gs[:, li.I:].astype(np.float32) * 2).astype(np.float16)
+    c, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, gs, li.d_codes, li.d_scales, li.k)
+    assert np.allclose(c - X, 2 * (a - X), rtol=0, atol=1e-12)
+
+
+def test_single_expert_is_a_dense_swiglu_ffn():
+    # E = 1, k = 1: routing weight 1, the layer is x + W_d (silu(W_g x) * W_u x)
+    li = workloads.make_layer("one", 5, 64, 32, 1, 1, seed=12, wr_std=0.1)
+    out, r = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, 1)
+    assert np.all(r["w"] == 1.0)
+    import torch
+    X = torch.tensor(O.bf16_bits_to_f64(li.x))
+    W = torch.tensor(li.gu_codes[0].astype(np.float64) - 8) * torch.tensor(
+        np.repeat(li.gu_scales[0].astype(np.float64), 32, axis=-1))
+    Wd = torch.tensor(li.d_codes[0].astype(np.float64) - 8) * torch.tensor(
+        np.repeat(li.d_scales[0].astype(np.float64), 32, axis=-1))
+    g, u = X @ W[:32].T, X @ W[32:].T
+    ref = X + (torch.nn.functional.silu(g) * u) @ Wd.T
+    assert np.allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_close_to_prefill_on_tiny():
+    li = workloads.tiny()
+    a, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    b, st = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    X = O.bf16_bits_to_f64(li.x)
+    # int8 activations carry ~1/254 relative error per element; the MoE term
+    # should move by a small fraction of its size
+    rel = O.rms(b - a) / O.rms(a - X)
+    assert rel < 0.03, rel
+    # stage consistency: routing identical to prefill's
+    assert np.array_equal(st["idx"], O.route(X, li.wr, li.k)[1])
