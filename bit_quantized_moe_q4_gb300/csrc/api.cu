@@ -1,0 +1,372 @@
+// C ABI of moeq4 (include/moeq4.h): argument checks, workspace carve-up,
+// tensor-map set-up and the launch sequence of each forward path.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moeq4 {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int set_err(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+// Per-device status word written by kernels whose bounded wait ran out.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    int* status = nullptr;  // device address of g_device_status
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Looks up (once per device, with that device current) the SM count, the
+// architecture and the address of the status word.
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return set_err(MOE_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(cudaGetLastError()));
+    if (dev < 0 || dev >= kMaxDevices) return set_err(MOE_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        d.supported = (major == 10 && minor == 3);
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess)
+            return set_err(MOE_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+        d.status = static_cast<int*>(p);
+        d.ready = true;
+        if (!d.supported)
+            return set_err(MOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                           dev, major, minor);
+    }
+    if (!d.supported) return set_err(MOE_ERR_UNSUPPORTED, "device %d is not sm_103a", dev);
+    *out = &d;
+    return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_check(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return set_err(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return MOE_OK;
+}
+
+// ---- tensor maps (driver entry point fetched through the runtime) --------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+constexpr int kPrefillTileN = 256;
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Lays the workspace out; with base == nullptr only the size is computed.
+size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspace* ws) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> uint8_t* {
+        uint8_t* p = base ? base + off : nullptr;
+        off += align256(bytes ? bytes : 1);
+        return p;
+    };
+    const size_t Tk = (size_t)T * k;
+    const int nc = nchunks(T);
+    const int tile_n = (mode == MOE_MODE_PREFILL) ? kPrefillTileN : 32;
+    const int max_tiles = (int)((Tk + tile_n - 1) / tile_n) + E;
+    Workspace w{};
+    w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+    w.topk_idx = reinterpret_cast<int32_t*>(take(Tk * 4));
+    w.topk_w = reinterpret_cast<float*>(take(Tk * 4));
+    w.chunk_count = reinterpret_cast<int32_t*>(take((size_t)nc * E * 4));
+    w.entry_rank = reinterpret_cast<int32_t*>(take(Tk * 4));
+    w.offsets = reinterpret_cast<int32_t*>(take((size_t)(E + 1) * 4));
+    w.touched = reinterpret_cast<int32_t*>(take((size_t)E * 4));
+    w.counters = reinterpret_cast<int32_t*>(take(8 * 4));
+    w.bucket_token = reinterpret_cast<int32_t*>(take(Tk * 4));
+    w.bucket_slot = reinterpret_cast<int32_t*>(take(Tk * 4));
+    w.slot_w = reinterpret_cast<float*>(take(Tk * 4));
+    w.slot_pos = reinterpret_cast<int32_t*>(take(Tk * 4));
+    w.tile_e = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
+    w.tile_n0 = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
+    w.tile_nn = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
+    w.y = reinterpret_cast<uint16_t*>(take(Tk * H * 2));
+    if (mode == MOE_MODE_PREFILL) {
+        w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
+    } else {
+        w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
+        w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
+        w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
+        w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
+    }
+    w.max_tiles = max_tiles;
+    w.tile_n = tile_n;
+    if (ws) *ws = w;
+    return off;
+}
+
+int check_layer_shape(int mode, int T, int H, int I, int E, int k) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0)
+        return set_err(MOE_ERR_SHAPE, "non-positive dimension (T=%d H=%d I=%d E=%d k=%d)", T, H, I,
+                       E, k);
+    if (E > MOE_MAX_EXPERTS) return set_err(MOE_ERR_SHAPE, "E=%d exceeds %d", E, MOE_MAX_EXPERTS);
+    if (k > E || k > MOE_MAX_TOPK)
+        return set_err(MOE_ERR_SHAPE, "k=%d must satisfy 1 <= k <= min(E, %d)", k, MOE_MAX_TOPK);
+    if (H % 128 || I % 128)
+        return set_err(MOE_ERR_SHAPE, "H=%d and I=%d must be multiples of 128", H, I);
+    const long long big = (long long)T * k * (H > I ? H : I);
+    if (big >= (1ll << 31)) return set_err(MOE_ERR_SHAPE, "T*k*max(H,I) = %lld too large", big);
+    if (mode == MOE_MODE_DECODE && T > MOE_DECODE_MAX_T)
+        return set_err(MOE_ERR_SHAPE, "decode takes at most %d tokens (T=%d)", MOE_DECODE_MAX_T, T);
+    return MOE_OK;
+}
+
+int copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+    if (!dst || bytes == 0) return MOE_OK;
+    return cuda_check(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s),
+                      "debug copy");
+}
+
+int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const void* wd, int T,
+            int H, int I, int E, int k, unsigned flags, void* out, void* workspace,
+            size_t ws_bytes, moe_debug* dbg, void* stream) {
+    int rc = check_layer_shape(mode, T, H, I, E, k);
+    if (rc) return rc;
+    if (flags & ~MOE_OUT_FP32) return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (T == 0) return MOE_OK;
+    if (!x || !wr || !wgu || !wd || !out)
+        return set_err(MOE_ERR_INVALID_ARG, "null tensor argument");
+    if (!aligned16(x) || !aligned16(wr) || !aligned16(wgu) || !aligned16(wd) || !aligned16(out) ||
+        !aligned16(workspace))
+        return set_err(MOE_ERR_ALIGN, "tensor arguments must be 16-byte aligned");
+    if (out == static_cast<const void*>(x)) return set_err(MOE_ERR_INVALID_ARG, "out may not alias x");
+    const size_t need = carve(mode, T, H, I, E, k, nullptr, nullptr);
+    if (!workspace || ws_bytes < need)
+        return set_err(MOE_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Workspace ws{};
+    carve(mode, T, H, I, E, k, static_cast<uint8_t*>(workspace), &ws);
+    const size_t Tk = (size_t)T * k;
+
+    void** ev = dbg ? dbg->stage_events : nullptr;
+    auto mark = [&](int i) -> int {
+        if (!ev || !ev[i]) return MOE_OK;
+        return cuda_check(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), s,
+                                                   cudaEventRecordExternal),
+                          "stage event");
+    };
+    if ((rc = mark(0))) return rc;
+    // 1. route
+    float* logits = (mode == MOE_MODE_DECODE) ? ws.logits : (dbg ? dbg->logits : nullptr);
+    if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w, s), "route")))
+        return rc;
+    if ((rc = mark(1))) return rc;
+    // 2. bucket
+    if ((rc = cuda_check(launch_bucket(ws.topk_idx, ws.topk_w, T, E, k, ws.tile_n, ws, s), "bucket")))
+        return rc;
+    if ((rc = mark(2))) return rc;
+    if (mode == MOE_MODE_PREFILL) {
+        CUtensorMap xmap, hmap;
+        if (!encode_tmap_2d_bf16(&xmap, x, T, H, 64, 1, true) ||
+            !encode_tmap_2d_bf16(&hmap, ws.h, Tk, I, 64, 16, true))
+            return set_err(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        if ((rc = mark(3))) return rc;
+        if ((rc = cuda_check(launch_prefill_gateup(&xmap, wgu, ws, T, H, I, E, k, dev->status,
+                                                   dev->num_sms, s), "prefill gate/up")))
+            return rc;
+        if ((rc = mark(4))) return rc;
+        if ((rc = cuda_check(launch_prefill_down(&hmap, wd, ws, T, H, I, E, k, dev->status,
+                                                 dev->num_sms, s), "prefill down")))
+            return rc;
+    } else {
+        if ((rc = cuda_check(launch_act_quant(x, T, H, ws.q_x, ws.d_x, s), "activation quantiser")))
+            return rc;
+        if ((rc = mark(3))) return rc;
+        if ((rc = cuda_check(launch_decode_gateup(wgu, ws, T, H, I, E, k, dbg ? dbg->dots_gu : nullptr, s),
+                             "decode gate/up")))
+            return rc;
+        if ((rc = mark(4))) return rc;
+        if ((rc = cuda_check(launch_decode_down(wd, ws, T, H, I, E, k, dbg ? dbg->dots_d : nullptr, s),
+                             "decode down")))
+            return rc;
+    }
+    if ((rc = mark(5))) return rc;
+    // 3. combine
+    if ((rc = cuda_check(launch_combine(x, ws.y, ws.slot_pos, T, H, k, (flags & MOE_OUT_FP32) != 0,
+                                        out, s), "combine")))
+        return rc;
+    if ((rc = mark(6))) return rc;
+    if (dbg) {
+        if (mode == MOE_MODE_DECODE && (rc = copy_d2d(dbg->logits, ws.logits, (size_t)T * E * 4, s))) return rc;
+        if ((rc = copy_d2d(dbg->topk_idx, ws.topk_idx, Tk * 4, s))) return rc;
+        if ((rc = copy_d2d(dbg->topk_w, ws.topk_w, Tk * 4, s))) return rc;
+        if ((rc = copy_d2d(dbg->expert_offsets, ws.offsets, (size_t)(E + 1) * 4, s))) return rc;
+        if ((rc = copy_d2d(dbg->bucket_token, ws.bucket_token, Tk * 4, s))) return rc;
+        if ((rc = copy_d2d(dbg->bucket_slot, ws.bucket_slot, Tk * 4, s))) return rc;
+        if (mode == MOE_MODE_PREFILL) {
+            if ((rc = copy_d2d(dbg->h, ws.h, Tk * I * 2, s))) return rc;
+        } else {
+            if ((rc = copy_d2d(dbg->q_x, ws.q_x, (size_t)T * H, s))) return rc;
+            if ((rc = copy_d2d(dbg->d_x, ws.d_x, (size_t)T * (H / kGroup) * 2, s))) return rc;
+            if ((rc = copy_d2d(dbg->q_h, ws.q_h, Tk * I, s))) return rc;
+            if ((rc = copy_d2d(dbg->d_h, ws.d_h, Tk * (I / kGroup) * 2, s))) return rc;
+        }
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moeq4
+
+using namespace moeq4;
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_last_error_string(void) { return g_err; }
+
+int moe_get_device_status(void* stream, int* status_out) {
+    if (!status_out) return set_err(MOE_ERR_INVALID_ARG, "status_out is null");
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if ((rc = cuda_check(cudaMemcpyAsync(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost, s),
+                         "read status")))
+        return rc;
+    if ((rc = cuda_check(cudaStreamSynchronize(s), "synchronize"))) return rc;
+    *status_out = v;
+    return MOE_OK;
+}
+
+int moe_clear_device_status(void* stream) {
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    return cuda_check(cudaMemsetAsync(dev->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)),
+                      "clear status");
+}
+
+size_t moe_q4_packed_bytes(int E, int N, int K) {
+    if (E <= 0 || N <= 0 || K <= 0 || N % kTileRows || K % kTileK) return 0;
+    return (size_t)E * (N / kTileRows) * (K / kTileK) * kTileBytes;
+}
+
+int moe_q4_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K, void* dst,
+                size_t dst_bytes, void* stream) {
+    if (fmt != MOE_Q4_CODES && fmt != MOE_Q4_BLOCK18)
+        return set_err(MOE_ERR_INVALID_ARG, "unknown pack format %d", fmt);
+    if (E <= 0 || N <= 0 || K <= 0 || N % kTileRows || K % kTileK)
+        return set_err(MOE_ERR_SHAPE, "pack needs E>0, N%%128==0, K%%64==0 (E=%d N=%d K=%d)", E, N, K);
+    if (!src || !dst || (fmt == MOE_Q4_CODES && !src_scales))
+        return set_err(MOE_ERR_INVALID_ARG, "null pointer");
+    if (fmt == MOE_Q4_BLOCK18 && src_scales)
+        return set_err(MOE_ERR_INVALID_ARG, "18-byte blocks carry their scales; src_scales must be NULL");
+    if (!aligned16(src) || !aligned16(dst) || (src_scales && !aligned16(src_scales)))
+        return set_err(MOE_ERR_ALIGN, "pointers must be 16-byte aligned");
+    const size_t need = moe_q4_packed_bytes(E, N, K);
+    if (dst_bytes < need)
+        return set_err(MOE_ERR_INVALID_ARG, "dst holds %zu bytes, %zu needed", dst_bytes, need);
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    return cuda_check(launch_pack(fmt, src, src_scales, E, N, K, dst, static_cast<cudaStream_t>(stream)),
+                      "pack");
+}
+
+int moe_route_topk(const uint16_t* x_bf16, const float* wr, int T, int H, int E, int k,
+                   int32_t* topk_idx, float* topk_w, float* logits_or_null, void* stream) {
+    if (T < 0 || H <= 0 || E <= 0 || E > MOE_MAX_EXPERTS || k <= 0 || k > E || k > MOE_MAX_TOPK ||
+        H % 8)
+        return set_err(MOE_ERR_SHAPE, "route shape T=%d H=%d E=%d k=%d outside limits", T, H, E, k);
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !wr || !topk_idx || !topk_w) return set_err(MOE_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x_bf16) || !aligned16(wr) || !aligned16(topk_idx) || !aligned16(topk_w) ||
+        (logits_or_null && !aligned16(logits_or_null)))
+        return set_err(MOE_ERR_ALIGN, "pointers must be 16-byte aligned");
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    return cuda_check(launch_route(x_bf16, wr, T, H, E, k, logits_or_null, topk_idx, topk_w,
+                                   static_cast<cudaStream_t>(stream)),
+                      "route");
+}
+
+size_t moe_workspace_bytes(int mode, int T, int H, int I, int E, int k) {
+    if ((mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) || T < 0 || H <= 0 || I <= 0 ||
+        E <= 0 || k <= 0)
+        return 0;
+    return carve(mode, T, H, I, E, k, nullptr, nullptr);
+}
+
+int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr, const void* wgu_packed,
+                           const void* wd_packed, int T, int H, int I, int E, int k,
+                           unsigned flags, void* out, void* workspace, size_t ws_bytes,
+                           moe_debug* dbg, void* stream) {
+    return forward(MOE_MODE_PREFILL, x_bf16, wr, wgu_packed, wd_packed, T, H, I, E, k, flags, out,
+                   workspace, ws_bytes, dbg, stream);
+}
+
+int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void* wgu_packed,
+                            const void* wd_packed, int T, int H, int I, int E, int k,
+                            unsigned flags, void* out, void* workspace, size_t ws_bytes,
+                            moe_debug* dbg, void* stream) {
+    return forward(MOE_MODE_DECODE, x_bf16, wr, wgu_packed, wd_packed, T, H, I, E, k, flags, out,
+                   workspace, ws_bytes, dbg, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Host-side declarations shared by the moeq4 translation units (not part of
+// the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moeq4.h"
+
+namespace moeq4 {
+
+// Workspace pieces of one forward call; every pointer is a device address
+// carved out of the caller's workspace (see api.cu).
+struct Workspace {
+    float* logits;          // [T, E]
+    int32_t* topk_idx;      // [T, k]
+    float* topk_w;          // [T, k]
+    int32_t* chunk_count;   // [nchunk, E]   bucket counts per 32-token chunk
+    int32_t* entry_rank;    // [T*k]         rank inside the chunk
+    int32_t* offsets;       // [E+1]
+    int32_t* touched;       // [E]           experts with a non-empty bucket
+    int32_t* counters;      // [8]           n_touched, n_tiles, n_items, ...
+    int32_t* bucket_token;  // [T*k]
+    int32_t* bucket_slot;   // [T*k]
+    float* slot_w;          // [T*k]         routing weight of each bucket row
+    int32_t* slot_pos;      // [T*k]         bucket row of (t, j)
+    int32_t* tile_e;        // [max_tiles]   expert of each token tile
+    int32_t* tile_n0;       // [max_tiles]   first bucket row of the tile
+    int32_t* tile_nn;       // [max_tiles]   rows in the tile
+    uint16_t* h;            // [T*k, I] bf16 (prefill)
+    uint16_t* y;            // [T*k, H] bf16 weighted expert outputs
+    int8_t* q_x;            // [T, H]        (decode)
+    uint16_t* d_x;          // [T, H/32]     (decode)
+    int8_t* q_h;            // [T*k, I]      (decode)
+    uint16_t* d_h;          // [T*k, I/32]   (decode)
+    int max_tiles;
+    int tile_n;             // tokens per GEMM tile (prefill)
+};
+
+// counters[] slots
+enum { kCntTouched = 0, kCntTiles = 1 };
+
+int nchunks(int T);
+
+// launchers; each returns cudaGetLastError() of its launch
+cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
+                        void* dst, cudaStream_t s);
+cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
+                         float* logits, int32_t* idx, float* w, cudaStream_t s);
+cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
+                          const Workspace& ws, cudaStream_t s);
+cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, const Workspace& ws,
+                                  int T, int H, int I, int E, int k, int* status, int num_sms,
+                                  cudaStream_t s);
+cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const Workspace& ws,
+                                int T, int H, int I, int E, int k, int* status, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_act_quant(const uint16_t* x, int T, int H, int8_t* q, uint16_t* d,
+                             cudaStream_t s);
+cudaError_t launch_decode_gateup(const void* wgu, const Workspace& ws, int T, int H, int I,
+                                 int E, int k, int32_t* dots_dbg, cudaStream_t s);
+cudaError_t launch_decode_down(const void* wd, const Workspace& ws, int T, int H, int I, int E,
+                               int k, int32_t* dots_dbg, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* x, const uint16_t* y, const int32_t* slot_pos, int T,
+                           int H, int k, bool out_fp32, void* out, cudaStream_t s);
+
+// tensor maps
+bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+}  // namespace moeq4

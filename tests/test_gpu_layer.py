@@ -1,0 +1,175 @@
+"""GPU parity of whole layers against the oracle, through the C ABI.
+
+Float outputs: max|gpu - oracle| <= 2e-2 * RMS(oracle output) per layer (in the
+fp32 output mode; the bf16 mode adds half a bf16 ulp of the oracle value).
+Integer stages of the W4A8 decode path are bit-exact: the int8 activation
+codes and scales, the int32 gate/up group dots, and the int32 down group dots
+recomputed by the oracle from the GPU's own int8 codes of h (h itself is fp32
+on the GPU and float64 in the oracle, so a code of h may differ by one at a
+rounding boundary; such differences are counted and bounded).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("bit_quantized_moe_q4_gb300")
+from gpu_util import DeviceLayer, assert_within_tol, out_to_f64  # noqa: E402
+
+
+def _sample_tokens(T, n, seed=0):
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    s.update({0, T - 1})
+    return np.array(sorted(s))
+
+
+# ------------------------------------------------------------------ prefill
+def test_prefill_tiny_full():
+    li = workloads.tiny()
+    dl = DeviceLayer(li)
+    d, dbg = moe.make_debug(moe.MOE_MODE_PREFILL, li.T, li.H, li.I, li.E, li.k)
+    out = out_to_f64(dl.prefill(debug=dbg))
+    ref, r = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    assert np.array_equal(d["topk_idx"].cpu().numpy(), r["idx"])
+    assert_within_tol(out, ref)
+    # the MoE term alone is also close (a stricter view than the full output)
+    X = O.bf16_bits_to_f64(li.x)
+    assert_within_tol(out - X, ref - X, tol=2e-2, what="MoE term")
+    # stage: h = silu(W_g x) * (W_u x) per bucket row, bf16
+    h = d["h"].cpu().numpy().view(np.uint16)
+    h = O.bf16_bits_to_f64(h)
+    tok = d["bucket_token"].cpu().numpy()
+    off = d["expert_offsets"].cpu().numpy()
+    href = np.zeros_like(h)
+    for e in range(li.E):
+        rows = slice(off[e], off[e + 1])
+        if off[e] == off[e + 1]:
+            continue
+        W = O.q4_dequant(li.gu_codes[e], li.gu_scales[e])
+        Xe = X[tok[rows]]
+        href[rows] = O.swiglu(Xe @ W[: li.I].T, Xe @ W[li.I:].T)
+    assert_within_tol(h, href, tol=2e-2, what="h")
+
+
+def test_prefill_tiny_bf16_output():
+    li = workloads.tiny()
+    out = out_to_f64(DeviceLayer(li).prefill(out_fp32=False))
+    ref, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    half_ulp = np.abs(ref) * 2.0 ** -8
+    r = O.rms(ref)
+    assert np.all(np.abs(out - ref) <= 2e-2 * r + half_ulp)
+
+
+@pytest.mark.parametrize("name,nsample", [("prefill", 48), ("skewed", 24)])
+def test_prefill_full_size_sampled(name, nsample):
+    li = workloads.CONFIGS[name]()
+    dl = DeviceLayer(li)
+    out = out_to_f64(dl.prefill())
+    toks = _sample_tokens(li.T, nsample, seed=3)
+    ref, r = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k,
+                           tokens=toks)
+    assert_within_tol(out[toks], ref)
+    # every row is finite and the residual dominates nowhere unexpectedly
+    assert np.all(np.isfinite(out))
+    # deterministic: a second call gives the same bits
+    out2 = out_to_f64(dl.prefill())
+    assert np.array_equal(out, out2)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 256, 128, 8, 2),      # a single token
+    (37, 256, 128, 8, 2),     # ragged token count
+    (300, 256, 128, 2, 1),    # buckets larger than one 256-token tile
+    (40, 256, 128, 6, 6),     # k = E: every token uses every expert
+    (9, 384, 256, 1, 1),      # one expert: a dense SwiGLU FFN; 3 row blocks
+    (700, 128, 128, 3, 2),    # smallest hidden size, several tiles per expert
+])
+def test_prefill_edge_shapes(T, H, I, E, k):
+    li = workloads.make_layer("edge", T, H, I, E, k, seed=T + H + E, wr_std=0.1)
+    out = out_to_f64(DeviceLayer(li).prefill())
+    ref, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, k)
+    assert_within_tol(out, ref)
+
+
+def test_prefill_zero_scales_identity_and_empty():
+    li = workloads.tiny()
+    li.d_scales[:] = 0
+    dl = DeviceLayer(li)
+    out = out_to_f64(dl.prefill())
+    assert np.array_equal(out, O.bf16_bits_to_f64(li.x))
+    # T = 0 is a no-op
+    x0 = torch.empty((0, li.H), dtype=torch.bfloat16, device="cuda")
+    o0 = moe.moe_q4_forward_prefill(x0, dl.wr, dl.wgu, dl.wd, li.I, li.k)
+    assert o0.shape == (0, li.H)
+
+
+# ------------------------------------------------------------------- decode
+def _decode_check(li, tol=2e-2):
+    dl = DeviceLayer(li)
+    d, dbg = moe.make_debug(moe.MOE_MODE_DECODE, li.T, li.H, li.I, li.E, li.k)
+    out = out_to_f64(dl.decode(debug=dbg))
+    ref, st = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k,
+                           keep_dots=True)
+    idx = d["topk_idx"].cpu().numpy()
+    assert np.array_equal(idx, st["idx"]), "routing differs from the oracle"
+    # int8 activations and their scales: bit-exact
+    assert np.array_equal(d["q_x"].cpu().numpy().astype(np.int64), st["qx"])
+    assert np.array_equal(d["d_x"].cpu().numpy().view(np.uint16), st["dx"].view(np.uint16))
+    # gate/up int32 group dots: bit-exact, bucket order
+    tok = d["bucket_token"].cpu().numpy()
+    slot = d["bucket_slot"].cpu().numpy()
+    dots_gu = d["dots_gu"].cpu().numpy()
+    dots_d = d["dots_d"].cpu().numpy()
+    q_h = d["q_h"].cpu().numpy().astype(np.int64)
+    for p in range(li.T * li.k):
+        t, j = tok[p], slot[p]
+        assert np.array_equal(dots_gu[p], st["dots_gu"][(t, j)]), f"gate/up dots differ at row {p}"
+        # down dots: the oracle's integer dots of the GPU's own q_h
+        e = idx[t, j]
+        assert np.array_equal(dots_d[p], O.group_dots(li.d_codes[e], q_h[p])), f"down dots at row {p}"
+    # q_h vs the oracle's: within one code
+    qh_o = np.stack([st["qh"][tok[p], slot[p]] for p in range(li.T * li.k)])
+    diff = np.abs(q_h - qh_o)
+    assert diff.max() <= 1
+    assert (diff > 0).mean() < 0.01
+    assert_within_tol(out, ref, tol=tol)
+    return out
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_decode_full_size(T):
+    _decode_check(workloads.decode(T))
+
+
+def test_decode_tiny_32_tokens():
+    li = workloads.tiny()
+    li.T = 32
+    li.x = li.x[:32].copy()
+    _decode_check(li)
+
+
+def test_decode_adversarial_integer_extremes():
+    # activations all +127 (q_x = 127); gate codes 15 (q - 8 = 7), up codes 0
+    # (q - 8 = -8): group dots of 32*7*127 and -32*8*127, the largest there
+    # are.  h is then about -6e8, so its fp16 scale saturates at 65504 and
+    # every code of h clamps to -127; the down codes 15 give 32*7*(-127).
+    li = workloads.make_layer("extreme", 3, 256, 128, 4, 2, seed=41, wr_std=0.1)
+    li.gu_codes[:, : li.I] = 15
+    li.gu_codes[:, li.I:] = 0
+    li.d_codes[:] = 15
+    li.x[:] = workloads.f32_to_bf16_bits(np.full(256, 127.0, np.float32))[None, :]
+    _decode_check(li)
+
+
+def test_decode_matches_prefill_closely():
+    li = workloads.decode(16)
+    dl = DeviceLayer(li)
+    a = out_to_f64(dl.decode())
+    b = out_to_f64(dl.prefill())
+    X = O.bf16_bits_to_f64(li.x)
+    assert O.rms(a - b) < 0.05 * O.rms(b - X)
