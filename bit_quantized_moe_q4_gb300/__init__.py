@@ -187,7 +187,7 @@ def make_debug(mode: int, T: int, H: int, I: int, E: int, k: int, device="cuda")
         "bucket_slot": torch.empty(Tk, dtype=torch.int32, device=device),
     }
     if mode == MOE_MODE_PREFILL:
-        d["h"] = torch.empty((Tk, I), dtype=torch.int16, device=device)
+        d["h"] = torch.empty((Tk, I), dtype=torch.float16, device=device)
     else:
         d["q_x"] = torch.empty((T, H), dtype=torch.int8, device=device)
         d["d_x"] = torch.empty((T, G), dtype=torch.int16, device=device)

@@ -82,8 +82,8 @@ std::once_flag g_encode_once;
 
 }  // namespace
 
-bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                         uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -97,7 +97,7 @@ bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint
     const cuuint64_t strides[1] = {cols * 2};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -139,10 +139,12 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
     w.tile_e = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_n0 = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_nn = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
-    w.y = reinterpret_cast<uint16_t*>(take(Tk * H * 2));
     if (mode == MOE_MODE_PREFILL) {
+        w.y = take(Tk * H * 2);
+        w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
     } else {
+        w.y = take(Tk * H * 4);
         w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
@@ -210,7 +212,8 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     if ((rc = mark(0))) return rc;
     // 1. route
     float* logits = (mode == MOE_MODE_DECODE) ? ws.logits : (dbg ? dbg->logits : nullptr);
-    if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w, s), "route")))
+    if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w, ws.x16, s),
+                         "route")))
         return rc;
     if ((rc = mark(1))) return rc;
     // 2. bucket
@@ -219,8 +222,8 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     if ((rc = mark(2))) return rc;
     if (mode == MOE_MODE_PREFILL) {
         CUtensorMap xmap, hmap;
-        if (!encode_tmap_2d_bf16(&xmap, x, T, H, 64, 1, true) ||
-            !encode_tmap_2d_bf16(&hmap, ws.h, Tk, I, 64, 16, true))
+        if (!encode_tmap_2d_f16(&xmap, ws.x16, T, H, 64, 1, true) ||
+            !encode_tmap_2d_f16(&hmap, ws.h, Tk, I, 64, 16, true))
             return set_err(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         if ((rc = mark(3))) return rc;
         if ((rc = cuda_check(launch_prefill_gateup(&xmap, wgu, ws, T, H, I, E, k, dev->status,
@@ -244,8 +247,8 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     }
     if ((rc = mark(5))) return rc;
     // 3. combine
-    if ((rc = cuda_check(launch_combine(x, ws.y, ws.slot_pos, T, H, k, (flags & MOE_OUT_FP32) != 0,
-                                        out, s), "combine")))
+    if ((rc = cuda_check(launch_combine(x, ws.y, mode == MOE_MODE_DECODE, ws.slot_pos, T, H, k,
+                                        (flags & MOE_OUT_FP32) != 0, out, s), "combine")))
         return rc;
     if ((rc = mark(6))) return rc;
     if (dbg) {
@@ -342,7 +345,7 @@ int moe_route_topk(const uint16_t* x_bf16, const float* wr, int T, int H, int E,
     int rc = device_info(&dev);
     if (rc) return rc;
     return cuda_check(launch_route(x_bf16, wr, T, H, E, k, logits_or_null, topk_idx, topk_w,
-                                   static_cast<cudaStream_t>(stream)),
+                                   nullptr, static_cast<cudaStream_t>(stream)),
                       "route");
 }
 

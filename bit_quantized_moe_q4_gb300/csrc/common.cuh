@@ -40,6 +40,12 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
     return __half2float(__ushort_as_half(h));
 }
+// fp32 -> fp16 (round to nearest even), saturating at +-65504 instead of
+// overflowing to infinity.
+__device__ __forceinline__ uint16_t float_to_half_bits_sat(float f) {
+    f = fminf(fmaxf(f, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(f));
+}
 
 // ---- shared-memory addresses and fences ------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -145,8 +151,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (kind::f16), fp32 accumulate.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -189,12 +195,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                    // swizzle: 128 bytes
     return d;
 }
-// Instruction descriptor for kind::f16 with bf16 A and B (both K-major) and an
-// fp32 accumulator of M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor for kind::f16 with fp16 A and B (both K-major) and an
+// fp32 accumulator of M x N.  (Format code 0 is fp16, 1 would be bf16.)
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4)                          // D format: f32
-           | (1u << 7)                        // A format: bf16
-           | (1u << 10)                       // B format: bf16
+           | (0u << 7)                        // A format: f16
+           | (0u << 10)                       // B format: f16
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }

@@ -12,7 +12,7 @@
 // bucket are all handled by the CTA, so each weight byte is read once):
 //   gate/up: 32 features x (gate, up) rows, K = H; then h = silu(g) * u and
 //            its int8 quantisation per 32 features (one group per CTA).
-//   down:    64 rows of W_d, K = I; y = routing weight * row sum (bf16).
+//   down:    64 rows of W_d, K = I; y = routing weight * row sum (fp32).
 #include "common.cuh"
 #include "internal.h"
 
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(
     const uint8_t* __restrict__ wd, const int8_t* __restrict__ q_h,
     const uint16_t* __restrict__ d_h, const int32_t* __restrict__ counters,
     const int32_t* __restrict__ touched, const int32_t* __restrict__ offsets,
-    const float* __restrict__ slot_w, int H, int I, uint16_t* __restrict__ y,
+    const float* __restrict__ slot_w, int H, int I, float* __restrict__ y,
     int32_t* __restrict__ dots_dbg) {
     extern __shared__ __align__(16) uint8_t smem[];
     if ((int)blockIdx.x >= counters[kCntTouched]) return;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(
     if ((lane & 17) == 0) {
 #pragma unroll
         for (int n = 0; n < TMAX; ++n)
-            if (n < c) y[((size_t)off + n) * H + row] = float_to_bf16_bits(acc[n] * slot_w[off + n]);
+            if (n < c) y[((size_t)off + n) * H + row] = acc[n] * slot_w[off + n];
     }
 }
 
@@ -224,7 +224,7 @@ cudaError_t launch_decode_down(const void* wd, const Workspace& ws, int T, int H
     dim3 grid(max_touched, H / 64);
     decode_down_kernel<<<grid, 256, smem, s>>>(static_cast<const uint8_t*>(wd), ws.q_h, ws.d_h,
                                                ws.counters, ws.touched, ws.offsets, ws.slot_w, H,
-                                               I, ws.y, dots_dbg);
+                                               I, static_cast<float*>(ws.y), dots_dbg);
     return cudaGetLastError();
 }
 

@@ -29,8 +29,10 @@ struct Workspace {
     int32_t* tile_e;        // [max_tiles]   expert of each token tile
     int32_t* tile_n0;       // [max_tiles]   first bucket row of the tile
     int32_t* tile_nn;       // [max_tiles]   rows in the tile
-    uint16_t* h;            // [T*k, I] bf16 (prefill)
-    uint16_t* y;            // [T*k, H] bf16 weighted expert outputs
+    uint16_t* x16;          // [T, H] fp16 copy of x (prefill GEMM operand)
+    uint16_t* h;            // [T*k, I] fp16 (prefill)
+    void* y;                // [T*k, H] weighted expert outputs: fp16
+                            // (prefill) or fp32 (decode)
     int8_t* q_x;            // [T, H]        (decode)
     uint16_t* d_x;          // [T, H/32]     (decode)
     int8_t* q_h;            // [T*k, I]      (decode)
@@ -48,7 +50,7 @@ int nchunks(int T);
 cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
                         void* dst, cudaStream_t s);
 cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
-                         float* logits, int32_t* idx, float* w, cudaStream_t s);
+                         float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
 cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, const Workspace& ws,
@@ -63,11 +65,12 @@ cudaError_t launch_decode_gateup(const void* wgu, const Workspace& ws, int T, in
                                  int E, int k, int32_t* dots_dbg, cudaStream_t s);
 cudaError_t launch_decode_down(const void* wd, const Workspace& ws, int T, int H, int I, int E,
                                int k, int32_t* dots_dbg, cudaStream_t s);
-cudaError_t launch_combine(const uint16_t* x, const uint16_t* y, const int32_t* slot_pos, int T,
-                           int H, int k, bool out_fp32, void* out, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
+                           int T, int H, int k, bool out_fp32, void* out, cudaStream_t s);
 
 // tensor maps
-bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                         uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// 2-D map over a row-major [rows, cols] tensor of 16-bit elements (fp16).
+bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 }  // namespace moeq4

@@ -26,11 +26,29 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int T, int H,
     if (lane == 0) d[(size_t)t * G + g] = db;
 }
 
+// Eight consecutive y values as floats: fp16 (prefill) or fp32 (decode).
+__device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 // out[t, :] = x[t, :] + sum_{j=0..k-1} y[slot_pos[t, j], :], accumulated in
 // fp32 in j order.  y rows already carry the routing weight.  One thread per
 // 8 columns.
-template <bool OUT_FP32>
-__global__ void combine_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y,
+template <bool OUT_FP32, typename Y>
+__global__ void combine_kernel(const uint16_t* __restrict__ x, const Y* __restrict__ y,
                                const int32_t* __restrict__ slot_pos, int T, int H, int k,
                                void* __restrict__ out) {
     const int cols8 = H / 8;
@@ -49,13 +67,10 @@ __global__ void combine_kernel(const uint16_t* __restrict__ x, const uint16_t* _
     }
     for (int j = 0; j < k; ++j) {
         const int pos = slot_pos[(size_t)t * k + j];
-        const uint4 v = *reinterpret_cast<const uint4*>(y + (size_t)pos * H + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float v[8];
+        load8(y + (size_t)pos * H + c, v);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            acc[2 * p] += __uint_as_float(w[p] << 16);
-            acc[2 * p + 1] += __uint_as_float(w[p] & 0xffff0000u);
-        }
+        for (int p = 0; p < 8; ++p) acc[p] += v[p];
     }
     if (OUT_FP32) {
         float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H + c);
@@ -82,16 +97,22 @@ cudaError_t launch_act_quant(const uint16_t* x, int T, int H, int8_t* q, uint16_
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const uint16_t* x, const uint16_t* y, const int32_t* slot_pos, int T,
-                           int H, int k, bool out_fp32, void* out, cudaStream_t s) {
+cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
+                           int T, int H, int k, bool out_fp32, void* out, cudaStream_t s) {
     const size_t n = (size_t)T * (H / 8);
     if (n == 0) return cudaSuccess;
     const int threads = 256;
     const unsigned blocks = (unsigned)((n + threads - 1) / threads);
-    if (out_fp32)
-        combine_kernel<true><<<blocks, threads, 0, s>>>(x, y, slot_pos, T, H, k, out);
+    const float* yf = static_cast<const float*>(y);
+    const uint16_t* yh = static_cast<const uint16_t*>(y);
+    if (out_fp32 && y_fp32)
+        combine_kernel<true><<<blocks, threads, 0, s>>>(x, yf, slot_pos, T, H, k, out);
+    else if (out_fp32)
+        combine_kernel<true><<<blocks, threads, 0, s>>>(x, yh, slot_pos, T, H, k, out);
+    else if (y_fp32)
+        combine_kernel<false><<<blocks, threads, 0, s>>>(x, yf, slot_pos, T, H, k, out);
     else
-        combine_kernel<false><<<blocks, threads, 0, s>>>(x, y, slot_pos, T, H, k, out);
+        combine_kernel<false><<<blocks, threads, 0, s>>>(x, yh, slot_pos, T, H, k, out);
     return cudaGetLastError();
 }
 

@@ -5,8 +5,11 @@
 // to each expert, run over the whole prompt in one pass (Methodology 4,
 // "Single-Pass Prefill": the batch is as large as possible).  There it ran on
 // a Fermi GPU without tensor cores; here each expert's token bucket is one
-// operand of tcgen05.mma with bf16 inputs and fp32 accumulators in tensor
-// memory.
+// operand of tcgen05.mma with fp16 inputs and fp32 accumulators in tensor
+// memory.  fp16 rather than bf16: the dequantised weights d(q - 8), the bf16
+// hidden states (exact in fp16 within its range) and h keep 3 more mantissa
+// bits, which cuts the layer's error against exact arithmetic about tenfold
+// at the same tensor-core rate.
 //
 // Weights sit on the MMA's M side (128 rows per tile) and tokens on N (up to
 // 256 per tile, padded to a multiple of 16), so a bucket of ~128 tokens wastes
@@ -15,11 +18,12 @@
 //                   and brings the bucket's token rows in: gate/up gathers
 //                   rows of x by token id (TMA gather4), down loads
 //                   consecutive rows of h (2-D TMA tiles);
-//   dequant warps   turn codes and fp16 scales into bf16 w = d (q - 8) in the
+//   dequant warps   turn codes and fp16 scales into fp16 w = d (q - 8) in the
 //                   128-byte-swizzled K-major layout the MMA reads;
 //   MMA warp        one thread issues 4 x K=16 MMAs per matrix into TMEM;
-//   epilogue warps  read TMEM: gate/up -> h = silu(g) * u (bf16), down ->
-//                   y = w_route * acc (bf16), in bucket order.
+//   epilogue warps  read TMEM: gate/up -> h = silu(g) * u, down ->
+//                   y = w_route * acc, both fp16 (saturating at +-65504), in
+//                   bucket order.
 // One persistent CTA per SM walks a static list of (token tile, row block)
 // work items.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the status word, drains its copies, frees TMEM and exits.
@@ -30,8 +34,8 @@ namespace moeq4 {
 namespace {
 
 constexpr int BN = 256;           // max tokens per tile
-constexpr int A_MAT_BYTES = 128 * 128;  // 128 rows x 64 bf16
-constexpr int B_BYTES = BN * 128;       // BN rows x 64 bf16
+constexpr int A_MAT_BYTES = 128 * 128;  // 128 rows x 64 fp16
+constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
 constexpr int NUM_THREADS = 448;  // 14 warps
 constexpr int WARP_PRODUCER = 0, WARP_MMA = 1, WARP_EPI0 = 2, WARP_DEQ0 = 6;
 constexpr int NUM_EPI_WARPS = 4, NUM_DEQ_WARPS = 8;
@@ -69,13 +73,13 @@ struct GemmArgs {
     int* status;
 };
 
-__device__ __forceinline__ uint32_t bf16x2_dequant(uint32_t nib2, uint32_t d2) {
-    // nib2 holds two codes at bits 0..3 and 16..19; 0x4300 is bf16 128.0 and
-    // its ulp is 1, so (0x4300 | q) is exactly 128 + q.
-    const uint32_t v = nib2 | 0x43004300u;
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
-    const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);  // 128 + 8
-    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&d2);
+__device__ __forceinline__ uint32_t f16x2_dequant(uint32_t nib2, uint32_t d2) {
+    // nib2 holds two codes at bits 0..3 and 16..19; 0x6400 is fp16 1024.0 and
+    // its ulp is 1, so (0x6400 | q) is exactly 1024 + q.
+    const uint32_t v = nib2 | 0x64006400u;
+    __half2 b = *reinterpret_cast<const __half2*>(&v);
+    const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);  // 1024 + 8
+    const __half2 d = *reinterpret_cast<const __half2*>(&d2);
     b = __hmul2(__hsub2(b, off), d);  // (q - 8) exact, then one rounding of d(q-8)
     return *reinterpret_cast<uint32_t*>(&b);
 }
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int tile = w / rb_count;
             const int nn = args.tile_nn[tile];
             const int npad = (nn + 15) & ~15;
-            const uint32_t idesc = idesc_bf16_f32(128, npad);
+            const uint32_t idesc = idesc_f16_f32(128, npad);
             if (*abort_flag || !mbar_wait(acc_empty, (item & 1) ^ 1)) {
                 fail();
                 ok = false;
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int m = 0; m < C::NMAT; ++m) {
                             const uint64_t adesc =
                                 sw128_kmajor_desc(a_sm + m * A_MAT_BYTES + kk * 32);
-                            mma_bf16(tmem + m * 256, adesc, bdesc, idesc, (kb | kk) != 0);
+                            mma_f16(tmem + m * 256, adesc, bdesc, idesc, (kb | kk) != 0);
                         }
                     }
                     mma_commit(empty(s));
@@ -281,13 +285,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t word = *reinterpret_cast<const uint32_t*>(t + r * 32 + c * 4);
                     const uint16_t dh =
                         *reinterpret_cast<const uint16_t*>(t + kTileCodeBytes + r * 4 + (c / 4) * 2);
-                    const uint16_t db = float_to_bf16_bits(half_bits_to_float(dh));
-                    const uint32_t d2 = (uint32_t)db | ((uint32_t)db << 16);
+                    const uint32_t d2 = (uint32_t)dh | ((uint32_t)dh << 16);
                     uint4 o;
-                    o.x = bf16x2_dequant(word & 0x000F000Fu, d2);
-                    o.y = bf16x2_dequant((word >> 4) & 0x000F000Fu, d2);
-                    o.z = bf16x2_dequant((word >> 8) & 0x000F000Fu, d2);
-                    o.w = bf16x2_dequant((word >> 12) & 0x000F000Fu, d2);
+                    o.x = f16x2_dequant(word & 0x000F000Fu, d2);
+                    o.y = f16x2_dequant((word >> 4) & 0x000F000Fu, d2);
+                    o.z = f16x2_dequant((word >> 8) & 0x000F000Fu, d2);
+                    o.w = f16x2_dequant((word >> 12) & 0x000F000Fu, d2);
                     *reinterpret_cast<uint4*>(a + m * A_MAT_BYTES + r * 128 + ((c ^ (r & 7)) * 16)) = o;
                 }
                 fence_proxy_async_smem();
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
                             const float h = gv / (1.0f + __expf(-gv)) * uv;
                             args.out[(size_t)(n0 + c0 + j) * args.out_ld + feat] =
-                                float_to_bf16_bits(h);
+                                float_to_half_bits_sat(h);
                         }
                     }
                 } else {
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (c0 + j < nn) {
                             const float yv = __uint_as_float(g[j]) * args.slot_w[n0 + c0 + j];
                             args.out[(size_t)(n0 + c0 + j) * args.out_ld + feat] =
-                                float_to_bf16_bits(yv);
+                                float_to_half_bits_sat(yv);
                         }
                     }
                 }
@@ -395,7 +398,7 @@ cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const 
     a.tile_nn = ws.tile_nn;
     a.bucket_token = ws.bucket_token;
     a.slot_w = ws.slot_w;
-    a.out = ws.y;
+    a.out = static_cast<uint16_t*>(ws.y);
     a.K = I;
     a.rows_per_e = H;
     a.out_rows = H;

@@ -11,7 +11,8 @@
 // Two shapes:
 //   fused  16 tokens x all experts per CTA; logits stay in shared memory and
 //          the CTA's warps pick the top-k.  Used for many tokens, and whenever
-//          no logits buffer is available.
+//          no logits buffer is available.  Optionally writes an fp16 copy of x
+//          (the prefill GEMM operand) while it reads x anyway.
 //   small  one warp per expert over all tokens (decode, T <= 32), spreading
 //          the router matrix over many SMs; a second kernel picks the top-k.
 #include "common.cuh"
@@ -84,7 +85,8 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
                                                           int H, int E, int k,
                                                           float* __restrict__ logits,
                                                           int32_t* __restrict__ idx,
-                                                          float* __restrict__ w) {
+                                                          float* __restrict__ w,
+                                                          uint16_t* __restrict__ x16) {
     // Padded to 33 columns so both the row-wise fills and the column reads of
     // the inner loop are free of bank conflicts.
     __shared__ float xs[RT][RK + 1];
@@ -102,7 +104,10 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
         for (int i = tid; i < RT * RK; i += 256) {
             const int t = i / RK, kk = i % RK;
             const int tg = t0 + t, kg = k0 + kk;
-            xs[t][kk] = (tg < T && kg < H) ? bf16_bits_to_float(x[(size_t)tg * H + kg]) : 0.f;
+            const bool in = tg < T && kg < H;
+            const float v = in ? bf16_bits_to_float(x[(size_t)tg * H + kg]) : 0.f;
+            xs[t][kk] = v;
+            if (x16 && in) x16[(size_t)tg * H + kg] = float_to_half_bits_sat(v);
         }
         for (int i = tid; i < EMAX * RK; i += 256) {
             const int e = i / RK, kk = i % RK;
@@ -202,9 +207,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 
 // `logits` may be null; the split path is taken only when it is not.
 cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
-                         float* logits, int32_t* idx, float* w, cudaStream_t s) {
+                         float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    if (logits && T <= 32 && (H % 128) == 0) {
+    if (logits && !x16 && T <= 32 && (H % 128) == 0) {
         const dim3 grid((E + 3) / 4);
         if (T <= 4)
             logits_small_kernel<4><<<grid, 128, 0, s>>>(x, wr, T, H, E, logits);
@@ -214,7 +219,7 @@ cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E
             logits_small_kernel<32><<<grid, 128, 0, s>>>(x, wr, T, H, E, logits);
         topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, idx, w);
     } else {
-        route_fused_kernel<<<(T + RT - 1) / RT, 256, 0, s>>>(x, wr, T, H, E, k, logits, idx, w);
+        route_fused_kernel<<<(T + RT - 1) / RT, 256, 0, s>>>(x, wr, T, H, E, k, logits, idx, w, x16);
     }
     return cudaGetLastError();
 }

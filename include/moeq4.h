@@ -15,8 +15,10 @@
  *             softmax over the k chosen logits
  *   expert    h = silu(W_g x) * (W_u x), y = W_d h   (SwiGLU FFN)
  *   combine   out[t] = x[t] + sum_j w[t, j] * y(t, j), j = 0..k-1 in order
- *   prefill   ("grouped 4-bit GEMM"): bf16 activations, weights dequantised
- *             to bf16 in the kernel, fp32 accumulation on the tensor cores
+ *   prefill   ("grouped 4-bit GEMM"): bf16 activations; the tensor-core
+ *             operands are fp16 (x converted exactly, weights d(q-8) rounded
+ *             once, h rounded once) with fp32 accumulation; values beyond the
+ *             fp16 range (|v| > 65504) saturate there
  *   decode    ("W4A8 integer kernel"): activations quantised to int8 per 32
  *             with an fp16 scale; exact int32 group dot products, scaled by
  *             d_w * d_x in fp32; h quantised the same way before the down
@@ -94,7 +96,7 @@ typedef struct moe_debug {
     int32_t*  expert_offsets;  /* [E+1] exclusive prefix sum of bucket sizes */
     int32_t*  bucket_token;    /* [T*k] token of each bucket-order row       */
     int32_t*  bucket_slot;     /* [T*k] slot j of each bucket-order row      */
-    uint16_t* h;               /* prefill: [T*k, I] bf16 SwiGLU output,
+    uint16_t* h;               /* prefill: [T*k, I] fp16 SwiGLU output,
                                   bucket order                               */
     int8_t*   q_x;             /* decode: [T, H] int8 activation codes       */
     uint16_t* d_x;             /* decode: [T, H/32] fp16 activation scales   */

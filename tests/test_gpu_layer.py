@@ -37,12 +37,11 @@ def test_prefill_tiny_full():
     ref, r = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
     assert np.array_equal(d["topk_idx"].cpu().numpy(), r["idx"])
     assert_within_tol(out, ref)
-    # the MoE term alone is also close (a stricter view than the full output)
+    # a stricter view: the MoE term alone (out - x) is within 1% too
     X = O.bf16_bits_to_f64(li.x)
-    assert_within_tol(out - X, ref - X, tol=2e-2, what="MoE term")
-    # stage: h = silu(W_g x) * (W_u x) per bucket row, bf16
-    h = d["h"].cpu().numpy().view(np.uint16)
-    h = O.bf16_bits_to_f64(h)
+    assert_within_tol(out - X, ref - X, tol=1e-2, what="MoE term")
+    # stage: h = silu(W_g x) * (W_u x) per bucket row, fp16
+    h = d["h"].cpu().numpy().astype(np.float64)
     tok = d["bucket_token"].cpu().numpy()
     off = d["expert_offsets"].cpu().numpy()
     href = np.zeros_like(h)
@@ -53,7 +52,7 @@ def test_prefill_tiny_full():
         W = O.q4_dequant(li.gu_codes[e], li.gu_scales[e])
         Xe = X[tok[rows]]
         href[rows] = O.swiglu(Xe @ W[: li.I].T, Xe @ W[li.I:].T)
-    assert_within_tol(h, href, tol=2e-2, what="h")
+    assert_within_tol(h, href, tol=1e-2, what="h")
 
 
 def test_prefill_tiny_bf16_output():
