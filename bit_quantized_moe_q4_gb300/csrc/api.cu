@@ -203,10 +203,19 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     const size_t Tk = (size_t)T * k;
 
     void** ev = dbg ? dbg->stage_events : nullptr;
+    bool capturing = false;
+    if (ev) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((rc = cuda_check(cudaStreamIsCapturing(s, &cs), "capture status"))) return rc;
+        capturing = cs == cudaStreamCaptureStatusActive;
+    }
+    // Inside a stream capture the events become external event-record nodes of
+    // the graph; otherwise they are plain records.
     auto mark = [&](int i) -> int {
         if (!ev || !ev[i]) return MOE_OK;
-        return cuda_check(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), s,
-                                                   cudaEventRecordExternal),
+        cudaEvent_t e = static_cast<cudaEvent_t>(ev[i]);
+        return cuda_check(capturing ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                    : cudaEventRecord(e, s),
                           "stage event");
     };
     if ((rc = mark(0))) return rc;
