@@ -359,6 +359,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="run one workload only (short profiling runs)")
+    ap.add_argument("--decode-tokens", type=str, default="1,4,16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -391,10 +394,16 @@ def main():
 
     peaks = load_peaks()
     warm = max(args.warmup, 3)
+    dec_T = [int(t) for t in args.decode_tokens.split(",")] if args.only != "prefill" else []
+    if args.only != "prefill" and 1 not in dec_T:
+        dec_T = [1] + dec_T
     with ClockSampler(local) as clk:
-        dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier) for T in (1, 4, 16)}
-        pre = None if args.no_prefill else bench_prefill("prefill", args.steps, warm, torch, moe,
-                                                         device, barrier)
+        dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier) for T in dec_T}
+        pre = None if (args.no_prefill or args.only == "decode") else bench_prefill(
+            "prefill", args.steps, warm, torch, moe, device, barrier)
+    if args.only == "prefill":
+        print(json.dumps({"prefill": pre, "clocks": clk.summary()}))
+        return 0
     clocks = clk.summary()
     status = moe.moe_get_device_status()
 

@@ -109,10 +109,10 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
             xs[t][kk] = v;
             if (x16 && in) x16[(size_t)tg * H + kg] = float_to_half_bits_sat(v);
         }
-        for (int i = tid; i < EMAX * RK; i += 256) {
+        for (int i = tid; i < E * RK; i += 256) {
             const int e = i / RK, kk = i % RK;
             const int kg = k0 + kk;
-            ws[e][kk] = (e < E && kg < H) ? wr[(size_t)e * H + kg] : 0.f;
+            ws[e][kk] = (kg < H) ? wr[(size_t)e * H + kg] : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -120,9 +120,11 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
             const float xa[2] = {xs[ty * 2][kk], xs[ty * 2 + 1][kk]};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float wv = ws[tx + 32 * j][kk];
-                acc[0][j] = fmaf(xa[0], wv, acc[0][j]);
-                acc[1][j] = fmaf(xa[1], wv, acc[1][j]);
+                if (tx + 32 * j < E) {  // experts beyond E are never read
+                    const float wv = ws[tx + 32 * j][kk];
+                    acc[0][j] = fmaf(xa[0], wv, acc[0][j]);
+                    acc[1][j] = fmaf(xa[1], wv, acc[1][j]);
+                }
             }
         }
         __syncthreads();
