@@ -41,8 +41,9 @@ MOE_DECODE_MAX_T = 32
 EXPORTED_SYMBOLS = (
     "moe_version", "moe_last_error_string", "moe_get_device_status", "moe_clear_device_status",
     "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk", "moe_workspace_bytes",
-    "moe_q4_forward_prefill", "moe_w4a8_forward_decode",
+    "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
 )
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class MoeError(RuntimeError):
@@ -90,6 +91,9 @@ def load_library(path: str | None = None):
                                         _vp, _vp, _sz, ctypes.POINTER(MoeDebug), _vp]),
         "moe_w4a8_forward_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_uint,
                                          _vp, _vp, _sz, ctypes.POINTER(MoeDebug), _vp]),
+        "moe_w4a8_forward_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                                 ctypes.c_uint, _vp, ctypes.POINTER(MoeDebug),
+                                                 _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -250,3 +254,22 @@ class StageEvents:
 
     def ms(self, i: int, j: int) -> float:
         return self.events[i].elapsed_time(self.events[j])
+
+
+def moe_w4a8_forward_decode_noalloc(x, wr, wgu_packed, wd_packed, I: int, k: int, out=None,
+                                    out_fp32: bool = True, debug: MoeDebug | None = None,
+                                    stream=None):
+    """The decode layer with the library's fixed scratch array instead of a
+    caller workspace, for callers that cannot allocate device memory (see
+    include/moeq4.h).  ``out`` should be preallocated by such callers; this
+    wrapper only creates it when it is not given."""
+    T, H = x.shape
+    E = wr.shape[0]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=x.device)
+    flags = MOE_OUT_FP32 if out_fp32 else 0
+    _check(load_library().moe_w4a8_forward_decode_noalloc(
+        _ptr(x), _ptr(wr), _ptr(wgu_packed), _ptr(wd_packed), T, H, I, E, k, flags, _ptr(out),
+        ctypes.byref(debug) if debug is not None else None, _stream(stream)))
+    return out

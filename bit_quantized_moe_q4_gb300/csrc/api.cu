@@ -280,6 +280,9 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
 }
 
 }  // namespace
+
+int record_error(int code, const char* msg) { return set_err(code, "%s", msg); }
+
 }  // namespace moeq4
 
 using namespace moeq4;

@@ -46,6 +46,9 @@ enum { kCntTouched = 0, kCntTiles = 1 };
 
 int nchunks(int T);
 
+// Sets the thread's error string (moe_last_error_string) and returns code.
+int record_error(int code, const char* msg);
+
 // launchers; each returns cudaGetLastError() of its launch
 cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
                         void* dst, cudaStream_t s);

@@ -200,6 +200,36 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
                             void* out, void* workspace, size_t ws_bytes,
                             moe_debug* dbg, void* stream);
 
+/*
+ * moe_w4a8_forward_decode_noalloc — the same decode layer as
+ * moe_w4a8_forward_decode, for callers that cannot allocate device memory:
+ * components hosted by an application or plugin interface that owns all
+ * device memory and offers no allocation, and latency-critical decode loops
+ * that must not call cudaMalloc (it can synchronise the device).  The paper
+ * has no counterpart; this is a convenience of this library.
+ *
+ * The caller passes inputs and outputs exactly as for
+ * moe_w4a8_forward_decode; the scratch workspace is a fixed device array of
+ * MOE_NOALLOC_SCRATCH_BYTES inside this library (every GPU that loads the
+ * library holds it until the process exits).  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Shapes whose workspace (moe_workspace_bytes(MOE_MODE_DECODE, ...)) is
+ *     larger than the array are rejected with MOE_ERR_WORKSPACE; 4 MiB covers
+ *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (no
+ *     value in it has to start at zero).  Calls whose work overlaps on the GPU
+ *     (several streams or host threads on one device) race on it: serialise
+ *     them.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int moe_w4a8_forward_decode_noalloc(const uint16_t* x_bf16, const float* wr,
+                                    const void* wgu_packed, const void* wd_packed,
+                                    int T, int H, int I, int E, int k, unsigned flags,
+                                    void* out, moe_debug* dbg, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
