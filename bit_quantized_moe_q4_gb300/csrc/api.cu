@@ -149,6 +149,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
+        w.tickets = reinterpret_cast<int32_t*>(take((size_t)(H / kDecodeDownRows) * 4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;
@@ -213,28 +214,36 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     // the graph; otherwise they are plain records.
     auto mark = [&](int i) -> int {
         if (!ev || !ev[i]) return MOE_OK;
-        cudaEvent_t e = static_cast<cudaEvent_t>(ev[i]);
-        return cuda_check(capturing ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
-                                    : cudaEventRecord(e, s),
-                          "stage event");
+        return cuda_check(record_stage(ev[i], s, capturing), "stage event");
     };
     if ((rc = mark(0))) return rc;
-    // 1. route
-    float* logits = (mode == MOE_MODE_DECODE) ? ws.logits : (dbg ? dbg->logits : nullptr);
-    if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w, ws.x16, s),
-                         "route")))
-        return rc;
-    if ((rc = mark(1))) return rc;
-    // 2. bucket
-    if ((rc = cuda_check(launch_bucket(ws.topk_idx, ws.topk_w, T, E, k, ws.tile_n, ws, s), "bucket")))
-        return rc;
-    if ((rc = mark(2))) return rc;
-    if (mode == MOE_MODE_PREFILL) {
+    if (mode == MOE_MODE_DECODE) {
+        // route + buckets + x codes, gate/up, down + combine: three kernels
+        if ((rc = cuda_check(launch_decode(x, wr, wgu, wd, T, H, I, E, k,
+                                           (flags & MOE_OUT_FP32) != 0, out, ws,
+                                           dbg ? dbg->dots_gu : nullptr,
+                                           dbg ? dbg->dots_d : nullptr, ev, capturing, s),
+                             "decode")))
+            return rc;
+    } else {
+        // 1. route (also writes the fp16 copy of x)
+        float* logits = dbg ? dbg->logits : nullptr;
+        if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w,
+                                          ws.x16, s),
+                             "route")))
+            return rc;
+        if ((rc = mark(1))) return rc;
+        // 2. bucket
+        if ((rc = cuda_check(launch_bucket(ws.topk_idx, ws.topk_w, T, E, k, ws.tile_n, ws, s),
+                             "bucket")))
+            return rc;
+        if ((rc = mark(2))) return rc;
         CUtensorMap xmap, hmap;
         if (!encode_tmap_2d_f16(&xmap, ws.x16, T, H, 64, 1, true) ||
             !encode_tmap_2d_f16(&hmap, ws.h, Tk, I, 64, 16, true))
             return set_err(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         if ((rc = mark(3))) return rc;
+        // 3. grouped GEMMs
         if ((rc = cuda_check(launch_prefill_gateup(&xmap, wgu, ws, T, H, I, E, k, dev->status,
                                                    dev->num_sms, s), "prefill gate/up")))
             return rc;
@@ -242,26 +251,16 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
         if ((rc = cuda_check(launch_prefill_down(&hmap, wd, ws, T, H, I, E, k, dev->status,
                                                  dev->num_sms, s), "prefill down")))
             return rc;
-    } else {
-        if ((rc = cuda_check(launch_act_quant(x, T, H, ws.q_x, ws.d_x, s), "activation quantiser")))
+        if ((rc = mark(5))) return rc;
+        // 4. combine
+        if ((rc = cuda_check(launch_combine(x, ws.y, false, ws.slot_pos, T, H, k,
+                                            (flags & MOE_OUT_FP32) != 0, out, s), "combine")))
             return rc;
-        if ((rc = mark(3))) return rc;
-        if ((rc = cuda_check(launch_decode_gateup(wgu, ws, T, H, I, E, k, dbg ? dbg->dots_gu : nullptr, s),
-                             "decode gate/up")))
-            return rc;
-        if ((rc = mark(4))) return rc;
-        if ((rc = cuda_check(launch_decode_down(wd, ws, T, H, I, E, k, dbg ? dbg->dots_d : nullptr, s),
-                             "decode down")))
-            return rc;
+        if ((rc = mark(6))) return rc;
     }
-    if ((rc = mark(5))) return rc;
-    // 3. combine
-    if ((rc = cuda_check(launch_combine(x, ws.y, mode == MOE_MODE_DECODE, ws.slot_pos, T, H, k,
-                                        (flags & MOE_OUT_FP32) != 0, out, s), "combine")))
-        return rc;
-    if ((rc = mark(6))) return rc;
     if (dbg) {
-        if (mode == MOE_MODE_DECODE && (rc = copy_d2d(dbg->logits, ws.logits, (size_t)T * E * 4, s))) return rc;
+        if (mode == MOE_MODE_DECODE && (rc = copy_d2d(dbg->logits, ws.logits, (size_t)T * E * 4, s)))
+            return rc;
         if ((rc = copy_d2d(dbg->topk_idx, ws.topk_idx, Tk * 4, s))) return rc;
         if ((rc = copy_d2d(dbg->topk_w, ws.topk_w, Tk * 4, s))) return rc;
         if ((rc = copy_d2d(dbg->expert_offsets, ws.offsets, (size_t)(E + 1) * 4, s))) return rc;
@@ -282,6 +281,12 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
 }  // namespace
 
 int record_error(int code, const char* msg) { return set_err(code, "%s", msg); }
+
+cudaError_t record_stage(void* event, cudaStream_t s, bool capturing) {
+    cudaEvent_t e = static_cast<cudaEvent_t>(event);
+    return capturing ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                     : cudaEventRecord(e, s);
+}
 
 }  // namespace moeq4
 

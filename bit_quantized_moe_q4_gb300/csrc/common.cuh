@@ -205,6 +205,39 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// ---- thread-block clusters and programmatic dependent launch ---------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster; release/acquire orders shared and
+// distributed-shared memory.  Cluster CTAs are co-scheduled, so it completes.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Programmatic dependent launch: wait for the prerequisite grid's completion
+// (and its memory), or let the dependent grid start being scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- warp helpers ------------------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -215,6 +248,62 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// ---- router top-k ----------------------------------------------------------
+// Comparator: larger logit wins; equal logits -> lower expert index wins.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// Top-k of one token's logits (row of `E` floats readable by the whole warp);
+// lane j < k returns the j-th choice in (sel_i, weight).
+__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int& sel_i,
+                                          float& weight) {
+    const int lane = threadIdx.x % 32;
+    constexpr int PER = kMaxExperts / 32;
+    float v[PER];
+    bool taken[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? row[e] : 0.f;
+        taken[i] = !(e < E);
+    }
+    float sel_v = 0.f;
+    sel_i = 0;
+    for (int r = 0; r < k; ++r) {
+        float bv = 0.f;
+        int bi = 0x7fffffff;  // "none yet"
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (!taken[i] && (bi == 0x7fffffff || better(v[i], e, bv, bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (lane + 32 * i == bi) taken[i] = true;
+        if (lane == r) {
+            sel_v = bv;
+            sel_i = bi;
+        }
+    }
+    const float m = __shfl_sync(0xffffffffu, sel_v, 0);  // the largest
+    const float z = (lane < k) ? expf(sel_v - m) : 0.f;
+    const float s = warp_sum(z);
+    weight = z / s;
 }
 
 // Activation quantiser decision, taken in fp32 (see act-quant kernels):

@@ -33,6 +33,7 @@ struct Workspace {
     uint16_t* h;            // [T*k, I] fp16 (prefill)
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
+    int32_t* tickets;       // [H / kDecodeDownRows] (decode) combine tickets
     int8_t* q_x;            // [T, H]        (decode)
     uint16_t* d_x;          // [T, H/32]     (decode)
     int8_t* q_h;            // [T*k, I]      (decode)
@@ -43,6 +44,12 @@ struct Workspace {
 
 // counters[] slots
 enum { kCntTouched = 0, kCntTiles = 1 };
+
+// Rows of W_d per decode down-projection CTA (one combine ticket each).
+constexpr int kDecodeDownRows = 64;
+
+// Records a stage event on s (as an external graph node while s is capturing).
+cudaError_t record_stage(void* event, cudaStream_t s, bool capturing);
 
 int nchunks(int T);
 
@@ -62,12 +69,13 @@ cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, con
 cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const Workspace& ws,
                                 int T, int H, int I, int E, int k, int* status, int num_sms,
                                 cudaStream_t s);
-cudaError_t launch_act_quant(const uint16_t* x, int T, int H, int8_t* q, uint16_t* d,
-                             cudaStream_t s);
-cudaError_t launch_decode_gateup(const void* wgu, const Workspace& ws, int T, int H, int I,
-                                 int E, int k, int32_t* dots_dbg, cudaStream_t s);
-cudaError_t launch_decode_down(const void* wd, const Workspace& ws, int T, int H, int I, int E,
-                               int k, int32_t* dots_dbg, cudaStream_t s);
+// The whole W4A8 decode layer (route + buckets + x codes, gate/up, down +
+// combine).  `events` is null or the caller's MOE_NUM_STAGE_EVENTS events;
+// boundaries 1..6 are recorded between the kernels.
+cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
+                          int T, int H, int I, int E, int k, bool out_fp32, void* out,
+                          const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
+                          void** events, bool capturing, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
                            int T, int H, int k, bool out_fp32, void* out, cudaStream_t s);
 

@@ -1,30 +1,11 @@
-// Activation quantiser (decode) and the weighted combine with residual.
-//
-// The decode path of the page "A 35B Hybrid-Attention Mixture-of-Experts
-// Model on a 6GB 2011 GPU" (Methodology 1 "Decode (CPU)" and 2
-// "Quantization") pairs the 4-bit weights with 8-bit activations.  Reading
-// taken here: per 32 consecutive values, d = fp16(amax / 127) and
-// q = clamp(round-half-away(x / d), -127, 127), both quotients in fp32.
+// Weighted combine with residual for the prefill layer (the decode layer
+// combines inside its down-projection kernel):
+//   out[t] = x[t] + sum_j w[t, j] * y(t, j), j = 0..k-1 in order.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moeq4 {
 namespace {
-
-// One warp per (token, group of 32).
-__global__ void act_quant_kernel(const uint16_t* __restrict__ x, int T, int H,
-                                 int8_t* __restrict__ q, uint16_t* __restrict__ d) {
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
-    const int G = H / kGroup;
-    if (gw >= T * G) return;
-    const int t = gw / G, g = gw % G;
-    const size_t i = (size_t)t * H + (size_t)g * kGroup + lane;
-    const float v = bf16_bits_to_float(x[i]);
-    const float amax = warp_max(fabsf(v));
-    const uint16_t db = act_scale_bits(amax);
-    q[i] = (int8_t)act_code(v, half_bits_to_float(db));
-    if (lane == 0) d[(size_t)t * G + g] = db;
-}
 
 // Eight consecutive y values as floats: fp16 (prefill) or fp32 (decode).
 __device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
@@ -88,14 +69,6 @@ __global__ void combine_kernel(const uint16_t* __restrict__ x, const Y* __restri
 }
 
 }  // namespace
-
-cudaError_t launch_act_quant(const uint16_t* x, int T, int H, int8_t* q, uint16_t* d,
-                             cudaStream_t s) {
-    const int warps = T * (H / kGroup);
-    if (warps == 0) return cudaSuccess;
-    act_quant_kernel<<<(warps + 7) / 8, 256, 0, s>>>(x, T, H, q, d);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
                            int T, int H, int k, bool out_fp32, void* out, cudaStream_t s) {

@@ -25,61 +25,6 @@ constexpr int RT = 16;   // tokens per fused CTA
 constexpr int RK = 32;   // k-chunk of the fused CTA
 constexpr int EMAX = kMaxExperts;
 
-// Comparator: larger logit wins; equal logits -> lower expert index wins.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
-}
-
-// Top-k of one token's logits (row of `E` floats readable by the whole warp);
-// lane j < k returns the j-th choice in (sel_i, weight).
-__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int& sel_i,
-                                          float& weight) {
-    const int lane = threadIdx.x % 32;
-    constexpr int PER = EMAX / 32;
-    float v[PER];
-    bool taken[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = (e < E) ? row[e] : 0.f;
-        taken[i] = !(e < E);
-    }
-    float sel_v = 0.f;
-    sel_i = 0;
-    for (int r = 0; r < k; ++r) {
-        float bv = 0.f;
-        int bi = 0x7fffffff;  // "none yet"
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (!taken[i] && (bi == 0x7fffffff || better(v[i], e, bv, bi))) {
-                bv = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if (lane + 32 * i == bi) taken[i] = true;
-        if (lane == r) {
-            sel_v = bv;
-            sel_i = bi;
-        }
-    }
-    const float m = __shfl_sync(0xffffffffu, sel_v, 0);  // the largest
-    const float z = (lane < k) ? expf(sel_v - m) : 0.f;
-    const float s = warp_sum(z);
-    weight = z / s;
-}
-
 __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ wr, int T,
                                                           int H, int E, int k,
