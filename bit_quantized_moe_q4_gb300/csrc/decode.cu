@@ -135,13 +135,15 @@ __device__ __forceinline__ int group_dot(const uint4 w, const uint32_t* a, int a
 // tbase): groups g = p, p + 4, ... (p = lane % 4), kGpl at a time, every load
 // of a pass issued before its first use.  The activations of the `c` bucket
 // rows are staged into shared memory while the first loads are in flight.
-// Accumulates each row's fp32 sum into acc (fixed per-lane order); optionally
-// writes the int32 group dots.
-template <int TM>
+// The weights stay in registers while the tokens go by kTc at a time; each
+// row's fp32 sums (fixed order: per lane over its groups, then over the 4
+// lanes of the row) land in row_sum[0..c-1] (shared memory, written by the
+// p == 0 lane).  Optionally writes the int32 group dots.
+constexpr int kTc = 4;
 __device__ __forceinline__ void row_w4a8(const uint8_t* __restrict__ tbase, int r, int K, int p,
                                          int c, const int* s_rows, const int8_t* q_src,
                                          const uint16_t* d_src, uint32_t* s_q, float* s_d,
-                                         int* s_sum, float (&acc)[TM], int32_t* dots,
+                                         int* s_sum, float* row_sum, int32_t* dots,
                                          size_t dots_tok_stride) {
     const int G = K / kGroup;
     for (int g0 = 0; g0 < G; g0 += 4 * kGpl) {
@@ -160,20 +162,36 @@ __device__ __forceinline__ void row_w4a8(const uint8_t* __restrict__ tbase, int 
             stage_activations(q_src, d_src, s_rows, c, K, s_q, s_d, s_sum);
             __syncthreads();
         }
+        for (int n0 = 0; n0 < c; n0 += kTc) {
+            float acc[kTc];
 #pragma unroll
-        for (int i = 0; i < kGpl; ++i) {
-            const int g = g0 + p + 4 * i;
-            if (g < G) {
-                const float dw = half_bits_to_float((uint16_t)dwb[i]);
+            for (int j = 0; j < kTc; ++j) acc[j] = 0.f;
 #pragma unroll
-                for (int n = 0; n < TM; ++n) {
-                    if (n < c) {
-                        const int dot = group_dot(w[i], s_q + (size_t)n * (K / 4) + g * 8,
-                                                  s_sum[n * G + g]);
-                        acc[n] = fmaf((float)dot, dw * s_d[n * G + g], acc[n]);
-                        if (dots) dots[(size_t)n * dots_tok_stride + g] = dot;
+            for (int i = 0; i < kGpl; ++i) {
+                const int g = g0 + p + 4 * i;
+                if (g < G) {
+                    const float dw = half_bits_to_float((uint16_t)dwb[i]);
+#pragma unroll
+                    for (int j = 0; j < kTc; ++j) {
+                        const int n = n0 + j;
+                        if (n < c) {
+                            const int dot = group_dot(w[i], s_q + (size_t)n * (K / 4) + g * 8,
+                                                      s_sum[n * G + g]);
+                            acc[j] = fmaf((float)dot, dw * s_d[n * G + g], acc[j]);
+                            if (dots) dots[(size_t)n * dots_tok_stride + g] = dot;
+                        }
                     }
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < kTc; ++j) {
+                acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 1);
+                acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 2);
+            }
+            if (p == 0) {
+#pragma unroll
+                for (int j = 0; j < kTc; ++j)
+                    if (n0 + j < c) row_sum[n0 + j] = (g0 == 0 ? 0.f : row_sum[n0 + j]) + acc[j];
             }
         }
     }
@@ -192,30 +210,54 @@ __global__ void __launch_bounds__(kRouteThreads) decode_route_kernel(const Decod
     const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     pdl_trigger();  // the gate/up grid may be scheduled now; it waits for our end
+    const int W = (int)ncta * (kRouteThreads / 32);
+    const int gw = (int)rank * (kRouteThreads / 32) + warp;
+    // The first 2048 columns of this warp's first router row are requested
+    // before x is staged, so both loads overlap.
+    constexpr int kWl = 16;  // float4 per lane per pass (2048 columns)
+    float4 wpre[kWl];
+    if (gw < E) {
+        const float* row = a.wr + (size_t)gw * H;
+#pragma unroll
+        for (int i = 0; i < kWl; ++i) {
+            const int c = lane * 4 + 128 * i;
+            if (c < H) wpre[i] = __ldg(reinterpret_cast<const float4*>(row + c));
+        }
+    }
     uint16_t* sx = reinterpret_cast<uint16_t*>(dsm);
     for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x)
         reinterpret_cast<uint4*>(sx)[i] = reinterpret_cast<const uint4*>(a.x)[i];
     __syncthreads();
 
-    const int W = (int)ncta * (kRouteThreads / 32);
-    const int gw = (int)rank * (kRouteThreads / 32) + warp;
     const uint32_t leader_logits = mapa_shared(smem_u32(&s_logits[0][0]), 0);
     for (int e = gw; e < E; e += W) {
         float acc[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) acc[t] = 0.f;
         const float* row = a.wr + (size_t)e * H;
-#pragma unroll 4
-        for (int c = lane * 4; c < H; c += 128) {
-            const float4 wv = __ldg(reinterpret_cast<const float4*>(row + c));
+        for (int c0 = 0; c0 < H; c0 += 128 * kWl) {
+            if (!(e == gw && c0 == 0)) {
 #pragma unroll
-            for (int t = 0; t < TM; ++t) {
-                if (t < T) {
-                    const uint2 xv = *reinterpret_cast<const uint2*>(sx + t * H + c);
-                    acc[t] = fmaf(__uint_as_float(xv.x << 16), wv.x, acc[t]);
-                    acc[t] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wv.y, acc[t]);
-                    acc[t] = fmaf(__uint_as_float(xv.y << 16), wv.z, acc[t]);
-                    acc[t] = fmaf(__uint_as_float(xv.y & 0xffff0000u), wv.w, acc[t]);
+                for (int i = 0; i < kWl; ++i) {
+                    const int c = c0 + lane * 4 + 128 * i;
+                    if (c < H) wpre[i] = __ldg(reinterpret_cast<const float4*>(row + c));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kWl; ++i) {
+                const int c = c0 + lane * 4 + 128 * i;
+                if (c < H) {
+                    const float4 wv = wpre[i];
+#pragma unroll
+                    for (int t = 0; t < TM; ++t) {
+                        if (t < T) {
+                            const uint2 xv = *reinterpret_cast<const uint2*>(sx + t * H + c);
+                            acc[t] = fmaf(__uint_as_float(xv.x << 16), wv.x, acc[t]);
+                            acc[t] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wv.y, acc[t]);
+                            acc[t] = fmaf(__uint_as_float(xv.y << 16), wv.z, acc[t]);
+                            acc[t] = fmaf(__uint_as_float(xv.y & 0xffff0000u), wv.w, acc[t]);
+                        }
+                    }
                 }
             }
         }
@@ -314,11 +356,10 @@ __global__ void __launch_bounds__(kRouteThreads) decode_route_kernel(const Decod
 }
 
 // -------------------------------------------------------------- gate/up
-template <int TM>
-__global__ void __launch_bounds__(kGuThreads) decode_gateup_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kGuThreads, 2) decode_gateup_kernel(const DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    __shared__ float s_acc[64][TM + 1];
-    __shared__ int s_rows[TM];
+    __shared__ float s_acc[64][MOE_DECODE_MAX_T + 1];
+    __shared__ int s_rows[MOE_DECODE_MAX_T];
     pdl_wait();     // routing, buckets and q_x of this call
     pdl_trigger();  // the down grid may be scheduled now
     if ((int)blockIdx.x >= a.counters[kCntTouched]) return;
@@ -333,28 +374,15 @@ __global__ void __launch_bounds__(kGuThreads) decode_gateup_kernel(const DecodeA
     const int prow = m * I + f;            // row of the [2I, H] gate/up tensor
     const int p = lane % 4;
     uint32_t* s_q = reinterpret_cast<uint32_t*>(dsm);
-    float* s_d = reinterpret_cast<float*>(dsm + (size_t)TM * H);
-    int* s_sum = reinterpret_cast<int*>(s_d + TM * G);
+    float* s_d = reinterpret_cast<float*>(dsm + (size_t)c * H);
+    int* s_sum = reinterpret_cast<int*>(s_d + c * G);
     if (threadIdx.x < c) s_rows[threadIdx.x] = a.bucket_token[off + threadIdx.x];
     __syncthreads();
     const uint8_t* tbase =
         a.wgu + ((size_t)e * (2 * I / kTileRows) + prow / kTileRows) * (H / kTileK) * kTileBytes;
-    float acc[TM];
-#pragma unroll
-    for (int n = 0; n < TM; ++n) acc[n] = 0.f;
     int32_t* dots = a.dots_gu ? a.dots_gu + ((size_t)off * 2 * I + prow) * G : nullptr;
-    row_w4a8<TM>(tbase, prow % kTileRows, H, p, c, s_rows, a.q_x, a.d_x, s_q, s_d, s_sum, acc,
-                 dots, (size_t)2 * I * G);
-#pragma unroll
-    for (int n = 0; n < TM; ++n) {
-        acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], 1);
-        acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], 2);
-    }
-    if (p == 0) {
-#pragma unroll
-        for (int n = 0; n < TM; ++n)
-            if (n < c) s_acc[rloc][n] = acc[n];
-    }
+    row_w4a8(tbase, prow % kTileRows, H, p, c, s_rows, a.q_x, a.d_x, s_q, s_d, s_sum,
+             &s_acc[rloc][0], dots, (size_t)2 * I * G);
     __syncthreads();
     // SwiGLU and the int8 quantisation of h: one 32-feature group per CTA
     for (int n = warp; n < c; n += kGuThreads / 32) {
@@ -369,10 +397,10 @@ __global__ void __launch_bounds__(kGuThreads) decode_gateup_kernel(const DecodeA
 }
 
 // ------------------------------------------------------- down + combine
-template <int TM>
-__global__ void __launch_bounds__(kDnThreads) decode_down_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDnThreads, 2) decode_down_kernel(const DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    __shared__ int s_rows[TM];
+    __shared__ float s_acc[kDecodeDownRows][MOE_DECODE_MAX_T + 1];
+    __shared__ int s_rows[MOE_DECODE_MAX_T];
     __shared__ int s_last;
     pdl_wait();  // h codes of this call (and, transitively, the routing)
     const int ntouched = a.counters[kCntTouched];
@@ -386,28 +414,17 @@ __global__ void __launch_bounds__(kDnThreads) decode_down_kernel(const DecodeArg
     const int row = rb * kDecodeDownRows + rloc;
     const int p = lane % 4;
     uint32_t* s_q = reinterpret_cast<uint32_t*>(dsm);
-    float* s_d = reinterpret_cast<float*>(dsm + (size_t)TM * I);
-    int* s_sum = reinterpret_cast<int*>(s_d + TM * G);
+    float* s_d = reinterpret_cast<float*>(dsm + (size_t)c * I);
+    int* s_sum = reinterpret_cast<int*>(s_d + c * G);
     if (threadIdx.x < c) s_rows[threadIdx.x] = off + threadIdx.x;  // h rows are bucket rows
     __syncthreads();
     const uint8_t* tbase =
         a.wd + ((size_t)e * (H / kTileRows) + row / kTileRows) * (I / kTileK) * kTileBytes;
-    float acc[TM];
-#pragma unroll
-    for (int n = 0; n < TM; ++n) acc[n] = 0.f;
     int32_t* dots = a.dots_d ? a.dots_d + ((size_t)off * H + row) * G : nullptr;
-    row_w4a8<TM>(tbase, row % kTileRows, I, p, c, s_rows, a.q_h, a.d_h, s_q, s_d, s_sum, acc,
-                 dots, (size_t)H * G);
-#pragma unroll
-    for (int n = 0; n < TM; ++n) {
-        acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], 1);
-        acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], 2);
-    }
-    if (p == 0) {
-#pragma unroll
-        for (int n = 0; n < TM; ++n)
-            if (n < c) a.y[((size_t)off + n) * H + row] = acc[n] * a.slot_w[off + n];
-    }
+    row_w4a8(tbase, row % kTileRows, I, p, c, s_rows, a.q_h, a.d_h, s_q, s_d, s_sum,
+             &s_acc[rloc][0], dots, (size_t)H * G);
+    if (p == 0)
+        for (int n = 0; n < c; ++n) a.y[((size_t)off + n) * H + row] = s_acc[rloc][n] * a.slot_w[off + n];
     // The last CTA to finish this 64-row block combines it for every token.
     __threadfence();
     __syncthreads();
@@ -500,8 +517,8 @@ cudaError_t launch_all(const DecodeArgs& a, void** ev, bool capturing, cudaStrea
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     {
-        const size_t smem = act_smem(TM, a.H);
-        err = cudaFuncSetAttribute(decode_gateup_kernel<TM>,
+        const size_t smem = act_smem(a.T, a.H);
+        err = cudaFuncSetAttribute(decode_gateup_kernel,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg{};
@@ -511,13 +528,13 @@ cudaError_t launch_all(const DecodeArgs& a, void** ev, bool capturing, cudaStrea
         cfg.stream = s;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, decode_gateup_kernel<TM>, a);
+        err = cudaLaunchKernelEx(&cfg, decode_gateup_kernel, a);
         if (err != cudaSuccess) return err;
     }
     if ((err = mark(4)) != cudaSuccess) return err;
     {
-        const size_t smem = act_smem(TM, a.I);
-        err = cudaFuncSetAttribute(decode_down_kernel<TM>,
+        const size_t smem = act_smem(a.T, a.I);
+        err = cudaFuncSetAttribute(decode_down_kernel,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         cudaLaunchConfig_t cfg{};
@@ -527,7 +544,7 @@ cudaError_t launch_all(const DecodeArgs& a, void** ev, bool capturing, cudaStrea
         cfg.stream = s;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, decode_down_kernel<TM>, a);
+        err = cudaLaunchKernelEx(&cfg, decode_down_kernel, a);
         if (err != cudaSuccess) return err;
     }
     if ((err = mark(5)) != cudaSuccess || (err = mark(6)) != cudaSuccess) return err;
