@@ -28,7 +28,7 @@ METRIC = "MoE-layer prefill tokens/s and decode µs/token; % of HBM / tensor roo
 DECODE_LAYERS = 16          # distinct weight copies per decode step
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
-KERNELS_PER_DECODE_LAYER = 9   # logits, top-k, 3 bucketing, act-quant, gate/up, down, combine
+KERNELS_PER_DECODE_LAYER = 2   # route (router, top-k, buckets, x codes); experts (gate/up, down, combine)
 KERNELS_PER_PREFILL_LAYER = 7  # fused router, 3 bucketing, gate/up, down, combine
 
 
@@ -152,12 +152,12 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
     ms_step = t0.elapsed_time(t1) / steps
     barrier()
     # per-kernel durations of the last layer of each replay (stage events)
-    gu_ms, dn_ms = [], []
+    rt_ms, ex_ms = [], []
     for _ in range(steps):
         g.replay()
         torch.cuda.synchronize()
-        gu_ms.append(stages.ms(3, 4))
-        dn_ms.append(stages.ms(4, 5))
+        rt_ms.append(stages.ms(0, 1))
+        ex_ms.append(stages.ms(3, 4))
     # end to end: pinned host x in, graph, last layer's output back to the host
     x_host = torch.empty((T, li.H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
@@ -186,13 +186,13 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
         "distinct_experts": distinct,
         "algorithmic_bytes_per_layer": layer_bytes,
         "layer_gbs": layer_bytes / (ms_step / L * 1e-3) / 1e9,
-        "gateup_us": statistics.mean(gu_ms) * 1e3, "down_us": statistics.mean(dn_ms) * 1e3,
+        "route_us": statistics.mean(rt_ms) * 1e3, "experts_us": statistics.mean(ex_ms) * 1e3,
         "gateup_bytes": gu_bytes, "down_bytes": dn_bytes,
         "e2e_us_per_token": e2e_ms * 1e3 / (L * T),
         "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 4,
         "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
     }
-    res["gateup_gbs"] = gu_bytes / (res["gateup_us"] * 1e-6) / 1e9
+    res["experts_gbs"] = (gu_bytes + dn_bytes) / (res["experts_us"] * 1e-6) / 1e9
     del layers, outs, ws, g
     torch.cuda.empty_cache()
     return res
@@ -411,7 +411,7 @@ def main():
     ms_step = max_over_ranks(d1["ms_per_step"])
     value = ms_step * 1e3 / (d1["layers_per_step"] * 1 * world)  # µs per token, all ranks
     e2e_ms = max_over_ranks(d1["e2e_us_per_token"] * d1["layers_per_step"] / 1e3)
-    roof_gbs = d1["gateup_gbs"]
+    roof_gbs = d1["experts_gbs"]
     line = {
         "metric": METRIC, "value": value, "unit": "µs/token", "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": ms_step,
@@ -425,12 +425,12 @@ def main():
             "l2": "inputs larger than L2: each step touches ~360 MB of distinct weights",
             "parallelism": "replicas only" if world > 1 else "single GPU",
         },
-        "roofline": {"bound": "hbm", "kernel": "decode_gateup_kernel", "achieved": roof_gbs,
+        "roofline": {"bound": "hbm", "kernel": "decode_experts_kernel", "achieved": roof_gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": roof_gbs / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": d1["gateup_bytes"],
-                     "launch_us": d1["gateup_us"]},
+                     "algorithmic_bytes_per_launch": d1["gateup_bytes"] + d1["down_bytes"],
+                     "launch_us": d1["experts_us"]},
         "e2e": {"value": e2e_ms * 1e3 / (d1["layers_per_step"] * world), "unit": "µs/token",
                 "h2d_bytes_per_step": d1["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": d1["d2h_bytes_per_step"]},

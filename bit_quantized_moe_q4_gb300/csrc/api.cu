@@ -55,6 +55,11 @@ int device_info(DeviceInfo** out) {
         if (e != cudaSuccess)
             return set_err(MOE_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
         d.status = static_cast<int*>(p);
+        if (d.supported) {
+            e = decode_prepare_device(dev);
+            if (e != cudaSuccess)
+                return set_err(MOE_ERR_CUDA, "decode set-up: %s", cudaGetErrorString(e));
+        }
         d.ready = true;
         if (!d.supported)
             return set_err(MOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
@@ -82,8 +87,8 @@ std::once_flag g_encode_once;
 
 }  // namespace
 
-bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                        uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+namespace {
+EncodeTiledFn encoder() {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -92,16 +97,37 @@ bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint6
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     });
-    if (!g_encode) return false;
+    return g_encode;
+}
+}  // namespace
+
+bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_packed(CUtensorMap* map, const void* packed, uint64_t ntiles, uint32_t box_words,
+                        uint32_t box_tiles) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(kTileBytes / 4), ntiles};
+    const cuuint64_t strides[1] = {(cuuint64_t)kTileBytes};
+    const cuuint32_t box[2] = {box_words, box_tiles};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(packed), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -144,12 +170,15 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
     } else {
-        w.y = take(Tk * H * 4);
+        int nsg = 1, nsd = 1;
+        decode_splits(T, H, I, E, k, &nsg, &nsd);
+        w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));
+        w.gu_sum = reinterpret_cast<float*>(take(Tk * 2 * I * 4));
         w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
-        w.tickets = reinterpret_cast<int32_t*>(take((size_t)(H / kDecodeDownRows) * 4));
+        w.done = reinterpret_cast<int32_t*>(take((size_t)E * 4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;
@@ -170,6 +199,10 @@ int check_layer_shape(int mode, int T, int H, int I, int E, int k) {
     if (big >= (1ll << 31)) return set_err(MOE_ERR_SHAPE, "T*k*max(H,I) = %lld too large", big);
     if (mode == MOE_MODE_DECODE && T > MOE_DECODE_MAX_T)
         return set_err(MOE_ERR_SHAPE, "decode takes at most %d tokens (T=%d)", MOE_DECODE_MAX_T, T);
+    if (mode == MOE_MODE_DECODE && !decode_shape_fits(T, H, I))
+        return set_err(MOE_ERR_SHAPE,
+                       "decode with T=%d H=%d I=%d does not fit the on-chip staging "
+                       "(T*(H+I) too large)", T, H, I);
     return MOE_OK;
 }
 
@@ -218,11 +251,13 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     };
     if ((rc = mark(0))) return rc;
     if (mode == MOE_MODE_DECODE) {
-        // route + buckets + x codes, gate/up, down + combine: three kernels
+        // route (+ buckets, x codes), then experts (gate/up, down, combine)
         if ((rc = cuda_check(launch_decode(x, wr, wgu, wd, T, H, I, E, k,
                                            (flags & MOE_OUT_FP32) != 0, out, ws,
                                            dbg ? dbg->dots_gu : nullptr,
-                                           dbg ? dbg->dots_d : nullptr, ev, capturing, s),
+                                           dbg ? dbg->dots_d : nullptr,
+                                           dbg != nullptr && dbg->q_h != nullptr, dev->status,
+                                           dev->num_sms, ev, capturing, s),
                              "decode")))
             return rc;
     } else {

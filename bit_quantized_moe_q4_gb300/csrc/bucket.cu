@@ -47,29 +47,6 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const int32_t* __rest
     for (int e = lane; e < E; e += 32) chunk_count[(size_t)chunk * E + e] = __popc(bits[warp][e]);
 }
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
-__device__ int block_exclusive_scan(int v, int* total) {
-    __shared__ int warp_tot[8];
-    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int base = 0, all = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        if (w < warp) base += warp_tot[w];
-        all += warp_tot[w];
-    }
-    __syncthreads();
-    *total = all;
-    return base + incl - v;
-}
-
 __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ chunk_count,
                                                           int nchunk, int E, int tile_n,
                                                           int32_t* __restrict__ offsets,
@@ -88,19 +65,19 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ 
         }
     }
     int total;
-    const int off = block_exclusive_scan(count, &total);
+    const int off = block256_exclusive_scan(count, &total);
     if (e < E) offsets[e] = off;
     if (e == 0) offsets[E] = total;
     const int ntiles = (count + tile_n - 1) / tile_n;
     int all_tiles;
-    const int toff = block_exclusive_scan(ntiles, &all_tiles);
+    const int toff = block256_exclusive_scan(ntiles, &all_tiles);
     for (int i = 0; i < ntiles; ++i) {
         tile_e[toff + i] = e;
         tile_n0[toff + i] = off + i * tile_n;
         tile_nn[toff + i] = min(tile_n, count - i * tile_n);
     }
     int ntouched;
-    const int pos = block_exclusive_scan(count > 0 ? 1 : 0, &ntouched);
+    const int pos = block256_exclusive_scan(count > 0 ? 1 : 0, &ntouched);
     if (count > 0) touched[pos] = e;
     if (e == 0) {
         counters[kCntTouched] = ntouched;

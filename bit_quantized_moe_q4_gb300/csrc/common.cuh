@@ -59,6 +59,11 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's earlier generic-proxy accesses to global memory before
+// its later bulk copies (async proxy) that read global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---- mbarrier --------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -250,56 +255,89 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Block-wide exclusive scan of one int per thread (blockDim.x == 256); the
+// block total lands in *total.  Every thread of the block must call it.
+__device__ __forceinline__ int block256_exclusive_scan(int v, int* total) {
+    __shared__ int warp_tot[8];
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) base += warp_tot[w];
+        all += warp_tot[w];
+    }
+    __syncthreads();
+    *total = all;
+    return base + incl - v;
+}
+
 // ---- router top-k ----------------------------------------------------------
-// Comparator: larger logit wins; equal logits -> lower expert index wins.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
+// Order-preserving 32-bit key of a float: larger float -> larger unsigned key.
+// -0.0 is first turned into +0.0 so the two compare equal, as floats do.
+__device__ __forceinline__ uint32_t float_order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Top-k of one token's logits (row of `E` floats readable by the whole warp);
-// lane j < k returns the j-th choice in (sel_i, weight).
+// lane j < k returns the j-th choice in (sel_i, weight).  Order: larger logit
+// first; equal logits -> lower expert index first.
+//
+// Lane l owns the contiguous experts [l*P, l*P + P), P = ceil(E/32) <= 8, and
+// keeps its best remaining one ("head": largest key, lowest index on a tie).
+// Each of the k rounds takes the warp maximum of the heads (redux.sync), and
+// among the lanes holding it the lowest one, which owns the lowest index
+// because lanes own ascending index ranges.  That lane drops its head and
+// finds the next.  The weights are a softmax over the k chosen logits.
 __device__ __forceinline__ void warp_topk(const float* row, int E, int k, int& sel_i,
                                           float& weight) {
     const int lane = threadIdx.x % 32;
-    constexpr int PER = kMaxExperts / 32;
-    float v[PER];
-    bool taken[PER];
+    constexpr int PMAX = kMaxExperts / 32;
+    const int P = (E + 31) / 32;
+    uint32_t key[PMAX];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = (e < E) ? row[e] : 0.f;
-        taken[i] = !(e < E);
+    for (int i = 0; i < PMAX; ++i) {
+        const int e = lane * P + i;
+        key[i] = (i < P && e < E) ? float_order_key(row[e]) : 0u;
     }
-    float sel_v = 0.f;
+    // key 0 marks "taken or absent"; a real logit has key >= 1 unless it is a
+    // NaN with every bit set, which is treated as absent.
+    auto head_of = [&](int& hi) {
+        uint32_t hk = 0u;
+        hi = -1;
+#pragma unroll
+        for (int i = 0; i < PMAX; ++i)
+            if (key[i] > hk) {
+                hk = key[i];
+                hi = i;
+            }
+        return hk;
+    };
+    int hi;
+    uint32_t hk = head_of(hi);
     sel_i = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = 0.f;
-        int bi = 0x7fffffff;  // "none yet"
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t ball = __ballot_sync(0xffffffffu, hk == kmax && hi >= 0);
+        const int wl = __ffs(ball) - 1;
+        const int e = __shfl_sync(0xffffffffu, lane * P + hi, wl);
+        if (lane == r) sel_i = e;
+        if (lane == wl) {
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (!taken[i] && (bi == 0x7fffffff || better(v[i], e, bv, bi))) {
-                bv = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if (lane + 32 * i == bi) taken[i] = true;
-        if (lane == r) {
-            sel_v = bv;
-            sel_i = bi;
+            for (int i = 0; i < PMAX; ++i)
+                if (i == hi) key[i] = 0u;
+            hk = head_of(hi);
         }
     }
+    const float sel_v = (lane < k) ? row[sel_i] : 0.f;
     const float m = __shfl_sync(0xffffffffu, sel_v, 0);  // the largest
     const float z = (lane < k) ? expf(sel_v - m) : 0.f;
     const float s = warp_sum(z);

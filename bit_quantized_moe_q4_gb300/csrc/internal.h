@@ -33,7 +33,9 @@ struct Workspace {
     uint16_t* h;            // [T*k, I] fp16 (prefill)
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
-    int32_t* tickets;       // [H / kDecodeDownRows] (decode) combine tickets
+    int32_t* done;          // [E]           (decode) finished gate/up tasks per touched expert
+    float* gu_sum;          // [T*k, 2I]     (decode) fp32 gate/up row sums, bucket order
+    float* y_part;          // [nsd, T*k, H]  (decode) fp32 partial weighted expert outputs
     int8_t* q_x;            // [T, H]        (decode)
     uint16_t* d_x;          // [T, H/32]     (decode)
     int8_t* q_h;            // [T*k, I]      (decode)
@@ -45,8 +47,6 @@ struct Workspace {
 // counters[] slots
 enum { kCntTouched = 0, kCntTiles = 1 };
 
-// Rows of W_d per decode down-projection CTA (one combine ticket each).
-constexpr int kDecodeDownRows = 64;
 
 // Records a stage event on s (as an external graph node while s is capturing).
 cudaError_t record_stage(void* event, cudaStream_t s, bool capturing);
@@ -69,13 +69,23 @@ cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, con
 cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const Workspace& ws,
                                 int T, int H, int I, int E, int k, int* status, int num_sms,
                                 cudaStream_t s);
-// The whole W4A8 decode layer (route + buckets + x codes, gate/up, down +
-// combine).  `events` is null or the caller's MOE_NUM_STAGE_EVENTS events;
-// boundaries 1..6 are recorded between the kernels.
+// The whole W4A8 decode layer: a route kernel (router, top-k, buckets, x
+// codes), one cooperative expert kernel (gate/up, down) and a combine kernel.
+// `events` is null or the caller's MOE_NUM_STAGE_EVENTS events; boundaries
+// 1..3 are recorded after the route kernel, 4..5 after the expert kernel and
+// 6 after the combine.
 cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
                           int T, int H, int I, int E, int k, bool out_fp32, void* out,
-                          const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
-                          void** events, bool capturing, cudaStream_t s);
+                          const Workspace& ws, int32_t* dots_gu, int32_t* dots_d, bool write_qh,
+                          int* status, int num_sms, void** events, bool capturing,
+                          cudaStream_t s);
+// Once per device, outside any stream capture: decides how the cooperative
+// expert kernel is launched.
+cudaError_t decode_prepare_device(int dev);
+// Whether the decode expert kernel's on-chip staging fits this shape.
+bool decode_shape_fits(int T, int H, int I);
+// K splits (partial-sum count) of the decode gate/up and down tasks.
+void decode_splits(int T, int H, int I, int E, int k, int* nsg, int* nsd);
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
                            int T, int H, int k, bool out_fp32, void* out, cudaStream_t s);
 
@@ -83,5 +93,9 @@ cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const 
 // 2-D map over a row-major [rows, cols] tensor of 16-bit elements (fp16).
 bool encode_tmap_2d_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// 2-D map over packed Q4 weights seen as [ntiles, 1152] 32-bit words (one row
+// per 4608-byte tile); box of box_words x box_tiles.
+bool encode_tmap_packed(CUtensorMap* map, const void* packed, uint64_t ntiles, uint32_t box_words,
+                        uint32_t box_tiles);
 
 }  // namespace moeq4

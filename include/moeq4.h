@@ -191,8 +191,20 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
 
 /*
  * moe_w4a8_forward_decode — one MoE layer on the W4A8 integer path: same
- * arguments and layouts as the prefill call, T <= MOE_DECODE_MAX_T.
- * The int32 group dots are exact; the float sums run in fp32.
+ * arguments and layouts as the prefill call, T <= MOE_DECODE_MAX_T, and the
+ * on-chip staging must fit: T * (H + I) * 1.25 bytes plus two weight tiles
+ * stay under ~170 KB (MOE_ERR_SHAPE otherwise; T = 32 at H = 2048, I = 768
+ * fits).  The int32 group dots are exact; the float sums run in fp32.
+ *
+ * The call launches three kernels that let their successors start early
+ * (programmatic dependent launch).  Its first kernel reads `wr` before the
+ * work that precedes it on the stream has finished, so `wr` must not be
+ * written by the kernel launched immediately before this call on the same
+ * stream; x, the output and the workspace are touched only after that work
+ * has finished.  The expert kernel is a cooperative launch (one CTA per SM).
+ * When few experts are touched (small T) the K range of the gate/up rows is
+ * split and the parts are added in fp32 in the order they arrive, so the
+ * last bits of h, and rarely an int8 code of h, may differ between runs.
  */
 int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
                             const void* wgu_packed, const void* wd_packed,

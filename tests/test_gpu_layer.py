@@ -145,6 +145,18 @@ def test_decode_full_size(T):
     _decode_check(workloads.decode(T))
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 256, 128, 8, 2),      # one token, few experts (all-thread top-k path)
+    (2, 256, 128, 8, 2),      # two tokens (one-warp bucketing)
+    (2, 2048, 768, 128, 8),   # two tokens at full size
+    (3, 256, 128, 6, 6),      # k = E
+    (1, 384, 256, 1, 1),      # one expert: a dense SwiGLU FFN, 3 row blocks
+    (5, 128, 128, 3, 2),      # smallest hidden size
+])
+def test_decode_edge_shapes(T, H, I, E, k):
+    _decode_check(workloads.make_layer("dedge", T, H, I, E, k, seed=7 * T + H + E, wr_std=0.1))
+
+
 def test_decode_tiny_32_tokens():
     li = workloads.tiny()
     li.T = 32
