@@ -168,6 +168,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
     if (mode == MOE_MODE_PREFILL) {
         w.y = take(Tk * H * 2);
         w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
+        w.route_parts = reinterpret_cast<float*>(take(route_parts_floats(T, H, E) * 4));
         w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
     } else {
         int nsg = 1, nsd = 1;
@@ -263,8 +264,8 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     } else {
         // 1. route (also writes the fp16 copy of x)
         float* logits = dbg ? dbg->logits : nullptr;
-        if ((rc = cuda_check(launch_route(x, wr, T, H, E, k, logits, ws.topk_idx, ws.topk_w,
-                                          ws.x16, s),
+        if ((rc = cuda_check(launch_route_gemm(x, wr, T, H, E, k, ws.route_parts, logits,
+                                               ws.topk_idx, ws.topk_w, ws.x16, s),
                              "route")))
             return rc;
         if ((rc = mark(1))) return rc;

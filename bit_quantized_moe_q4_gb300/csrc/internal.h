@@ -30,6 +30,7 @@ struct Workspace {
     int32_t* tile_n0;       // [max_tiles]   first bucket row of the tile
     int32_t* tile_nn;       // [max_tiles]   rows in the tile
     uint16_t* x16;          // [T, H] fp16 copy of x (prefill GEMM operand)
+    float* route_parts;     // [ksplit, T, E] router K-slice sums (prefill)
     uint16_t* h;            // [T*k, I] fp16 (prefill)
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
@@ -61,6 +62,13 @@ cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E,
                         void* dst, cudaStream_t s);
 cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                          float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s);
+// Router as a K-sliced fp32 GEMM into `parts` (route_parts_floats floats; H %
+// 16 == 0), then top-k; optionally writes the logits and the fp16 copy of x.
+int route_ksplit(int T, int H, int E);
+size_t route_parts_floats(int T, int H, int E);
+cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
+                              float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
+                              cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
 cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, const Workspace& ws,

@@ -8,13 +8,17 @@
 // integer comparison of the indices; the weights are a softmax over the k
 // chosen logits (equal to a full softmax renormalised over the k).
 //
-// Two shapes:
+// Three shapes:
+//   gemm   (many tokens, a buffer for K parts available) a register-blocked
+//          fp32 GEMM: each CTA forms 64 tokens x 128 experts over one slice
+//          of the hidden dimension (the slices keep every SM busy); a second
+//          kernel adds the slices in order and picks the top-k, one warp per
+//          token.  The GEMM CTAs also write the fp16 copy of x that the
+//          prefill tensor-core GEMM reads, each for its own tokens and slice.
 //   fused  16 tokens x all experts per CTA; logits stay in shared memory and
-//          the CTA's warps pick the top-k.  Used for many tokens, and whenever
-//          no logits buffer is available.  Optionally writes an fp16 copy of x
-//          (the prefill GEMM operand) while it reads x anyway.
-//   small  one warp per expert over all tokens (decode, T <= 32), spreading
-//          the router matrix over many SMs; a second kernel picks the top-k.
+//          the CTA's warps pick the top-k (no buffer needed).
+//   small  one warp per expert over all tokens (T <= 32), spreading the
+//          router matrix over many SMs; a second kernel picks the top-k.
 #include "common.cuh"
 #include "internal.h"
 
@@ -150,12 +154,191 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
 }
 
+// ---- register-blocked fp32 router GEMM ------------------------------------
+constexpr int GT = 64;    // tokens per CTA
+constexpr int GE = 128;   // experts per CTA
+constexpr int GK = 16;    // hidden columns per shared-memory stage
+constexpr int G_THREADS = 256;
+
+// parts[s][t][e] = sum over h in slice s of x[t, h] * W[e, h] (fp32).
+// Warp w owns tokens 8w..8w+7, lane l experts 4l..4l+3: per column 32 FMAs
+// for two broadcast 16-byte loads of x and one 16-byte load of W.
+__global__ void __launch_bounds__(G_THREADS) router_gemm_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, int T, int H, int E, int ksplit,
+    float* __restrict__ parts, uint16_t* __restrict__ x16) {
+    __shared__ __align__(16) float xs[2][GK][GT];
+    __shared__ __align__(16) float ws[2][GK][GE];
+    const int t0 = blockIdx.x * GT, e0 = blockIdx.y * GE, split = blockIdx.z;
+    const int kspan = H / ksplit, kbeg = split * kspan;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    // loader roles: W: rows e = e0 + (tid % 64) + 64 r (r = 0, 1), column quad
+    // q = tid / 64 (4 columns); x: token tid / 2, half tid % 2 (8 columns)
+    const int we = tid % 64, wq = tid / 64;
+    const int xt = tid / 2, xh = tid % 2;
+    const bool x_loader = tid < 2 * GT;
+    const bool write_x16 = x16 != nullptr && blockIdx.y == 0;
+    float4 wreg[2];
+    uint4 xreg;
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int e = e0 + we + 64 * r;
+            wreg[r] = (e < E) ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)e * H + k0 + wq * 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (x_loader) {
+            const int t = t0 + xt;
+            xreg = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + k0 + xh * 8))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    auto store = [&](int buf, int k0) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            ws[buf][wq * 4 + 0][we + 64 * r] = wreg[r].x;
+            ws[buf][wq * 4 + 1][we + 64 * r] = wreg[r].y;
+            ws[buf][wq * 4 + 2][we + 64 * r] = wreg[r].z;
+            ws[buf][wq * 4 + 3][we + 64 * r] = wreg[r].w;
+        }
+        if (x_loader) {
+            const uint32_t w4[4] = {xreg.x, xreg.y, xreg.z, xreg.w};
+            uint32_t h4[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float lo = __uint_as_float(w4[c] << 16), hi = __uint_as_float(w4[c] & 0xffff0000u);
+                xs[buf][xh * 8 + 2 * c][xt] = lo;
+                xs[buf][xh * 8 + 2 * c + 1][xt] = hi;
+                h4[c] = (uint32_t)float_to_half_bits_sat(lo) | ((uint32_t)float_to_half_bits_sat(hi) << 16);
+            }
+            const int t = t0 + xt;
+            if (write_x16 && t < T)
+                *reinterpret_cast<uint4*>(x16 + (size_t)t * H + k0 + xh * 8) =
+                    make_uint4(h4[0], h4[1], h4[2], h4[3]);
+        }
+    };
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int nstage = kspan / GK;
+    load(kbeg);
+    store(0, kbeg);
+    __syncthreads();
+    for (int st = 0; st < nstage; ++st) {
+        const int buf = st & 1;
+        if (st + 1 < nstage) load(kbeg + (st + 1) * GK);  // next stage in flight
+#pragma unroll
+        for (int kk = 0; kk < GK; ++kk) {
+            const float4 xa = *reinterpret_cast<const float4*>(&xs[buf][kk][warp * 8]);
+            const float4 xb = *reinterpret_cast<const float4*>(&xs[buf][kk][warp * 8 + 4]);
+            const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][kk][lane * 4]);
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+            const float wvv[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wvv[j], acc[i][j]);
+        }
+        if (st + 1 < nstage) {
+            store(buf ^ 1, kbeg + (st + 1) * GK);
+            __syncthreads();
+        }
+    }
+    float* out = parts + (size_t)split * T * E;
+    const int e = e0 + lane * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + warp * 8 + i;
+        if (t >= T) break;
+        if (e + 3 < E && (E % 4) == 0) {  // 16-byte aligned only when E % 4 == 0
+            *reinterpret_cast<float4*>(out + (size_t)t * E + e) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e + j < E) out[(size_t)t * E + e + j] = acc[i][j];
+        }
+    }
+}
+
+// One warp per token: logits = the K-slice parts added in slice order, then
+// the top-k.  `logits` (optional, may equal parts when there is one slice)
+// receives the sums.
+__global__ void __launch_bounds__(256) topk_from_parts_kernel(const float* __restrict__ parts,
+                                                              int ksplit, int T, int E, int k,
+                                                              float* logits, int32_t* idx, float* w) {
+    __shared__ float row[8][EMAX];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;  // whole warp
+    constexpr int PER = EMAX / 32;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) v[i] = 0.f;
+    for (int s0 = 0; s0 < ksplit; s0 += 4) {
+        float pv[4][PER];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = lane + 32 * i;
+                pv[u][i] = (s0 + u < ksplit && e < E)
+                               ? __ldcg(parts + ((size_t)(s0 + u) * T + t) * E + e) : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) v[i] += pv[u][i];  // slices in order (adding 0 is exact)
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            row[warp][e] = v[i];
+            if (logits) logits[(size_t)t * E + e] = v[i];
+        }
+    }
+    __syncwarp();
+    int si;
+    float sw;
+    warp_topk(row[warp], E, k, si, sw);
+    if (lane < k) {
+        idx[(size_t)t * k + lane] = si;
+        w[(size_t)t * k + lane] = sw;
+    }
+}
+
 }  // namespace
+
+int route_ksplit(int T, int H, int E) {
+    const int ctas = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
+    int s = 1;
+    while (s < 8 && ctas * s * 2 <= 2 * 152 && H % (GK * s * 2) == 0) s *= 2;
+    return s;
+}
+
+size_t route_parts_floats(int T, int H, int E) { return (size_t)route_ksplit(T, H, E) * T * E; }
+
+cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
+                              float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
+                              cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    // with the logits buffer as the only part, the sums are already in place
+    const int ks = (parts == logits) ? 1 : route_ksplit(T, H, E);
+    const dim3 grid((T + GT - 1) / GT, (E + GE - 1) / GE, ks);
+    router_gemm_kernel<<<grid, G_THREADS, 0, s>>>(x, wr, T, H, E, ks, parts, x16);
+    topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k,
+                                                       parts == logits ? nullptr : logits, idx, w);
+    return cudaGetLastError();
+}
 
 // `logits` may be null; the split path is taken only when it is not.
 cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                          float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (logits && !x16 && T > 32 && (H % GK) == 0)
+        return launch_route_gemm(x, wr, T, H, E, k, logits, logits, idx, w, nullptr, s);
     if (logits && !x16 && T <= 32 && (H % 128) == 0) {
         const dim3 grid((E + 3) / 4);
         if (T <= 4)
