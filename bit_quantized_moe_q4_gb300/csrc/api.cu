@@ -133,7 +133,7 @@ bool encode_tmap_packed(CUtensorMap* map, const void* packed, uint64_t ntiles, u
 
 namespace {
 
-constexpr int kPrefillTileN = 256;
+constexpr int kPrefillTileN = 144;  // tokens per prefill GEMM tile (the GEMM's BN)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -274,17 +274,13 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
                              "bucket")))
             return rc;
         if ((rc = mark(2))) return rc;
-        CUtensorMap xmap, hmap;
-        if (!encode_tmap_2d_f16(&xmap, ws.x16, T, H, 64, 1, true) ||
-            !encode_tmap_2d_f16(&hmap, ws.h, Tk, I, 64, 16, true))
-            return set_err(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         if ((rc = mark(3))) return rc;
         // 3. grouped GEMMs
-        if ((rc = cuda_check(launch_prefill_gateup(&xmap, wgu, ws, T, H, I, E, k, dev->status,
+        if ((rc = cuda_check(launch_prefill_gateup(wgu, ws, T, H, I, E, k, dev->status,
                                                    dev->num_sms, s), "prefill gate/up")))
             return rc;
         if ((rc = mark(4))) return rc;
-        if ((rc = cuda_check(launch_prefill_down(&hmap, wd, ws, T, H, I, E, k, dev->status,
+        if ((rc = cuda_check(launch_prefill_down(wd, ws, T, H, I, E, k, dev->status,
                                                  dev->num_sms, s), "prefill down")))
             return rc;
         if ((rc = mark(5))) return rc;

@@ -71,10 +71,15 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ 
     const int ntiles = (count + tile_n - 1) / tile_n;
     int all_tiles;
     const int toff = block256_exclusive_scan(ntiles, &all_tiles);
-    for (int i = 0; i < ntiles; ++i) {
+    // a bucket is cut into ntiles tiles of near-equal size (the first
+    // count % ntiles tiles one row longer), each at most tile_n rows
+    const int tbase = ntiles ? count / ntiles : 0, textra = ntiles ? count % ntiles : 0;
+    for (int i = 0, r0 = 0; i < ntiles; ++i) {
+        const int nn = tbase + (i < textra ? 1 : 0);
         tile_e[toff + i] = e;
-        tile_n0[toff + i] = off + i * tile_n;
-        tile_nn[toff + i] = min(tile_n, count - i * tile_n);
+        tile_n0[toff + i] = off + r0;
+        tile_nn[toff + i] = nn;
+        r0 += nn;
     }
     int ntouched;
     const int pos = block256_exclusive_scan(count > 0 ? 1 : 0, &ntouched);

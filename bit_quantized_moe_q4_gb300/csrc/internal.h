@@ -71,10 +71,10 @@ cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, 
                               cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
-cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, const Workspace& ws,
+cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,
                                   int T, int H, int I, int E, int k, int* status, int num_sms,
                                   cudaStream_t s);
-cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const Workspace& ws,
+cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
                                 int T, int H, int I, int E, int k, int* status, int num_sms,
                                 cudaStream_t s);
 // The whole W4A8 decode layer: a route kernel (router, top-k, buckets, x

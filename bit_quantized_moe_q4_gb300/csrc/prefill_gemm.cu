@@ -12,53 +12,75 @@
 // at the same tensor-core rate.
 //
 // Weights sit on the MMA's M side (128 rows per tile) and tokens on N (up to
-// 256 per tile, padded to a multiple of 16), so a bucket of ~128 tokens wastes
-// little.  Per 64-column K-block:
-//   producer warp   bulk-copies the packed 4-bit tile(s) (4608 bytes each)
-//                   and brings the bucket's token rows in: gate/up gathers
-//                   rows of x by token id (TMA gather4), down loads
-//                   consecutive rows of h (2-D TMA tiles);
-//   dequant warps   turn codes and fp16 scales into fp16 w = d (q - 8) in the
-//                   128-byte-swizzled K-major layout the MMA reads;
-//   MMA warp        one thread issues 4 x K=16 MMAs per matrix into TMEM;
-//   epilogue warps  read TMEM: gate/up -> h = silu(g) * u, down ->
-//                   y = w_route * acc, both fp16 (saturating at +-65504), in
-//                   bucket order.
+// 144 per tile, padded to a multiple of 16; larger buckets are cut into
+// tiles of near-equal size), so an expert's bucket of ~128 tokens is one
+// tile and every weight is dequantised once.  Per 64-column
+// K-block, three decoupled rings:
+//   raw    the packed 4-bit tiles (4608 bytes each), two K-blocks of each
+//          weight block per bulk copy (contiguous in the packed layout), by
+//          the weight producer warp six K-blocks ahead (these come from HBM);
+//   A      the dequantised fp16 weights in the 128-byte-swizzled K-major
+//          layout the MMA reads, written by eight dequant warps;
+//   B      the bucket's token rows, brought in by four token-loader warps
+//          with 16-byte cp.async copies straight into the 128-byte-swizzled
+//          layout (gate/up: rows of x picked by token id; down: consecutive
+//          rows of h); they mostly hit L2, whose latency still needs a ring
+//          six or seven K-blocks deep.  (Many small TMA copies - gather4 or
+//          16-row boxes - proved slower here: the copy engine spent ~40 ns on
+//          each.)
+// The weight copies carry an L2 evict-first hint: they are read once, and
+// should not push the reused token rows out of L2.
+// One thread of the MMA warp issues 4 x K=16 MMAs per matrix into TMEM; four
+// epilogue warps read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
+// weight * acc, both fp16 (saturating at +-65504), in bucket order.
 // One persistent CTA per SM walks a static list of (token tile, row block)
 // work items.  Every wait is bounded; on expiry the CTA records
-// MOE_ERR_TIMEOUT in the status word, drains its copies, frees TMEM and exits.
+// MOE_ERR_TIMEOUT in the status word, stops, drains its copies, frees TMEM
+// and exits.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moeq4 {
 namespace {
 
-constexpr int BN = 256;           // max tokens per tile
+constexpr int BN = 144;                 // max tokens per tile (buckets are cut evenly)
 constexpr int A_MAT_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
-constexpr int NUM_THREADS = 448;  // 14 warps
-constexpr int WARP_PRODUCER = 0, WARP_MMA = 1, WARP_EPI0 = 2, WARP_DEQ0 = 6;
-constexpr int NUM_EPI_WARPS = 4, NUM_DEQ_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 4, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
+constexpr int WARP_WPROD = 0, WARP_MMA = 1, WARP_B0 = 2;
+constexpr int WARP_EPI0 = WARP_B0 + NUM_B_WARPS;
+constexpr int WARP_DEQ0 = WARP_EPI0 + NUM_EPI_WARPS;
+constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 18 warps
+constexpr int B_ROWS_PER_THREAD = BN * 8 / (NUM_B_WARPS * 32);  // 16-byte chunks: 9
+static_assert(BN * 8 % (NUM_B_WARPS * 32) == 0, "B chunks per loader thread");
 
+// Both GEMMs multiply two 128-row weight blocks by the same token tile:
+// gate/up the gate rows and the matching up rows, down two adjacent row
+// blocks of W_d (so each token row is read from L2 once per 256 output rows).
 template <bool GATEUP>
 struct Cfg {
-    static constexpr int NMAT = GATEUP ? 2 : 1;
-    static constexpr int STAGES = GATEUP ? 3 : 4;
-    static constexpr int RAW_BYTES = NMAT * kTileBytes;
+    static constexpr int NMAT = 2;
+    static constexpr int RK = 2;  // K-blocks per weight copy (contiguous tiles)
+    static constexpr int RAW_STAGES = 3;
+    static constexpr int A_STAGES = 2;
+    static constexpr int B_STAGES = 5;
+    static constexpr int RAW_BYTES = NMAT * RK * kTileBytes;
     static constexpr int A_BYTES = NMAT * A_MAT_BYTES;
     static constexpr int TMEM_COLS = NMAT * 256;
     // shared memory carve-up (offsets from a 1024-aligned base)
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BAR = OFF_RAW + STAGES * RAW_BYTES;
-    static constexpr int NUM_BARS = 4 * STAGES + 3;
+    static constexpr int OFF_B = OFF_A + A_STAGES * A_BYTES;
+    static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_RAW + RAW_STAGES * RAW_BYTES;
+    static constexpr int NUM_BARS = 2 * (RAW_STAGES + A_STAGES + B_STAGES) + 3;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 struct GemmArgs {
     const uint8_t* wpk;        // packed weights
+    const uint16_t* bsrc;      // fp16 token rows: x16 [T, H] (gate/up) or h [T*k, I] (down)
     const int32_t* counters;   // kCntTiles
     const int32_t* tile_e;
     const int32_t* tile_n0;
@@ -68,34 +90,57 @@ struct GemmArgs {
     uint16_t* out;             // h [T*k, I] (gate/up) or y [T*k, H] (down)
     int K;                     // reduction length: H (gate/up) or I (down)
     int rows_per_e;            // packed rows per expert: 2I (gate/up) or H (down)
-    int out_rows;              // output features per expert: I or H
+    int rb_items;              // work items per token tile: I/128 or H/256
+    int rb_mul;                // first row block of item i: i * rb_mul (1 or 2)
+    int rb_second;             // second row block = first + rb_second (I/128 or 1)
     int out_ld;                // leading dimension of out
     int* status;
 };
 
-__device__ __forceinline__ uint32_t f16x2_dequant(uint32_t nib2, uint32_t d2) {
-    // nib2 holds two codes at bits 0..3 and 16..19; 0x6400 is fp16 1024.0 and
-    // its ulp is 1, so (0x6400 | q) is exactly 1024 + q.
-    const uint32_t v = nib2 | 0x64006400u;
-    __half2 b = *reinterpret_cast<const __half2*>(&v);
-    const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);  // 1024 + 8
+// Eight 4-bit codes of one packed word (columns 8c..8c+7: even columns in the
+// low 16 bits, odd in the high, nibble m = column pair m) to fp16 d(q - 8).
+// 0x6400 is fp16 1024 with ulp 1, so (0x6400 | q) is 1024 + q and
+// (0x6400 | q << 4) is 1024 + 16 q: q - 8 comes out exactly as
+// (1024 + q) - 1032 or (1024 + 16 q) / 16 - 72, and one rounding of (q - 8) d
+// follows.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t d2) {
+    const uint32_t w8 = w >> 8;
+    uint32_t t[4];
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(t[0]) : "r"(w));
+    asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(t[1]) : "r"(w));
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(t[2]) : "r"(w8));
+    asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(t[3]) : "r"(w8));
+    const __half2 k1032 = __floats2half2_rn(1032.0f, 1032.0f);
+    const __half2 k16th = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 km72 = __floats2half2_rn(-72.0f, -72.0f);
     const __half2 d = *reinterpret_cast<const __half2*>(&d2);
-    b = __hmul2(__hsub2(b, off), d);  // (q - 8) exact, then one rounding of d(q-8)
-    return *reinterpret_cast<uint32_t*>(&b);
+    __half2 v[4];
+    v[0] = __hsub2(*reinterpret_cast<const __half2*>(&t[0]), k1032);
+    v[1] = __hfma2(*reinterpret_cast<const __half2*>(&t[1]), k16th, km72);
+    v[2] = __hsub2(*reinterpret_cast<const __half2*>(&t[2]), k1032);
+    v[3] = __hfma2(*reinterpret_cast<const __half2*>(&t[3]), k16th, km72);
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 r = __hmul2(v[i], d);
+        op[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+    return o;
 }
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_q4_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const GemmArgs args) {
+    grouped_q4_gemm_kernel(const GemmArgs args) {
     using C = Cfg<GATEUP>;
-    constexpr int S = C::STAGES;
+    constexpr int SR = C::RAW_STAGES, SA = C::A_STAGES, SB = C::B_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* sbase = smem_raw + (base - raw_base);
 
     const int n_items_tiles = args.counters[kCntTiles];
-    const int rb_count = args.out_rows / kTileRows;
+    const int rb_count = args.rb_items;
     const int n_items = n_items_tiles * rb_count;
     if ((int)blockIdx.x >= n_items) return;
 
@@ -105,22 +150,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int rbs_per_e = args.rows_per_e / kTileRows;
 
     const uint32_t bar0 = base + C::OFF_BAR;
-    auto full_raw = [&](int s) { return bar0 + 8u * s; };
-    auto full_b = [&](int s) { return bar0 + 8u * (S + s); };
-    auto full_a = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (3 * S + s); };
-    const uint32_t acc_full = bar0 + 8u * (4 * S);
-    const uint32_t acc_empty = bar0 + 8u * (4 * S + 1);
-    const uint32_t mma_done = bar0 + 8u * (4 * S + 2);
+    auto raw_full = [&](int s) { return bar0 + 8u * s; };
+    auto raw_empty = [&](int s) { return bar0 + 8u * (SR + s); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * SR + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (2 * SR + SA + s); };
+    auto b_full = [&](int s) { return bar0 + 8u * (2 * SR + 2 * SA + s); };
+    auto b_empty = [&](int s) { return bar0 + 8u * (2 * SR + 2 * SA + SB + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * (SR + SA + SB));
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t mma_done = acc_full + 16u;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + C::OFF_TMEM + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::OFF_TMEM);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_raw(s), 1);
-            mbar_init(full_b(s), 1);
-            mbar_init(full_a(s), NUM_DEQ_WARPS);
-            mbar_init(empty(s), 1);
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(raw_full(s), 1);
+            mbar_init(raw_empty(s), NUM_DEQ_WARPS);
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(a_full(s), NUM_DEQ_WARPS);
+            mbar_init(a_empty(s), 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(b_full(s), NUM_B_WARPS * 32);
+            mbar_init(b_empty(s), 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, NUM_EPI_WARPS);
@@ -128,7 +181,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == WARP_PRODUCER && lane == 0) prefetch_tensormap(&bmap);
     if (warp == WARP_MMA) {
         tmem_alloc(base + C::OFF_TMEM, C::TMEM_COLS);
         tmem_relinquish();
@@ -143,74 +195,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
     };
 
-    if (warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ producer
-        int it = 0;  // global K-block counter
-        int issued = 0;
+    if (warp == WARP_WPROD) {
+        // ------------------------------------------------ weight (raw) producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int it = 0;  // global K-block counter
+            bool ok = true;
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+                const int tile = w / rb_count, ri = w % rb_count;
+                const int e = args.tile_e[tile];
+                const int rb0 = ri * args.rb_mul;
+                // an odd last block of W_d has no partner: load it twice (the
+                // epilogue drops the copy)
+                const int rb1 = (rb0 + args.rb_second < rbs_per_e) ? rb0 + args.rb_second : rb0;
+                const uint8_t* wt0 = args.wpk + ((size_t)e * rbs_per_e + rb0) * tiles_per_rb * kTileBytes;
+                const uint8_t* wt1 = args.wpk + ((size_t)e * rbs_per_e + rb1) * tiles_per_rb * kTileBytes;
+                for (int kb = 0; kb < KB; kb += C::RK, ++it) {
+                    const int s = it % SR;
+                    if (*abort_flag || !mbar_wait(raw_empty(s), ((it / SR) & 1) ^ 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t raw = base + C::OFF_RAW + s * C::RAW_BYTES;
+                    constexpr uint32_t half = C::RK * kTileBytes;
+                    mbar_arrive_expect_tx(raw_full(s), C::RAW_BYTES);
+                    bulk_g2s_hint(raw, wt0 + (size_t)kb * kTileBytes, half, raw_full(s), pol);
+                    bulk_g2s_hint(raw + half, wt1 + (size_t)kb * kTileBytes, half, raw_full(s), pol);
+                }
+            }
+            // the copies already issued land before the CTA can go away
+            for (int j = (it > SR ? it - SR : 0); j < it; ++j) mbar_wait(raw_full(j % SR), (j / SR) & 1);
+        }
+    } else if (warp >= WARP_B0 && warp < WARP_B0 + NUM_B_WARPS) {
+        // ----------------------------------------------- token-row loaders
+        // thread bt: 16-byte chunk c = bt % 8 of rows bt / 8 + 16 i
+        const int bt = threadIdx.x - WARP_B0 * 32;
+        const int c = bt % 8, r0 = bt / 8;
+        int it = 0, issued = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-            const int tile = w / rb_count, rb = w % rb_count;
-            const int e = args.tile_e[tile], n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
+            const int tile = w / rb_count;
+            const int n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
             const int npad = (nn + 15) & ~15;
-            // token rows for the gathers: lane handles 4-row groups lane, lane+32
-            int rows[8];
-            if (GATEUP) {
+            const uint16_t* src[B_ROWS_PER_THREAD];
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = (lane + 32 * q) * 4 + i;
-                        rows[q * 4 + i] = args.bucket_token[n0 + (r < nn ? r : 0)];
-                    }
+            for (int i = 0; i < B_ROWS_PER_THREAD; ++i) {
+                const int r = r0 + 16 * i;
+                const int rr = r < nn ? r : 0;  // padding rows repeat row 0
+                const size_t row = GATEUP ? (size_t)args.bucket_token[n0 + rr] : (size_t)(n0 + rr);
+                src[i] = args.bsrc + row * args.K + c * 8;
             }
-            const uint8_t* wtile =
-                args.wpk + ((size_t)e * rbs_per_e + rb) * tiles_per_rb * kTileBytes;
-            const uint8_t* wtile_up =
-                args.wpk + ((size_t)e * rbs_per_e + rb + rb_count) * tiles_per_rb * kTileBytes;
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
-                if (*abort_flag || !mbar_wait(empty(s), ph ^ 1)) {
+                const int s = it % SB;
+                if (*abort_flag || !mbar_wait(b_empty(s), ((it / SB) & 1) ^ 1)) {
                     fail();
                     ok = false;
                     break;
                 }
-                const uint32_t raw = base + C::OFF_RAW + s * C::RAW_BYTES;
                 const uint32_t bsm = base + C::OFF_B + s * B_BYTES;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full_raw(s), C::RAW_BYTES);
-                    bulk_g2s(raw, wtile + (size_t)kb * kTileBytes, kTileBytes, full_raw(s));
-                    if (GATEUP)
-                        bulk_g2s(raw + kTileBytes, wtile_up + (size_t)kb * kTileBytes, kTileBytes,
-                                 full_raw(s));
-                    mbar_arrive_expect_tx(full_b(s), npad * 128);
-                }
-                __syncwarp();
-                if (GATEUP) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int g4 = lane + 32 * q;
-                        if (g4 * 4 < npad)
-                            tma_gather4(bsm + g4 * 512, &bmap, kb * kTileK, rows[q * 4 + 0],
-                                        rows[q * 4 + 1], rows[q * 4 + 2], rows[q * 4 + 3],
-                                        full_b(s));
-                    }
-                } else {
-                    if (lane * 16 < npad)
-                        tma_load_2d(bsm + lane * 16 * 128, &bmap, kb * kTileK, n0 + lane * 16,
-                                    full_b(s));
+                for (int i = 0; i < B_ROWS_PER_THREAD; ++i) {
+                    const int r = r0 + 16 * i;
+                    if (r < npad)
+                        cp_async16(bsm + r * 128 + ((c ^ (r & 7)) * 16), src[i] + kb * kTileK);
                 }
+                cp_async_arrive_noinc(b_full(s));
                 ++issued;
             }
         }
-        if (!ok) {
-            // let the copies already issued land before the CTA goes away
-            const int first = issued > S ? issued - S : 0;
-            for (int j = first; j < issued; ++j) {
-                mbar_wait(full_raw(j % S), (j / S) & 1);
-                mbar_wait(full_b(j % S), (j / S) & 1);
-            }
-        }
+        // the copies already issued land before the CTA can go away
+        for (int j = (issued > SB ? issued - SB : 0); j < issued; ++j)
+            mbar_wait(b_full(j % SB), (j / SB) & 1);
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------------- MMA
         int it = 0, item = 0;
@@ -227,17 +283,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
-                if (*abort_flag || !mbar_wait(full_b(s), ph) || !mbar_wait(full_a(s), ph)) {
+                const int sa = it % SA, sb = it % SB;
+                if (*abort_flag || !mbar_wait(b_full(sb), (it / SB) & 1) ||
+                    !mbar_wait(a_full(sa), (it / SA) & 1)) {
                     fail();
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
                 if (lane == 0) {
-                    const uint32_t a_sm = base + C::OFF_A + s * C::A_BYTES;
-                    const uint32_t b_sm = base + C::OFF_B + s * B_BYTES;
+                    const uint32_t a_sm = base + C::OFF_A + sa * C::A_BYTES;
+                    const uint32_t b_sm = base + C::OFF_B + sb * B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bdesc = sw128_kmajor_desc(b_sm + kk * 32);
@@ -248,7 +305,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             mma_f16(tmem + m * 256, adesc, bdesc, idesc, (kb | kk) != 0);
                         }
                     }
-                    mma_commit(empty(s));
+                    mma_commit(a_empty(sa));
+                    mma_commit(b_empty(sb));
                 }
                 __syncwarp();
             }
@@ -269,33 +327,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
-                if (*abort_flag || !mbar_wait(full_raw(s), ph)) {
+                const int ir = it / C::RK, sub = it % C::RK;  // weight copy and its K-block
+                const int sr = ir % SR, sa = it % SA;
+                if (*abort_flag || !mbar_wait(raw_full(sr), (ir / SR) & 1) ||
+                    !mbar_wait(a_empty(sa), ((it / SA) & 1) ^ 1)) {
                     fail();
                     ok = false;
                     break;
                 }
-                const uint8_t* raw = sbase + C::OFF_RAW + s * C::RAW_BYTES;
-                uint8_t* a = sbase + C::OFF_A + s * C::A_BYTES;
+                const uint8_t* raw = sbase + C::OFF_RAW + sr * C::RAW_BYTES + sub * kTileBytes;
+                uint8_t* a = sbase + C::OFF_A + sa * C::A_BYTES;
+                // 8 consecutive threads read one row's 32 code bytes (a warp:
+                // 4 rows, 128 contiguous bytes) and write its 128-byte swizzled
+                // fp16 row
+                uint32_t words[C::NMAT * 4], scales[C::NMAT * 4];
 #pragma unroll
-                for (int q = dt; q < C::NMAT * 1024; q += NUM_DEQ_WARPS * 32) {
+                for (int i = 0; i < C::NMAT * 4; ++i) {
+                    const int q = dt + i * NUM_DEQ_WARPS * 32;
                     const int m = q / 1024, r = (q / 8) % 128, c = q % 8;
-                    const uint8_t* t = raw + m * kTileBytes;
-                    const uint32_t word = *reinterpret_cast<const uint32_t*>(t + r * 32 + c * 4);
-                    const uint16_t dh =
-                        *reinterpret_cast<const uint16_t*>(t + kTileCodeBytes + r * 4 + (c / 4) * 2);
-                    const uint32_t d2 = (uint32_t)dh | ((uint32_t)dh << 16);
-                    uint4 o;
-                    o.x = f16x2_dequant(word & 0x000F000Fu, d2);
-                    o.y = f16x2_dequant((word >> 4) & 0x000F000Fu, d2);
-                    o.z = f16x2_dequant((word >> 8) & 0x000F000Fu, d2);
-                    o.w = f16x2_dequant((word >> 12) & 0x000F000Fu, d2);
+                    const uint8_t* t = raw + m * (C::RK * kTileBytes);
+                    words[i] = *reinterpret_cast<const uint32_t*>(t + r * 32 + c * 4);
+                    scales[i] = *reinterpret_cast<const uint16_t*>(t + kTileCodeBytes + r * 4 + (c / 4) * 2);
+                }
+                __syncwarp();
+                if (lane == 0 && sub == C::RK - 1) mbar_arrive(raw_empty(sr));  // copy read
+#pragma unroll
+                for (int i = 0; i < C::NMAT * 4; ++i) {
+                    const int q = dt + i * NUM_DEQ_WARPS * 32;
+                    const int m = q / 1024, r = (q / 8) % 128, c = q % 8;
+                    const uint4 o = dequant8(words[i], scales[i] | (scales[i] << 16));
                     *reinterpret_cast<uint4*>(a + m * A_MAT_BYTES + r * 128 + ((c ^ (r & 7)) * 16)) = o;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(s));
+                if (lane == 0) mbar_arrive(a_full(sa));
             }
         }
     } else {
@@ -304,20 +369,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = quad * 32 + lane;
         int item = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
-            const int tile = w / rb_count, rb = w % rb_count;
+            const int tile = w / rb_count, ri = w % rb_count;
             const int n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
             if (*abort_flag || !mbar_wait(acc_full, item & 1)) {
                 fail();
                 break;
             }
             tc_fence_after();
-            const int feat = rb * kTileRows + row;
+            const int feat = ri * args.rb_mul * kTileRows + row;  // down: first of two blocks
+            const bool second = ri * args.rb_mul + args.rb_second < rbs_per_e;  // down: partner exists
             for (int c0 = 0; c0 < nn; c0 += 16) {
-                uint32_t g[16];
+                uint32_t g[16], u[16];
                 tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, g);
+                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 256 + c0, u);
                 if (GATEUP) {
-                    uint32_t u[16];
-                    tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 256 + c0, u);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -333,9 +398,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < nn) {
-                            const float yv = __uint_as_float(g[j]) * args.slot_w[n0 + c0 + j];
-                            args.out[(size_t)(n0 + c0 + j) * args.out_ld + feat] =
-                                float_to_half_bits_sat(yv);
+                            const float sw = args.slot_w[n0 + c0 + j];
+                            uint16_t* o = args.out + (size_t)(n0 + c0 + j) * args.out_ld + feat;
+                            o[0] = float_to_half_bits_sat(__uint_as_float(g[j]) * sw);
+                            if (second) o[kTileRows] = float_to_half_bits_sat(__uint_as_float(u[j]) * sw);
                         }
                     }
                 }
@@ -353,24 +419,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <bool GATEUP>
-cudaError_t launch_gemm(const CUtensorMap* map, const GemmArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     using C = Cfg<GATEUP>;
     cudaError_t err = cudaFuncSetAttribute(grouped_q4_gemm_kernel<GATEUP>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    grouped_q4_gemm_kernel<GATEUP><<<num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(*map, a);
+    grouped_q4_gemm_kernel<GATEUP><<<num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, const Workspace& ws,
+cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,
                                   int T, int H, int I, int E, int k, int* status, int num_sms,
                                   cudaStream_t s) {
     (void)T; (void)E; (void)k;
     GemmArgs a{};
     a.wpk = static_cast<const uint8_t*>(wgu);
+    a.bsrc = ws.x16;
     a.counters = ws.counters;
     a.tile_e = ws.tile_e;
     a.tile_n0 = ws.tile_n0;
@@ -380,18 +447,21 @@ cudaError_t launch_prefill_gateup(const CUtensorMap* x_map, const void* wgu, con
     a.out = ws.h;
     a.K = H;
     a.rows_per_e = 2 * I;
-    a.out_rows = I;
+    a.rb_items = I / kTileRows;
+    a.rb_mul = 1;
+    a.rb_second = I / kTileRows;  // the matching up rows
     a.out_ld = I;
     a.status = status;
-    return launch_gemm<true>(x_map, a, num_sms, s);
+    return launch_gemm<true>(a, num_sms, s);
 }
 
-cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const Workspace& ws,
+cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
                                 int T, int H, int I, int E, int k, int* status, int num_sms,
                                 cudaStream_t s) {
     (void)T; (void)E; (void)k;
     GemmArgs a{};
     a.wpk = static_cast<const uint8_t*>(wd);
+    a.bsrc = ws.h;
     a.counters = ws.counters;
     a.tile_e = ws.tile_e;
     a.tile_n0 = ws.tile_n0;
@@ -401,10 +471,12 @@ cudaError_t launch_prefill_down(const CUtensorMap* h_map, const void* wd, const 
     a.out = static_cast<uint16_t*>(ws.y);
     a.K = I;
     a.rows_per_e = H;
-    a.out_rows = H;
+    a.rb_items = (H / kTileRows + 1) / 2;
+    a.rb_mul = 2;
+    a.rb_second = 1;  // the next row block
     a.out_ld = H;
     a.status = status;
-    return launch_gemm<false>(h_map, a, num_sms, s);
+    return launch_gemm<false>(a, num_sms, s);
 }
 
 }  // namespace moeq4
