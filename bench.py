@@ -28,8 +28,13 @@ METRIC = "MoE-layer prefill tokens/s and decode µs/token; % of HBM / tensor roo
 DECODE_LAYERS = 16          # distinct weight copies per decode step
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
-KERNELS_PER_DECODE_LAYER = 2   # route (router, top-k, buckets, x codes); experts (gate/up, down, combine)
-KERNELS_PER_PREFILL_LAYER = 7  # fused router, 3 bucketing, gate/up, down, combine
+# DRAM bytes (read + write) per launch from the ncu captures summarised in
+# profiles/decode_experts_T1.md and profiles/grouped_q4_gemm_prefill_T2048.md,
+# taken with the kernels as they are in this tree.
+NCU_TRAFFIC_DECODE_EXPERTS_T1 = 21_377_792
+NCU_TRAFFIC_PREFILL_GATEUP = 235_081_984 + 7_198_208
+KERNELS_PER_DECODE_LAYER = 3   # route (router, top-k, buckets, x codes); experts (gate/up, down); combine
+KERNELS_PER_PREFILL_LAYER = 8  # router GEMM, top-k, 3 bucketing, gate/up, down, combine
 
 
 def load_peaks():
@@ -427,7 +432,7 @@ def main():
         },
         "roofline": {"bound": "hbm", "kernel": "decode_experts_kernel", "achieved": roof_gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": roof_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": roof_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_DECODE_EXPERTS_T1,
                      "peak_source": peaks["source"],
                      "algorithmic_bytes_per_launch": d1["gateup_bytes"] + d1["down_bytes"],
                      "launch_us": d1["experts_us"]},
@@ -444,7 +449,8 @@ def main():
         line["prefill_roofline"] = {
             "bound": "tensor", "kernel": "grouped_q4_gemm_kernel<gate/up>",
             "achieved": pre["gateup_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": pre["gateup_tflops"] / peaks["bf16_tflops"], "traffic": None,
+            "frac": pre["gateup_tflops"] / peaks["bf16_tflops"],
+            "traffic": NCU_TRAFFIC_PREFILL_GATEUP,
             "peak_source": peaks["source"]}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(1)
