@@ -28,9 +28,9 @@ METRIC = "MoE-layer prefill tokens/s and decode µs/token; % of HBM / tensor roo
 DECODE_LAYERS = 16          # distinct weight copies per decode step
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
-# DRAM bytes (read + write) per launch from the ncu captures summarised in
-# profiles/decode_experts_T1.md and profiles/grouped_q4_gemm_prefill_T2048.md,
-# taken with the kernels as they are in this tree.
+# DRAM bytes (read + write) per launch from one ncu capture of each kernel as
+# it is in this tree: the decode expert kernel (T=1) and the prefill gate/up
+# GEMM (T=2048).  Set to None when the kernel changes before a new capture.
 NCU_TRAFFIC_DECODE_EXPERTS_T1 = 21_377_792
 NCU_TRAFFIC_PREFILL_GATEUP = 235_081_984 + 7_198_208
 KERNELS_PER_DECODE_LAYER = 3   # route (router, top-k, buckets, x codes); experts (gate/up, down); combine
