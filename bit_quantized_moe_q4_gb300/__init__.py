@@ -34,6 +34,7 @@ MOE_ERR_WORKSPACE = -7
 MOE_Q4_CODES = 0
 MOE_Q4_BLOCK18 = 1
 MOE_OUT_FP32 = 1
+MOE_STACKED_PRENORM = 2
 MOE_MODE_PREFILL = 0
 MOE_MODE_DECODE = 1
 MOE_DECODE_MAX_T = 32
@@ -204,7 +205,7 @@ def make_debug(mode: int, T: int, H: int, I: int, E: int, k: int, device="cuda")
 
 
 def _forward(fn_name, x, wr, wgu_packed, wd_packed, I, k, out, out_fp32, workspace, debug,
-             stream):
+             stream, prenorm=False):
     T, H = x.shape
     E = wr.shape[0]
     mode = MOE_MODE_PREFILL if fn_name == "moe_q4_forward_prefill" else MOE_MODE_DECODE
@@ -214,7 +215,7 @@ def _forward(fn_name, x, wr, wgu_packed, wd_packed, I, k, out, out_fp32, workspa
     if workspace is None:
         workspace = torch.empty(max(moe_workspace_bytes(mode, T, H, I, E, k), 1),
                                 dtype=torch.uint8, device=x.device)
-    flags = MOE_OUT_FP32 if out_fp32 else 0
+    flags = (MOE_OUT_FP32 if out_fp32 else 0) | (MOE_STACKED_PRENORM if prenorm else 0)
     fn = getattr(load_library(), fn_name)
     _check(fn(_ptr(x), _ptr(wr), _ptr(wgu_packed), _ptr(wd_packed), T, H, I, E, k, flags,
               _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -224,19 +225,20 @@ def _forward(fn_name, x, wr, wgu_packed, wd_packed, I, k, out, out_fp32, workspa
 
 def moe_q4_forward_prefill(x, wr, wgu_packed, wd_packed, I: int, k: int, out=None,
                            out_fp32: bool = True, workspace=None, debug: MoeDebug | None = None,
-                           stream=None):
+                           stream=None, prenorm: bool = False):
     """One prefill MoE layer.  x bf16 [T,H]; wr fp32 [E,H]; packed gate/up
-    ([E,2I,H]) and down ([E,H,I]) weights.  Returns out [T,H] (fp32 or bf16)."""
+    ([E,2I,H]) and down ([E,H,I]) weights.  Returns out [T,H] (fp32 or bf16).
+    ``prenorm`` sets MOE_STACKED_PRENORM (route and multiply RMSNorm(x))."""
     return _forward("moe_q4_forward_prefill", x, wr, wgu_packed, wd_packed, I, k, out, out_fp32,
-                    workspace, debug, stream)
+                    workspace, debug, stream, prenorm)
 
 
 def moe_w4a8_forward_decode(x, wr, wgu_packed, wd_packed, I: int, k: int, out=None,
                             out_fp32: bool = True, workspace=None,
-                            debug: MoeDebug | None = None, stream=None):
+                            debug: MoeDebug | None = None, stream=None, prenorm: bool = False):
     """One decode MoE layer on the W4A8 integer path (T <= 32)."""
     return _forward("moe_w4a8_forward_decode", x, wr, wgu_packed, wd_packed, I, k, out, out_fp32,
-                    workspace, debug, stream)
+                    workspace, debug, stream, prenorm)
 
 
 class StageEvents:

@@ -165,6 +165,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
     w.tile_e = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_n0 = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_nn = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
+    w.xn = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
     if (mode == MOE_MODE_PREFILL) {
         w.y = take(Tk * H * 2);
         w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
@@ -218,7 +219,8 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
             size_t ws_bytes, moe_debug* dbg, void* stream) {
     int rc = check_layer_shape(mode, T, H, I, E, k);
     if (rc) return rc;
-    if (flags & ~MOE_OUT_FP32) return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (flags & ~(MOE_OUT_FP32 | MOE_STACKED_PRENORM))
+        return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (T == 0) return MOE_OK;
     if (!x || !wr || !wgu || !wd || !out)
         return set_err(MOE_ERR_INVALID_ARG, "null tensor argument");
@@ -251,9 +253,15 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
         return cuda_check(record_stage(ev[i], s, capturing), "stage event");
     };
     if ((rc = mark(0))) return rc;
+    // the routed and multiplied input: x, or RMSNorm(x) for a stacked layer
+    const uint16_t* xin = x;
+    if (flags & MOE_STACKED_PRENORM) {
+        if ((rc = cuda_check(launch_rmsnorm(x, T, H, 1e-6f, ws.xn, s), "rmsnorm"))) return rc;
+        xin = ws.xn;
+    }
     if (mode == MOE_MODE_DECODE) {
-        // route (+ buckets, x codes), then experts (gate/up, down, combine)
-        if ((rc = cuda_check(launch_decode(x, wr, wgu, wd, T, H, I, E, k,
+        // route (+ buckets, x codes), then experts (gate/up, down), then combine
+        if ((rc = cuda_check(launch_decode(xin, x, wr, wgu, wd, T, H, I, E, k,
                                            (flags & MOE_OUT_FP32) != 0, out, ws,
                                            dbg ? dbg->dots_gu : nullptr,
                                            dbg ? dbg->dots_d : nullptr,
@@ -264,7 +272,7 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
     } else {
         // 1. route (also writes the fp16 copy of x)
         float* logits = dbg ? dbg->logits : nullptr;
-        if ((rc = cuda_check(launch_route_gemm(x, wr, T, H, E, k, ws.route_parts, logits,
+        if ((rc = cuda_check(launch_route_gemm(xin, wr, T, H, E, k, ws.route_parts, logits,
                                                ws.topk_idx, ws.topk_w, ws.x16, s),
                              "route")))
             return rc;

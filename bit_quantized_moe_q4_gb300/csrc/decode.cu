@@ -81,7 +81,8 @@ __host__ __device__ constexpr int act_scale_bytes(int T, int G) { return (T * G 
 __host__ __device__ constexpr int align128(int v) { return (v + 127) & ~127; }
 
 struct DecodeArgs {
-    const uint16_t* x;
+    const uint16_t* x;      // layer input as routed and multiplied
+    const uint16_t* x_res;  // residual added by the combine (x, or the un-normalised input)
     const float* wr;
     const uint8_t* wgu;
     const uint8_t* wd;
@@ -797,7 +798,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= a.T * H) return;
     const int t = q / H, col = q % H;
-    float v = bf16_bits_to_float(a.x[q]);
+    float v = bf16_bits_to_float(a.x_res[q]);
     for (int j0 = 0; j0 < k; j0 += 8) {
         int rows[8];
 #pragma unroll
@@ -1029,7 +1030,8 @@ void decode_splits(int T, int H, int I, int E, int k, int* nsg, int* nsd) {
     choose_splits(T, H, I, E, k, nsg, nsd);
 }
 
-cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
+cudaError_t launch_decode(const uint16_t* x, const uint16_t* x_res, const float* wr,
+                          const void* wgu, const void* wd,
                           int T, int H, int I, int E, int k, bool out_fp32, void* out,
                           const Workspace& ws, int32_t* dots_gu, int32_t* dots_d, bool write_qh,
                           int* status, int num_sms, void** events, bool capturing,
@@ -1037,6 +1039,7 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     if (T == 0) return cudaSuccess;
     DecodeArgs a{};
     a.x = x;
+    a.x_res = x_res;
     a.wr = wr;
     a.wgu = static_cast<const uint8_t*>(wgu);
     a.wd = static_cast<const uint8_t*>(wd);

@@ -29,6 +29,7 @@ struct Workspace {
     int32_t* tile_e;        // [max_tiles]   expert of each token tile
     int32_t* tile_n0;       // [max_tiles]   first bucket row of the tile
     int32_t* tile_nn;       // [max_tiles]   rows in the tile
+    uint16_t* xn;           // [T, H] bf16 RMSNorm(x) (stacked pre-norm layers)
     uint16_t* x16;          // [T, H] fp16 copy of x (prefill GEMM operand)
     float* route_parts;     // [ksplit, T, E] router K-slice sums (prefill)
     uint16_t* h;            // [T*k, I] fp16 (prefill)
@@ -82,7 +83,8 @@ cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
 // `events` is null or the caller's MOE_NUM_STAGE_EVENTS events; boundaries
 // 1..3 are recorded after the route kernel, 4..5 after the expert kernel and
 // 6 after the combine.
-cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
+cudaError_t launch_decode(const uint16_t* x, const uint16_t* x_res, const float* wr,
+                          const void* wgu, const void* wd,
                           int T, int H, int I, int E, int k, bool out_fp32, void* out,
                           const Workspace& ws, int32_t* dots_gu, int32_t* dots_d, bool write_qh,
                           int* status, int num_sms, void** events, bool capturing,
@@ -94,6 +96,9 @@ cudaError_t decode_prepare_device(int dev);
 bool decode_shape_fits(int T, int H, int I);
 // K splits (partial-sum count) of the decode gate/up and down tasks.
 void decode_splits(int T, int H, int I, int E, int k, int* nsg, int* nsd);
+// xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), one warp per token.
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
+                           cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
                            int T, int H, int k, bool out_fp32, void* out, cudaStream_t s);
 

@@ -68,7 +68,49 @@ __global__ void combine_kernel(const uint16_t* __restrict__ x, const Y* __restri
     }
 }
 
+// One warp per token: the sum of squares in fp32 (each lane over its columns
+// in order, then a butterfly), r = 1 / sqrt(mean + eps) (correctly rounded
+// divide and square root), xn = bf16_rn(x * r).
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                      float eps, uint16_t* __restrict__ xn) {
+    const int t = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (t >= T) return;  // whole warp
+    const uint16_t* row = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int c = lane * 8; c < H; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float a = __uint_as_float(w[p] << 16), b = __uint_as_float(w[p] & 0xffff0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+        }
+    }
+    ss = warp_sum(ss);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + eps));
+    uint16_t* orow = xn + (size_t)t * H;
+    for (int c = lane * 8; c < H; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float a = __uint_as_float(w[p] << 16) * r, b = __uint_as_float(w[p] & 0xffff0000u) * r;
+            o[p] = (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
+        }
+        *reinterpret_cast<uint4*>(orow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
+                           cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    rmsnorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, eps, xn);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
                            int T, int H, int k, bool out_fp32, void* out, cudaStream_t s) {

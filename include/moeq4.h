@@ -77,6 +77,14 @@ extern "C" {
 
 /* ---- forward flags ------------------------------------------------------- */
 #define MOE_OUT_FP32  1u   /* out is fp32 [T, H]; otherwise bf16 [T, H]      */
+/* MOE_STACKED_PRENORM: a pre-norm residual layer for stacking.  The router
+ * and the experts read xn = RMSNorm(x) (per token: x / sqrt(mean(x^2) +
+ * 1e-6), unit gain, computed in fp32 and rounded to bf16); the residual added
+ * to the MoE term is x itself: out = x + sum_j w_j y_j(xn).  With bf16
+ * output, layer l+1 takes layer l's out as its x.  The pages do not print
+ * the layer's norm; this is the plainest pre-norm reading that keeps many
+ * stacked residual layers finite. */
+#define MOE_STACKED_PRENORM 2u
 
 /* ---- forward modes for moe_workspace_bytes ------------------------------- */
 #define MOE_MODE_PREFILL 0

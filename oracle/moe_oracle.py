@@ -52,6 +52,30 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def f64_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round to bf16 (nearest, ties to even) through fp32: fp64 -> fp32 -> bf16.
+    (The two roundings differ from one exact rounding only when the fp32 value
+    falls exactly on a bf16 midpoint.)"""
+    u = np.asarray(a, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# Pre-norm for stacked layers (reading: the pages print no layer norm; a
+# stack of residual MoE layers needs one to stay finite, and the plainest is
+# an RMSNorm of the layer input with unit gain)
+# --------------------------------------------------------------------------
+RMS_EPS = 1e-6
+
+
+def rmsnorm_bf16_bits(X: np.ndarray) -> np.ndarray:
+    """Per row: X / sqrt(mean(X^2) + 1e-6), rounded to bf16 bit patterns."""
+    X = np.asarray(X, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + RMS_EPS)
+    return f64_to_bf16_bits(X * r)
+
+
 # --------------------------------------------------------------------------
 # Q4_0-family weights (Methodology 2, "Quantization")
 # --------------------------------------------------------------------------
@@ -242,20 +266,26 @@ def _split_gate_up(gu: np.ndarray, I: int):
     return gu[..., :I, :], gu[..., I:, :]
 
 
-def moe_prefill(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=None):
+def moe_prefill(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=None,
+                prenorm=False):
     """Prefill layer with bf16 activations, computed exactly in float64.
 
     out[t] = x[t] + sum_j w[t, j] * W_d,e (silu(W_g,e x[t]) * (W_u,e x[t])),
     e = idx[t, j], each W the Q4_0-decoded matrix.  ``tokens`` restricts the
     evaluation to a subset of rows (routing is per token, so a row's result
-    does not depend on the others).  Returns (out [n, H], routing dict).
+    does not depend on the others).  With ``prenorm`` the router and the
+    experts read xn = bf16(RMSNorm(x)) while the residual stays x.  Returns
+    (out [n, H], routing dict).
     """
     X = bf16_bits_to_f64(x_bits)
     if tokens is not None:
         X = X[np.asarray(tokens)]
+    residual = X
+    if prenorm:
+        X = bf16_bits_to_f64(rmsnorm_bf16_bits(X))
     I = gu_codes.shape[1] // 2
     logits, idx, w = route(X, wr, k)
-    out = X.copy()
+    out = residual.copy()
     for e in np.unique(idx):
         rows, js = np.nonzero(idx == e)
         Wg, Wu = _split_gate_up(q4_dequant(gu_codes[e], gu_scales[e]), I)
@@ -290,7 +320,7 @@ def moe_dense_bruteforce(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k):
 
 
 def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=None,
-               keep_dots=False):
+               keep_dots=False, prenorm=False):
     """Decode layer with W4A8 arithmetic (Methodology 1, "Decode (CPU)").
 
     The bf16 hidden state is quantised to int8 per 32 (``act_quant``); gate
@@ -299,16 +329,19 @@ def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=Non
     precision in which the kernels take that decision); the down projection
     is again integer group dots, scaled by d_w * d_h and by the routing
     weight; the residual is added.  Returns (out float64 [n, H], stages)."""
+    x_bits = np.asarray(x_bits)
+    if tokens is not None:
+        x_bits = x_bits[np.asarray(tokens)]
+    residual = bf16_bits_to_f64(x_bits)
+    if prenorm:
+        x_bits = rmsnorm_bf16_bits(residual)
     X64 = bf16_bits_to_f64(x_bits)
     X32 = bf16_bits_to_f32(x_bits)
-    if tokens is not None:
-        X64 = X64[np.asarray(tokens)]
-        X32 = X32[np.asarray(tokens)]
     n, H = X64.shape
     I = gu_codes.shape[1] // 2
     logits, idx, w = route(X64, wr, k)
     qx, dx = act_quant(X32)
-    out = X64.copy()
+    out = residual.copy()
     qh = np.zeros((n, k, I), np.int64)
     dh = np.zeros((n, k, I // GROUP), np.float16)
     hh = np.zeros((n, k, I))
@@ -329,6 +362,25 @@ def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=Non
     stages = {"logits": logits, "idx": idx, "w": w, "qx": qx, "dx": dx,
               "h": hh, "qh": qh, "dh": dh, "dots_gu": dots_gu, "dots_d": dots_d}
     return out, stages
+
+
+def moe_stack_prefill(x_bits, layer, L, k, tokens=None, keep=False):
+    """L stacked pre-norm prefill layers with bf16 outputs:
+    x_{l+1} = bf16(x_l + MoE_l(bf16(RMSNorm(x_l)))).  ``layer(l)`` returns
+    (wr, gu_codes, gu_scales, d_codes, d_scales) of layer l.  Returns the
+    final bf16 bits [n, H] (and, with ``keep``, every layer's output bits and
+    routing)."""
+    xb = np.asarray(x_bits)
+    if tokens is not None:
+        xb = xb[np.asarray(tokens)]
+    hist = []
+    for l in range(L):
+        wr, gc, gs, dc, ds = layer(l)
+        out, r = moe_prefill(xb, wr, gc, gs, dc, ds, k, prenorm=True)
+        xb = f64_to_bf16_bits(out)
+        if keep:
+            hist.append((xb, r))
+    return (xb, hist) if keep else xb
 
 
 def rms(a: np.ndarray) -> float:

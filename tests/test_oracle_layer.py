@@ -155,3 +155,65 @@ def test_decode_close_to_prefill_on_tiny():
     assert rel < 0.03, rel
     # stage consistency: routing identical to prefill's
     assert np.array_equal(st["idx"], O.route(X, li.wr, li.k)[1])
+
+
+# ------------------------------------------------------------ stacked pre-norm
+def test_rmsnorm_properties():
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((6, 256)) * 3.0
+    xn = O.bf16_bits_to_f64(O.rmsnorm_bf16_bits(X))
+    # unit mean square up to the bf16 rounding of each element
+    assert np.allclose(np.mean(xn * xn, axis=1), 1.0, atol=1e-2)
+    # invariant under exact (power-of-two) scaling of the row
+    for c in (0.25, 8.0, -2.0):
+        xs = O.bf16_bits_to_f64(O.rmsnorm_bf16_bits(X * c))
+        assert np.array_equal(xs, np.sign(c) * xn)
+    # a constant row c maps to sign(c) / sqrt(1 + eps / c^2): 1 in bf16
+    const = O.bf16_bits_to_f64(O.rmsnorm_bf16_bits(np.full((1, 64), -5.0)))
+    assert np.all(const == -1.0)
+
+
+def test_bf16_rounding_ties_to_even():
+    a = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -7, -(1.0 + 2.0 ** -8)])
+    assert O.f64_to_bf16_bits(a).tolist() == [0x3F80, 0x3F82, 0x3F81, 0xBF80]
+
+
+def test_prenorm_layer_residual_and_norm():
+    li = workloads.make_layer("pn", 12, 256, 128, 8, 2, seed=51, wr_std=0.05)
+    args = (li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    X = O.bf16_bits_to_f64(li.x)
+    # the residual is x itself, not its normalised copy
+    zero = (li.wr, li.gu_codes, li.gu_scales, li.d_codes, np.zeros_like(li.d_scales), li.k)
+    out0, _ = O.moe_prefill(li.x, *zero, prenorm=True)
+    assert np.array_equal(out0, X)
+    # the MoE term sees RMSNorm(x): scaling x by 4 scales only the residual
+    x4 = O.f64_to_bf16_bits(X * 4.0)
+    o1, r1 = O.moe_prefill(li.x, *args, prenorm=True)
+    o4, r4 = O.moe_prefill(x4, *args, prenorm=True)
+    assert np.array_equal(r1["idx"], r4["idx"])
+    assert np.allclose(o4 - 4.0 * X, o1 - X, rtol=0, atol=1e-12)
+    # without the norm the MoE term does change with the scale
+    p1, _ = O.moe_prefill(li.x, *args)
+    p4, _ = O.moe_prefill(x4, *args)
+    assert not np.allclose(p4 - 4.0 * X, p1 - X, atol=1e-3)
+    # decode applies the same norm before its int8 codes
+    d0, _ = O.moe_decode(li.x, *zero, prenorm=True)
+    assert np.array_equal(d0, X)
+
+
+def test_stack_equals_layer_composition():
+    layers = [workloads.make_layer("st", 9, 256, 128, 6, 2, seed=60 + l, wr_std=0.05) for l in range(2)]
+    x0 = layers[0].x
+
+    def layer(l):
+        li = layers[l]
+        return li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales
+
+    xb = x0
+    for l in range(2):
+        out, _ = O.moe_prefill(xb, *layer(l), 2, prenorm=True)
+        xb = O.f64_to_bf16_bits(out)
+    assert np.array_equal(O.moe_stack_prefill(x0, layer, 2, 2), xb)
+    # a subset of tokens gives the same rows (each token is independent)
+    sub = O.moe_stack_prefill(x0, layer, 2, 2, tokens=[1, 7])
+    assert np.array_equal(sub, xb[[1, 7]])

@@ -28,8 +28,11 @@ top-8 routing; the shapes follow that model family):
 * prefill  T=2048, H=2048, I=768, E=128, k=8, wr~N(0,0.02), seed 2
 * skewed   T=10240, same shapes, Zipf(1.1) expert popularity through a bias
            channel, 16 experts never chosen, seed 3
-* stacked  one layer of a 40-layer stack, T=4096, H=2048, I=768, E=256, k=8,
-           fresh weights per layer, seed 4
+* stacked  a 40-layer stack of pre-norm layers, T=4096, H=2048, I=768, E=256,
+           k=8, fresh weights per layer (27.2 GB packed), seed 4.  Its
+           weights come from a counter-based generator (below) so that the
+           GPU can draw all of them and the oracle only the experts a sampled
+           token reaches, bit for bit the same.
 
 Codes are uniform on 0..15; scales are uniform on [0.005, 0.02] rounded to fp16.
 """
@@ -142,13 +145,147 @@ def skewed(seed: int = 3, T: int = 10240, zipf_s: float = 1.1, dead: int = 16) -
     return li
 
 
-def stacked_layer(layer: int, seed: int = 4, T: int = 4096) -> LayerInputs:
-    """Layer ``layer`` (0-based) of the 40-layer stack: fresh weights per layer.
+# --------------------------------------------------------------------------
+# Counter-based weights for the stacked workload
+# --------------------------------------------------------------------------
+# SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast splittable pseudorandom number
+# generators", OOPSLA 2014): output i of the stream with seed s is
+# mix(s + (i + 1) * GAMMA), mix(z) = z1 ^ (z1 >> 31) with
+# z1 = (z0 ^ (z0 >> 27)) * M2, z0 = (z ^ (z >> 30)) * M1, all modulo 2^64.
+# The index of a value encodes (layer, expert, part, row, block):
+#   i = (((layer * 512 + expert) * 4 + part) * 4096 + row) * 256 + block
+# part 0: gate/up codes, 1: down codes (one output = 16 codes, code c of the
+# block in bits 4c..4c+3), 2: gate/up scales, 3: down scales (one output per
+# 32-column group: d = fp16(fp32(0.005 + 0.015 * (out >> 11) / 2^53))).
+STACK = dict(L=40, T=4096, H=2048, I=768, E=256, k=8, seed=4)
+SM_GAMMA = 0x9E3779B97F4A7C15
+SM_M1 = 0xBF58476D1CE4E5B9
+SM_M2 = 0x94D049BB133111EB
+_U64 = (1 << 64) - 1
 
-    Only layer 0 carries its own hidden states; deeper layers take the previous
-    layer's output.  The router is N(0, 0.02) as in the single-layer prefill.
-    """
-    return make_layer(f"stacked_L{layer}", T, 2048, 768, 256, 8, seed * 1000 + layer, 0.02)
+
+def _stack_index(layer, expert, part, row, block):
+    return (((layer * 512 + expert) * 4 + part) * 4096 + row) * 256 + block
+
+
+def splitmix64_np(index: np.ndarray, seed: int) -> np.ndarray:
+    """SplitMix64 outputs for uint64 stream positions ``index`` (numpy)."""
+    z = np.asarray(index, dtype=np.uint64) + np.uint64(1)
+    z = z * np.uint64(SM_GAMMA) + np.uint64(seed & _U64)
+    z = (z ^ (z >> np.uint64(30))) * np.uint64(SM_M1)
+    z = (z ^ (z >> np.uint64(27))) * np.uint64(SM_M2)
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64_torch(index, seed: int):
+    """The same outputs for an int64 torch tensor of positions (two's
+    complement int64 arithmetic; right shifts masked to act as logical)."""
+    import torch
+
+    def c64(v):  # unsigned 64-bit constant as a signed int64
+        v &= _U64
+        return v - (1 << 64) if v >= 1 << 63 else v
+
+    def lsr(z, n):
+        return (z >> n) & ((1 << (64 - n)) - 1)
+
+    z = (index.to(torch.int64) + 1) * c64(SM_GAMMA) + c64(seed)
+    z = (z ^ lsr(z, 30)) * c64(SM_M1)
+    z = (z ^ lsr(z, 27)) * c64(SM_M2)
+    return z ^ lsr(z, 31)
+
+
+def _codes_from_words_np(words: np.ndarray) -> np.ndarray:
+    shifts = (np.arange(16, dtype=np.uint64) * np.uint64(4))
+    return ((words[..., None] >> shifts) & np.uint64(15)).astype(np.uint8).reshape(*words.shape[:-1], -1)
+
+
+def _scales_from_words_np(words: np.ndarray) -> np.ndarray:
+    # fp64 -> fp32 -> fp16, the same two roundings on both generators
+    u = (words >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    return (0.005 + 0.015 * u).astype(np.float32).astype(np.float16)
+
+
+def stacked_expert(layer: int, expert: int, seed: int = STACK["seed"], H: int = STACK["H"],
+                   I: int = STACK["I"]):
+    """One expert of one stacked layer on the host: (gu_codes [2I, H],
+    gu_scales [2I, H/32], d_codes [H, I], d_scales [H, I/32])."""
+    def words(part, rows, cols_per_word, ncols):
+        r = np.arange(rows, dtype=np.uint64)[:, None]
+        b = np.arange(ncols // cols_per_word, dtype=np.uint64)[None, :]
+        idx = (((np.uint64(layer) * np.uint64(512) + np.uint64(expert)) * np.uint64(4) +
+                np.uint64(part)) * np.uint64(4096) + r) * np.uint64(256) + b
+        return splitmix64_np(idx, seed)
+    gu_codes = _codes_from_words_np(words(0, 2 * I, 16, H))
+    d_codes = _codes_from_words_np(words(1, H, 16, I))
+    gu_scales = _scales_from_words_np(words(2, 2 * I, GROUP, H))
+    d_scales = _scales_from_words_np(words(3, H, GROUP, I))
+    return gu_codes, gu_scales, d_codes, d_scales
+
+
+def stacked_experts_torch(layer: int, e0: int, e1: int, device, seed: int = STACK["seed"],
+                          H: int = STACK["H"], I: int = STACK["I"]):
+    """Experts e0..e1-1 of one stacked layer as torch tensors on ``device``:
+    codes uint8 [n, 2I, H] / [n, H, I] and scales float16, equal bit for bit
+    to ``stacked_expert``."""
+    import torch
+    n = e1 - e0
+    e = torch.arange(e0, e1, device=device, dtype=torch.int64)[:, None, None]
+
+    def words(part, rows, cols_per_word, ncols):
+        r = torch.arange(rows, device=device, dtype=torch.int64)[None, :, None]
+        b = torch.arange(ncols // cols_per_word, device=device, dtype=torch.int64)[None, None, :]
+        idx = (((layer * 512 + e) * 4 + part) * 4096 + r) * 256 + b
+        return splitmix64_torch(idx, seed)
+
+    def codes(w):
+        sh = torch.arange(16, device=device, dtype=torch.int64) * 4
+        c = ((w[..., None] >> sh) & 15).to(torch.uint8)  # low bits only: the sign fill is masked
+        return c.reshape(n, w.shape[1], -1)
+
+    def scales(w):
+        u = ((w >> 11) & ((1 << 53) - 1)).to(torch.float64) * 2.0 ** -53
+        return (0.005 + 0.015 * u).to(torch.float32).to(torch.float16)
+
+    return codes(words(0, 2 * I, 16, H)), scales(words(2, 2 * I, GROUP, H)), \
+        codes(words(1, H, 16, I)), scales(words(3, H, GROUP, I))
+
+
+def stacked_router(layer: int, seed: int = STACK["seed"]) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(seed * 1000 + layer))
+    return (rng.standard_normal((STACK["E"], STACK["H"]), dtype=np.float32) *
+            np.float32(0.02)).astype(np.float32)
+
+
+def stacked_x(seed: int = STACK["seed"], T: int = STACK["T"]) -> np.ndarray:
+    return _hidden(np.random.Generator(np.random.PCG64(seed)), T, STACK["H"])
+
+
+class LazyExperts:
+    """Array-like view of one stacked layer's experts for the oracle: indexing
+    by expert draws (and caches) that expert from the counter-based stream."""
+
+    def __init__(self, layer: int, which: int, seed: int = STACK["seed"]):
+        self.layer, self.which, self.seed = layer, which, seed
+        H, I, E = STACK["H"], STACK["I"], STACK["E"]
+        self.shape = [(E, 2 * I, H), (E, 2 * I, H // GROUP), (E, H, I), (E, H, I // GROUP)][which]
+        self._cache = {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self._cache:
+            self._cache[e] = stacked_expert(self.layer, e, self.seed)
+        return self._cache[e][self.which]
+
+
+def stacked_layer_lazy(layer: int, seed: int = STACK["seed"]):
+    """(wr, gu_codes, gu_scales, d_codes, d_scales) of a stacked layer, the
+    weights as LazyExperts (sharing one per-expert cache)."""
+    gc = LazyExperts(layer, 0, seed)
+    views = [gc] + [LazyExperts(layer, w, seed) for w in (1, 2, 3)]
+    for v in views[1:]:
+        v._cache = gc._cache
+    return (stacked_router(layer, seed), *views)
 
 
 CONFIGS = {
