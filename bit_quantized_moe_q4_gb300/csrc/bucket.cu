@@ -58,10 +58,17 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ 
     const int e = threadIdx.x;
     int count = 0;
     if (e < E) {
-        for (int c = 0; c < nchunk; ++c) {
-            const int n = chunk_count[(size_t)c * E + e];
-            chunk_count[(size_t)c * E + e] = count;  // becomes the chunk base
-            count += n;
+        // 16 chunk counts in flight at a time; each becomes its chunk's base
+        for (int c0 = 0; c0 < nchunk; c0 += 16) {
+            int n[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                n[u] = (c0 + u < nchunk) ? chunk_count[(size_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                if (c0 + u < nchunk) chunk_count[(size_t)(c0 + u) * E + e] = count;
+                count += n[u];
+            }
         }
     }
     int total;

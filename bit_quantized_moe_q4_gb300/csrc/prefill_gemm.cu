@@ -30,7 +30,7 @@
 //          each.)
 // The weight copies carry an L2 evict-first hint: they are read once, and
 // should not push the reused token rows out of L2.
-// One thread of the MMA warp issues 4 x K=16 MMAs per matrix into TMEM; four
+// One thread of the MMA warp issues 4 x K=16 MMAs per matrix into TMEM; eight
 // epilogue warps read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
 // weight * acc, both fp16 (saturating at +-65504), in bucket order.
 // One persistent CTA per SM walks a static list of (token tile, row block)
@@ -46,11 +46,11 @@ namespace {
 constexpr int BN = 144;                 // max tokens per tile (buckets are cut evenly)
 constexpr int A_MAT_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
-constexpr int NUM_EPI_WARPS = 4, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 8, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
 constexpr int WARP_WPROD = 0, WARP_MMA = 1, WARP_B0 = 2;
 constexpr int WARP_EPI0 = WARP_B0 + NUM_B_WARPS;
 constexpr int WARP_DEQ0 = WARP_EPI0 + NUM_EPI_WARPS;
-constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 18 warps
+constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 22 warps
 constexpr int B_ROWS_PER_THREAD = BN * 8 / (NUM_B_WARPS * 32);  // 16-byte chunks: 9
 static_assert(BN * 8 % (NUM_B_WARPS * 32) == 0, "B chunks per loader thread");
 
@@ -365,8 +365,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        const int quad = warp % 4;
+        // warp w reads TMEM lanes 32 (w % 4) .. +31 (one accumulator row per
+        // thread); the two warps of a lane quarter take alternate 16-column
+        // chunks, each loading 2 x 16 columns before one wait
+        const int quad = warp % 4, half = (warp - WARP_EPI0) / 4;
         const int row = quad * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         int item = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
             const int tile = w / rb_count, ri = w % rb_count;
@@ -378,27 +382,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int feat = ri * args.rb_mul * kTileRows + row;  // down: first of two blocks
             const bool second = ri * args.rb_mul + args.rb_second < rbs_per_e;  // down: partner exists
-            for (int c0 = 0; c0 < nn; c0 += 16) {
+            for (int c0 = half * 16; c0 < nn; c0 += 32) {
                 uint32_t g[16], u[16];
-                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, g);
-                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + 256 + c0, u);
+                tmem_ld16(trow + c0, g);
+                tmem_ld16(trow + 256 + c0, u);
+                tmem_ld_wait();
                 if (GATEUP) {
-                    tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < nn) {
                             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                            const float h = gv / (1.0f + __expf(-gv)) * uv;
+                            // silu(g) u; the result is rounded to fp16 next, so the
+                            // fast reciprocal division is ample
+                            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                             args.out[(size_t)(n0 + c0 + j) * args.out_ld + feat] =
-                                float_to_half_bits_sat(h);
+                                float_to_half_bits_sat(hv);
                         }
                     }
                 } else {
-                    tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < nn) {
-                            const float sw = args.slot_w[n0 + c0 + j];
+                            const float sw = __ldg(args.slot_w + n0 + c0 + j);
                             uint16_t* o = args.out + (size_t)(n0 + c0 + j) * args.out_ld + feat;
                             o[0] = float_to_half_bits_sat(__uint_as_float(g[j]) * sw);
                             if (second) o[kTileRows] = float_to_half_bits_sat(__uint_as_float(u[j]) * sw);
