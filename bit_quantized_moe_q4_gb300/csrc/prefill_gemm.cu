@@ -18,9 +18,11 @@
 // K-block, three decoupled rings:
 //   raw    the packed 4-bit tiles (4608 bytes each), two K-blocks of each
 //          weight block per bulk copy (contiguous in the packed layout), by
-//          the weight producer warp six K-blocks ahead (these come from HBM);
-//   A      the dequantised fp16 weights in the 128-byte-swizzled K-major
-//          layout the MMA reads, written by eight dequant warps;
+//          the weight producer warp ten K-blocks ahead (these come from HBM);
+//   A      the dequantised fp16 weights, in tensor memory (one weight row per
+//          TMEM lane, written by eight dequant warps with tcgen05.st; the MMA
+//          reads A from TMEM), which leaves shared memory to the two rings
+//          that wait on memory;
 //   B      the bucket's token rows, brought in by four token-loader warps
 //          with 16-byte cp.async copies straight into the 128-byte-swizzled
 //          layout (gate/up: rows of x picked by token id; down: consecutive
@@ -44,7 +46,6 @@ namespace moeq4 {
 namespace {
 
 constexpr int BN = 144;                 // max tokens per tile (buckets are cut evenly)
-constexpr int A_MAT_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
 constexpr int NUM_EPI_WARPS = 8, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
 constexpr int WARP_WPROD = 0, WARP_MMA = 1, WARP_B0 = 2;
@@ -61,15 +62,18 @@ template <bool GATEUP>
 struct Cfg {
     static constexpr int NMAT = 2;
     static constexpr int RK = 2;  // K-blocks per weight copy (contiguous tiles)
-    static constexpr int RAW_STAGES = 3;
-    static constexpr int A_STAGES = 2;
-    static constexpr int B_STAGES = 5;
+    static constexpr int RAW_STAGES = 5;
+    static constexpr int A_STAGES = 3;  // in tensor memory
+    static constexpr int B_STAGES = 7;
     static constexpr int RAW_BYTES = NMAT * RK * kTileBytes;
-    static constexpr int A_BYTES = NMAT * A_MAT_BYTES;
+    // tensor memory: accumulator m at column m * 256 (BN columns); A stage s
+    // of matrix m at column m * 256 + A_COL0 + s * 32 (64 fp16 per row, two
+    // per column), in the columns the accumulator leaves free
+    static constexpr int A_COL0 = 160;
     static constexpr int TMEM_COLS = NMAT * 256;
+    static_assert(BN <= A_COL0 && A_COL0 + A_STAGES * 32 <= 256, "tensor memory budget");
     // shared memory carve-up (offsets from a 1024-aligned base)
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + A_STAGES * A_BYTES;
+    static constexpr int OFF_B = 0;
     static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_RAW + RAW_STAGES * RAW_BYTES;
     static constexpr int NUM_BARS = 2 * (RAW_STAGES + A_STAGES + B_STAGES) + 3;
@@ -293,16 +297,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
                 if (lane == 0) {
-                    const uint32_t a_sm = base + C::OFF_A + sa * C::A_BYTES;
                     const uint32_t b_sm = base + C::OFF_B + sb * B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bdesc = sw128_kmajor_desc(b_sm + kk * 32);
 #pragma unroll
                         for (int m = 0; m < C::NMAT; ++m) {
-                            const uint64_t adesc =
-                                sw128_kmajor_desc(a_sm + m * A_MAT_BYTES + kk * 32);
-                            mma_f16(tmem + m * 256, adesc, bdesc, idesc, (kb | kk) != 0);
+                            const uint32_t a_t = tmem + m * 256 + C::A_COL0 + sa * 32 + kk * 8;
+                            mma_f16_ta(tmem + m * 256, a_t, bdesc, idesc, (kb | kk) != 0);
                         }
                     }
                     mma_commit(a_empty(sa));
@@ -322,43 +324,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp >= WARP_DEQ0) {
         // ------------------------------------------------------------ dequant
-        const int dt = threadIdx.x - WARP_DEQ0 * 32;  // 0..255
+        // thread = one weight row: warp w handles rows 32 (w % 4) .. +31 (its
+        // TMEM lane quarter) of matrix (w - WARP_DEQ0) / 4; per K-block it
+        // reads the row's 32 code bytes and 2 scales and writes its 64 fp16
+        // weights to the A stage in tensor memory (32 columns)
+        const int quad = warp % 4, mm = (warp - WARP_DEQ0) / 4;
+        const int r = quad * 32 + lane;
+        const uint32_t tlane = (uint32_t)(quad * 32) << 16;
         int it = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ir = it / C::RK, sub = it % C::RK;  // weight copy and its K-block
                 const int sr = ir % SR, sa = it % SA;
-                if (*abort_flag || !mbar_wait(raw_full(sr), (ir / SR) & 1) ||
-                    !mbar_wait(a_empty(sa), ((it / SA) & 1) ^ 1)) {
+                const bool bad = *abort_flag || !mbar_wait(raw_full(sr), (ir / SR) & 1) ||
+                                 !mbar_wait(a_empty(sa), ((it / SA) & 1) ^ 1);
+                if (__any_sync(0xffffffffu, bad)) {  // tcgen05.st below needs the whole warp
                     fail();
                     ok = false;
                     break;
                 }
-                const uint8_t* raw = sbase + C::OFF_RAW + sr * C::RAW_BYTES + sub * kTileBytes;
-                uint8_t* a = sbase + C::OFF_A + sa * C::A_BYTES;
-                // 8 consecutive threads read one row's 32 code bytes (a warp:
-                // 4 rows, 128 contiguous bytes) and write its 128-byte swizzled
-                // fp16 row
-                uint32_t words[C::NMAT * 4], scales[C::NMAT * 4];
-#pragma unroll
-                for (int i = 0; i < C::NMAT * 4; ++i) {
-                    const int q = dt + i * NUM_DEQ_WARPS * 32;
-                    const int m = q / 1024, r = (q / 8) % 128, c = q % 8;
-                    const uint8_t* t = raw + m * (C::RK * kTileBytes);
-                    words[i] = *reinterpret_cast<const uint32_t*>(t + r * 32 + c * 4);
-                    scales[i] = *reinterpret_cast<const uint16_t*>(t + kTileCodeBytes + r * 4 + (c / 4) * 2);
-                }
+                tc_fence_after();
+                const uint8_t* t = sbase + C::OFF_RAW + sr * C::RAW_BYTES +
+                                   mm * (C::RK * kTileBytes) + sub * kTileBytes;
+                const uint4 c0 = *reinterpret_cast<const uint4*>(t + r * 32);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(t + r * 32 + 16);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(t + kTileCodeBytes + r * 4);
                 __syncwarp();
                 if (lane == 0 && sub == C::RK - 1) mbar_arrive(raw_empty(sr));  // copy read
+                const uint32_t d0 = (sc & 0xFFFFu) * 0x10001u, d1 = (sc >> 16) * 0x10001u;
+                const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint32_t o[32];
 #pragma unroll
-                for (int i = 0; i < C::NMAT * 4; ++i) {
-                    const int q = dt + i * NUM_DEQ_WARPS * 32;
-                    const int m = q / 1024, r = (q / 8) % 128, c = q % 8;
-                    const uint4 o = dequant8(words[i], scales[i] | (scales[i] << 16));
-                    *reinterpret_cast<uint4*>(a + m * A_MAT_BYTES + r * 128 + ((c ^ (r & 7)) * 16)) = o;
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 v = dequant8(words[i], i < 4 ? d0 : d1);
+                    o[4 * i] = v.x;
+                    o[4 * i + 1] = v.y;
+                    o[4 * i + 2] = v.z;
+                    o[4 * i + 3] = v.w;
                 }
-                fence_proxy_async_smem();
+                tmem_st32(tmem + tlane + mm * 256 + C::A_COL0 + sa * 32, o);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(a_full(sa));
             }
@@ -375,7 +382,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
             const int tile = w / rb_count, ri = w % rb_count;
             const int n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
-            if (*abort_flag || !mbar_wait(acc_full, item & 1)) {
+            const bool bad = *abort_flag || !mbar_wait(acc_full, item & 1);
+            if (__any_sync(0xffffffffu, bad)) {  // tcgen05.ld below needs the whole warp
                 fail();
                 break;
             }
