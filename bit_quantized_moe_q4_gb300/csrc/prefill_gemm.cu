@@ -78,7 +78,10 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_RAW + RAW_STAGES * RAW_BYTES;
     static constexpr int NUM_BARS = 2 * (RAW_STAGES + A_STAGES + B_STAGES) + 3;
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;  // + alignment slack
+    // per epilogue warp: a 16-token x 32-feature fp16 transpose buffer
+    static constexpr int OFF_STAGE = (OFF_TMEM + 16 + 127) & ~127;
+    static_assert(OFF_STAGE % 128 == 0, "16-byte vector access into the transpose buffers");
+    static constexpr int SMEM_BYTES = OFF_STAGE + NUM_EPI_WARPS * 1024 + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -376,7 +379,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // thread); the two warps of a lane quarter take alternate 16-column
         // chunks, each loading 2 x 16 columns before one wait
         const int quad = warp % 4, half = (warp - WARP_EPI0) / 4;
-        const int row = quad * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         int item = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
@@ -388,8 +390,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int feat = ri * args.rb_mul * kTileRows + row;  // down: first of two blocks
             const bool second = ri * args.rb_mul + args.rb_second < rbs_per_e;  // down: partner exists
+            // 16 columns (tokens) x 32 rows (features) go through the warp's
+            // transpose buffer so that each lane stores 8 consecutive features
+            // of one token (16 bytes): two 16-byte stores per lane instead of
+            // sixteen 2-byte ones
+            uint16_t* stg = reinterpret_cast<uint16_t*>(sbase + C::OFF_STAGE) + (warp - WARP_EPI0) * 512;
+            const int fbase = ri * args.rb_mul * kTileRows + quad * 32;
+            auto flush = [&](int c0, int fo) {
+                __syncwarp();
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int tok = r * 8 + lane / 4, ch = lane % 4;
+                    const uint4 v = *reinterpret_cast<const uint4*>(stg + tok * 32 + ch * 8);
+                    if (c0 + tok < nn)
+                        *reinterpret_cast<uint4*>(args.out + (size_t)(n0 + c0 + tok) * args.out_ld +
+                                                  fbase + fo + ch * 8) = v;
+                }
+                __syncwarp();
+            };
             for (int c0 = half * 16; c0 < nn; c0 += 32) {
                 uint32_t g[16], u[16];
                 tmem_ld16(trow + c0, g);
@@ -398,24 +417,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (GATEUP) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        if (c0 + j < nn) {
-                            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                            // silu(g) u; the result is rounded to fp16 next, so the
-                            // fast reciprocal division is ample
-                            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                            args.out[(size_t)(n0 + c0 + j) * args.out_ld + feat] =
-                                float_to_half_bits_sat(hv);
-                        }
+                        const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+                        // silu(g) u; the result is rounded to fp16 next, so the
+                        // fast reciprocal division is ample
+                        const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                        stg[j * 32 + lane] = float_to_half_bits_sat(hv);
                     }
+                    flush(c0, 0);
                 } else {
+                    float sw[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (c0 + j < nn) {
-                            const float sw = __ldg(args.slot_w + n0 + c0 + j);
-                            uint16_t* o = args.out + (size_t)(n0 + c0 + j) * args.out_ld + feat;
-                            o[0] = float_to_half_bits_sat(__uint_as_float(g[j]) * sw);
-                            if (second) o[kTileRows] = float_to_half_bits_sat(__uint_as_float(u[j]) * sw);
-                        }
+                    for (int j = 0; j < 16; ++j)
+                        sw[j] = (c0 + j < nn) ? __ldg(args.slot_w + n0 + c0 + j) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        stg[j * 32 + lane] = float_to_half_bits_sat(__uint_as_float(g[j]) * sw[j]);
+                    flush(c0, 0);
+                    if (second) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            stg[j * 32 + lane] = float_to_half_bits_sat(__uint_as_float(u[j]) * sw[j]);
+                        flush(c0, kTileRows);
                     }
                 }
             }
