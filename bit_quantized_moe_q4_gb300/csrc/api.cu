@@ -170,6 +170,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.y = take(Tk * H * 2);
         w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.route_parts = reinterpret_cast<float*>(take(route_parts_floats(T, H, E) * 4));
+        w.wr_planes = reinterpret_cast<uint16_t*>(take(route_planes_bytes(T, H, E)));
         w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
     } else {
         int nsg = 1, nsd = 1;
@@ -273,7 +274,9 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
         // 1. route (also writes the fp16 copy of x)
         float* logits = dbg ? dbg->logits : nullptr;
         if ((rc = cuda_check(launch_route_gemm(xin, wr, T, H, E, k, ws.route_parts, logits,
-                                               ws.topk_idx, ws.topk_w, ws.x16, s),
+                                               ws.topk_idx, ws.topk_w, ws.x16,
+                                               route_planes_bytes(T, H, E) ? ws.wr_planes : nullptr,
+                                               dev->status, s),
                              "route")))
             return rc;
         if ((rc = mark(1))) return rc;

@@ -32,6 +32,7 @@ struct Workspace {
     uint16_t* xn;           // [T, H] bf16 RMSNorm(x) (stacked pre-norm layers)
     uint16_t* x16;          // [T, H] fp16 copy of x (prefill GEMM operand)
     float* route_parts;     // [ksplit, T, E] router K-slice sums (prefill)
+    uint16_t* wr_planes;    // [3, E, H] bf16 parts of W_r (prefill, tensor-core router)
     uint16_t* h;            // [T*k, I] fp16 (prefill)
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
@@ -65,11 +66,14 @@ cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E
                          float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s);
 // Router as a K-sliced fp32 GEMM into `parts` (route_parts_floats floats; H %
 // 16 == 0), then top-k; optionally writes the logits and the fp16 copy of x.
+// With `planes` (route_planes_bytes bytes; non-zero for prefill token
+// counts the tensor-core router takes) the product runs on the tensor cores.
 int route_ksplit(int T, int H, int E);
 size_t route_parts_floats(int T, int H, int E);
+size_t route_planes_bytes(int T, int H, int E);
 cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                               float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
-                              cudaStream_t s);
+                              uint16_t* planes, int* status, cudaStream_t s);
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
 cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,

@@ -19,6 +19,16 @@
 //          the CTA's warps pick the top-k (no buffer needed).
 //   small  one warp per expert over all tokens (T <= 32), spreading the
 //          router matrix over many SMs; a second kernel picks the top-k.
+//   tensor (prefill, T >= 128) the same K-sliced product on the tensor cores:
+//          W_r is first split exactly into three bf16 matrices
+//          (W_r = hi + mid + lo, each part the bf16 rounding of what the
+//          earlier parts leave), so every product of a bf16 x with a part is
+//          exact in the fp32 accumulator and the sum over the three parts is
+//          x W_r^T with fp32 accumulation, as in the fp32 kernels.  One CTA
+//          forms 128 experts x 128 tokens over one slice of the hidden
+//          dimension with tcgen05.mma (TMA-loaded 128-byte-swizzled tiles,
+//          accumulator in tensor memory); the top-k kernel of the gemm shape
+//          adds the slices in order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -309,9 +319,235 @@ __global__ void __launch_bounds__(256) topk_from_parts_kernel(const float* __res
     }
 }
 
+
+// ---- tensor-core router (prefill) -----------------------------------------
+constexpr int TC_M = 128;                          // experts per CTA (MMA M)
+constexpr int TC_N = 128;                          // tokens per CTA (MMA N)
+constexpr int TC_STAGES = 3;
+constexpr int TC_TILE_BYTES = 128 * 128;           // 128 rows x 64 bf16, swizzled
+constexpr int TC_STAGE_BYTES = 4 * TC_TILE_BYTES;  // three W_r parts + x
+constexpr int TC_OFF_BAR = TC_STAGES * TC_STAGE_BYTES;
+constexpr int TC_SMEM = TC_OFF_BAR + 128 + 1024;   // barriers, TMEM slot, alignment slack
+constexpr int TC_THREADS = 192;  // warp 0: TMA; warp 1: MMA; warps 2..5: x16 copy + epilogue
+constexpr int TC_SMS = 148;      // SM count the slice choice plans for
+constexpr int TC_MIN_T = 128;
+
+// planes[p][e][h], p = 0, 1, 2: w = planes[0] + planes[1] + planes[2] exactly
+// (bf16 keeps fp32's exponent range; each part takes the next 8 significant
+// bits of what is left).
+__global__ void __launch_bounds__(256) split_wr_kernel(const float* __restrict__ wr, int n4,
+                                                       uint16_t* __restrict__ planes) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(wr) + i);
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint16_t q[3][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float r = f[j];
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+            q[p][j] = float_to_bf16_bits(r);
+            r -= bf16_bits_to_float(q[p][j]);  // exact: the rounding error of the part
+        }
+    }
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+        reinterpret_cast<uint2*>(planes + (size_t)p * n4 * 4)[i] =
+            make_uint2(q[p][0] | ((uint32_t)q[p][1] << 16), q[p][2] | ((uint32_t)q[p][3] << 16));
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an
+// fp32 accumulator of M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// parts[split][t][e] for experts e0..e0+127 and tokens t0..t0+127 over the
+// hidden slice of this CTA.  tm_w maps the three parts as one [max(3E, 128),
+// H] bf16 tensor (the rows past 3E are padding), tm_x maps x as [T, H] (T >=
+// 128); rows past the end read as zero.  A box row past the CTA's part (the
+// next part, or padding) only feeds an accumulator row of an expert >= E,
+// which is not stored.  CTAs of the first expert block also write the fp16 copy of
+// their x slice.
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                     int T, int H, int E, int ksplit, float* __restrict__ parts,
+                     uint16_t* __restrict__ x16, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* sbase = smem_raw + (base - raw_base);
+    const int t0 = blockIdx.x * TC_N, e0 = blockIdx.y * TC_M, split = blockIdx.z;
+    const int nkb = H / (kTileK * ksplit), kb0 = split * nkb;
+    const bool conv = x16 != nullptr && blockIdx.y == 0;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr int S = TC_STAGES;
+    const uint32_t bar0 = base + TC_OFF_BAR;
+    auto full = [&](int st) { return bar0 + 8u * st; };
+    auto empty = [&](int st) { return bar0 + 8u * (S + st); };
+    const uint32_t acc_full = bar0 + 8u * (2 * S);
+    const uint32_t mma_done = acc_full + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + TC_OFF_BAR + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + TC_OFF_BAR + 68);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < S; ++st) {
+            mbar_init(full(st), 1);
+            mbar_init(empty(st), 1 + (conv ? 4 : 0));
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(base + TC_OFF_BAR + 64, TC_N);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        record_status(status, kStatusTimeout);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            int i = 0;
+            for (; i < nkb; ++i) {
+                const int st = i % S;
+                if (*abort_flag || !mbar_wait(empty(st), ((i / S) & 1) ^ 1)) {
+                    fail();
+                    break;
+                }
+                const uint32_t dst = base + st * TC_STAGE_BYTES;
+                const int kx = (kb0 + i) * kTileK;
+                mbar_arrive_expect_tx(full(st), TC_STAGE_BYTES);
+#pragma unroll
+                for (int p = 0; p < 3; ++p)
+                    tma_load_2d(dst + p * TC_TILE_BYTES, &tm_w, kx, p * E + e0, full(st));
+                tma_load_2d(dst + 3 * TC_TILE_BYTES, &tm_x, kx, t0, full(st));
+            }
+            // the copies already issued land before the CTA can go away
+            for (int j = (i > S ? i - S : 0); j < i; ++j) mbar_wait(full(j % S), (j / S) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        const uint32_t idesc = idesc_bf16_f32(TC_M, TC_N);
+        bool ok = true;
+        for (int i = 0; i < nkb; ++i) {
+            const int st = i % S;
+            if (*abort_flag || !mbar_wait(full(st), (i / S) & 1)) {
+                fail();
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sb = base + st * TC_STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bdesc = sw128_kmajor_desc(sb + 3 * TC_TILE_BYTES + kk * 32);
+#pragma unroll
+                    for (int p = 0; p < 3; ++p)
+                        mma_f16(tmem, sw128_kmajor_desc(sb + p * TC_TILE_BYTES + kk * 32), bdesc,
+                                idesc, (i | kk | p) != 0);
+                }
+                mma_commit(empty(st));
+            }
+            __syncwarp();
+        }
+        if (ok && lane == 0) mma_commit(acc_full);
+        // every MMA issued here completes before tensor memory is released
+        if (lane == 0) {
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------- x16 copy, epilogue
+        const int quad = warp % 4;
+        bool ok = true;
+        if (conv) {
+            const int ct = (warp - 2) * 32 + lane;  // 0..127
+            for (int i = 0; i < nkb && ok; ++i) {
+                const int st = i % S;
+                if (*abort_flag || !mbar_wait(full(st), (i / S) & 1)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                const uint8_t* xs = sbase + st * TC_STAGE_BYTES + 3 * TC_TILE_BYTES;
+                const int kx = (kb0 + i) * kTileK;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int q = ct + 128 * u, r = q / 8, c = q % 8;
+                    const uint4 v = *reinterpret_cast<const uint4*>(xs + r * 128 + ((c ^ (r & 7)) * 16));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t h4[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        h4[j] = (uint32_t)float_to_half_bits_sat(__uint_as_float(w4[j] << 16)) |
+                                ((uint32_t)float_to_half_bits_sat(__uint_as_float(w4[j] & 0xffff0000u)) << 16);
+                    if (t0 + r < T)
+                        *reinterpret_cast<uint4*>(x16 + (size_t)(t0 + r) * H + kx + c * 8) =
+                            make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(st));
+            }
+        }
+        const bool bad = !ok || *abort_flag || !mbar_wait(acc_full, 0);
+        if (__any_sync(0xffffffffu, bad)) {  // tcgen05.ld below needs the whole warp
+            fail();
+        } else {
+            tc_fence_after();
+            const int e = e0 + quad * 32 + lane;
+            float* out = parts + (size_t)split * T * E;
+            for (int c0 = 0; c0 < TC_N && t0 + c0 < T; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + c0 + j < T && e < E) out[(size_t)(t0 + c0 + j) * E + e] = __uint_as_float(v[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TC_N);
+}
+
+bool use_tc_router(int T) { return T >= TC_MIN_T; }
+
+// Slices of the hidden dimension: fewest waves x K-blocks per CTA, fewer
+// slices on a tie.
+int tc_ksplit(int T, int H, int E) {
+    const int tiles = ((T + TC_N - 1) / TC_N) * ((E + TC_M - 1) / TC_M);
+    int best = 1;
+    long best_cost = -1;
+    for (int ks = 1; ks <= 8; ks *= 2) {
+        if (H % (kTileK * ks)) break;
+        const long waves = (tiles * ks + TC_SMS - 1) / TC_SMS;
+        const long cost = waves * (H / (kTileK * ks));
+        if (best_cost < 0 || cost < best_cost) {
+            best = ks;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
 }  // namespace
 
 int route_ksplit(int T, int H, int E) {
+    if (use_tc_router(T)) return tc_ksplit(T, H, E);
     const int ctas = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
     int s = 1;
     while (s < 8 && ctas * s * 2 <= 2 * 152 && H % (GK * s * 2) == 0) s *= 2;
@@ -320,10 +556,33 @@ int route_ksplit(int T, int H, int E) {
 
 size_t route_parts_floats(int T, int H, int E) { return (size_t)route_ksplit(T, H, E) * T * E; }
 
+int tc_plane_rows(int E) { return 3 * E > TC_M ? 3 * E : TC_M; }
+
+size_t route_planes_bytes(int T, int H, int E) {
+    return use_tc_router(T) ? (size_t)tc_plane_rows(E) * H * 2 : 0;
+}
+
 cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                               float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
-                              cudaStream_t s) {
+                              uint16_t* planes, int* status, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (planes != nullptr && parts != logits && use_tc_router(T)) {
+        const int ks = tc_ksplit(T, H, E);
+        const int n4 = E * H / 4;
+        split_wr_kernel<<<(n4 + 255) / 256, 256, 0, s>>>(wr, n4, planes);
+        CUtensorMap tm_w, tm_x;
+        if (!encode_tmap_2d_f16(&tm_w, planes, (uint64_t)tc_plane_rows(E), H, kTileK, TC_M, true) ||
+            !encode_tmap_2d_f16(&tm_x, x, T, H, kTileK, TC_N, true))
+            return cudaErrorInvalidValue;
+        cudaError_t err = cudaFuncSetAttribute(router_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (err != cudaSuccess) return err;
+        const dim3 grid((T + TC_N - 1) / TC_N, (E + TC_M - 1) / TC_M, ks);
+        router_tc_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(tm_w, tm_x, T, H, E, ks, parts, x16,
+                                                           status);
+        topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k, logits, idx, w);
+        return cudaGetLastError();
+    }
     // with the logits buffer as the only part, the sums are already in place
     const int ks = (parts == logits) ? 1 : route_ksplit(T, H, E);
     const dim3 grid((T + GT - 1) / GT, (E + GE - 1) / GE, ks);
@@ -338,7 +597,8 @@ cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E
                          float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (logits && !x16 && T > 32 && (H % GK) == 0)
-        return launch_route_gemm(x, wr, T, H, E, k, logits, logits, idx, w, nullptr, s);
+        return launch_route_gemm(x, wr, T, H, E, k, logits, logits, idx, w, nullptr, nullptr, nullptr,
+                                 s);
     if (logits && !x16 && T <= 32 && (H % 128) == 0) {
         const dim3 grid((E + 3) / 4);
         if (T <= 4)

@@ -150,6 +150,34 @@ def test_route_small_token_path():
         check_routing(li, lg, idx, w)
 
 
+def _prefill_route(li):
+    dl = DeviceLayer(li)
+    d, dbg = moe.make_debug(moe.MOE_MODE_PREFILL, li.T, li.H, li.I, li.E, li.k)
+    dl.prefill(debug=dbg)
+    torch.cuda.synchronize()
+    return d["logits"].cpu().numpy(), d["topk_idx"].cpu().numpy(), d["topk_w"].cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill", "skewed"])
+def test_prefill_routing(name):
+    # the prefill forward routes with its own kernels (tensor cores from 128
+    # tokens on); its logits, choices and weights meet the same contract
+    li = workloads.CONFIGS[name]()
+    near = check_routing(li, *_prefill_route(li))
+    assert near <= max(2, li.T // 50), f"{near} near-tie tokens"
+
+
+@pytest.mark.parametrize("T,H,E,k", [
+    (128, 256, 2, 1),     # one token tile; three parts of W_r fill less than one box
+    (300, 384, 3, 2),     # ragged token tile, E not a multiple of 4
+    (260, 256, 256, 8),   # two expert blocks
+    (1000, 128, 129, 4),  # one hidden K-block per slice, an expert block of one
+])
+def test_prefill_routing_shapes(T, H, E, k):
+    li = workloads.make_layer("proute", T, H, 128, E, k, seed=T + E, wr_std=0.1)
+    check_routing(li, *_prefill_route(li))
+
+
 @pytest.mark.parametrize("name", ["tiny", "prefill", "skewed"])
 def test_bucketing_bit_exact(name):
     li = workloads.CONFIGS[name]()
