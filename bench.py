@@ -31,10 +31,10 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel as
 # it is in this tree: the decode expert kernel (T=1) and the prefill gate/up
 # GEMM (T=2048).  Set to None when the kernel changes before a new capture.
-NCU_TRAFFIC_DECODE_EXPERTS_T1 = 21_377_792
-NCU_TRAFFIC_PREFILL_GATEUP = 235_081_984 + 7_198_208
-KERNELS_PER_DECODE_LAYER = 3   # route (router, top-k, buckets, x codes); experts (gate/up, down); combine
-KERNELS_PER_PREFILL_LAYER = 8  # router GEMM, top-k, 3 bucketing, gate/up, down, combine
+NCU_TRAFFIC_DECODE_EXPERTS_T1 = None
+NCU_TRAFFIC_PREFILL_GATEUP = 235_103_744 + 6_745_856
+KERNELS_PER_DECODE_LAYER = 2   # layer (router, top-k, buckets, x codes, gate/up, down); combine
+KERNELS_PER_PREFILL_LAYER = 9  # W_r split, router GEMM, top-k, 3 bucketing, gate/up, down, combine
 
 
 def load_peaks():
@@ -157,12 +157,12 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
     ms_step = t0.elapsed_time(t1) / steps
     barrier()
     # per-kernel durations of the last layer of each replay (stage events)
-    rt_ms, ex_ms = [], []
+    ex_ms, cb_ms = [], []
     for _ in range(steps):
         g.replay()
         torch.cuda.synchronize()
-        rt_ms.append(stages.ms(0, 1))
-        ex_ms.append(stages.ms(3, 4))
+        ex_ms.append(stages.ms(0, 1))
+        cb_ms.append(stages.ms(5, 6))
     # end to end: pinned host x in, graph, last layer's output back to the host
     x_host = torch.empty((T, li.H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
@@ -191,13 +191,14 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
         "distinct_experts": distinct,
         "algorithmic_bytes_per_layer": layer_bytes,
         "layer_gbs": layer_bytes / (ms_step / L * 1e-3) / 1e9,
-        "route_us": statistics.mean(rt_ms) * 1e3, "experts_us": statistics.mean(ex_ms) * 1e3,
-        "gateup_bytes": gu_bytes, "down_bytes": dn_bytes,
+        # the layer kernel: routing, then gate/up and down
+        "experts_us": statistics.mean(ex_ms) * 1e3, "combine_us": statistics.mean(cb_ms) * 1e3,
+        "gateup_bytes": gu_bytes, "down_bytes": dn_bytes, "router_bytes": li.E * li.H * 4,
         "e2e_us_per_token": e2e_ms * 1e3 / (L * T),
         "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 4,
         "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
     }
-    res["experts_gbs"] = (gu_bytes + dn_bytes) / (res["experts_us"] * 1e-6) / 1e9
+    res["experts_gbs"] = (gu_bytes + dn_bytes + li.E * li.H * 4) / (res["experts_us"] * 1e-6) / 1e9
     del layers, outs, ws, g
     torch.cuda.empty_cache()
     return res
@@ -434,7 +435,8 @@ def main():
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": roof_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_DECODE_EXPERTS_T1,
                      "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": d1["gateup_bytes"] + d1["down_bytes"],
+                     "algorithmic_bytes_per_launch": d1["gateup_bytes"] + d1["down_bytes"] +
+                                                     d1["router_bytes"],
                      "launch_us": d1["experts_us"]},
         "e2e": {"value": e2e_ms * 1e3 / (d1["layers_per_step"] * world), "unit": "µs/token",
                 "h2d_bytes_per_step": d1["h2d_bytes_per_step"],

@@ -182,6 +182,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
         w.done = reinterpret_cast<int32_t*>(take((size_t)E * 4));
+        w.gbar = reinterpret_cast<int32_t*>(take(2 * 4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;

@@ -8,23 +8,30 @@
 // sum q*a (codes unsigned, activations signed) minus 8 * sum a, both exact in
 // int32 (|G| <= 32 * 8 * 127).  A row is sum_g d_w[g] * d_a[g] * G[g] in fp32.
 //
-// One decode layer is three kernels chained with programmatic dependent launch
-// (each next grid is resident, and has issued its weight-only loads, before
-// its predecessor ends):
+// One decode layer is two kernels chained with programmatic dependent launch
+// (each next grid is scheduled, and waits, before its predecessor ends):
 //
-//   route    a thread-block cluster.  Each warp reads one router row into
-//            registers before waiting for the preceding work (the router does
-//            not depend on it), then forms that expert's logits for all tokens
-//            and writes them into the leader CTA's shared memory (distributed
-//            shared memory).  The cluster also quantises x to int8 per 32.
-//            After a cluster barrier the leader picks the top-k and the
-//            softmax weights (one warp per token), builds the expert buckets
-//            (one thread per expert: bitmask, popcount, block scan) and clears
-//            the completion counters the expert kernel uses.  With few
-//            (token, slot) pairs one warp does the bucketing with shuffles.
-//
-//   experts  one CTA per SM, launched cooperatively (all CTAs resident: they
-//            wait on one another).  The packed weights of every touched expert
+//   layer    one CTA per SM, launched cooperatively (all CTAs resident: they
+//            wait on one another).  It starts with the routing:
+//              - CTA b owns router rows [bE/G, (b+1)E/G) (at most two); it
+//                stages them into shared memory with one bulk copy before
+//                waiting for the preceding work (the router does not depend
+//                on it), then forms their logits for every token (fixed
+//                summation order: per thread over its columns, then over the
+//                lanes, then over the warps) and writes them to global memory;
+//              - every CTA quantises x to int8 per 32 columns straight into
+//                its own shared memory (the activations every gate/up task
+//                reads), so no CTA waits for another's codes;
+//              - one grid barrier (an arrival counter and a generation word,
+//                bounded wait) publishes the logits;
+//              - every CTA then reads all T x E logits and takes the same
+//                decisions itself: top-k and softmax weights (one warp per
+//                token), the expert buckets (a token bitmask per expert,
+//                block scans for the offsets and the touched list).  CTA 0
+//                also stores the routing results for the combine and the
+//                debug outputs.
+//            Then the expert work:
+//            The packed weights of every touched expert
 //            are cut into tasks of whole 4608-byte tiles: one 128-row block
 //            times a range of 64-column blocks (the K range is split in
 //            `ns` parts when there are too few row blocks to keep every SM
@@ -52,13 +59,16 @@
 // Every weight byte of a touched expert is read once, by one CTA, from
 // contiguous 4608-byte tiles.  Every wait is bounded; on expiry the kernel
 // records MOE_ERR_TIMEOUT and stops.
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moeq4 {
 namespace {
 
-constexpr int kRouteThreads = 256;            // 8 warps per cluster CTA
+constexpr int kMaxRouteRows = 2;              // router rows per CTA (E <= 2 x CTAs)
 constexpr int kConsumerWarps = 8;             // 8 warps x 16 rows = one 128-row block
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kExpertThreads = kConsumerThreads + 32;  // + one producer warp
@@ -78,7 +88,6 @@ constexpr int kMaxSplitD = 4;  // K parts of a down task
 // (rounded up to 16; the workspace slot behind d_x is at least that long).
 __host__ __device__ constexpr int act_scale_bytes(int T, int G) { return (T * G * 2 + 15) & ~15; }
 
-__host__ __device__ constexpr int align128(int v) { return (v + 127) & ~127; }
 
 struct DecodeArgs {
     const uint16_t* x;      // layer input as routed and multiplied
@@ -103,7 +112,7 @@ struct DecodeArgs {
     int8_t* q_h;
     uint16_t* d_h;
     float* gu_sum;      // [T*k, 2I] fp32 sums of gate (0..I-1) and up (I..2I-1) rows;
-                        // with a K split the parts are added into it (zeroed by route)
+                        // with a K split the parts are added into it (zeroed first)
     float* y_part;      // [nsd, T*k, H] fp32 partial sums of the weighted expert outputs
     int nsg, nsd;       // K splits of the gate/up and down tasks
     void* out;
@@ -112,6 +121,7 @@ struct DecodeArgs {
     int32_t* dots_d;
     int write_qh;       // 1: the CTA that owns down task (expert, 0) stores q_h / d_h
     int* status;
+    int* gbar;          // [2] grid barrier: arrival count (0 between calls; the combine clears it)
     // expert-kernel shared-memory plan (bytes from the dynamic base)
     int nslot;          // ring slots of kSlotBytes
     int off_bar, off_ax, off_ah;
@@ -128,11 +138,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // (mask 0x0F0F0F0F) are columns 0,4,1,5 and the high nibbles 2,6,3,7.
 __device__ __forceinline__ uint2 permute_chunk(uint32_t a, uint32_t b) {
     return make_uint2(__byte_perm(a, b, 0x5140), __byte_perm(a, b, 0x7362));
-}
-// Byte position of column c (0..31) of a group in that permuted order.
-__device__ __forceinline__ int permuted_pos(int c) {
-    const int cc = c & 7;
-    return (c & ~7) + (cc & 3) * 2 + (cc >> 2);
 }
 
 // Group dot of one packed 32-code group (4 words) with one staged activation
@@ -163,291 +168,31 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
-// ---------------------------------------------------------------- route
-// For T <= 8 at most 104 registers a thread (256 x 104 = 26,624): the CTA fits beside
-// an expert CTA (288 threads x 128 registers) on the same SM, so the next
-// layer's router becomes resident while the current layer streams its
-// weights.
-template <int TM>
-__global__ void __maxnreg__(TM <= 8 ? 104 : 224) decode_route_kernel(const DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t dsm[];  // x bf16 [T][H], then logits [T][E] fp32
-    __shared__ int s_idx[MOE_DECODE_MAX_T * MOE_MAX_TOPK];
-    __shared__ float s_w[MOE_DECODE_MAX_T * MOE_MAX_TOPK];
-    __shared__ uint32_t s_mask[kMaxExperts];
-    __shared__ int s_off[kMaxExperts];
-    __shared__ __align__(8) uint64_t s_xbar;
-    const int T = a.T, H = a.H, E = a.E, k = a.k;
-    uint16_t* sx = reinterpret_cast<uint16_t*>(dsm);
-    float* s_logits = reinterpret_cast<float*>(dsm + (size_t)T * H * 2);  // used in the leader
-    const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int W = (int)ncta * (kRouteThreads / 32);
-    const int gw = (int)rank * (kRouteThreads / 32) + warp;
-    const uint32_t xbar = smem_u32(&s_xbar);
-    if (threadIdx.x == 0) {
-        mbar_init(xbar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    // This warp's first router row (its first 2048 columns) does not depend
-    // on the preceding work: request it before waiting.
-    constexpr int kWl = 16;  // float4 per lane per pass (2048 columns)
-    float4 wpre[kWl];
-    if (gw < E) {
-        const float* row = a.wr + (size_t)gw * H;
+// Exclusive prefix sum over the 256 consumer threads (thread order); `wt` is
+// eight ints of shared memory.  Every consumer thread calls it.
+__device__ __forceinline__ int consumers_exclusive_scan(int v, int* total, int* wt) {
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int incl = v;
 #pragma unroll
-        for (int i = 0; i < kWl; ++i) {
-            const int c = lane * 4 + 128 * i;
-            if (c < H) wpre[i] = __ldg(reinterpret_cast<const float4*>(row + c));
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
-    pdl_wait();     // x and the workspace belong to this call from here on
-    pdl_trigger();  // the expert grid may be scheduled; it waits for our end
-    // the gate/up sums are accumulated over K parts by the expert kernel
-    if (a.nsg > 1) {
-        float4* z = reinterpret_cast<float4*>(a.gu_sum);
-        const int n4 = T * k * 2 * a.I / 4;
-        for (int i = (int)rank * kRouteThreads + threadIdx.x; i < n4; i += (int)ncta * kRouteThreads)
-            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 31) wt[warp] = incl;
+    consumers_sync();
+    int base = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+        if (w < warp) base += wt[w];
+        all += wt[w];
     }
-    // x into shared memory with one bulk copy
-    if (threadIdx.x == 0) {
-        fence_proxy_async_global();
-        mbar_arrive_expect_tx(xbar, (uint32_t)(T * H * 2));
-        bulk_g2s(smem_u32(sx), a.x, (uint32_t)(T * H * 2), xbar);
-    }
-    if (!mbar_wait(xbar, 0)) record_status(a.status, kStatusTimeout);
-
-    const uint32_t leader_logits = mapa_shared(smem_u32(s_logits), 0);
-    for (int e = gw; e < E; e += W) {
-        float acc[TM], acc2[TM];  // two chains per token (columns 4c..4c+1 and 4c+2..4c+3)
-#pragma unroll
-        for (int t = 0; t < TM; ++t) acc[t] = acc2[t] = 0.f;
-        const float* row = a.wr + (size_t)e * H;
-        for (int c0 = 0; c0 < H; c0 += 128 * kWl) {
-            if (!(e == gw && c0 == 0)) {
-#pragma unroll
-                for (int i = 0; i < kWl; ++i) {
-                    const int c = c0 + lane * 4 + 128 * i;
-                    if (c < H) wpre[i] = __ldg(reinterpret_cast<const float4*>(row + c));
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kWl; ++i) {
-                const int c = c0 + lane * 4 + 128 * i;
-                if (c < H) {
-                    const float4 wv = wpre[i];
-#pragma unroll
-                    for (int t = 0; t < TM; ++t) {
-                        if (t < T) {
-                            const uint2 xv = *reinterpret_cast<const uint2*>(sx + t * H + c);
-                            acc[t] = fmaf(__uint_as_float(xv.x << 16), wv.x, acc[t]);
-                            acc[t] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wv.y, acc[t]);
-                            acc2[t] = fmaf(__uint_as_float(xv.y << 16), wv.z, acc2[t]);
-                            acc2[t] = fmaf(__uint_as_float(xv.y & 0xffff0000u), wv.w, acc2[t]);
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < TM; ++t) {
-            if (t < T) {
-                const float v = warp_sum(acc[t] + acc2[t]);
-                if (lane == 0) st_cluster_f32(leader_logits + (uint32_t)(t * E + e) * 4u, v);
-            }
-        }
-    }
-    // The logits are in the leader's shared memory once every CTA has
-    // arrived (release); the int8 quantisation of x runs while the barrier
-    // completes (its results are read only by the next kernel).
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    const int G = H / kGroup;
-    for (int q = gw; q < T * G; q += W) {
-        const int t = q / G, g = q % G;
-        const float v = bf16_bits_to_float(sx[t * H + g * kGroup + lane]);
-        const float amax = warp_max(fabsf(v));
-        const uint16_t db = act_scale_bits(amax);
-        a.q_x[(size_t)t * H + g * kGroup + lane] = (int8_t)act_code(v, half_bits_to_float(db));
-        if (lane == 0) a.d_x[(size_t)t * G + g] = db;
-    }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (rank != 0) return;
-
-    // ---- leader CTA: top-k, weights, buckets, counters ----
-    const int tid = threadIdx.x;
-    const int Tk = T * k;
-    if (T <= 2) {
-        // Every thread: the rank of (token, expert) pairs among the token's
-        // E logits (two threads per pair, half the experts each); the pairs
-        // of rank < k are the choices, in rank order.  Then one thread per
-        // (token, slot) pair and one per expert build the buckets; no loop
-        // carries a dependence from one expert or pair to the next.
-        __shared__ float s_val[2 * MOE_MAX_TOPK];
-        for (int base = 0; base < 2 * T * E; base += kRouteThreads) {  // whole warps take part
-            const int p2 = base + tid;
-            const bool act = p2 < 2 * T * E;
-            const int p = act ? p2 >> 1 : 0, half = p2 & 1;
-            const int t = p / E, e = p % E;
-            const float* lg = s_logits + t * E;
-            const float v = lg[e];
-            int rank = 0;
-            const int e0 = half ? E / 2 : 0, e1 = act ? (half ? E : E / 2) : 0;
-#pragma unroll 16
-            for (int e2 = e0; e2 < e1; ++e2) {
-                const float v2 = lg[e2];
-                rank += (v2 > v) || (v2 == v && e2 < e);
-            }
-            rank += __shfl_xor_sync(0xffffffffu, rank, 1);  // pair of threads
-            if (act && !half && rank < k) {
-                s_idx[t * k + rank] = e;
-                s_val[t * k + rank] = v;
-            }
-        }
-        for (int e = tid; e < E; e += kRouteThreads) a.done[e] = 0;
-        __syncthreads();
-        // weights: softmax over the token's k chosen logits; bucket rows
-        if (tid < Tk) {
-            const int t = tid / k;
-            const float m = s_val[t * k];
-            float den = 0.f;
-            for (int j = 0; j < k; ++j) den += expf(s_val[t * k + j] - m);
-            const float w = expf(s_val[tid] - m) / den;
-            s_w[tid] = w;
-            a.topk_idx[tid] = s_idx[tid];
-            a.topk_w[tid] = w;
-        }
-        for (int i = tid; i < T * E; i += kRouteThreads) a.logits[i] = s_logits[i];
-        __syncthreads();
-        if (T == 1) {
-            // One token: its k experts are distinct, so an expert's bucket
-            // offset is the number of chosen experts below it, which is also
-            // a chosen expert's index in the touched list and its bucket row.
-            for (int e = tid; e <= E; e += kRouteThreads) {
-                int lt = 0;
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_TOPK; ++j) lt += (j < k) && s_idx[j] < e;
-                a.offsets[e] = lt;
-            }
-            if (tid < k) {
-                const int ex = s_idx[tid];
-                int pos = 0;
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_TOPK; ++j) pos += (j < k) && s_idx[j] < ex;
-                a.touched[pos] = ex;
-                a.bucket_token[pos] = 0;
-                a.bucket_slot[pos] = tid;
-                a.slot_w[pos] = s_w[tid];
-                a.slot_pos[tid] = pos;
-            }
-            if (tid == 0) a.counters[kCntTouched] = k;
-            return;
-        }
-        __syncthreads();
-    } else {
-        for (int t = warp; t < T; t += kRouteThreads / 32) {
-            int si;
-            float sw;
-            warp_topk(s_logits + t * E, E, k, si, sw);
-            if (lane < k) {
-                s_idx[t * k + lane] = si;
-                s_w[t * k + lane] = sw;
-                a.topk_idx[t * k + lane] = si;
-                a.topk_w[t * k + lane] = sw;
-            }
-        }
-        for (int i = tid; i < T * E; i += kRouteThreads) a.logits[i] = s_logits[i];
-        for (int e = tid; e < E; e += kRouteThreads) a.done[e] = 0;
-        __syncthreads();
-    }
-    if (Tk <= 32) {
-        // One warp: counts per expert, a warp scan over the experts (eight
-        // per lane) for the offsets and the list of touched experts, and each
-        // (token, slot) pair's row: its expert's offset plus the number of
-        // lower lanes (= earlier tokens) that chose the same expert.
-        if (warp != 0) return;
-        for (int e = lane; e < kMaxExperts; e += 32) s_off[e] = 0;
-        __syncwarp();
-        const bool act = lane < Tk;
-        const int ex = act ? s_idx[lane] : 0;
-        if (act) atomicAdd(&s_off[ex], 1);
-        __syncwarp();
-        constexpr int EPL = kMaxExperts / 32;
-        int cnt[EPL];
-        int tot = 0, ntl = 0;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane * EPL + i;
-            cnt[i] = e < E ? s_off[e] : 0;
-            tot += cnt[i];
-            ntl += cnt[i] > 0;
-        }
-        int inc = tot, incn = ntl;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, inc, o);
-            const int vn = __shfl_up_sync(0xffffffffu, incn, o);
-            if (lane >= o) {
-                inc += v;
-                incn += vn;
-            }
-        }
-        int base = inc - tot, nbase = incn - ntl;
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane * EPL + i;
-            if (e < E) {
-                s_off[e] = base;
-                a.offsets[e] = base;
-                if (cnt[i] > 0) a.touched[nbase++] = e;
-                base += cnt[i];
-            }
-        }
-        if (lane == 31) {
-            a.offsets[E] = inc;
-            a.counters[kCntTouched] = incn;
-        }
-        __syncwarp();
-        const unsigned same = __match_any_sync(0xffffffffu, act ? ex : -1 - lane);
-        if (act) {
-            const int pos = s_off[ex] + __popc(same & ((1u << lane) - 1u));
-            a.bucket_token[pos] = lane / k;
-            a.bucket_slot[pos] = lane % k;
-            a.slot_w[pos] = s_w[lane];
-            a.slot_pos[lane] = pos;
-        }
-        return;
-    }
-    for (int e = tid; e < kMaxExperts; e += kRouteThreads) s_mask[e] = 0u;
-    __syncthreads();
-    // token t's bit in the mask of each expert it chose (T <= 32)
-    for (int p = tid; p < Tk; p += kRouteThreads) atomicOr(&s_mask[s_idx[p]], 1u << (p / k));
-    __syncthreads();
-    const int e = tid;  // one thread per expert (E <= 256)
-    const int cnt = (e < E) ? __popc(s_mask[e]) : 0;
-    int total, ntouched;
-    const int off = block256_exclusive_scan(cnt, &total);
-    const int tpos = block256_exclusive_scan(cnt > 0 ? 1 : 0, &ntouched);
-    if (e < E) {
-        s_off[e] = off;
-        a.offsets[e] = off;
-        if (cnt > 0) a.touched[tpos] = e;
-    }
-    if (tid == 0) {
-        a.offsets[E] = total;
-        a.counters[kCntTouched] = ntouched;
-    }
-    __syncthreads();
-    for (int p = tid; p < Tk; p += kRouteThreads) {
-        const int t = p / k, j = p % k, ex = s_idx[p];
-        const int pos = s_off[ex] + __popc(s_mask[ex] & ((1u << t) - 1u));
-        a.bucket_token[pos] = t;
-        a.bucket_slot[pos] = j;
-        a.slot_w[pos] = s_w[p];
-        a.slot_pos[p] = pos;
-    }
+    consumers_sync();
+    *total = all;
+    return base + incl - v;
 }
 
 // -------------------------------------------------------------- experts
@@ -456,8 +201,7 @@ struct IntC {
     static constexpr int value = N;
 };
 
-// At most 128 registers a thread, so that a route CTA of the next layer fits
-// beside this CTA on its SM.
+// At most 128 registers a thread.
 __global__ void __maxnreg__(128)
     decode_experts_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -469,6 +213,15 @@ __global__ void __maxnreg__(128)
     __shared__ volatile int s_cok[2];
     __shared__ volatile int s_abort;
     __shared__ __align__(8) uint64_t s_actbar;
+    // routing (every CTA holds the whole decision)
+    __shared__ float s_part[MOE_DECODE_MAX_T * kConsumerWarps * kMaxRouteRows];
+    __shared__ int s_idx[MOE_DECODE_MAX_T * MOE_MAX_TOPK];
+    __shared__ float s_w[MOE_DECODE_MAX_T * MOE_MAX_TOPK];
+    __shared__ int s_btok[MOE_DECODE_MAX_T * MOE_MAX_TOPK];   // bucket rows: token
+    __shared__ float s_bsw[MOE_DECODE_MAX_T * MOE_MAX_TOPK];  // bucket rows: routing weight
+    __shared__ uint32_t s_mask[kMaxExperts];
+    __shared__ int s_off[kMaxExperts + 1];
+    __shared__ int s_wt[kConsumerWarps];
 
     const int T = a.T, H = a.H, I = a.I, k = a.k;
     const int KBg = H / kTileK, KBd = I / kTileK;  // 64-column blocks per row
@@ -489,7 +242,16 @@ __global__ void __maxnreg__(128)
     float* ah_d = reinterpret_cast<float*>(ah_q + (size_t)T * I);
     int* ah_s = reinterpret_cast<int*>(ah_d + T * Gh);
 
+    const int E = a.E, G = gridDim.x, b = blockIdx.x;
+    auto fail = [&]() {
+        record_status(a.status, kStatusTimeout);
+        s_abort = 1;
+    };
     const uint32_t actbar = smem_u32(&s_actbar);
+    // router rows of this CTA, staged in the (still unused) ring area
+    const int eb0 = (int)((long long)b * E / G), eb1 = (int)((long long)(b + 1) * E / G);
+    const int ne = eb1 - eb0;  // <= kMaxRouteRows (checked at launch)
+    const float* s_wr = reinterpret_cast<const float*>(dsm);
     if (tid == 0) {
         for (int s = 0; s < kMaxSlots; ++s) {
             mbar_init(full_bar(s), 1);
@@ -498,34 +260,264 @@ __global__ void __maxnreg__(128)
         mbar_init(actbar, 1);
         s_abort = 0;
         fence_mbar_init();
+        if (ne > 0) {
+            mbar_arrive_expect_tx(actbar, (uint32_t)(ne * H * 4));
+            bulk_g2s(sbase, a.wr + (size_t)eb0 * H, (uint32_t)(ne * H * 4), actbar);
+        }
     }
-    pdl_wait();     // routing, buckets, x codes and cleared counters of this call
-    pdl_trigger();  // the next layer's router may be scheduled
-    for (int i = tid; i < kMaxExperts; i += kExpertThreads)
-        s_touched[i] = (i < a.E) ? a.touched[i] : 0;  // entries past n_touched are unused
-    if (tid == 0) s_nt = a.counters[kCntTouched];
+    __syncthreads();
+    pdl_wait();     // x and the workspace belong to this call from here on
+    pdl_trigger();  // the combine may be scheduled; it waits for our end
+    // this CTA's share of the completion counters and of the K-split sums
+    for (int i = eb0 + tid; i < eb1; i += kExpertThreads) a.done[i] = 0;
+    if (nsg > 1) {
+        const int n4 = Tk * 2 * I / 4;
+        float4* z = reinterpret_cast<float4*>(a.gu_sum);
+        for (int i = (int)((long long)b * n4 / G) + tid; i < (int)((long long)(b + 1) * n4 / G);
+             i += kExpertThreads)
+            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (warp != kWarpProducer) {
+        // logits of the CTA's router rows, and the int8 codes of x: thread
+        // unit u = 8 consecutive columns of one token; four consecutive
+        // lanes hold one 32-column group
+        if (ne > 0 && !mbar_wait(actbar, 0)) fail();
+        const int H8 = H / 8, nU = (H8 + 31) & ~31;
+        for (int t = 0; t < T; ++t) {
+            float acc[kMaxRouteRows] = {0.f, 0.f};
+            for (int u = tid; u < nU; u += kConsumerThreads) {  // warp-uniform bound
+                const bool valid = u < H8;
+                const uint4 xv = valid ? __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + u)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                float xf[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xf[2 * i] = __uint_as_float(xw[i] << 16);
+                    xf[2 * i + 1] = __uint_as_float(xw[i] & 0xffff0000u);
+                    amax = fmaxf(amax, fmaxf(fabsf(xf[2 * i]), fabsf(xf[2 * i + 1])));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const uint16_t db = act_scale_bits(amax);
+                const float d = half_bits_to_float(db);
+                uint32_t lo = 0u, hi = 0u;
+                int gsum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int q = act_code(xf[i], d);
+                    gsum += q;
+                    if (i < 4) lo |= ((uint32_t)q & 0xffu) << (8 * i);
+                    else hi |= ((uint32_t)q & 0xffu) << (8 * (i - 4));
+                }
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+                if (valid) {
+                    *reinterpret_cast<uint2*>(ax_q + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
+                    if ((lane & 3) == 0) {
+                        ax_dh[t * Gx + u / 4] = db;
+                        ax_s[t * Gx + u / 4] = gsum;
+                    }
+                    if (b == 0) {  // the codes as stage outputs
+                        *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
+                        if ((lane & 3) == 0) a.d_x[t * Gx + u / 4] = db;
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMaxRouteRows; ++r) {
+                        if (r < ne) {
+                            const float4 w0 = *reinterpret_cast<const float4*>(s_wr + r * H + u * 8);
+                            const float4 w1 = *reinterpret_cast<const float4*>(s_wr + r * H + u * 8 + 4);
+                            float v = acc[r];
+                            v = fmaf(xf[0], w0.x, v);
+                            v = fmaf(xf[1], w0.y, v);
+                            v = fmaf(xf[2], w0.z, v);
+                            v = fmaf(xf[3], w0.w, v);
+                            v = fmaf(xf[4], w1.x, v);
+                            v = fmaf(xf[5], w1.y, v);
+                            v = fmaf(xf[6], w1.z, v);
+                            v = fmaf(xf[7], w1.w, v);
+                            acc[r] = v;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kMaxRouteRows; ++r) {
+                const float v = warp_sum(acc[r]);
+                if (lane == 0) s_part[(t * kConsumerWarps + warp) * kMaxRouteRows + r] = v;
+            }
+        }
+        consumers_sync();
+        for (int q = tid; q < T * ne; q += kConsumerThreads) {
+            const int t = q / ne, r = q % ne;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) v += s_part[(t * kConsumerWarps + w) * kMaxRouteRows + r];
+            a.logits[(size_t)t * E + eb0 + r] = v;
+        }
+    }
+    // grid barrier: every CTA's logits and zeroed counters are published.
+    // The count is zero when the call starts (the combine of the previous
+    // call cleared it) and reaches G once every CTA has arrived.
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        red_release_add(a.gbar, 1);
+        const unsigned long long t0 = globaltimer_ns();
+        while (ld_acquire(a.gbar) < G) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                fail();
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    // every CTA: all logits -> top-k, weights and buckets (the same in every CTA)
+    float* s_lg = reinterpret_cast<float*>(dsm);  // [T][E], over the staged router rows
+    for (int i = tid; i < T * E; i += kExpertThreads) s_lg[i] = __ldcg(a.logits + i);
+    __syncthreads();
+    if (T == 1) {
+        // One token: expert e's rank among the E logits (larger first, equal
+        // logits by lower index); ranks below k are the choices.  Its k
+        // experts are distinct, so an expert's bucket offset is the number of
+        // chosen experts below it, which is also a chosen expert's row.
+        // Order keys rank every bit pattern (NaN included), so the ranks are
+        // a permutation of 0..E-1.
+        __shared__ float s_val[MOE_MAX_TOPK];
+        __shared__ float s_ex[MOE_MAX_TOPK];
+        __shared__ uint32_t s_key[kMaxExperts];
+        for (int e = tid; e < E; e += kExpertThreads) s_key[e] = float_order_key(s_lg[e]);
+        __syncthreads();
+        const int P = (2 * E <= kExpertThreads) ? 2 : 1;  // threads per expert
+        const int half = (E + 1) / 2;
+        for (int base = 0; base < P * E; base += kExpertThreads) {  // warp-uniform
+            const int q = base + tid;
+            const bool act = q < P * E;
+            const int e = act ? q / P : 0, part = q % P;
+            const uint32_t kv = s_key[e];
+            const int lo = (P == 2 && part == 1) ? half : 0;
+            const int hi = !act ? 0 : (P == 2 && part == 0) ? half : E;
+            int rank = 0;
+#pragma unroll 8
+            for (int e2 = lo; e2 < hi; ++e2) {
+                const uint32_t k2 = s_key[e2];
+                rank += (k2 > kv) | ((k2 == kv) & (e2 < e));
+            }
+            if (P == 2) rank += __shfl_xor_sync(0xffffffffu, rank, 1);  // the pair (2m, 2m + 1)
+            if (act && part == 0 && rank < k) {
+                s_idx[rank] = e;
+                s_val[rank] = s_lg[e];
+            }
+        }
+        __syncthreads();
+        if (tid < k) s_ex[tid] = expf(s_val[tid] - s_val[0]);
+        for (int e = tid; e <= E; e += kExpertThreads) {
+            int lt = 0;
+            for (int j = 0; j < k; ++j) lt += s_idx[j] < e;
+            s_off[e] = lt;
+            if (b == 0) a.offsets[e] = lt;
+        }
+        __syncthreads();
+        if (tid < k) {
+            float den = 0.f;
+            for (int j = 0; j < k; ++j) den += s_ex[j];
+            const float w = s_ex[tid] / den;
+            const int ex = s_idx[tid], pos = s_off[ex];
+            s_touched[pos] = ex;
+            s_btok[pos] = 0;
+            s_bsw[pos] = w;
+            if (b == 0) {
+                a.topk_idx[tid] = ex;
+                a.topk_w[tid] = w;
+                a.touched[pos] = ex;
+                a.bucket_token[pos] = 0;
+                a.bucket_slot[pos] = tid;
+                a.slot_w[pos] = w;
+                a.slot_pos[tid] = pos;
+            }
+        }
+        if (tid == 0) {
+            s_nt = k;
+            if (b == 0) a.counters[kCntTouched] = k;
+        }
+    } else if (warp != kWarpProducer) {
+        for (int t = warp; t < T; t += kConsumerWarps) {
+            int si;
+            float sw;
+            warp_topk(s_lg + t * E, E, k, si, sw);
+            if (lane < k) {
+                s_idx[t * k + lane] = si;
+                s_w[t * k + lane] = sw;
+            }
+        }
+        s_mask[tid] = 0u;  // kMaxExperts == kConsumerThreads
+        consumers_sync();
+        // token t's bit in the mask of each expert it chose (T <= 32)
+        for (int p = tid; p < Tk; p += kConsumerThreads) atomicOr(&s_mask[s_idx[p]], 1u << (p / k));
+        consumers_sync();
+        const int e = tid;  // one thread per expert (E <= 256)
+        const int cnt = (e < E) ? __popc(s_mask[e]) : 0;
+        int total, ntouched;
+        const int off = consumers_exclusive_scan(cnt, &total, s_wt);
+        const int tpos = consumers_exclusive_scan(cnt > 0 ? 1 : 0, &ntouched, s_wt);
+        if (e < E) {
+            s_off[e] = off;
+            if (cnt > 0) s_touched[tpos] = e;
+        }
+        if (tid == 0) {
+            s_off[E] = total;
+            s_nt = ntouched;
+        }
+        consumers_sync();
+        for (int p = tid; p < Tk; p += kConsumerThreads) {
+            const int t = p / k, ex = s_idx[p];
+            const int pos = s_off[ex] + __popc(s_mask[ex] & ((1u << t) - 1u));
+            s_btok[pos] = t;
+            s_bsw[pos] = s_w[p];
+            if (b == 0) {
+                a.topk_idx[p] = ex;
+                a.topk_w[p] = s_w[p];
+                a.bucket_token[pos] = t;
+                a.bucket_slot[pos] = p % k;
+                a.slot_w[pos] = s_w[p];
+                a.slot_pos[p] = pos;
+            }
+        }
+        if (b == 0) {
+            for (int i = tid; i <= E; i += kConsumerThreads) a.offsets[i] = s_off[i];
+            for (int i = tid; i < ntouched; i += kConsumerThreads) a.touched[i] = s_touched[i];
+            if (tid == 0) a.counters[kCntTouched] = ntouched;
+        }
+    }
+    // the ring area was used through generic accesses; bulk copies refill it next
+    fence_proxy_async_smem();
     __syncthreads();
     const int nt = s_nt;
-    const int G = gridDim.x, b = blockIdx.x;
     const int per_g = RBg * nsg, per_d = RBd * nsd;  // tasks per touched expert
     const int n_gu = nt * per_g, n_dn = nt * per_d;
-    const int gu0 = (int)((long long)b * n_gu / G), gu1 = (int)((long long)(b + 1) * n_gu / G);
-    const int dn0 = (int)((long long)b * n_dn / G), dn1 = (int)((long long)(b + 1) * n_dn / G);
-
-    auto fail = [&]() {
-        record_status(a.status, kStatusTimeout);
-        s_abort = 1;
-    };
+    // (32-bit products: launch_decode checks that G x the task counts fits)
+    const int gu0 = b * n_gu / G, gu1 = (b + 1) * n_gu / G;
+    const int dn0 = b * n_dn / G, dn1 = (b + 1) * n_dn / G;
 
     if (warp == kWarpProducer) {
         // ----------------------------------------------------------- producer
         // gate/up tasks, then down tasks; each task's tiles in chunks of up to
-        // kChunkTiles contiguous tiles, one bulk copy per chunk.
+        // kChunkTiles contiguous tiles, one bulk copy per chunk.  The down
+        // weights are requested once this CTA's gate/up weights have landed:
+        // every CTA's gate/up bytes then have the memory system to
+        // themselves, and the down bytes arrive while gate/up is computed
+        // and handed over.
         if (lane == 0) {
             int j = 0;  // ring position
             bool ok = true;
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 const bool gu = pass == 0;
+                if (!gu && j > 0 && dn1 > dn0 &&
+                    (s_abort || !mbar_wait(full_bar((j - 1) % a.nslot), ((j - 1) / a.nslot) & 1))) {
+                    fail();
+                    break;
+                }
                 const int t0 = gu ? gu0 : dn0, t1 = gu ? gu1 : dn1;
                 const int per = gu ? per_g : per_d, ns = gu ? nsg : nsd;
                 const int KB = gu ? KBg : KBd, KC = gu ? KCg : KCd, RB = gu ? RBg : RBd;
@@ -557,28 +549,7 @@ __global__ void __maxnreg__(128)
     }
 
     // -------------------------------------------------------------- consumers
-    // 1. the int8 codes of x (every token) and their fp16 scales: two bulk
-    //    copies, then the codes are permuted in place and summed per group
-    if (tid == 0) {
-        fence_proxy_async_global();
-        const uint32_t sb = (uint32_t)act_scale_bytes(T, Gx);  // rounded up to 16 bytes
-        mbar_arrive_expect_tx(actbar, (uint32_t)(T * H) + sb);
-        bulk_g2s(smem_u32(ax_q), a.q_x, (uint32_t)(T * H), actbar);
-        bulk_g2s(smem_u32(ax_dh), a.d_x, sb, actbar);
-    }
-    if (!mbar_wait(actbar, 0)) fail();
-    for (int i = tid; i < T * Gx; i += kConsumerThreads) {
-        uint2* g = reinterpret_cast<uint2*>(ax_q + (size_t)i * kGroup);
-        int sum = 0;
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            const uint2 v = g[c8];
-            sum = __dp4a((int)v.x, 0x01010101, sum);  // signed byte sum
-            sum = __dp4a((int)v.y, 0x01010101, sum);
-            g[c8] = permute_chunk(v.x, v.y);
-        }
-        ax_s[i] = sum;
-    }
+    // (the int8 codes of x are in shared memory since the routing phase)
     // Consumer control flow must stay uniform (the consumers share named
     // barriers): the task loops always run to their end, and a decision that
     // can differ between threads (a timed wait, the abort flag the producer
@@ -610,14 +581,14 @@ __global__ void __maxnreg__(128)
         consumers_sync();
         const int ex = s_touched[slot_i];
         if (tid == 0) {
-            s_route[0] = a.offsets[ex];
-            s_route[1] = a.offsets[ex + 1] - s_route[0];
+            s_route[0] = s_off[ex];
+            s_route[1] = s_off[ex + 1] - s_off[ex];
         }
         consumers_sync();
         const int off = s_route[0], c = s_route[1];
         if (tid < c) {
-            s_tok[tid] = a.bucket_token[off + tid];
-            s_sw[tid] = a.slot_w[off + tid];
+            s_tok[tid] = s_btok[off + tid];
+            s_sw[tid] = s_bsw[off + tid];
         }
         consumers_sync();
     };
@@ -740,40 +711,54 @@ __global__ void __maxnreg__(128)
             }
             have_h = agree(got);
             // h = silu(g) * u (partial sums added in K order), int8 per 32
+            // features: a warp takes four groups at once, eight lanes a group,
+            // four consecutive features a lane
             const int off = s_route[0], c = s_route[1];
             const bool store = a.write_qh && rb == 0 && kc == 0;
-            // four groups per warp at a time, every load first
-            for (int q0 = warp; q0 < (have_h ? c * Gh : 0); q0 += 4 * kConsumerWarps) {
-                float gv[4], uv[4];
+            const int sub = lane / 8, l8 = lane % 8;
+            for (int q0 = warp * 4; q0 < (have_h ? c * Gh : 0); q0 += 4 * kConsumerWarps) {
+                const int q = q0 + sub;
+                const bool ok = q < c * Gh;
+                const int n = ok ? q / Gh : 0, gg = ok ? q % Gh : 0, f0 = gg * kGroup + l8 * 4;
+                const float* gs = a.gu_sum + (size_t)(off + n) * 2 * I + f0;
+                const float4 g4 = ok ? __ldcg(reinterpret_cast<const float4*>(gs)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 u4 = ok ? __ldcg(reinterpret_cast<const float4*>(gs + I)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+                float h[4];
+                float amax = 0.f;
 #pragma unroll
-                for (int o = 0; o < 4; ++o) {
-                    const int q = q0 + o * kConsumerWarps;
-                    const bool ld = q < c * Gh;
-                    const float* gs = a.gu_sum + (size_t)(off + (ld ? q / Gh : 0)) * 2 * I +
-                                      (ld ? q % Gh : 0) * kGroup + lane;
-                    gv[o] = ld ? __ldcg(gs) : 0.f;
-                    uv[o] = ld ? __ldcg(gs + I) : 0.f;
+                for (int i = 0; i < 4; ++i) {
+                    h[i] = gv[i] / (1.0f + __expf(-gv[i])) * uv[i];
+                    amax = fmaxf(amax, fabsf(h[i]));
                 }
 #pragma unroll
-                for (int o = 0; o < 4; ++o) {
-                    const int q = q0 + o * kConsumerWarps;
-                    if (q >= c * Gh) continue;  // warp-uniform
-                    const int n = q / Gh, gg = q % Gh, f = gg * kGroup + lane;
-                    const float h = gv[o] / (1.0f + __expf(-gv[o])) * uv[o];
-                    const float amax = warp_max(fabsf(h));
-                    const uint16_t db = act_scale_bits(amax);
-                    const int qv = act_code(h, half_bits_to_float(db));
-                    ah_q[(size_t)n * I + gg * kGroup + permuted_pos(lane)] = (uint8_t)(int8_t)qv;
-                    int sum = qv;
+                for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const uint16_t db = act_scale_bits(amax);
+                const float d = half_bits_to_float(db);
+                uint32_t w4 = 0u;
+                int sum = 0;
 #pragma unroll
-                    for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-                    if (lane == 0) {
-                        ah_d[n * Gh + gg] = half_bits_to_float(db);
+                for (int i = 0; i < 4; ++i) {
+                    const int qv = act_code(h[i], d);
+                    sum += qv;
+                    w4 |= ((uint32_t)qv & 0xffu) << (8 * i);
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                // lanes 2m and 2m+1 hold columns 8m..8m+3 and 8m+4..8m+7 of the
+                // group: the even lane stores the chunk in the permuted order
+                const uint32_t w4o = __shfl_xor_sync(0xffffffffu, w4, 1);
+                if (ok) {
+                    if ((l8 & 1) == 0)
+                        *reinterpret_cast<uint2*>(ah_q + (size_t)n * I + gg * kGroup + l8 * 4) =
+                            permute_chunk(w4, w4o);
+                    if (l8 == 0) {
+                        ah_d[n * Gh + gg] = d;
                         ah_s[n * Gh + gg] = sum;
                     }
                     if (store) {
-                        a.q_h[(size_t)(off + n) * I + f] = (int8_t)qv;
-                        if (lane == 0) a.d_h[(size_t)(off + n) * Gh + gg] = db;
+                        *reinterpret_cast<uint32_t*>(a.q_h + (size_t)(off + n) * I + f0) = w4;
+                        if (l8 == 0) a.d_h[(size_t)(off + n) * Gh + gg] = db;
                     }
                 }
             }
@@ -792,8 +777,11 @@ __global__ void __maxnreg__(128)
 // down tasks (in order) of y_part[part][slot_pos[t, j]].  One output per
 // thread; all of a thread's loads are issued before the first add.
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
-    pdl_wait();     // the expert kernel's y parts
-    pdl_trigger();  // the next layer's router may be scheduled
+    pdl_wait();     // the layer kernel's y parts
+    pdl_trigger();  // the next layer may be scheduled
+    // the layer kernel has ended: its grid barrier count is zero again (also
+    // after a timed-out call)
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.gbar[0] = 0;
     const int H = a.H, k = a.k, nsd = a.nsd, Tk = a.T * a.k;
     const int q = blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= a.T * H) return;
@@ -824,39 +812,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
 
 // ---------------------------------------------------------------- launch
 int g_expert_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
-
-// Cluster size of the route kernel: 16 CTAs where the device can place such a
-// cluster, else the portable 8.  Cached per device and shared-memory size.
-template <int TM>
-int route_cluster_size(int dev, size_t smem) {
-    static int cache[64] = {};
-    static size_t cache_smem[64] = {};
-    int& cs = cache[dev & 63];
-    if (cs != 0 && cache_smem[dev & 63] == smem) return cs;
-    cache_smem[dev & 63] = smem;
-    cudaFuncSetAttribute(decode_route_kernel<TM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaFuncSetAttribute(decode_route_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    cudaLaunchConfig_t q{};
-    cudaLaunchAttribute qa[1];
-    q.gridDim = dim3(16);
-    q.blockDim = dim3(kRouteThreads);
-    q.dynamicSmemBytes = smem;
-    qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = 16;
-    qa[0].val.clusterDim.y = 1;
-    qa[0].val.clusterDim.z = 1;
-    q.attrs = qa;
-    q.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, decode_route_kernel<TM>, &q) == cudaSuccess &&
-        nclusters > 0)
-        cs = 16;
-    else
-        cs = 8;
-    cudaGetLastError();  // a refused query leaves no error behind
-    return cs;
-}
+int* g_gbar_seen[64] = {};  // per device: the last workspace whose barrier words were cleared
+std::mutex g_gbar_mu;
 
 // Smallest divisor of KB that is >= want; if that exceeds cap, the largest
 // divisor of KB that is <= cap.
@@ -892,6 +849,8 @@ bool plan_experts(DecodeArgs& a) {
     int ns = (kExpertSmemBudget - ax - ah - bars) / kSlotBytes;
     ns = ns > kMaxSlots ? kMaxSlots : ns;
     if (ns < 2) return false;
+    // the routing phase keeps the CTA's router rows, then all logits, in the ring
+    if (kMaxRouteRows * a.H * 4 > ns * kSlotBytes || a.T * a.E * 4 > ns * kSlotBytes) return false;
     a.nslot = ns;
     a.off_bar = ns * kSlotBytes;
     a.off_ax = al(a.off_bar + bars);
@@ -903,7 +862,6 @@ int expert_smem_bytes(const DecodeArgs& a) {
     return a.off_ah + ((a.T * a.I + a.T * (a.I / kGroup) * 8 + 127) & ~127);
 }
 
-template <int TM>
 cudaError_t launch_all(DecodeArgs& a, int num_sms, void** ev, bool capturing, cudaStream_t s) {
     cudaError_t err;
     int dev = 0;
@@ -914,37 +872,7 @@ cudaError_t launch_all(DecodeArgs& a, int num_sms, void** ev, bool capturing, cu
     cudaLaunchAttribute pdl{};
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl.val.programmaticStreamSerializationAllowed = 1;
-    // ---- route ----
-    const size_t rsm = (size_t)a.T * a.H * 2 + (size_t)a.T * a.E * 4;
-    const int cs = route_cluster_size<TM>(dev, rsm);
-    if (cs > 8) {
-        err = cudaFuncSetAttribute(decode_route_kernel<TM>,
-                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (err != cudaSuccess) return err;
-    }
-    err = cudaFuncSetAttribute(decode_route_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)rsm);
-    if (err != cudaSuccess) return err;
-    {
-        cudaLaunchConfig_t cfg{};
-        cudaLaunchAttribute at[2];
-        cfg.gridDim = dim3(cs);
-        cfg.blockDim = dim3(kRouteThreads);
-        cfg.dynamicSmemBytes = rsm;
-        cfg.stream = s;
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = cs;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        at[1] = pdl;
-        cfg.attrs = at;
-        cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, decode_route_kernel<TM>, a);
-        if (err != cudaSuccess) return err;
-    }
-    for (int i = 1; i <= 3; ++i)
-        if ((err = mark(i)) != cudaSuccess) return err;
-    // ---- experts ----
+    // ---- layer: routing and experts ----
     const int smem = expert_smem_bytes(a);
     err = cudaFuncSetAttribute(decode_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                smem);
@@ -963,7 +891,8 @@ cudaError_t launch_all(DecodeArgs& a, int num_sms, void** ev, bool capturing, cu
     cfg.numAttrs = (mode == 2) ? 1 : 2;
     err = cudaLaunchKernelEx(&cfg, decode_experts_kernel, a);
     if (err != cudaSuccess) return err;
-    if ((err = mark(4)) != cudaSuccess || (err = mark(5)) != cudaSuccess) return err;
+    for (int i = 1; i <= 5; ++i)
+        if ((err = mark(i)) != cudaSuccess) return err;
     // ---- combine ----
     {
         cudaLaunchConfig_t cc{};
@@ -1072,13 +1001,29 @@ cudaError_t launch_decode(const uint16_t* x, const uint16_t* x_res, const float*
     a.dots_d = dots_d;
     a.write_qh = write_qh ? 1 : 0;
     a.status = status;
+    a.gbar = ws.gbar;
     if (!plan_experts(a)) return cudaErrorInvalidValue;
-    if (T <= 1) return launch_all<1>(a, num_sms, events, capturing, s);
-    if (T <= 2) return launch_all<2>(a, num_sms, events, capturing, s);
-    if (T <= 4) return launch_all<4>(a, num_sms, events, capturing, s);
-    if (T <= 8) return launch_all<8>(a, num_sms, events, capturing, s);
-    if (T <= 16) return launch_all<16>(a, num_sms, events, capturing, s);
-    return launch_all<32>(a, num_sms, events, capturing, s);
+    if ((E + num_sms - 1) / num_sms > kMaxRouteRows) return cudaErrorInvalidValue;
+    {
+        const long long nt_max = E < T * k ? E : T * k;
+        const long long per = std::max((long long)(2 * I / kTileRows) * a.nsg,
+                                       (long long)(H / kTileRows) * a.nsd);
+        if ((long long)(num_sms + 1) * nt_max * per >= (1ll << 31)) return cudaErrorInvalidValue;
+    }
+    // The grid barrier's count must start at zero; every call leaves it
+    // there.  A workspace not seen before gets it cleared once.
+    {
+        std::lock_guard<std::mutex> lock(g_gbar_mu);
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (g_gbar_seen[dev & 63] != ws.gbar) {
+            err = cudaMemsetAsync(ws.gbar, 0, 2 * sizeof(int), s);
+            if (err != cudaSuccess) return err;
+            g_gbar_seen[dev & 63] = ws.gbar;
+        }
+    }
+    return launch_all(a, num_sms, events, capturing, s);
 }
 
 }  // namespace moeq4

@@ -37,6 +37,7 @@ struct Workspace {
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
     int32_t* done;          // [E]           (decode) finished gate/up tasks per touched expert
+    int32_t* gbar;          // [2]           (decode) grid barrier: arrival count, generation
     float* gu_sum;          // [T*k, 2I]     (decode) fp32 gate/up row sums, bucket order
     float* y_part;          // [nsd, T*k, H]  (decode) fp32 partial weighted expert outputs
     int8_t* q_x;            // [T, H]        (decode)
@@ -82,11 +83,11 @@ cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,
 cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
                                 int T, int H, int I, int E, int k, int* status, int num_sms,
                                 cudaStream_t s);
-// The whole W4A8 decode layer: a route kernel (router, top-k, buckets, x
-// codes), one cooperative expert kernel (gate/up, down) and a combine kernel.
-// `events` is null or the caller's MOE_NUM_STAGE_EVENTS events; boundaries
-// 1..3 are recorded after the route kernel, 4..5 after the expert kernel and
-// 6 after the combine.
+// The whole W4A8 decode layer: one cooperative layer kernel (router, top-k,
+// buckets and x codes in every CTA after one grid barrier, then gate/up and
+// down) and a combine kernel.  `events` is null or the caller's
+// MOE_NUM_STAGE_EVENTS events; boundaries 1..5 are recorded after the layer
+// kernel and 6 after the combine.
 cudaError_t launch_decode(const uint16_t* x, const uint16_t* x_res, const float* wr,
                           const void* wgu, const void* wd,
                           int T, int H, int I, int E, int k, bool out_fp32, void* out,
