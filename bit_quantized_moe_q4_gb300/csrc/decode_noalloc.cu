@@ -18,8 +18,10 @@
 // stream capture.  All calls share the one array: calls whose work overlaps
 // on the GPU (different streams, or different host threads on one device)
 // race on it.  The array keeps the last call's contents; nothing in it needs
-// to start at zero, because the decode path writes every scratch value it
-// reads earlier in the same call.
+// to start at zero: the decode path writes every scratch value it reads
+// earlier in the same call, except its grid-barrier counter, which the
+// decode call clears the first time it sees this scratch and every call
+// leaves at zero.
 #include <stdio.h>
 
 #include <mutex>

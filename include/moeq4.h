@@ -204,12 +204,19 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
  * stay under ~170 KB (MOE_ERR_SHAPE otherwise; T = 32 at H = 2048, I = 768
  * fits).  The int32 group dots are exact; the float sums run in fp32.
  *
- * The call launches three kernels that let their successors start early
- * (programmatic dependent launch).  Its first kernel reads `wr` before the
- * work that precedes it on the stream has finished, so `wr` must not be
- * written by the kernel launched immediately before this call on the same
- * stream; x, the output and the workspace are touched only after that work
- * has finished.  The expert kernel is a cooperative launch (one CTA per SM).
+ * The call launches two kernels that let their successors start early
+ * (programmatic dependent launch): a cooperative layer kernel (one CTA per
+ * SM: routing, then gate/up and down) and a combine.  The layer kernel reads
+ * `wr` before the work that precedes it on the stream has finished, so `wr`
+ * must not be written by the kernel launched immediately before this call
+ * on the same stream; x, the output and the workspace are touched only after
+ * that work has finished.  The layer kernel's CTAs meet once at a grid
+ * barrier whose counter lives in the workspace: it must be zero when a call
+ * starts, which the library arranges (it clears it the first time it sees a
+ * workspace address on a device, and every call leaves it at zero).  After a
+ * MOE_ERR_TIMEOUT, pass a workspace the library has not seen before (or the
+ * same one after the next call, whose combine clears the counter).  Routing
+ * needs E <= 2 x (number of SMs).
  * When few experts are touched (small T) the K range of the gate/up rows is
  * split and the parts are added in fp32 in the order they arrive, so the
  * last bits of h, and rarely an int8 code of h, may differ between runs.
