@@ -22,10 +22,11 @@
 //              - every CTA quantises x to int8 per 32 columns straight into
 //                its own shared memory (the activations every gate/up task
 //                reads), so no CTA waits for another's codes;
-//              - one grid barrier (an arrival counter and a generation word,
-//                bounded wait) publishes the logits;
+//              - one grid barrier (an arrival counter, bounded wait)
+//                publishes the logits; the codes of x are formed meanwhile;
 //              - every CTA then reads all T x E logits and takes the same
-//                decisions itself: top-k and softmax weights (one warp per
+//                decisions itself: top-k and softmax weights (one token:
+//                each expert's rank among the logits; more: one warp per
 //                token), the expert buckets (a token bitmask per expert,
 //                block scans for the offsets and the touched list).  CTA 0
 //                also stores the routing results for the combine and the
@@ -277,51 +278,22 @@ __global__ void __maxnreg__(128)
              i += kExpertThreads)
             z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    const int H8 = H / 8, nU = (H8 + 31) & ~31;  // 8-column units of a token, whole warps
     if (warp != kWarpProducer) {
-        // logits of the CTA's router rows, and the int8 codes of x: thread
-        // unit u = 8 consecutive columns of one token; four consecutive
-        // lanes hold one 32-column group
+        // logits of the CTA's router rows: thread unit u = 8 consecutive
+        // columns of one token
         if (ne > 0 && !mbar_wait(actbar, 0)) fail();
-        const int H8 = H / 8, nU = (H8 + 31) & ~31;
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < T && ne > 0; ++t) {
             float acc[kMaxRouteRows] = {0.f, 0.f};
             for (int u = tid; u < nU; u += kConsumerThreads) {  // warp-uniform bound
-                const bool valid = u < H8;
-                const uint4 xv = valid ? __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + u)
-                                       : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                float xf[8];
-                float amax = 0.f;
+                if (u < H8) {
+                    const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + u);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    float xf[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    xf[2 * i] = __uint_as_float(xw[i] << 16);
-                    xf[2 * i + 1] = __uint_as_float(xw[i] & 0xffff0000u);
-                    amax = fmaxf(amax, fmaxf(fabsf(xf[2 * i]), fabsf(xf[2 * i + 1])));
-                }
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const uint16_t db = act_scale_bits(amax);
-                const float d = half_bits_to_float(db);
-                uint32_t lo = 0u, hi = 0u;
-                int gsum = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int q = act_code(xf[i], d);
-                    gsum += q;
-                    if (i < 4) lo |= ((uint32_t)q & 0xffu) << (8 * i);
-                    else hi |= ((uint32_t)q & 0xffu) << (8 * (i - 4));
-                }
-                gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
-                gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
-                if (valid) {
-                    *reinterpret_cast<uint2*>(ax_q + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
-                    if ((lane & 3) == 0) {
-                        ax_dh[t * Gx + u / 4] = db;
-                        ax_s[t * Gx + u / 4] = gsum;
-                    }
-                    if (b == 0) {  // the codes as stage outputs
-                        *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
-                        if ((lane & 3) == 0) a.d_x[t * Gx + u / 4] = db;
+                    for (int i = 0; i < 4; ++i) {
+                        xf[2 * i] = __uint_as_float(xw[i] << 16);
+                        xf[2 * i + 1] = __uint_as_float(xw[i] & 0xffff0000u);
                     }
 #pragma unroll
                     for (int r = 0; r < kMaxRouteRows; ++r) {
@@ -359,16 +331,64 @@ __global__ void __maxnreg__(128)
     }
     // grid barrier: every CTA's logits and zeroed counters are published.
     // The count is zero when the call starts (the combine of the previous
-    // call cleared it) and reaches G once every CTA has arrived.
+    // call cleared it) and reaches G once every CTA has arrived.  The
+    // producer warp arrives and waits; meanwhile the consumers quantise x.
     __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        red_release_add(a.gbar, 1);
-        const unsigned long long t0 = globaltimer_ns();
-        while (ld_acquire(a.gbar) < G) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                fail();
-                break;
+    if (warp == kWarpProducer) {
+        if (lane == 0) {
+            __threadfence();
+            red_release_add(a.gbar, 1);
+            const unsigned long long t0 = globaltimer_ns();
+            while (ld_acquire(a.gbar) < G) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    fail();
+                    break;
+                }
+            }
+        }
+    } else {
+        // the int8 codes of x: unit u = 8 columns of one token, four
+        // consecutive lanes one 32-column group
+        for (int t = 0; t < T; ++t) {
+            for (int u = tid; u < nU; u += kConsumerThreads) {  // warp-uniform bound
+                const bool valid = u < H8;
+                const uint4 xv = valid ? __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + u)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                float xf[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xf[2 * i] = __uint_as_float(xw[i] << 16);
+                    xf[2 * i + 1] = __uint_as_float(xw[i] & 0xffff0000u);
+                    amax = fmaxf(amax, fmaxf(fabsf(xf[2 * i]), fabsf(xf[2 * i + 1])));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const uint16_t db = act_scale_bits(amax);
+                const float d = half_bits_to_float(db);
+                uint32_t lo = 0u, hi = 0u;
+                int gsum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int qc = act_code(xf[i], d);
+                    gsum += qc;
+                    if (i < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * i);
+                    else hi |= ((uint32_t)qc & 0xffu) << (8 * (i - 4));
+                }
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+                if (valid) {
+                    *reinterpret_cast<uint2*>(ax_q + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
+                    if ((lane & 3) == 0) {
+                        ax_dh[t * Gx + u / 4] = db;
+                        ax_s[t * Gx + u / 4] = gsum;
+                    }
+                    if (b == 0) {  // the codes as stage outputs
+                        *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
+                        if ((lane & 3) == 0) a.d_x[t * Gx + u / 4] = db;
+                    }
+                }
             }
         }
     }
@@ -386,23 +406,31 @@ __global__ void __maxnreg__(128)
         // a permutation of 0..E-1.
         __shared__ float s_val[MOE_MAX_TOPK];
         __shared__ float s_ex[MOE_MAX_TOPK];
-        __shared__ uint32_t s_key[kMaxExperts];
-        for (int e = tid; e < E; e += kExpertThreads) s_key[e] = float_order_key(s_lg[e]);
+        // keys padded with 0 to a multiple of 8 (a padding key, index >= E,
+        // never ranks above a real one)
+        __shared__ __align__(16) uint32_t s_key[kMaxExperts];
+        const int E8 = (E + 7) & ~7;
+        for (int e = tid; e < E8; e += kExpertThreads) s_key[e] = e < E ? float_order_key(s_lg[e]) : 0u;
         __syncthreads();
         const int P = (2 * E <= kExpertThreads) ? 2 : 1;  // threads per expert
-        const int half = (E + 1) / 2;
+        const int half4 = E8 / 8;                           // uint4 groups per half
+        const uint4* key4 = reinterpret_cast<const uint4*>(s_key);
         for (int base = 0; base < P * E; base += kExpertThreads) {  // warp-uniform
             const int q = base + tid;
             const bool act = q < P * E;
             const int e = act ? q / P : 0, part = q % P;
             const uint32_t kv = s_key[e];
-            const int lo = (P == 2 && part == 1) ? half : 0;
-            const int hi = !act ? 0 : (P == 2 && part == 0) ? half : E;
+            const int lo = (P == 2 && part == 1) ? half4 : 0;
+            const int hi = !act ? 0 : (P == 2 && part == 0) ? half4 : 2 * half4;
             int rank = 0;
-#pragma unroll 8
-            for (int e2 = lo; e2 < hi; ++e2) {
-                const uint32_t k2 = s_key[e2];
-                rank += (k2 > kv) | ((k2 == kv) & (e2 < e));
+#pragma unroll 4
+            for (int c4 = lo; c4 < hi; ++c4) {
+                const uint4 k4 = key4[c4];
+                const int e2 = 4 * c4;
+                rank += (k4.x > kv) | ((k4.x == kv) & (e2 < e));
+                rank += (k4.y > kv) | ((k4.y == kv) & (e2 + 1 < e));
+                rank += (k4.z > kv) | ((k4.z == kv) & (e2 + 2 < e));
+                rank += (k4.w > kv) | ((k4.w == kv) & (e2 + 3 < e));
             }
             if (P == 2) rank += __shfl_xor_sync(0xffffffffu, rank, 1);  // the pair (2m, 2m + 1)
             if (act && part == 0 && rank < k) {
