@@ -184,3 +184,21 @@ def test_decode_matches_prefill_closely():
     b = out_to_f64(dl.prefill())
     X = O.bf16_bits_to_f64(li.x)
     assert O.rms(a - b) < 0.05 * O.rms(b - X)
+
+
+def test_decode_workspace_garbage_and_reuse():
+    # The decode kernel's CTAs meet at a grid barrier whose arrival count
+    # lives in the workspace: a workspace full of garbage is cleared on its
+    # first use, and alternating two workspaces (and the library's default
+    # allocation) keeps every call correct.
+    li = workloads.decode(1)
+    dl = DeviceLayer(li)
+    ref, _ = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    nbytes = moe.moe_workspace_bytes(moe.MOE_MODE_DECODE, li.T, li.H, li.I, li.E, li.k)
+    ws_a = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws_b = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    for ws in (ws_a, ws_a, ws_b, ws_b, ws_a, None, None, ws_b):
+        out = out_to_f64(dl.decode(workspace=ws))
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status() == 0
+        assert_within_tol(out, ref)
