@@ -34,7 +34,7 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 NCU_TRAFFIC_DECODE_EXPERTS_T1 = 22_540_288
 NCU_TRAFFIC_PREFILL_GATEUP = 235_103_744 + 6_745_856
 KERNELS_PER_DECODE_LAYER = 2   # layer (router, top-k, buckets, x codes, gate/up, down); combine
-KERNELS_PER_PREFILL_LAYER = 9  # W_r split, router GEMM, top-k, 3 bucketing, gate/up, down, combine
+KERNELS_PER_PREFILL_LAYER = 8  # W_r split, router GEMM, top-k + chunk counts, bucket scan, scatter, gate/up, down, combine
 
 
 def load_peaks():

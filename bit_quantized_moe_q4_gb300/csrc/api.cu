@@ -277,7 +277,7 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
         if ((rc = cuda_check(launch_route_gemm(xin, wr, T, H, E, k, ws.route_parts, logits,
                                                ws.topk_idx, ws.topk_w, ws.x16,
                                                route_planes_bytes(T, H, E) ? ws.wr_planes : nullptr,
-                                               dev->status, s),
+                                               dev->status, ws.chunk_count, ws.entry_rank, s),
                              "route")))
             return rc;
         if ((rc = mark(1))) return rc;

@@ -6,10 +6,13 @@
 // ascending token order; buckets follow each other in expert order.  The
 // result is deterministic: no atomics decide an order.
 //
-//   1. count:   each warp takes 32 consecutive tokens; a per-expert bitmask of
-//               the lanes that chose it gives, by popcount, the chunk's count
-//               per expert and each pair's rank inside the chunk.
-//   2. scan:    per expert, an exclusive scan over chunks (chunk bases), then
+//   1. count:   per chunk of 32 consecutive tokens, a per-expert bitmask of
+//               the tokens that chose it gives, by popcount, the chunk's
+//               count per expert and each pair's rank inside the chunk.  The
+//               router's top-k kernel does this (route.cu, one CTA per
+//               chunk), so the bucketing starts from its chunk counts.
+//   2. scan:    per expert, an exclusive scan over chunks (chunk bases; four
+//               threads per expert, each over a quarter of the chunks), then
 //               one over experts (offsets); the same pass lists the token
 //               tiles of the grouped GEMM and the non-empty experts.
 //   3. scatter: row = offsets[e] + chunk base + rank.
@@ -22,62 +25,86 @@ int nchunks(int T) { return (T + 31) / 32; }
 
 namespace {
 
-__global__ void __launch_bounds__(256) bucket_count_kernel(const int32_t* __restrict__ idx, int T,
-                                                           int E, int k,
-                                                           int32_t* __restrict__ chunk_count,
-                                                           int32_t* __restrict__ entry_rank) {
-    __shared__ uint32_t bits[8][kMaxExperts];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int chunk = blockIdx.x * 8 + warp;
-    if (chunk * 32 >= T) return;  // whole warp leaves together
-    for (int e = lane; e < E; e += 32) bits[warp][e] = 0u;
-    __syncwarp();
-    const int t = chunk * 32 + lane;
-    const bool valid = t < T;
-    if (valid)
-        for (int j = 0; j < k; ++j) atomicOr(&bits[warp][idx[(size_t)t * k + j]], 1u << lane);
-    __syncwarp();
-    if (valid) {
-        const uint32_t below = (1u << lane) - 1u;
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[(size_t)t * k + j];
-            entry_rank[(size_t)t * k + j] = __popc(bits[warp][e] & below);
-        }
+// Exclusive prefix sum over a 1024-thread block (thread order).
+__device__ __forceinline__ int block1024_exclusive_scan(int v, int* total) {
+    __shared__ int warp_tot[32];
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
-    for (int e = lane; e < E; e += 32) chunk_count[(size_t)chunk * E + e] = __popc(bits[warp][e]);
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int wv = lane < 32 ? warp_tot[lane] : 0;
+    int wincl = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += n;
+    }
+    const int base = __shfl_sync(0xffffffffu, wincl - wv, warp);  // warps before this one
+    const int all = __shfl_sync(0xffffffffu, wincl, 31);
+    __syncthreads();
+    *total = all;
+    return base + incl - v;
 }
 
-__global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ chunk_count,
-                                                          int nchunk, int E, int tile_n,
-                                                          int32_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ touched,
-                                                          int32_t* __restrict__ counters,
-                                                          int32_t* __restrict__ tile_e,
-                                                          int32_t* __restrict__ tile_n0,
-                                                          int32_t* __restrict__ tile_nn) {
-    const int e = threadIdx.x;
-    int count = 0;
+constexpr int kScanParts = 4;  // threads per expert in the chunk scan
+
+__global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t* __restrict__ chunk_count,
+                                                           int nchunk, int E, int tile_n,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ touched,
+                                                           int32_t* __restrict__ counters,
+                                                           int32_t* __restrict__ tile_e,
+                                                           int32_t* __restrict__ tile_n0,
+                                                           int32_t* __restrict__ tile_nn) {
+    __shared__ int part_tot[kScanParts][kMaxExperts];
+    const int e = threadIdx.x % kMaxExperts, part = threadIdx.x / kMaxExperts;
+    const int c0 = part * nchunk / kScanParts, c1 = (part + 1) * nchunk / kScanParts;
+    // this quarter's total, 16 chunk counts in flight at a time
+    int tot = 0;
     if (e < E) {
-        // 16 chunk counts in flight at a time; each becomes its chunk's base
-        for (int c0 = 0; c0 < nchunk; c0 += 16) {
+        for (int c = c0; c < c1; c += 16) {
             int n[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                n[u] = (c0 + u < nchunk) ? chunk_count[(size_t)(c0 + u) * E + e] : 0;
+            for (int u = 0; u < 16; ++u) n[u] = (c + u < c1) ? chunk_count[(size_t)(c + u) * E + e] : 0;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) tot += n[u];
+        }
+        part_tot[part][e] = tot;
+    }
+    __syncthreads();
+    // each count becomes its chunk's base: the expert's tokens in earlier chunks
+    int count = 0;
+    if (e < E) {
+        int run = 0;
+        for (int p = 0; p < kScanParts; ++p) {
+            if (p < part) run += part_tot[p][e];
+            count += part_tot[p][e];
+        }
+        for (int c = c0; c < c1; c += 16) {
+            int n[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) n[u] = (c + u < c1) ? chunk_count[(size_t)(c + u) * E + e] : 0;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                if (c0 + u < nchunk) chunk_count[(size_t)(c0 + u) * E + e] = count;
-                count += n[u];
+                if (c + u < c1) chunk_count[(size_t)(c + u) * E + e] = run;
+                run += n[u];
             }
         }
     }
+    // experts in order (threads of part 0 carry them; the others add 0)
+    const bool lead = part == 0 && e < E;
     int total;
-    const int off = block256_exclusive_scan(count, &total);
-    if (e < E) offsets[e] = off;
-    if (e == 0) offsets[E] = total;
-    const int ntiles = (count + tile_n - 1) / tile_n;
+    const int off = block1024_exclusive_scan(lead ? count : 0, &total);
+    if (lead) offsets[e] = off;
+    if (threadIdx.x == 0) offsets[E] = total;
+    const int ntiles = lead ? (count + tile_n - 1) / tile_n : 0;
     int all_tiles;
-    const int toff = block256_exclusive_scan(ntiles, &all_tiles);
+    const int toff = block1024_exclusive_scan(ntiles, &all_tiles);
     // a bucket is cut into ntiles tiles of near-equal size (the first
     // count % ntiles tiles one row longer), each at most tile_n rows
     const int tbase = ntiles ? count / ntiles : 0, textra = ntiles ? count % ntiles : 0;
@@ -89,9 +116,9 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t* __restrict__ 
         r0 += nn;
     }
     int ntouched;
-    const int pos = block256_exclusive_scan(count > 0 ? 1 : 0, &ntouched);
-    if (count > 0) touched[pos] = e;
-    if (e == 0) {
+    const int pos = block1024_exclusive_scan(lead && count > 0 ? 1 : 0, &ntouched);
+    if (lead && count > 0) touched[pos] = e;
+    if (threadIdx.x == 0) {
         counters[kCntTouched] = ntouched;
         counters[kCntTiles] = all_tiles;
     }
@@ -121,11 +148,8 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ idx,
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s) {
     const int nc = nchunks(T);
-    if (T > 0)
-        bucket_count_kernel<<<(nc + 7) / 8, 256, 0, s>>>(idx, T, E, k, ws.chunk_count,
-                                                         ws.entry_rank);
-    bucket_scan_kernel<<<1, 256, 0, s>>>(ws.chunk_count, nc, E, tile_n, ws.offsets, ws.touched,
-                                         ws.counters, ws.tile_e, ws.tile_n0, ws.tile_nn);
+    bucket_scan_kernel<<<1, 1024, 0, s>>>(ws.chunk_count, nc, E, tile_n, ws.offsets, ws.touched,
+                                          ws.counters, ws.tile_e, ws.tile_n0, ws.tile_nn);
     if (T > 0)
         bucket_scatter_kernel<<<(T * k + 255) / 256, 256, 0, s>>>(
             idx, w, T, E, k, ws.chunk_count, ws.entry_rank, ws.offsets, ws.bucket_token,

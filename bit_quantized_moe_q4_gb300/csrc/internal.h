@@ -72,9 +72,15 @@ cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E
 int route_ksplit(int T, int H, int E);
 size_t route_parts_floats(int T, int H, int E);
 size_t route_planes_bytes(int T, int H, int E);
+// With `chunk_count` and `entry_rank` (the bucketing's per-32-token-chunk
+// arrays) the top-k kernel also counts the chunks, the first pass of the
+// bucketing that launch_bucket completes.
 cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                               float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
-                              uint16_t* planes, int* status, cudaStream_t s);
+                              uint16_t* planes, int* status, int32_t* chunk_count,
+                              int32_t* entry_rank, cudaStream_t s);
+// Bucketing from the chunk counts and ranks the router's top-k kernel left in
+// ws (chunk bases, offsets, tile list, touched list, then the scatter).
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
 cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,

@@ -320,6 +320,64 @@ __global__ void __launch_bounds__(256) topk_from_parts_kernel(const float* __res
 }
 
 
+// One CTA per 32-token chunk, one warp per token: the token's logits (the
+// K-slice parts added in slice order), its top-k, and then the chunk's
+// bucketing counts: a per-expert bitmask of the chunk's tokens that chose it
+// gives each expert's count in the chunk and each (token, slot) pair's rank
+// among the chunk's tokens of its expert (the first pass of the bucketing).
+__global__ void __launch_bounds__(1024, 1) topk_chunk_kernel(
+    const float* __restrict__ parts, int ksplit, int T, int E, int k, float* logits, int32_t* idx,
+    float* w, int32_t* __restrict__ chunk_count, int32_t* __restrict__ entry_rank) {
+    __shared__ float row[32][EMAX];
+    __shared__ uint32_t bits[EMAX];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int chunk = blockIdx.x, t = chunk * 32 + warp;
+    for (int e = threadIdx.x; e < EMAX; e += blockDim.x) bits[e] = 0u;
+    __syncthreads();
+    constexpr int PER = EMAX / 32;
+    int si = 0;
+    if (t < T) {  // whole warp
+        float v[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) v[i] = 0.f;
+        for (int s0 = 0; s0 < ksplit; s0 += 2) {
+            float pv[2][PER];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int e = lane + 32 * i;
+                    pv[u][i] = (s0 + u < ksplit && e < E)
+                                   ? __ldcg(parts + ((size_t)(s0 + u) * T + t) * E + e) : 0.f;
+                }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < PER; ++i) v[i] += pv[u][i];  // slices in order (adding 0 is exact)
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                row[warp][e] = v[i];
+                if (logits) logits[(size_t)t * E + e] = v[i];
+            }
+        }
+        __syncwarp();
+        float sw;
+        warp_topk(row[warp], E, k, si, sw);
+        if (lane < k) {
+            idx[(size_t)t * k + lane] = si;
+            w[(size_t)t * k + lane] = sw;
+            atomicOr(&bits[si], 1u << warp);
+        }
+    }
+    __syncthreads();
+    if (t < T && lane < k) entry_rank[(size_t)t * k + lane] = __popc(bits[si] & ((1u << warp) - 1u));
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_count[(size_t)chunk * E + e] = __popc(bits[e]);
+}
+
 // ---- tensor-core router (prefill) -----------------------------------------
 constexpr int TC_M = 128;                          // experts per CTA (MMA M)
 constexpr int TC_N = 128;                          // tokens per CTA (MMA N)
@@ -564,8 +622,21 @@ size_t route_planes_bytes(int T, int H, int E) {
 
 cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                               float* parts, float* logits, int32_t* idx, float* w, uint16_t* x16,
-                              uint16_t* planes, int* status, cudaStream_t s) {
+                              uint16_t* planes, int* status, int32_t* chunk_count,
+                              int32_t* entry_rank, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    // the top-k over the K-slice parts; with chunk buffers it also counts
+    // the bucketing's 32-token chunks
+    auto topk = [&](int ks) {
+        if (chunk_count && entry_rank)
+            topk_chunk_kernel<<<(T + 31) / 32, 1024, 0, s>>>(parts, ks, T, E, k,
+                                                             parts == logits ? nullptr : logits, idx,
+                                                             w, chunk_count, entry_rank);
+        else
+            topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k,
+                                                               parts == logits ? nullptr : logits,
+                                                               idx, w);
+    };
     if (planes != nullptr && parts != logits && use_tc_router(T)) {
         const int ks = tc_ksplit(T, H, E);
         const int n4 = E * H / 4;
@@ -580,15 +651,14 @@ cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, 
         const dim3 grid((T + TC_N - 1) / TC_N, (E + TC_M - 1) / TC_M, ks);
         router_tc_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(tm_w, tm_x, T, H, E, ks, parts, x16,
                                                            status);
-        topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k, logits, idx, w);
+        topk(ks);
         return cudaGetLastError();
     }
     // with the logits buffer as the only part, the sums are already in place
     const int ks = (parts == logits) ? 1 : route_ksplit(T, H, E);
     const dim3 grid((T + GT - 1) / GT, (E + GE - 1) / GE, ks);
     router_gemm_kernel<<<grid, G_THREADS, 0, s>>>(x, wr, T, H, E, ks, parts, x16);
-    topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k,
-                                                       parts == logits ? nullptr : logits, idx, w);
+    topk(ks);
     return cudaGetLastError();
 }
 
@@ -598,7 +668,7 @@ cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E
     if (T == 0) return cudaSuccess;
     if (logits && !x16 && T > 32 && (H % GK) == 0)
         return launch_route_gemm(x, wr, T, H, E, k, logits, logits, idx, w, nullptr, nullptr, nullptr,
-                                 s);
+                                 nullptr, nullptr, s);
     if (logits && !x16 && T <= 32 && (H % 128) == 0) {
         const dim3 grid((E + 3) / 4);
         if (T <= 4)
