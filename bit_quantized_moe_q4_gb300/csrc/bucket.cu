@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t* __restrict__
                                                            int32_t* __restrict__ tile_n0,
                                                            int32_t* __restrict__ tile_nn) {
     __shared__ int part_tot[kScanParts][kMaxExperts];
+    pdl_wait();  // the chunk counts of the top-k kernel
+    pdl_trigger();
     const int e = threadIdx.x % kMaxExperts, part = threadIdx.x / kMaxExperts;
     const int c0 = part * nchunk / kScanParts, c1 = (part + 1) * nchunk / kScanParts;
     // this quarter's total, 16 chunk counts in flight at a time
@@ -132,6 +134,8 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ idx,
                                       int32_t* __restrict__ bucket_token,
                                       int32_t* __restrict__ bucket_slot,
                                       float* __restrict__ slot_w, int32_t* __restrict__ slot_pos) {
+    pdl_wait();  // the chunk bases and offsets of the scan
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= T * k) return;
     const int t = i / k, j = i % k;
@@ -148,12 +152,16 @@ __global__ void bucket_scatter_kernel(const int32_t* __restrict__ idx,
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s) {
     const int nc = nchunks(T);
-    bucket_scan_kernel<<<1, 1024, 0, s>>>(ws.chunk_count, nc, E, tile_n, ws.offsets, ws.touched,
-                                          ws.counters, ws.tile_e, ws.tile_n0, ws.tile_nn);
+    cudaError_t err = launch_pdl(bucket_scan_kernel, dim3(1), dim3(1024), 0, s, ws.chunk_count, nc,
+                                 E, tile_n, ws.offsets, ws.touched, ws.counters, ws.tile_e,
+                                 ws.tile_n0, ws.tile_nn);
+    if (err != cudaSuccess) return err;
     if (T > 0)
-        bucket_scatter_kernel<<<(T * k + 255) / 256, 256, 0, s>>>(
-            idx, w, T, E, k, ws.chunk_count, ws.entry_rank, ws.offsets, ws.bucket_token,
-            ws.bucket_slot, ws.slot_w, ws.slot_pos);
+        err = launch_pdl(bucket_scatter_kernel, dim3((T * k + 255) / 256), dim3(256), 0, s, idx, w,
+                         T, E, k, (const int32_t*)ws.chunk_count, (const int32_t*)ws.entry_rank,
+                         (const int32_t*)ws.offsets, ws.bucket_token, ws.bucket_slot, ws.slot_w,
+                         ws.slot_pos);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -9,6 +9,8 @@
 
 #include "moeq4.h"
 
+#include <utility>
+
 namespace moeq4 {
 
 // Workspace pieces of one forward call; every pointer is a device address
@@ -47,6 +49,26 @@ struct Workspace {
     int max_tiles;
     int tile_n;             // tokens per GEMM tile (prefill)
 };
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic
+// dependent launch allowed: the grid may be scheduled before the preceding
+// kernel on s has finished; the kernel orders itself after it with
+// griddepcontrol.wait before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // counters[] slots
 enum { kCntTouched = 0, kCntTiles = 1 };

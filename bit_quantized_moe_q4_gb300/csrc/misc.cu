@@ -32,6 +32,8 @@ template <bool OUT_FP32, typename Y>
 __global__ void combine_kernel(const uint16_t* __restrict__ x, const Y* __restrict__ y,
                                const int32_t* __restrict__ slot_pos, int T, int H, int k,
                                void* __restrict__ out) {
+    pdl_wait();  // the down GEMM's rows
+    pdl_trigger();
     const int cols8 = H / 8;
     const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (i >= (size_t)T * cols8) return;
@@ -73,6 +75,8 @@ __global__ void combine_kernel(const uint16_t* __restrict__ x, const Y* __restri
 // divide and square root), xn = bf16_rn(x * r).
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int T, int H,
                                                       float eps, uint16_t* __restrict__ xn) {
+    pdl_wait();  // x (the preceding work on the stream)
+    pdl_trigger();
     const int t = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
     if (t >= T) return;  // whole warp
     const uint16_t* row = x + (size_t)t * H;
@@ -108,8 +112,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    rmsnorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, eps, xn);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_kernel, dim3((T + 7) / 8), dim3(256), 0, s, x, T, H, eps, xn);
 }
 
 cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const int32_t* slot_pos,
@@ -120,15 +123,14 @@ cudaError_t launch_combine(const uint16_t* x, const void* y, bool y_fp32, const 
     const unsigned blocks = (unsigned)((n + threads - 1) / threads);
     const float* yf = static_cast<const float*>(y);
     const uint16_t* yh = static_cast<const uint16_t*>(y);
+    const dim3 g(blocks), b(threads);
     if (out_fp32 && y_fp32)
-        combine_kernel<true><<<blocks, threads, 0, s>>>(x, yf, slot_pos, T, H, k, out);
-    else if (out_fp32)
-        combine_kernel<true><<<blocks, threads, 0, s>>>(x, yh, slot_pos, T, H, k, out);
-    else if (y_fp32)
-        combine_kernel<false><<<blocks, threads, 0, s>>>(x, yf, slot_pos, T, H, k, out);
-    else
-        combine_kernel<false><<<blocks, threads, 0, s>>>(x, yh, slot_pos, T, H, k, out);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<true, float>, g, b, 0, s, x, yf, slot_pos, T, H, k, out);
+    if (out_fp32)
+        return launch_pdl(combine_kernel<true, uint16_t>, g, b, 0, s, x, yh, slot_pos, T, H, k, out);
+    if (y_fp32)
+        return launch_pdl(combine_kernel<false, float>, g, b, 0, s, x, yf, slot_pos, T, H, k, out);
+    return launch_pdl(combine_kernel<false, uint16_t>, g, b, 0, s, x, yh, slot_pos, T, H, k, out);
 }
 
 }  // namespace moeq4

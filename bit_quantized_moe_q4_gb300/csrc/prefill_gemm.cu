@@ -36,7 +36,11 @@
 // epilogue warps read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
 // weight * acc, both fp16 (saturating at +-65504), in bucket order.
 // One persistent CTA per SM walks a static list of (token tile, row block)
-// work items.  Every wait is bounded; on expiry the CTA records
+// work items.  The kernel is launched with programmatic dependent launch:
+// the weight producer and the dequant warps start on their first weight
+// tiles (which depend only on the tile list, two kernels back) while the
+// preceding kernel drains; the token loaders, the MMA and the epilogue wait
+// for it first.  Every wait is bounded; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the status word, stops, drains its copies, frees TMEM
 // and exits.
 #include "common.cuh"
@@ -237,6 +241,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp >= WARP_B0 && warp < WARP_B0 + NUM_B_WARPS) {
         // ----------------------------------------------- token-row loaders
         // thread bt: 16-byte chunk c = bt % 8 of rows bt / 8 + 16 i
+        pdl_wait();  // the token rows and bucket lists of the preceding kernels
+        pdl_trigger();
         const int bt = threadIdx.x - WARP_B0 * 32;
         const int c = bt % 8, r0 = bt / 8;
         int it = 0, issued = 0;
@@ -276,6 +282,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_wait(b_full(j % SB), (j / SB) & 1);
     } else if (warp == WARP_MMA) {
         // ---------------------------------------------------------------- MMA
+        pdl_wait();
+        pdl_trigger();
         int it = 0, item = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++item) {
@@ -380,6 +388,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // chunks, each loading 2 x 16 columns before one wait
         const int quad = warp % 4, half = (warp - WARP_EPI0) / 4;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        pdl_wait();  // the output buffer and routing weights of the preceding kernels
+        pdl_trigger();
         int item = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
             const int tile = w / rb_count, ri = w % rb_count;
@@ -460,8 +470,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    grouped_q4_gemm_kernel<GATEUP><<<num_sms, NUM_THREADS, C::SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(grouped_q4_gemm_kernel<GATEUP>, dim3(num_sms), dim3(NUM_THREADS),
+                      C::SMEM_BYTES, s, a);
 }
 
 }  // namespace

@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(G_THREADS) router_gemm_kernel(
     float* __restrict__ parts, uint16_t* __restrict__ x16) {
     __shared__ __align__(16) float xs[2][GK][GT];
     __shared__ __align__(16) float ws[2][GK][GE];
+    pdl_wait();  // x (the preceding work on the stream)
+    pdl_trigger();
     const int t0 = blockIdx.x * GT, e0 = blockIdx.y * GE, split = blockIdx.z;
     const int kspan = H / ksplit, kbeg = split * kspan;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -279,6 +281,8 @@ __global__ void __launch_bounds__(256) topk_from_parts_kernel(const float* __res
                                                               int ksplit, int T, int E, int k,
                                                               float* logits, int32_t* idx, float* w) {
     __shared__ float row[8][EMAX];
+    pdl_wait();  // the K-slice parts
+    pdl_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;  // whole warp
@@ -330,6 +334,8 @@ __global__ void __launch_bounds__(1024, 1) topk_chunk_kernel(
     float* w, int32_t* __restrict__ chunk_count, int32_t* __restrict__ entry_rank) {
     __shared__ float row[32][EMAX];
     __shared__ uint32_t bits[EMAX];
+    pdl_wait();  // the K-slice parts
+    pdl_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int chunk = blockIdx.x, t = chunk * 32 + warp;
     for (int e = threadIdx.x; e < EMAX; e += blockDim.x) bits[e] = 0u;
@@ -395,6 +401,8 @@ constexpr int TC_MIN_T = 128;
 // bits of what is left).
 __global__ void __launch_bounds__(256) split_wr_kernel(const float* __restrict__ wr, int n4,
                                                        uint16_t* __restrict__ planes) {
+    pdl_wait();  // the preceding work on the stream has finished
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     const float4 v = __ldg(reinterpret_cast<const float4*>(wr) + i);
@@ -472,6 +480,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         record_status(status, kStatusTimeout);
         *abort_flag = 1;
     };
+    pdl_wait();  // the W_r parts (preceding kernel) and x
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
@@ -628,38 +638,40 @@ cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, 
     // the top-k over the K-slice parts; with chunk buffers it also counts
     // the bucketing's 32-token chunks
     auto topk = [&](int ks) {
+        float* lg = parts == logits ? nullptr : logits;
         if (chunk_count && entry_rank)
-            topk_chunk_kernel<<<(T + 31) / 32, 1024, 0, s>>>(parts, ks, T, E, k,
-                                                             parts == logits ? nullptr : logits, idx,
-                                                             w, chunk_count, entry_rank);
-        else
-            topk_from_parts_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, ks, T, E, k,
-                                                               parts == logits ? nullptr : logits,
-                                                               idx, w);
+            return launch_pdl(topk_chunk_kernel, dim3((T + 31) / 32), dim3(1024), 0, s,
+                              (const float*)parts, ks, T, E, k, lg, idx, w, chunk_count,
+                              entry_rank);
+        return launch_pdl(topk_from_parts_kernel, dim3((T + 7) / 8), dim3(256), 0, s,
+                          (const float*)parts, ks, T, E, k, lg, idx, w);
     };
     if (planes != nullptr && parts != logits && use_tc_router(T)) {
         const int ks = tc_ksplit(T, H, E);
         const int n4 = E * H / 4;
-        split_wr_kernel<<<(n4 + 255) / 256, 256, 0, s>>>(wr, n4, planes);
+        cudaError_t err = launch_pdl(split_wr_kernel, dim3((n4 + 255) / 256), dim3(256), 0, s, wr,
+                                     n4, planes);
+        if (err != cudaSuccess) return err;
         CUtensorMap tm_w, tm_x;
         if (!encode_tmap_2d_f16(&tm_w, planes, (uint64_t)tc_plane_rows(E), H, kTileK, TC_M, true) ||
             !encode_tmap_2d_f16(&tm_x, x, T, H, kTileK, TC_N, true))
             return cudaErrorInvalidValue;
-        cudaError_t err = cudaFuncSetAttribute(router_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   TC_SMEM);
         if (err != cudaSuccess) return err;
         const dim3 grid((T + TC_N - 1) / TC_N, (E + TC_M - 1) / TC_M, ks);
-        router_tc_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(tm_w, tm_x, T, H, E, ks, parts, x16,
-                                                           status);
-        topk(ks);
-        return cudaGetLastError();
+        err = launch_pdl(router_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, s, tm_w, tm_x, T, H, E,
+                         ks, parts, x16, status);
+        if (err != cudaSuccess) return err;
+        return topk(ks);
     }
     // with the logits buffer as the only part, the sums are already in place
     const int ks = (parts == logits) ? 1 : route_ksplit(T, H, E);
     const dim3 grid((T + GT - 1) / GT, (E + GE - 1) / GE, ks);
-    router_gemm_kernel<<<grid, G_THREADS, 0, s>>>(x, wr, T, H, E, ks, parts, x16);
-    topk(ks);
-    return cudaGetLastError();
+    cudaError_t err = launch_pdl(router_gemm_kernel, grid, dim3(G_THREADS), 0, s, x, wr, T, H, E,
+                                 ks, parts, x16);
+    if (err != cudaSuccess) return err;
+    return topk(ks);
 }
 
 // `logits` may be null; the split path is taken only when it is not.
