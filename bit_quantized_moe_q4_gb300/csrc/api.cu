@@ -133,7 +133,7 @@ bool encode_tmap_packed(CUtensorMap* map, const void* packed, uint64_t ntiles, u
 
 namespace {
 
-constexpr int kPrefillTileN = 144;  // tokens per prefill GEMM tile (the GEMM's BN)
+constexpr int kPrefillTileN = 160;  // tokens per prefill GEMM tile (the GEMM's BN)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 

@@ -12,9 +12,12 @@
 // at the same tensor-core rate.
 //
 // Weights sit on the MMA's M side (128 rows per tile) and tokens on N (up to
-// 144 per tile, padded to a multiple of 16; larger buckets are cut into
+// 160 per tile, padded to a multiple of 16; larger buckets are cut into
 // tiles of near-equal size), so an expert's bucket of ~128 tokens is one
-// tile and every weight is dequantised once.  Per 64-column
+// tile and every weight is dequantised once.  160 is the widest accumulator
+// that leaves each matrix's 256 tensor-memory columns room for three A
+// stages; the operand stream costs about the same per K-block whatever the
+// tile's width, so fewer, wider tiles are faster.  Per 64-column
 // K-block, three decoupled rings:
 //   raw    the packed 4-bit tiles (4608 bytes each), two K-blocks of each
 //          weight block per bulk copy (contiguous in the packed layout), by
@@ -27,7 +30,7 @@
 //          with 16-byte cp.async copies straight into the 128-byte-swizzled
 //          layout (gate/up: rows of x picked by token id; down: consecutive
 //          rows of h); they mostly hit L2, whose latency still needs a ring
-//          six or seven K-blocks deep.  (Many small TMA copies - gather4 or
+//          six K-blocks deep.  (Many small TMA copies - gather4 or
 //          16-row boxes - proved slower here: the copy engine spent ~40 ns on
 //          each.)
 // The weight copies carry an L2 evict-first hint: they are read once, and
@@ -49,14 +52,14 @@
 namespace moeq4 {
 namespace {
 
-constexpr int BN = 144;                 // max tokens per tile (buckets are cut evenly)
+constexpr int BN = 160;                 // max tokens per tile (buckets are cut evenly)
 constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
 constexpr int NUM_EPI_WARPS = 8, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
 constexpr int WARP_WPROD = 0, WARP_MMA = 1, WARP_B0 = 2;
 constexpr int WARP_EPI0 = WARP_B0 + NUM_B_WARPS;
 constexpr int WARP_DEQ0 = WARP_EPI0 + NUM_EPI_WARPS;
 constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 22 warps
-constexpr int B_ROWS_PER_THREAD = BN * 8 / (NUM_B_WARPS * 32);  // 16-byte chunks: 9
+constexpr int B_ROWS_PER_THREAD = BN * 8 / (NUM_B_WARPS * 32);  // 16-byte chunks: 10
 static_assert(BN * 8 % (NUM_B_WARPS * 32) == 0, "B chunks per loader thread");
 
 // Both GEMMs multiply two 128-row weight blocks by the same token tile:
@@ -68,7 +71,7 @@ struct Cfg {
     static constexpr int RK = 2;  // K-blocks per weight copy (contiguous tiles)
     static constexpr int RAW_STAGES = 5;
     static constexpr int A_STAGES = 3;  // in tensor memory
-    static constexpr int B_STAGES = 7;
+    static constexpr int B_STAGES = 6;
     static constexpr int RAW_BYTES = NMAT * RK * kTileBytes;
     // tensor memory: accumulator m at column m * 256 (BN columns); A stage s
     // of matrix m at column m * 256 + A_COL0 + s * 32 (64 fp16 per row, two
