@@ -83,7 +83,8 @@ struct Cfg {
     static constexpr int OFF_B = 0;
     static constexpr int OFF_RAW = OFF_B + B_STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_RAW + RAW_STAGES * RAW_BYTES;
-    static constexpr int NUM_BARS = 2 * (RAW_STAGES + A_STAGES + B_STAGES) + 3;
+    static constexpr int NUM_BARS = 2 * RAW_STAGES + A_STAGES + 2 * B_STAGES + 3;
+    static_assert(B_STAGES > A_STAGES, "A stages are freed through the token-stage barriers");
     static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
     // per epilogue warp: a 16-token x 32-feature fp16 transpose buffer
     static constexpr int OFF_STAGE = (OFF_TMEM + 16 + 127) & ~127;
@@ -166,11 +167,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar0 = base + C::OFF_BAR;
     auto raw_full = [&](int s) { return bar0 + 8u * s; };
     auto raw_empty = [&](int s) { return bar0 + 8u * (SR + s); };
+    // (no "A empty" barriers: the MMA commits once per K-block, to its
+    // token-row stage, and A stage it % SA is free again once K-block it - SA
+    // has completed, which that commit shows; SB > SA keeps the phase of
+    // K-block it - SA the latest one the dequant can see on that barrier)
     auto a_full = [&](int s) { return bar0 + 8u * (2 * SR + s); };
-    auto a_empty = [&](int s) { return bar0 + 8u * (2 * SR + SA + s); };
-    auto b_full = [&](int s) { return bar0 + 8u * (2 * SR + 2 * SA + s); };
-    auto b_empty = [&](int s) { return bar0 + 8u * (2 * SR + 2 * SA + SB + s); };
-    const uint32_t acc_full = bar0 + 8u * (2 * (SR + SA + SB));
+    auto b_full = [&](int s) { return bar0 + 8u * (2 * SR + SA + s); };
+    auto b_empty = [&](int s) { return bar0 + 8u * (2 * SR + SA + SB + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * SR + SA + 2 * SB);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t mma_done = acc_full + 16u;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + C::OFF_TMEM + 4);
@@ -181,10 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(raw_full(s), 1);
             mbar_init(raw_empty(s), NUM_DEQ_WARPS);
         }
-        for (int s = 0; s < SA; ++s) {
-            mbar_init(a_full(s), NUM_DEQ_WARPS);
-            mbar_init(a_empty(s), 1);
-        }
+        for (int s = 0; s < SA; ++s) mbar_init(a_full(s), NUM_DEQ_WARPS);
         for (int s = 0; s < SB; ++s) {
             mbar_init(b_full(s), NUM_B_WARPS * 32);
             mbar_init(b_empty(s), 1);
@@ -321,8 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             mma_f16_ta(tmem + m * 256, a_t, bdesc, idesc, (kb | kk) != 0);
                         }
                     }
-                    mma_commit(a_empty(sa));
-                    mma_commit(b_empty(sb));
+                    mma_commit(b_empty(sb));  // frees token stage sb and A stage sa
                 }
                 __syncwarp();
             }
@@ -351,8 +351,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ir = it / C::RK, sub = it % C::RK;  // weight copy and its K-block
                 const int sr = ir % SR, sa = it % SA;
-                const bool bad = *abort_flag || !mbar_wait(raw_full(sr), (ir / SR) & 1) ||
-                                 !mbar_wait(a_empty(sa), ((it / SA) & 1) ^ 1);
+                const bool bad =
+                    *abort_flag || !mbar_wait(raw_full(sr), (ir / SR) & 1) ||
+                    (it >= SA && !mbar_wait(b_empty((it - SA) % SB), ((it - SA) / SB) & 1));
                 if (__any_sync(0xffffffffu, bad)) {  // tcgen05.st below needs the whole warp
                     fail();
                     ok = false;
