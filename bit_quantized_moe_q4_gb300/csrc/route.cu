@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(256) topk_from_parts_kernel(const float* __res
 __global__ void __launch_bounds__(1024, 1) topk_chunk_kernel(
     const float* __restrict__ parts, int ksplit, int T, int E, int k, float* logits, int32_t* idx,
     float* w, int32_t* __restrict__ chunk_count, int32_t* __restrict__ entry_rank) {
-    __shared__ float row[32][EMAX];
+    __shared__ __align__(16) float row[32][EMAX];
     __shared__ uint32_t bits[EMAX];
     pdl_wait();  // the K-slice parts
     pdl_trigger();
@@ -340,33 +340,67 @@ __global__ void __launch_bounds__(1024, 1) topk_chunk_kernel(
     const int chunk = blockIdx.x, t = chunk * 32 + warp;
     for (int e = threadIdx.x; e < EMAX; e += blockDim.x) bits[e] = 0u;
     __syncthreads();
-    constexpr int PER = EMAX / 32;
     int si = 0;
     if (t < T) {  // whole warp
-        float v[PER];
+        if ((E % 4) == 0 && E <= 128 && ksplit <= 8) {
+            // lane: experts 4 lane .. 4 lane + 3, one 16-byte load per slice,
+            // every slice in flight at once
+            const int e = 4 * lane;
+            float4 pv[8];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) v[i] = 0.f;
-        for (int s0 = 0; s0 < ksplit; s0 += 2) {
-            float pv[2][PER];
+            for (int u = 0; u < 8; ++u)
+                pv[u] = (u < ksplit && e < E)
+                            ? __ldcg(reinterpret_cast<const float4*>(parts + ((size_t)u * T + t) * E + e))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int i = 0; i < PER; ++i) {
-                    const int e = lane + 32 * i;
-                    pv[u][i] = (s0 + u < ksplit && e < E)
-                                   ? __ldcg(parts + ((size_t)(s0 + u) * T + t) * E + e) : 0.f;
-                }
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int i = 0; i < PER; ++i) v[i] += pv[u][i];  // slices in order (adding 0 is exact)
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
+            for (int u = 0; u < 8; ++u) {  // slices in order (adding 0 is exact)
+                v.x += pv[u].x;
+                v.y += pv[u].y;
+                v.z += pv[u].z;
+                v.w += pv[u].w;
+            }
             if (e < E) {
-                row[warp][e] = v[i];
-                if (logits) logits[(size_t)t * E + e] = v[i];
+                *reinterpret_cast<float4*>(&row[warp][e]) = v;
+                if (logits) {
+                    float* lr = logits + (size_t)t * E + e;
+                    if ((reinterpret_cast<uintptr_t>(lr) & 15u) == 0) {
+                        *reinterpret_cast<float4*>(lr) = v;
+                    } else {
+                        lr[0] = v.x;
+                        lr[1] = v.y;
+                        lr[2] = v.z;
+                        lr[3] = v.w;
+                    }
+                }
+            }
+        } else {
+            constexpr int PER = EMAX / 32;
+            float v[PER];
+#pragma unroll
+            for (int i = 0; i < PER; ++i) v[i] = 0.f;
+            for (int s0 = 0; s0 < ksplit; s0 += 2) {
+                float pv[2][PER];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) {
+                        const int e = lane + 32 * i;
+                        pv[u][i] = (s0 + u < ksplit && e < E)
+                                       ? __ldcg(parts + ((size_t)(s0 + u) * T + t) * E + e) : 0.f;
+                    }
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) v[i] += pv[u][i];  // slices in order
+            }
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) {
+                    row[warp][e] = v[i];
+                    if (logits) logits[(size_t)t * E + e] = v[i];
+                }
             }
         }
         __syncwarp();
@@ -401,26 +435,30 @@ constexpr int TC_MIN_T = 128;
 // bits of what is left).
 __global__ void __launch_bounds__(256) split_wr_kernel(const float* __restrict__ wr, int n4,
                                                        uint16_t* __restrict__ planes) {
-    pdl_wait();  // the preceding work on the stream has finished
-    pdl_trigger();
+    // Before the wait for the preceding kernel: W_r is the caller's (not
+    // written by the kernel launched just before this call), and the parts
+    // buffer is last read by an earlier call's router, which has finished.
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n4) return;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(wr) + i);
-    const float f[4] = {v.x, v.y, v.z, v.w};
-    uint16_t q[3][4];
+    if (i < n4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(wr) + i);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        uint16_t q[3][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float r = f[j];
+        for (int j = 0; j < 4; ++j) {
+            float r = f[j];
 #pragma unroll
-        for (int p = 0; p < 3; ++p) {
-            q[p][j] = float_to_bf16_bits(r);
-            r -= bf16_bits_to_float(q[p][j]);  // exact: the rounding error of the part
+            for (int p = 0; p < 3; ++p) {
+                q[p][j] = float_to_bf16_bits(r);
+                r -= bf16_bits_to_float(q[p][j]);  // exact: the rounding error of the part
+            }
         }
-    }
 #pragma unroll
-    for (int p = 0; p < 3; ++p)
-        reinterpret_cast<uint2*>(planes + (size_t)p * n4 * 4)[i] =
-            make_uint2(q[p][0] | ((uint32_t)q[p][1] << 16), q[p][2] | ((uint32_t)q[p][3] << 16));
+        for (int p = 0; p < 3; ++p)
+            reinterpret_cast<uint2*>(planes + (size_t)p * n4 * 4)[i] =
+                make_uint2(q[p][0] | ((uint32_t)q[p][1] << 16), q[p][2] | ((uint32_t)q[p][3] << 16));
+    }
+    pdl_wait();  // the next kernel may rely on everything before this call
+    pdl_trigger();
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an

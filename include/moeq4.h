@@ -190,6 +190,11 @@ size_t moe_workspace_bytes(int mode, int T, int H, int I, int E, int k);
  *   dbg        NULL or stage outputs to fill
  * Limits: H % 128 == 0, I % 128 == 0, 1 <= E <= 256, 1 <= k <= min(E, 16),
  * 0 <= T, T * k * max(H, I) < 2^31.
+ * The call's kernels are launched with programmatic dependent launch; the
+ * first one reads `wr` before the work that precedes it on the stream has
+ * finished, so `wr` must not be written by the kernel launched immediately
+ * before this call on the same stream.  x, the output and the workspace are
+ * touched only after that work has finished.
  */
 int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
                            const void* wgu_packed, const void* wd_packed,
