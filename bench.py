@@ -32,7 +32,7 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # it is in this tree: the decode expert kernel (T=1) and the prefill gate/up
 # GEMM (T=2048).  Set to None when the kernel changes before a new capture.
 NCU_TRAFFIC_DECODE_EXPERTS_T1 = 22_540_288
-NCU_TRAFFIC_PREFILL_GATEUP = 235_012_608 + 6_615_808
+NCU_TRAFFIC_PREFILL_GATEUP = 235_009_536 + 6_357_248
 KERNELS_PER_DECODE_LAYER = 2   # layer (router, top-k, buckets, x codes, gate/up, down); combine
 KERNELS_PER_PREFILL_LAYER = 8  # W_r split, router GEMM, top-k + chunk counts, bucket scan, scatter, gate/up, down, combine
 

@@ -35,8 +35,9 @@
 //          each.)
 // The weight copies carry an L2 evict-first hint: they are read once, and
 // should not push the reused token rows out of L2.
-// One thread of the MMA warp issues 4 x K=16 MMAs per matrix into TMEM; eight
-// epilogue warps read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
+// One thread of the MMA warp issues 4 x K=16 MMAs per matrix into TMEM; twelve
+// epilogue warps (the tensor pipe waits while they drain the accumulators)
+// read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
 // weight * acc, both fp16 (saturating at +-65504), in bucket order.
 // One persistent CTA per SM walks a static list of (token tile, row block)
 // work items.  The kernel is launched with programmatic dependent launch:
@@ -54,11 +55,11 @@ namespace {
 
 constexpr int BN = 160;                 // max tokens per tile (buckets are cut evenly)
 constexpr int B_BYTES = BN * 128;       // BN rows x 64 fp16
-constexpr int NUM_EPI_WARPS = 8, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 12, NUM_DEQ_WARPS = 8, NUM_B_WARPS = 4;
 constexpr int WARP_WPROD = 0, WARP_MMA = 1, WARP_B0 = 2;
 constexpr int WARP_EPI0 = WARP_B0 + NUM_B_WARPS;
 constexpr int WARP_DEQ0 = WARP_EPI0 + NUM_EPI_WARPS;
-constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 22 warps
+constexpr int NUM_THREADS = (WARP_DEQ0 + NUM_DEQ_WARPS) * 32;  // 26 warps
 constexpr int B_ROWS_PER_THREAD = BN * 8 / (NUM_B_WARPS * 32);  // 16-byte chunks: 10
 static_assert(BN * 8 % (NUM_B_WARPS * 32) == 0, "B chunks per loader thread");
 
@@ -388,9 +389,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ----------------------------------------------------------- epilogue
         // warp w reads TMEM lanes 32 (w % 4) .. +31 (one accumulator row per
-        // thread); the two warps of a lane quarter take alternate 16-column
-        // chunks, each loading 2 x 16 columns before one wait
-        const int quad = warp % 4, half = (warp - WARP_EPI0) / 4;
+        // thread); the three warps of a lane quarter take every third
+        // 16-column chunk, each loading 2 x 16 columns before one wait
+        constexpr int kEpiPerQuad = NUM_EPI_WARPS / 4;
+        static_assert(NUM_EPI_WARPS % 4 == 0, "whole lane quarters");
+        const int quad = warp % 4, half = (warp - WARP_EPI0) / 4;  // 0 .. kEpiPerQuad - 1
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         pdl_wait();  // the output buffer and routing weights of the preceding kernels
         pdl_trigger();
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 __syncwarp();
             };
-            for (int c0 = half * 16; c0 < nn; c0 += 32) {
+            for (int c0 = half * 16; c0 < nn; c0 += 16 * kEpiPerQuad) {
                 uint32_t g[16], u[16];
                 tmem_ld16(trow + c0, g);
                 tmem_ld16(trow + 256 + c0, u);
