@@ -276,6 +276,61 @@ def bench_prefill(name, steps, warmup, torch, moe, device, barrier):
     return res
 
 
+def bench_prefill_stack(steps, warmup, torch, moe, device, barrier):
+    """The 40-layer pre-norm stack (T=4096, H=2048, I=768, E=256, k=8, fresh
+    counter-generated Q4_0 weights per layer, 27.2 GB resident): one step runs
+    all layers, bf16 between them; reports ms per layer."""
+    import workloads as W
+    S = W.STACK
+    L, T, H, I, E, k = S["L"], S["T"], S["H"], S["I"], S["E"], S["k"]
+    chunk = 32
+    layers = []
+    for l in range(L):
+        wgu = torch.empty(moe.moe_q4_packed_bytes(E, 2 * I, H), dtype=torch.uint8, device=device)
+        wd = torch.empty(moe.moe_q4_packed_bytes(E, H, I), dtype=torch.uint8, device=device)
+        per_gu, per_d = wgu.numel() // E, wd.numel() // E
+        for e0 in range(0, E, chunk):
+            gc, gs, dc, ds = W.stacked_experts_torch(l, e0, e0 + chunk, device)
+            moe.moe_q4_pack(gc, gs.view(torch.int16), chunk, 2 * I, H,
+                            out=wgu[e0 * per_gu:(e0 + chunk) * per_gu])
+            moe.moe_q4_pack(dc, ds.view(torch.int16), chunk, H, I,
+                            out=wd[e0 * per_d:(e0 + chunk) * per_d])
+            del gc, gs, dc, ds
+        layers.append((torch.from_numpy(W.stacked_router(l)).to(device), wgu, wd))
+    x0 = torch.from_numpy(W.stacked_x().view(np.int16)).to(device).view(torch.bfloat16)
+    bufs = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(2)]
+    ws = torch.empty(moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL, T, H, I, E, k),
+                     dtype=torch.uint8, device=device)
+
+    def step():
+        cur = x0
+        for l, (wr, wgu, wd) in enumerate(layers):
+            nxt = bufs[l % 2]
+            moe.moe_q4_forward_prefill(cur, wr, wgu, wd, I, k, out=nxt, out_fp32=False,
+                                       workspace=ws, prenorm=True)
+            cur = nxt
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_stack = t0.elapsed_time(t1) / steps
+    flop = 2.0 * T * k * 3 * H * I
+    res = {"workload": "stacked", "layers": L, "T": T, "E": E, "ms_per_stack": ms_stack,
+           "ms_per_layer": ms_stack / L, "tokens_per_s": T / (ms_stack * 1e-3),
+           "expert_tflops": flop * L / (ms_stack * 1e-3) / 1e12}
+    del layers, x0, bufs, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 # --------------------------------------------------------------------------
 def _cpu_usage(fn):
     """Runs fn(); returns (wall seconds, effective cores = cpu time / wall)."""
@@ -368,10 +423,16 @@ def main():
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one workload only (short profiling runs)")
     ap.add_argument("--decode-tokens", type=str, default="1,4,16")
+    ap.add_argument("--prefill-workload", choices=["prefill", "skewed", "stacked"],
+                    default="prefill",
+                    help="with --only prefill: the T=2048 layer, the Zipf-skewed T=10240 "
+                         "layer or the 40-layer E=256 stack")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill_workload != "prefill" and args.only != "prefill":
+        ap.error("--prefill-workload other than prefill needs --only prefill")
 
     import torch
     import torch.distributed as dist
@@ -405,8 +466,13 @@ def main():
         dec_T = [1] + dec_T
     with ClockSampler(local) as clk:
         dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier) for T in dec_T}
-        pre = None if (args.no_prefill or args.only == "decode") else bench_prefill(
-            "prefill", args.steps, warm, torch, moe, device, barrier)
+        if args.no_prefill or args.only == "decode":
+            pre = None
+        elif args.prefill_workload == "stacked":
+            pre = bench_prefill_stack(min(args.steps, 10), warm, torch, moe, device, barrier)
+        else:
+            pre = bench_prefill(args.prefill_workload, args.steps, warm, torch, moe, device,
+                                barrier)
     if args.only == "prefill":
         print(json.dumps({"prefill": pre, "clocks": clk.summary()}))
         return 0
