@@ -172,6 +172,7 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.route_parts = reinterpret_cast<float*>(take(route_parts_floats(T, H, E) * 4));
         w.wr_planes = reinterpret_cast<uint16_t*>(take(route_planes_bytes(T, H, E)));
         w.h = reinterpret_cast<uint16_t*>(take(Tk * I * 2));
+        w.tile_done = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     } else {
         int nsg = 1, nsd = 1;
         decode_splits(T, H, I, E, k, &nsg, &nsd);
@@ -287,14 +288,12 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
             return rc;
         if ((rc = mark(2))) return rc;
         if ((rc = mark(3))) return rc;
-        // 3. grouped GEMMs
-        if ((rc = cuda_check(launch_prefill_gateup(wgu, ws, T, H, I, E, k, dev->status,
-                                                   dev->num_sms, s), "prefill gate/up")))
+        // 3. grouped GEMMs (gate/up, then down, in one launch; boundaries 4 and 5
+        // both follow it)
+        if ((rc = cuda_check(launch_prefill_experts(wgu, wd, ws, H, I, dev->status, dev->num_sms,
+                                                    s), "prefill experts")))
             return rc;
         if ((rc = mark(4))) return rc;
-        if ((rc = cuda_check(launch_prefill_down(wd, ws, T, H, I, E, k, dev->status,
-                                                 dev->num_sms, s), "prefill down")))
-            return rc;
         if ((rc = mark(5))) return rc;
         // 4. combine
         if ((rc = cuda_check(launch_combine(x, ws.y, false, ws.slot_pos, T, H, k,

@@ -60,10 +60,15 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t* __restrict__
                                                            int32_t* __restrict__ counters,
                                                            int32_t* __restrict__ tile_e,
                                                            int32_t* __restrict__ tile_n0,
-                                                           int32_t* __restrict__ tile_nn) {
+                                                           int32_t* __restrict__ tile_nn,
+                                                           int32_t* __restrict__ tile_done,
+                                                           int max_tiles) {
     __shared__ int part_tot[kScanParts][kMaxExperts];
     pdl_wait();  // the chunk counts of the top-k kernel
     pdl_trigger();
+    // the expert GEMMs count finished gate/up items per token tile from zero
+    // (the previous call's GEMMs completed before the top-k kernel did)
+    for (int i = threadIdx.x; i < max_tiles; i += blockDim.x) tile_done[i] = 0;
     const int e = threadIdx.x % kMaxExperts, part = threadIdx.x / kMaxExperts;
     const int c0 = part * nchunk / kScanParts, c1 = (part + 1) * nchunk / kScanParts;
     // this quarter's total, 16 chunk counts in flight at a time
@@ -154,7 +159,7 @@ cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int 
     const int nc = nchunks(T);
     cudaError_t err = launch_pdl(bucket_scan_kernel, dim3(1), dim3(1024), 0, s, ws.chunk_count, nc,
                                  E, tile_n, ws.offsets, ws.touched, ws.counters, ws.tile_e,
-                                 ws.tile_n0, ws.tile_nn);
+                                 ws.tile_n0, ws.tile_nn, ws.tile_done, ws.max_tiles);
     if (err != cudaSuccess) return err;
     if (T > 0)
         err = launch_pdl(bucket_scatter_kernel, dim3((T * k + 255) / 256), dim3(256), 0, s, idx, w,

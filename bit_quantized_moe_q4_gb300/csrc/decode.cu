@@ -164,15 +164,6 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Exclusive prefix sum over the 256 consumer threads (thread order); `wt` is
 // eight ints of shared memory.  Every consumer thread calls it.
 __device__ __forceinline__ int consumers_exclusive_scan(int v, int* total, int* wt) {

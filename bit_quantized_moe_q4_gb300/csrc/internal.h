@@ -36,6 +36,7 @@ struct Workspace {
     float* route_parts;     // [ksplit, T, E] router K-slice sums (prefill)
     uint16_t* wr_planes;    // [3, E, H] bf16 parts of W_r (prefill, tensor-core router)
     uint16_t* h;            // [T*k, I] fp16 (prefill)
+    int32_t* tile_done;     // [max_tiles] (prefill) gate/up epilogue warps done per token tile
     void* y;                // [T*k, H] weighted expert outputs: fp16
                             // (prefill) or fp32 (decode)
     int32_t* done;          // [E]           (decode) finished gate/up tasks per touched expert
@@ -105,12 +106,10 @@ cudaError_t launch_route_gemm(const uint16_t* x, const float* wr, int T, int H, 
 // ws (chunk bases, offsets, tile list, touched list, then the scatter).
 cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int k, int tile_n,
                           const Workspace& ws, cudaStream_t s);
-cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,
-                                  int T, int H, int I, int E, int k, int* status, int num_sms,
-                                  cudaStream_t s);
-cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
-                                int T, int H, int I, int E, int k, int* status, int num_sms,
-                                cudaStream_t s);
+// Both expert GEMMs of the prefill layer in one launch: gate/up + SwiGLU -> h,
+// then down x routing weight -> y (bucket order).
+cudaError_t launch_prefill_experts(const void* wgu, const void* wd, const Workspace& ws, int H,
+                                   int I, int* status, int num_sms, cudaStream_t s);
 // The whole W4A8 decode layer: one cooperative layer kernel (router, top-k,
 // buckets and x codes in every CTA after one grid barrier, then gate/up and
 // down) and a combine kernel.  `events` is null or the caller's

@@ -39,8 +39,17 @@
 // epilogue warps (the tensor pipe waits while they drain the accumulators)
 // read TMEM: gate/up -> h = silu(g) * u, down -> y = routing
 // weight * acc, both fp16 (saturating at +-65504), in bucket order.
-// One persistent CTA per SM walks a static list of (token tile, row block)
-// work items.  The kernel is launched with programmatic dependent launch:
+// Both GEMMs run in one launch: one persistent CTA per SM walks a static
+// round-robin list of work items, first every gate/up item (token tile, 128
+// rows of h), then every down item (token tile, 256 rows of y).  A down item
+// reads the h rows of its token tile, so its token loaders wait until the
+// tile's gate/up items have all published theirs (a per-tile count each
+// epilogue warp raises with release semantics after storing its rows; a
+// bounded acquire spin).  Every CTA is resident and every CTA finishes its
+// gate/up items before its down items, so the waits always end; the CTAs
+// that finish the gate/up items early go on to down items instead of idling
+// until the last gate/up item is done.  The kernel is launched with
+// programmatic dependent launch:
 // the weight producer and the dequant warps start on their first weight
 // tiles (which depend only on the tile list, two kernels back) while the
 // preceding kernel drains; the token loaders, the MMA and the epilogue wait
@@ -66,7 +75,6 @@ static_assert(BN * 8 % (NUM_B_WARPS * 32) == 0, "B chunks per loader thread");
 // Both GEMMs multiply two 128-row weight blocks by the same token tile:
 // gate/up the gate rows and the matching up rows, down two adjacent row
 // blocks of W_d (so each token row is read from L2 once per 256 output rows).
-template <bool GATEUP>
 struct Cfg {
     static constexpr int NMAT = 2;
     static constexpr int RK = 2;  // K-blocks per weight copy (contiguous tiles)
@@ -94,15 +102,10 @@ struct Cfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-struct GemmArgs {
+// One of the two GEMMs (0: gate/up, 1: down).
+struct GemmOp {
     const uint8_t* wpk;        // packed weights
     const uint16_t* bsrc;      // fp16 token rows: x16 [T, H] (gate/up) or h [T*k, I] (down)
-    const int32_t* counters;   // kCntTiles
-    const int32_t* tile_e;
-    const int32_t* tile_n0;
-    const int32_t* tile_nn;
-    const int32_t* bucket_token;
-    const float* slot_w;
     uint16_t* out;             // h [T*k, I] (gate/up) or y [T*k, H] (down)
     int K;                     // reduction length: H (gate/up) or I (down)
     int rows_per_e;            // packed rows per expert: 2I (gate/up) or H (down)
@@ -110,8 +113,35 @@ struct GemmArgs {
     int rb_mul;                // first row block of item i: i * rb_mul (1 or 2)
     int rb_second;             // second row block = first + rb_second (I/128 or 1)
     int out_ld;                // leading dimension of out
+};
+
+struct GemmArgs {
+    GemmOp op[2];
+    const int32_t* counters;   // kCntTiles
+    const int32_t* tile_e;
+    const int32_t* tile_n0;
+    const int32_t* tile_nn;
+    const int32_t* bucket_token;
+    const float* slot_w;
+    int* tile_done;            // [max_tiles] gate/up epilogue warps done per token tile
+                               // (zeroed by the bucket scan before every call)
     int* status;
 };
+
+// Work item w of the combined list: its GEMM, token tile, row-block index
+// and K-blocks.
+struct Item {
+    int op, tile, ri, KB;
+};
+__device__ __forceinline__ Item item_of(const GemmOp* ops, int w, int n_gu) {
+    Item it;
+    it.op = w < n_gu ? 0 : 1;
+    const int wl = it.op ? w - n_gu : w;
+    it.tile = wl / ops[it.op].rb_items;
+    it.ri = wl % ops[it.op].rb_items;
+    it.KB = ops[it.op].K / kTileK;
+    return it;
+}
 
 // Eight 4-bit codes of one packed word (columns 8c..8c+7: even columns in the
 // low 16 bits, odd in the high, nibble m = column pair m) to fp16 d(q - 8).
@@ -145,25 +175,25 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t d2) {
     return o;
 }
 
-template <bool GATEUP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_q4_gemm_kernel(const GemmArgs args) {
-    using C = Cfg<GATEUP>;
+    using C = Cfg;
     constexpr int SR = C::RAW_STAGES, SA = C::A_STAGES, SB = C::B_STAGES;
     extern __shared__ uint8_t smem_raw[];
+    __shared__ GemmOp ops[2];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* sbase = smem_raw + (base - raw_base);
 
-    const int n_items_tiles = args.counters[kCntTiles];
-    const int rb_count = args.rb_items;
-    const int n_items = n_items_tiles * rb_count;
+    const int n_tiles = args.counters[kCntTiles];
+    const int n_gu = n_tiles * args.op[0].rb_items;
+    const int n_items = n_gu + n_tiles * args.op[1].rb_items;
     if ((int)blockIdx.x >= n_items) return;
+    // a down item's h rows are complete once every epilogue warp of each of
+    // the tile's gate/up items has counted itself
+    const int tile_ready = NUM_EPI_WARPS * args.op[0].rb_items;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int KB = args.K / kTileK;
-    const int tiles_per_rb = KB;  // packed tiles per (expert, row block)
-    const int rbs_per_e = args.rows_per_e / kTileRows;
 
     const uint32_t bar0 = base + C::OFF_BAR;
     auto raw_full = [&](int s) { return bar0 + 8u * s; };
@@ -182,6 +212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::OFF_TMEM);
 
     if (threadIdx.x == 0) {
+        ops[0] = args.op[0];
+        ops[1] = args.op[1];
         for (int s = 0; s < SR; ++s) {
             mbar_init(raw_full(s), 1);
             mbar_init(raw_empty(s), NUM_DEQ_WARPS);
@@ -218,15 +250,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int it = 0;  // global K-block counter
             bool ok = true;
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-                const int tile = w / rb_count, ri = w % rb_count;
-                const int e = args.tile_e[tile];
-                const int rb0 = ri * args.rb_mul;
+                const Item im = item_of(ops, w, n_gu);
+                const GemmOp& o = ops[im.op];
+                const int e = args.tile_e[im.tile];
+                const int rbs_per_e = o.rows_per_e / kTileRows;
+                const int rb0 = im.ri * o.rb_mul;
                 // an odd last block of W_d has no partner: load it twice (the
                 // epilogue drops the copy)
-                const int rb1 = (rb0 + args.rb_second < rbs_per_e) ? rb0 + args.rb_second : rb0;
-                const uint8_t* wt0 = args.wpk + ((size_t)e * rbs_per_e + rb0) * tiles_per_rb * kTileBytes;
-                const uint8_t* wt1 = args.wpk + ((size_t)e * rbs_per_e + rb1) * tiles_per_rb * kTileBytes;
-                for (int kb = 0; kb < KB; kb += C::RK, ++it) {
+                const int rb1 = (rb0 + o.rb_second < rbs_per_e) ? rb0 + o.rb_second : rb0;
+                // im.KB packed tiles per (expert, row block)
+                const uint8_t* wt0 = o.wpk + ((size_t)e * rbs_per_e + rb0) * im.KB * kTileBytes;
+                const uint8_t* wt1 = o.wpk + ((size_t)e * rbs_per_e + rb1) * im.KB * kTileBytes;
+                for (int kb = 0; kb < im.KB; kb += C::RK, ++it) {
                     const int s = it % SR;
                     if (*abort_flag || !mbar_wait(raw_empty(s), ((it / SR) & 1) ^ 1)) {
                         fail();
@@ -253,18 +288,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0, issued = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-            const int tile = w / rb_count;
-            const int n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
+            const Item im = item_of(ops, w, n_gu);
+            const GemmOp& o = ops[im.op];
+            const int n0 = args.tile_n0[im.tile], nn = args.tile_nn[im.tile];
             const int npad = (nn + 15) & ~15;
+            if (im.op == 1) {  // the tile's h rows: wait for its gate/up items
+                const int* done = args.tile_done + im.tile;
+                if (ld_acquire(done) < tile_ready) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (ld_acquire(done) < tile_ready) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!ok) {
+                    fail();
+                    break;
+                }
+            }
             const uint16_t* src[B_ROWS_PER_THREAD];
 #pragma unroll
             for (int i = 0; i < B_ROWS_PER_THREAD; ++i) {
                 const int r = r0 + 16 * i;
                 const int rr = r < nn ? r : 0;  // padding rows repeat row 0
-                const size_t row = GATEUP ? (size_t)args.bucket_token[n0 + rr] : (size_t)(n0 + rr);
-                src[i] = args.bsrc + row * args.K + c * 8;
+                const size_t row = im.op == 0 ? (size_t)args.bucket_token[n0 + rr] : (size_t)(n0 + rr);
+                src[i] = o.bsrc + row * o.K + c * 8;
             }
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int kb = 0; kb < im.KB; ++kb, ++it) {
                 const int s = it % SB;
                 if (*abort_flag || !mbar_wait(b_empty(s), ((it / SB) & 1) ^ 1)) {
                     fail();
@@ -292,8 +344,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0, item = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++item) {
-            const int tile = w / rb_count;
-            const int nn = args.tile_nn[tile];
+            const Item im = item_of(ops, w, n_gu);
+            const int nn = args.tile_nn[im.tile];
             const int npad = (nn + 15) & ~15;
             const uint32_t idesc = idesc_f16_f32(128, npad);
             if (*abort_flag || !mbar_wait(acc_empty, (item & 1) ^ 1)) {
@@ -302,7 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (int kb = 0; kb < im.KB; ++kb, ++it) {
                 const int sa = it % SA, sb = it % SB;
                 if (*abort_flag || !mbar_wait(b_full(sb), (it / SB) & 1) ||
                     !mbar_wait(a_full(sa), (it / SA) & 1)) {
@@ -349,6 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int it = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+            const int KB = item_of(ops, w, n_gu).KB;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int ir = it / C::RK, sub = it % C::RK;  // weight copy and its K-block
                 const int sr = ir % SR, sa = it % SA;
@@ -399,7 +452,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pdl_trigger();
         int item = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++item) {
-            const int tile = w / rb_count, ri = w % rb_count;
+            const Item im = item_of(ops, w, n_gu);
+            const GemmOp& o = ops[im.op];
+            const bool gateup = im.op == 0;
+            const int tile = im.tile, ri = im.ri;
+            const int rbs_per_e = o.rows_per_e / kTileRows;
             const int n0 = args.tile_n0[tile], nn = args.tile_nn[tile];
             const bool bad = *abort_flag || !mbar_wait(acc_full, item & 1);
             if (__any_sync(0xffffffffu, bad)) {  // tcgen05.ld below needs the whole warp
@@ -407,13 +464,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const bool second = ri * args.rb_mul + args.rb_second < rbs_per_e;  // down: partner exists
+            const bool second = ri * o.rb_mul + o.rb_second < rbs_per_e;  // down: partner exists
             // 16 columns (tokens) x 32 rows (features) go through the warp's
             // transpose buffer so that each lane stores 8 consecutive features
             // of one token (16 bytes): two 16-byte stores per lane instead of
             // sixteen 2-byte ones
             uint16_t* stg = reinterpret_cast<uint16_t*>(sbase + C::OFF_STAGE) + (warp - WARP_EPI0) * 512;
-            const int fbase = ri * args.rb_mul * kTileRows + quad * 32;
+            const int fbase = ri * o.rb_mul * kTileRows + quad * 32;
             auto flush = [&](int c0, int fo) {
                 __syncwarp();
 #pragma unroll
@@ -421,7 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int tok = r * 8 + lane / 4, ch = lane % 4;
                     const uint4 v = *reinterpret_cast<const uint4*>(stg + tok * 32 + ch * 8);
                     if (c0 + tok < nn)
-                        *reinterpret_cast<uint4*>(args.out + (size_t)(n0 + c0 + tok) * args.out_ld +
+                        *reinterpret_cast<uint4*>(o.out + (size_t)(n0 + c0 + tok) * o.out_ld +
                                                   fbase + fo + ch * 8) = v;
                 }
                 __syncwarp();
@@ -431,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld16(trow + c0, g);
                 tmem_ld16(trow + 256 + c0, u);
                 tmem_ld_wait();
-                if (GATEUP) {
+                if (gateup) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
@@ -459,6 +516,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             tc_fence_before();
+            if (gateup) {  // this warp's rows of h are stored: count them for the tile
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) red_release_add(args.tile_done + tile, 1);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
         }
@@ -470,65 +532,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <bool GATEUP>
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
-    using C = Cfg<GATEUP>;
-    cudaError_t err = cudaFuncSetAttribute(grouped_q4_gemm_kernel<GATEUP>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_q4_gemm_kernel<GATEUP>, dim3(num_sms), dim3(NUM_THREADS),
-                      C::SMEM_BYTES, s, a);
-}
-
 }  // namespace
 
-cudaError_t launch_prefill_gateup(const void* wgu, const Workspace& ws,
-                                  int T, int H, int I, int E, int k, int* status, int num_sms,
-                                  cudaStream_t s) {
-    (void)T; (void)E; (void)k;
+cudaError_t launch_prefill_experts(const void* wgu, const void* wd, const Workspace& ws, int H,
+                                   int I, int* status, int num_sms, cudaStream_t s) {
     GemmArgs a{};
-    a.wpk = static_cast<const uint8_t*>(wgu);
-    a.bsrc = ws.x16;
+    GemmOp& g = a.op[0];
+    g.wpk = static_cast<const uint8_t*>(wgu);
+    g.bsrc = ws.x16;
+    g.out = ws.h;
+    g.K = H;
+    g.rows_per_e = 2 * I;
+    g.rb_items = I / kTileRows;
+    g.rb_mul = 1;
+    g.rb_second = I / kTileRows;  // the matching up rows
+    g.out_ld = I;
+    GemmOp& d = a.op[1];
+    d.wpk = static_cast<const uint8_t*>(wd);
+    d.bsrc = ws.h;
+    d.out = static_cast<uint16_t*>(ws.y);
+    d.K = I;
+    d.rows_per_e = H;
+    d.rb_items = (H / kTileRows + 1) / 2;
+    d.rb_mul = 2;
+    d.rb_second = 1;  // the next row block
+    d.out_ld = H;
     a.counters = ws.counters;
     a.tile_e = ws.tile_e;
     a.tile_n0 = ws.tile_n0;
     a.tile_nn = ws.tile_nn;
     a.bucket_token = ws.bucket_token;
     a.slot_w = ws.slot_w;
-    a.out = ws.h;
-    a.K = H;
-    a.rows_per_e = 2 * I;
-    a.rb_items = I / kTileRows;
-    a.rb_mul = 1;
-    a.rb_second = I / kTileRows;  // the matching up rows
-    a.out_ld = I;
+    a.tile_done = ws.tile_done;
     a.status = status;
-    return launch_gemm<true>(a, num_sms, s);
-}
-
-cudaError_t launch_prefill_down(const void* wd, const Workspace& ws,
-                                int T, int H, int I, int E, int k, int* status, int num_sms,
-                                cudaStream_t s) {
-    (void)T; (void)E; (void)k;
-    GemmArgs a{};
-    a.wpk = static_cast<const uint8_t*>(wd);
-    a.bsrc = ws.h;
-    a.counters = ws.counters;
-    a.tile_e = ws.tile_e;
-    a.tile_n0 = ws.tile_n0;
-    a.tile_nn = ws.tile_nn;
-    a.bucket_token = ws.bucket_token;
-    a.slot_w = ws.slot_w;
-    a.out = static_cast<uint16_t*>(ws.y);
-    a.K = I;
-    a.rows_per_e = H;
-    a.rb_items = (H / kTileRows + 1) / 2;
-    a.rb_mul = 2;
-    a.rb_second = 1;  // the next row block
-    a.out_ld = H;
-    a.status = status;
-    return launch_gemm<false>(a, num_sms, s);
+    cudaError_t err = cudaFuncSetAttribute(grouped_q4_gemm_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Cfg::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(grouped_q4_gemm_kernel, dim3(num_sms), dim3(NUM_THREADS), Cfg::SMEM_BYTES, s,
+                      a);
 }
 
 }  // namespace moeq4

@@ -123,7 +123,9 @@ typedef struct moe_debug {
                                   0 start, 1 routed, 2 bucketed,
                                   3 activations quantised (decode; equal to
                                   2 in prefill), 4 gate/up done, 5 down
-                                  done, 6 combined (end)                     */
+                                  done (prefill runs both expert GEMMs in
+                                  one launch: 4 and 5 both follow it),
+                                  6 combined (end)                           */
 } moe_debug;
 
 #define MOE_NUM_STAGE_EVENTS 7
