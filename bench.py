@@ -29,8 +29,8 @@ DECODE_LAYERS = 16          # distinct weight copies per decode step
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel as
-# it is in this tree: the decode expert kernel (T=1) and the prefill gate/up
-# GEMM (T=2048).  Set to None when the kernel changes before a new capture.
+# it is in this tree: the decode expert kernel (T=1) and the prefill expert
+# GEMMs (T=2048).  Set to None when the kernel changes before a new capture.
 NCU_TRAFFIC_DECODE_EXPERTS_T1 = 22_540_288
 NCU_TRAFFIC_PREFILL_EXPERTS = None  # not yet captured for the single-launch expert GEMMs
 KERNELS_PER_DECODE_LAYER = 2   # layer (router, top-k, buckets, x codes, gate/up, down); combine
