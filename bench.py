@@ -411,6 +411,32 @@ def run_reference(args):
     return 0
 
 
+def rank_ops(dist, world, device):
+    """barrier() and max_over_ranks(v) over the default process group (no-ops
+    for a single process); `device` holds the reduction buffer (the GPU under
+    NCCL, the CPU under gloo)."""
+    import torch
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return float(v)
+        t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def decode_value(ms_step_max, layers_per_step, world):
+    """Whole-job µs per token: the slowest rank's step time over the tokens
+    all ranks decoded in it (one token per layer per rank)."""
+    return ms_step_max * 1e3 / (layers_per_step * world)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,16 +472,7 @@ def main():
     moe.build()
     moe.load_library()
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rank_ops(dist, world, device)
 
     peaks = load_peaks()
     warm = max(args.warmup, 3)
@@ -479,7 +496,7 @@ def main():
 
     d1 = dec[1]
     ms_step = max_over_ranks(d1["ms_per_step"])
-    value = ms_step * 1e3 / (d1["layers_per_step"] * 1 * world)  # µs per token, all ranks
+    value = decode_value(ms_step, d1["layers_per_step"], world)
     e2e_ms = max_over_ranks(d1["e2e_us_per_token"] * d1["layers_per_step"] / 1e3)
     roof_gbs = d1["experts_gbs"]
     line = {
