@@ -217,3 +217,41 @@ def test_stack_equals_layer_composition():
     # a subset of tokens gives the same rows (each token is independent)
     sub = O.moe_stack_prefill(x0, layer, 2, 2, tokens=[1, 7])
     assert np.array_equal(sub, xb[[1, 7]])
+
+
+def test_rmsnorm_eps_inside_the_root_hand_worked():
+    # A row of 2^-10 (exact in bf16): mean square 2^-20 = 9.5367431640625e-7,
+    # plus eps 1e-6 gives 1.95367431640625e-6, whose root is 1.3977390e-3;
+    # 2^-10 over that is 0.6987712 = 1.3975424 x 2^-1, which bf16 (7 stored
+    # mantissa bits: 1.3975424 x 128 = 178.89 -> 179) rounds to 179/256 =
+    # 0.69921875, bits 0x3F33.  With eps outside the root the quotient would
+    # be 0.99902 (bf16 1.0, 0x3F80), and without eps exactly 1.0.
+    xn = O.rmsnorm_bf16_bits(np.full((1, 64), 2.0 ** -10))
+    assert np.all(xn == 0x3F33)
+    # a zero row stays zero (eps keeps the root positive)
+    assert np.all(O.rmsnorm_bf16_bits(np.zeros((1, 32))) == 0)
+
+
+def test_stack_prefill_hand_worked_two_layers():
+    # Layer 0 is the hand layer above (its router sends every token to expert
+    # 0, k = 1) and its input is 2.0 everywhere.  The pre-norm gives
+    # 2 / sqrt(4 + 1e-6) = 0.99999988, 1.0 in bf16, so the MoE term is the
+    # hand-computed one for x = 1 (h = 6 / (1 + e^-1.5) = 4.9054469) and the
+    # residual is 2: even rows 2 - 16 h = -76.487 -> bf16 -76.5, odd rows
+    # 2 + 32 h = 158.97 -> bf16 159.0 (both 8 significant bits).
+    # Layer 1 has all scales zero, so its MoE term vanishes and its output is
+    # its residual, which must be layer 0's output (not the stack's input).
+    x, wr, gc, gs, dc, ds = _hand_layer(2.0)
+    zero = (wr, gc, np.zeros_like(gs), dc, np.zeros_like(ds))
+
+    def layer(l):
+        return (wr, gc, gs, dc, ds) if l == 0 else zero
+
+    expect = O.f64_to_bf16_bits(np.where(np.arange(64) % 2 == 0, -76.5, 159.0))[None, :]
+    assert np.array_equal(O.moe_stack_prefill(x, layer, 1, 1), expect)
+    assert np.array_equal(O.moe_stack_prefill(x, layer, 2, 1), expect)
+    # the layers are taken in order: the zero layer first leaves x unchanged
+    # and the hand layer then acts on it
+    swapped = lambda l: layer(1 - l)  # noqa: E731
+    assert np.array_equal(O.moe_stack_prefill(x, swapped, 1, 1), x)
+    assert np.array_equal(O.moe_stack_prefill(x, swapped, 2, 1), expect)

@@ -2,7 +2,8 @@
 
 Each mutant replaces one oracle function with a plausible wrong version (an
 off-by-one offset, swapped projections, the opposite tie order, a dropped
-offset, another rounding rule, the other nibble order); with it in place at
+offset, another rounding rule, the other nibble order, the norm's eps
+outside the root, stacked layers that all read the stack's input); with it in place at
 least one of the listed pins must fail.  This shows the pins can tell the
 oracle's definitions from their likely misreadings.
 """
@@ -66,6 +67,22 @@ def blocks18_nibbles_swapped(blocks):
     return codes.reshape(*lead, nb * O.GROUP), scales
 
 
+def rmsnorm_eps_outside_root(X):
+    X = np.asarray(X, dtype=np.float64)
+    r = 1.0 / (np.sqrt(np.mean(X * X, axis=-1, keepdims=True)) + O.RMS_EPS)
+    return O.f64_to_bf16_bits(X * r)
+
+
+def stack_every_layer_reads_the_input(x_bits, layer, L, k, tokens=None, keep=False):
+    xb = np.asarray(x_bits)
+    out = xb
+    for l in range(L):
+        wr, gc, gs, dc, ds = layer(l)
+        o, _ = O.moe_prefill(xb, wr, gc, gs, dc, ds, k, prenorm=True)
+        out = O.f64_to_bf16_bits(o)
+    return out
+
+
 MUTANTS = {
     "offset -7": ("q4_dequant", dequant_offset7,
                   [PQ.test_dequant_worked_example_two_blocks, PG.test_q4_0_blocks18_decode,
@@ -83,6 +100,10 @@ MUTANTS = {
     "codes rounded half to even": ("act_quant", act_quant_half_even,
                                    [PR.test_act_quant_round_half_away_at_exact_halves,
                                     PG.test_w4a8_group_dot]),
+    "eps outside the root": ("rmsnorm_bf16_bits", rmsnorm_eps_outside_root,
+                             [PL.test_rmsnorm_eps_inside_the_root_hand_worked]),
+    "stacked layers all read the input": ("moe_stack_prefill", stack_every_layer_reads_the_input,
+                                          [PL.test_stack_prefill_hand_worked_two_layers]),
     "nibble order swapped": ("q4_from_blocks18", blocks18_nibbles_swapped,
                              [PQ.test_blocks18_hand_built, PG.test_q4_0_blocks18_decode]),
 }

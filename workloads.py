@@ -26,8 +26,9 @@ top-8 routing; the shapes follow that model family):
 * decode   T in {1,4,16}, H=2048, I=768, E=128, k=8, wr~N(0,1/sqrt(H)) so the
            router logits are ~N(0,1), seed 1
 * prefill  T=2048, H=2048, I=768, E=128, k=8, wr~N(0,0.02), seed 2
-* skewed   T=10240, same shapes, Zipf(1.1) expert popularity through a bias
-           channel, 16 experts never chosen, seed 3
+* skewed   T=10240, same shapes, expert popularity a water-filled Zipf(1.1)
+           law through a calibrated bias channel, 16 experts never chosen,
+           seed 3
 * stacked  a 40-layer stack of pre-norm layers, T=4096, H=2048, I=768, E=256,
            k=8, fresh weights per layer (27.2 GB packed), seed 4.  Its
            weights come from a counter-based generator (below) so that the
@@ -118,31 +119,123 @@ def prefill(seed: int = 2) -> LayerInputs:
     return make_layer("prefill", 2048, 2048, 768, 128, 8, seed, 0.02)
 
 
-def skewed(seed: int = 3, T: int = 10240, zipf_s: float = 1.1, dead: int = 16) -> LayerInputs:
-    """Long prefill whose expert popularity follows a Zipf law.
+def zipf_water_filled(n: int, k: int, s: float) -> np.ndarray:
+    """Per-rank selection fractions f_r = min(1, c * r^-s), r = 1..n, with c
+    chosen (bisection) so that sum_r f_r = k: a Zipf law of exponent s
+    water-filled under the cap of 1 (an expert cannot be chosen by more than
+    every token)."""
+    base = np.arange(1, n + 1, dtype=np.float64) ** -s
+    lo, hi = 0.0, float(k) * n / base.sum()
+    for _ in range(200):
+        c = 0.5 * (lo + hi)
+        if np.minimum(1.0, c * base).sum() > k:
+            hi = c
+        else:
+            lo = c
+    return np.minimum(1.0, 0.5 * (lo + hi) * base)
 
-    The last hidden channel is a constant 1 (a bias channel) and the router's
-    weight on it is b_e = s * ln(1 / rank_e) for the E - ``dead`` live experts
-    (ranks drawn as a random permutation) and -1e4 for ``dead`` experts, which
-    are then never chosen.  The other router weights are N(0, 0.02), so each
-    logit carries N(0, ~0.9) noise on top of its bias; with that noise the
-    chance of an expert being picked falls with its rank roughly as a Zipf law
-    of exponent s (exactly so for Gumbel noise of unit scale).  The realised
-    expert histogram is whatever the routing makes of these inputs.
+
+def _gaussian_selection_prob(b: np.ndarray, sig: np.ndarray, k: int, z: np.ndarray) -> np.ndarray:
+    """P_i = Pr(fewer than k of the other variables exceed L_i) for independent
+    L_i ~ N(b_i, sig_i^2): the density of L_i integrated (on the uniform grid
+    z) against the Poisson-binomial probability that at most k - 1 of the
+    others lie above it.  The count distribution of the others is built from
+    prefix and suffix products over the variables, truncated at k."""
+    from scipy.special import ndtr
+    n, G = b.size, z.size
+    p = ndtr((b[:, None] - z[None, :]) / sig[:, None])        # Pr(L_j > z)
+
+    def step(q, pj):
+        nxt = q * (1.0 - pj)[:, None]
+        nxt[:, 1:] += q[:, :-1] * pj[:, None]
+        nxt[:, k] += q[:, k] * pj                              # state k means ">= k"
+        return nxt
+
+    pre = np.zeros((n + 1, G, k + 1))
+    pre[0, :, 0] = 1.0
+    for j in range(n):
+        pre[j + 1] = step(pre[j], p[j])
+    suf = np.zeros((n + 1, G, k + 1))
+    suf[n, :, 0] = 1.0
+    for j in range(n - 1, -1, -1):
+        suf[j] = step(suf[j + 1], p[j])
+    below = np.cumsum(suf[1:, :, :k], axis=2)                 # Pr(suffix count <= m)
+    q = np.einsum("igm,igm->ig", pre[:-1, :, :k], below[:, :, ::-1])
+    dens = np.exp(-0.5 * ((z[None, :] - b[:, None]) / sig[:, None]) ** 2) / (
+        sig[:, None] * np.sqrt(2.0 * np.pi))
+    return (dens * q).sum(axis=1) * (z[1] - z[0])
+
+
+def calibrate_zipf_biases(sig: np.ndarray, k: int, s: float, T: int) -> np.ndarray:
+    """Biases b (one per live expert, in rank order) such that, with logits
+    b_i + N(0, sig_i^2) drawn independently per token, expert i is among a
+    token's k largest with probability f_i of ``zipf_water_filled``.  An
+    expert whose f_i is capped at 1 is pushed up until it misses fewer than
+    half a token in T.  Deterministic fixed-point iterations: b_i moves by
+    half the log ratio of target to current probability (the logit ratio for
+    capped experts, which only move up), re-centred on the uncapped mean
+    (the probabilities do not change under a common shift)."""
+    n = sig.size
+    f = zipf_water_filled(n, k, s)
+    cap = f >= 1.0
+    target = np.where(cap, 1.0 - 0.5 / T, f)
+
+    def logit(v):
+        return np.log(v) - np.log1p(-v)
+
+    b = np.log(f)
+    for _ in range(400):
+        z = np.linspace(b.min() - 8.0 * sig.max(), b.max() + 8.0 * sig.max(), 600)
+        P = np.clip(_gaussian_selection_prob(b, sig, k, z), 1e-12, 1.0 - 1e-12)
+        d = np.where(cap, np.maximum(0.0, logit(target) - logit(P)), np.log(target) - np.log(P))
+        if np.abs(d).max() < 1e-4:
+            break
+        b += np.clip(0.5 * d, -0.5, 0.5)
+        b -= b[~cap].mean()
+    return b
+
+
+_SKEWED_CACHE: dict = {}
+
+
+def skewed(seed: int = 3, T: int = 10240, zipf_s: float = 1.1, dead: int = 16) -> LayerInputs:
+    """Long prefill whose expert popularity follows a water-filled Zipf law.
+
+    The last hidden channel is a constant 1 (a bias channel), so the router's
+    weight on it, b_e, is added to expert e's logit exactly.  Experts are
+    ranked by a seeded permutation; the last ``dead`` of them get b = -1e4 and
+    are never chosen.  For the E - dead live ones, b is calibrated so that the
+    fraction of tokens choosing the expert of rank r is f_r = min(1, c r^-s)
+    with sum_r f_r = k (``zipf_water_filled``; at s = 1.1 the rank-1 expert is
+    chosen by every token, rank 80 by ~1.7% and rank 112 by ~1.2%).  The
+    calibration treats the rest of each logit, x[:, :H-1] . wr[e, :H-1], as
+    independent N(0, |wr[e, :H-1]|^2) noise (x ~ N(0, 1)) and solves for b by
+    fixed-point iterations on the Gaussian order statistics
+    (``calibrate_zipf_biases``); the realised histogram of the actual tokens
+    then follows the targets up to sampling noise.  The other router weights
+    are N(0, 0.02).
     """
-    H, I, E, k = 2048, 768, 128, 8
-    li = make_layer("skewed", T, H, I, E, k, seed, 0.02)
-    rng = np.random.Generator(np.random.PCG64(seed + 1000))
-    perm = rng.permutation(E)
-    live = perm[: E - dead]
-    bias = np.full(E, -1.0e4, dtype=np.float64)
-    ranks = np.arange(1, E - dead + 1, dtype=np.float64)
-    bias[live] = zipf_s * np.log(1.0 / ranks)
-    li.wr[:, H - 1] = bias.astype(np.float32)
-    li.x[:, H - 1] = f32_to_bf16_bits(np.ones(1, np.float32))[0]
-    li.notes = {"zipf_s": zipf_s, "dead_experts": sorted(int(e) for e in perm[E - dead:]),
-                "rank_order": [int(e) for e in live]}
-    return li
+    key = (seed, T, zipf_s, dead)
+    if key not in _SKEWED_CACHE:
+        H, I, E, k = 2048, 768, 128, 8
+        li = make_layer("skewed", T, H, I, E, k, seed, 0.02)
+        rng = np.random.Generator(np.random.PCG64(seed + 1000))
+        perm = rng.permutation(E)
+        live = perm[: E - dead]
+        sig = np.sqrt(np.sum(li.wr[live, : H - 1].astype(np.float64) ** 2, axis=1))
+        b_live = calibrate_zipf_biases(sig, k, zipf_s, T)
+        bias = np.full(E, -1.0e4, dtype=np.float64)
+        bias[live] = b_live
+        li.wr[:, H - 1] = bias.astype(np.float32)
+        li.x[:, H - 1] = f32_to_bf16_bits(np.ones(1, np.float32))[0]
+        li.notes = {"zipf_s": zipf_s, "dead_experts": sorted(int(e) for e in perm[E - dead:]),
+                    "rank_order": [int(e) for e in live],
+                    "target_fraction": zipf_water_filled(E - dead, k, zipf_s).tolist()}
+        _SKEWED_CACHE[key] = li
+    src = _SKEWED_CACHE[key]
+    return dataclasses.replace(src, x=src.x.copy(), wr=src.wr.copy(), gu_codes=src.gu_codes,
+                               gu_scales=src.gu_scales, d_codes=src.d_codes,
+                               d_scales=src.d_scales, notes=dict(src.notes))
 
 
 # --------------------------------------------------------------------------
