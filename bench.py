@@ -1,13 +1,15 @@
 """Benchmark of the 4-bit MoE expert-FFN layer on one GB300 (or N replicas).
 
 Default workload: the batch-1 W4A8 decode layer (T=1, H=2048, I=768, E=128,
-top-8), timed as CUDA-graph replays of a chain of 16 layers whose packed
-weights are distinct copies, so each step touches ~360 MB (> the 129 MB L2).
-The same line carries the T=4 and T=16 decode layers and the T=2048 prefill
-layer (one call per step; its 340 MB of packed weights exceed L2).
+top-8) in its decode loop: a step is one CUDA-graph replay of a chain of 16
+pre-norm layers whose packed weights are distinct copies, layer l + 1
+decoding layer l's bf16 output, so each step touches ~360 MB (> the 129 MB
+L2).  The same line carries the T=4 and T=16 chains, the T=2048 prefill
+layer, the Zipf-skewed T=10240 prefill layer and the 40-layer E=256 prefill
+stack (27 GB of weights resident).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-on a bounded sample of the same workload instead.
+on a bounded sample of the same workload instead, on all host cores.
 """
 from __future__ import annotations
 
@@ -31,9 +33,12 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel as
 # it is in this tree: the decode expert kernel (T=1) and the prefill expert
 # GEMMs (T=2048).  Set to None when the kernel changes before a new capture.
-NCU_TRAFFIC_DECODE_EXPERTS_T1 = 22_540_288
+NCU_TRAFFIC_DECODE_LAYER_T1 = None  # not yet captured for the prep + layer kernels
 NCU_TRAFFIC_PREFILL_EXPERTS = None  # not yet captured for the single-launch expert GEMMs
-KERNELS_PER_DECODE_LAYER = 2   # layer (router, top-k, buckets, x codes, gate/up, down); combine
+KERNELS_PER_DECODE_LAYER = 2   # prep (logits, x codes); layer (top-k, buckets, experts, combine)
+DECODE_WORKLOAD = ("decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 (batch-1 decode "
+                   "config), in a chain of 16 pre-norm layers with distinct weight copies, "
+                   "each layer decoding the previous one's bf16 output")
 KERNELS_PER_PREFILL_LAYER = 7  # W_r split, router GEMM, top-k + chunk counts, bucket scan, scatter, expert GEMMs, combine
 
 
@@ -118,31 +123,34 @@ def _device_layer(li, torch, moe, device):
     return x, wr, pack(li.gu_codes, li.gu_scales), pack(li.d_codes, li.d_scales)
 
 
-def bench_decode(T, steps, warmup, torch, moe, device, barrier):
+def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS):
+    """A chain of L pre-norm decode layers (distinct weight copies) in one CUDA
+    graph: layer l + 1 decodes layer l's bf16 output."""
     import workloads
     li = workloads.decode(T)
     x, wr, wgu, wd = _device_layer(li, torch, moe, device)
-    L = DECODE_LAYERS
     layers = [(wr.clone(), wgu.clone(), wd.clone()) for _ in range(L)]
-    del wgu, wd
-    outs = [torch.empty((T, li.H), dtype=torch.float32, device=device) for _ in range(L)]
+    del wr, wgu, wd
+    outs = [torch.empty((T, li.H), dtype=torch.bfloat16, device=device) for _ in range(L)]
     ws = torch.empty(moe.moe_workspace_bytes(moe.MOE_MODE_DECODE, T, li.H, li.I, li.E, li.k),
                      dtype=torch.uint8, device=device)
-    stages = moe.StageEvents()
-    # distinct experts this token batch touches (from the library's own routing)
-    idx, _ = moe.moe_route_topk(x, wr, li.k)
-    distinct = int(torch.unique(idx).numel())
+    idx = [torch.empty((T, li.k), dtype=torch.int32, device=device) for _ in range(L)]
+    dbgs = [moe.MoeDebug(topk_idx=b.data_ptr()) for b in idx]
 
-    def run_layers():
+    def run_chain(debug=False):
+        cur = x
         for l, (wr_l, wgu_l, wd_l) in enumerate(layers):
-            moe.moe_w4a8_forward_decode(x, wr_l, wgu_l, wd_l, li.I, li.k, out=outs[l],
-                                        workspace=ws, debug=stages.debug if l == L - 1 else None)
+            moe.moe_w4a8_forward_decode(cur, wr_l, wgu_l, wd_l, li.I, li.k, out=outs[l],
+                                        out_fp32=False, workspace=ws, prenorm=True,
+                                        debug=dbgs[l] if debug else None)
+            cur = outs[l]
 
-    run_layers()  # load modules outside capture
+    run_chain(debug=True)  # loads the modules outside the capture; routing per layer
     torch.cuda.synchronize()
+    distinct = [int(torch.unique(b).numel()) for b in idx]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, capture_error_mode="relaxed"):
-        run_layers()
+        run_chain()
     stream = torch.cuda.current_stream()
     for _ in range(max(warmup, 3)):
         g.replay()
@@ -156,17 +164,11 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
     torch.cuda.synchronize()
     ms_step = t0.elapsed_time(t1) / steps
     barrier()
-    # per-kernel durations of the last layer of each replay (stage events)
-    ex_ms, cb_ms = [], []
-    for _ in range(steps):
-        g.replay()
-        torch.cuda.synchronize()
-        ex_ms.append(stages.ms(0, 1))
-        cb_ms.append(stages.ms(5, 6))
-    # end to end: pinned host x in, graph, last layer's output back to the host
+    # end to end: each step takes the chain's input from pinned host memory
+    # and returns its output there (T tokens in, T tokens out per step)
     x_host = torch.empty((T, li.H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
-    out_host = torch.empty((T, li.H), dtype=torch.float32, pin_memory=True)
+    out_host = torch.empty((T, li.H), dtype=torch.bfloat16, pin_memory=True)
     for _ in range(3):
         x.copy_(x_host, non_blocking=True)
         g.replay()
@@ -181,24 +183,21 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / steps
-    gu_bytes = distinct * GU_BYTES_PER_EXPERT
-    dn_bytes = distinct * D_BYTES_PER_EXPERT
-    layer_bytes = gu_bytes + dn_bytes + li.E * li.H * 4 + T * li.H * (2 + 4)
+    expert_bytes = GU_BYTES_PER_EXPERT + D_BYTES_PER_EXPERT
+    # algorithmic bytes of each layer: its touched experts' packed weights,
+    # the router, x in and the output out (bf16)
+    layer_bytes = [d * expert_bytes + li.E * li.H * 4 + T * li.H * (2 + 2) for d in distinct]
+    us_layer = ms_step * 1e3 / L
     res = {
-        "T": T, "layers_per_step": L, "ms_per_step": ms_step,
-        "us_per_token": ms_step * 1e3 / (L * T),
-        "us_per_layer": ms_step * 1e3 / L,
-        "distinct_experts": distinct,
-        "algorithmic_bytes_per_layer": layer_bytes,
-        "layer_gbs": layer_bytes / (ms_step / L * 1e-3) / 1e9,
-        # the layer kernel: routing, then gate/up and down
-        "experts_us": statistics.mean(ex_ms) * 1e3, "combine_us": statistics.mean(cb_ms) * 1e3,
-        "gateup_bytes": gu_bytes, "down_bytes": dn_bytes, "router_bytes": li.E * li.H * 4,
+        "T": T, "layers_per_step": L, "chained": True, "prenorm": True, "ms_per_step": ms_step,
+        "us_per_token": us_layer / T, "us_per_layer": us_layer,
+        "distinct_experts_per_layer": distinct,
+        "algorithmic_bytes_per_layer": statistics.mean(layer_bytes),
+        "layer_gbs": statistics.mean(layer_bytes) / (us_layer * 1e-6) / 1e9,
         "e2e_us_per_token": e2e_ms * 1e3 / (L * T),
-        "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 4,
+        "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 2,
         "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
     }
-    res["experts_gbs"] = (gu_bytes + dn_bytes + li.E * li.H * 4) / (res["experts_us"] * 1e-6) / 1e9
     del layers, outs, ws, g
     torch.cuda.empty_cache()
     return res
@@ -330,81 +329,119 @@ def bench_prefill_stack(steps, warmup, torch, moe, device, barrier):
 
 
 # --------------------------------------------------------------------------
-def _cpu_usage(fn):
-    """Runs fn(); returns (wall seconds, effective cores = cpu time / wall)."""
-    c0, w0 = time.process_time(), time.perf_counter()
-    fn()
-    c1, w1 = time.process_time(), time.perf_counter()
-    wall = w1 - w0
-    return wall, (c1 - c0) / wall if wall > 0 else 1.0
-
-
-def cpu_baseline_decode(T=1, budget_s=12.0):
-    """The oracle's W4A8 decode of T=1 tokens, repeated for about budget_s."""
-    import workloads
-    from oracle import moe_oracle as O
-    li = workloads.decode(T)
-    n = [0]
-
-    def run():
-        t_end = time.perf_counter() + budget_s
-        while True:
-            O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
-            n[0] += 1
-            if time.perf_counter() > t_end:
+def cpu_info():
+    """CPU model and the cores this process may run on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
                 break
-
-    wall, cores = _cpu_usage(run)
-    return {"value": wall * 1e6 / (n[0] * T), "unit": "µs/token", "cores": round(cores, 1),
-            "kind": "oracle",
-            "sample": f"{n[0]} oracle decode layer call(s) of T={T} (H=2048, I=768, E=128, k=8), "
-                      f"{wall:.1f} s wall"}
+    except Exception:
+        pass
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"model": model or "unknown", "cores": int(cores)}
 
 
-def cpu_baseline_prefill(ntok=16):
-    import workloads
-    from oracle import moe_oracle as O
-    li = workloads.prefill()
-    toks = np.arange(ntok)
-    wall, cores = _cpu_usage(lambda: O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales,
-                                                   li.d_codes, li.d_scales, li.k, tokens=toks))
-    return {"value": ntok / wall, "unit": "tokens/s", "cores": round(cores, 1), "kind": "oracle",
-            "sample": f"{ntok} of the 2048 prefill tokens through the oracle, {wall:.1f} s wall"}
-
-
-def run_reference(args):
-    """The CPU oracle as the reference arm: each step is one decode layer call
-    on one token (a bounded sample of the decode workload)."""
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
-        return 0
+def _oracle_decode_worker(args):
+    """One worker of the CPU baseline: the oracle's W4A8 decode of the T=1
+    workload, repeated until `budget_s` has passed (after one untimed call).
+    Returns (calls, seconds)."""
+    budget_s, = args
     import workloads
     from oracle import moe_oracle as O
     li = workloads.decode(1)
+    call = lambda: O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes,  # noqa: E731
+                                li.d_scales, li.k)
+    call()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        call()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            return n, time.perf_counter() - t0
 
-    def step():
-        O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
 
-    for _ in range(args.warmup):
-        step()
-    times = []
-    c0, w0 = time.process_time(), time.perf_counter()
-    for _ in range(args.steps):
-        s0 = time.perf_counter()
-        step()
-        times.append(time.perf_counter() - s0)
-    wall = time.perf_counter() - w0
-    cores = (time.process_time() - c0) / wall
+def _oracle_prefill_worker(args):
+    """The oracle's prefill layer on a subset of the T=2048 workload's tokens;
+    returns the seconds it took (after loading the inputs)."""
+    tokens, = args
+    import workloads
+    from oracle import moe_oracle as O
+    li = workloads.prefill()
+    t0 = time.perf_counter()
+    O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k,
+                  tokens=np.asarray(tokens))
+    return time.perf_counter() - t0
+
+
+def _pool(n):
+    import concurrent.futures
+    import multiprocessing
+    return concurrent.futures.ProcessPoolExecutor(n, mp_context=multiprocessing.get_context("spawn"))
+
+
+def cpu_baseline_decode(budget_s=8.0, workers=None):
+    """The oracle's decode layer (T=1) on every host core: one process per core,
+    each repeating the call; µs per token = wall time / calls."""
+    info = cpu_info()
+    n = workers or info["cores"]
+    with _pool(n) as ex:
+        res = list(ex.map(_oracle_decode_worker, [(budget_s,)] * n))
+    calls = sum(c for c, _ in res)
+    wall = max(t for _, t in res)
+    return {"value": wall * 1e6 / calls, "unit": "µs/token", "cores": n, "kind": "oracle",
+            "cpu_model": info["model"],
+            "sample": f"{calls} oracle decode layer calls of T=1 (H=2048, I=768, E=128, k=8) "
+                      f"in {n} processes over {wall:.1f} s"}
+
+
+def cpu_baseline_prefill(tokens_per_worker=2, workers=None):
+    """The oracle's prefill layer on a bounded sample of the T=2048 workload's
+    tokens, split over every host core; tokens/s = sampled tokens / wall."""
+    info = cpu_info()
+    n = workers or info["cores"]
+    chunks = [list(range(i * tokens_per_worker, (i + 1) * tokens_per_worker)) for i in range(n)]
+    with _pool(n) as ex:
+        secs = list(ex.map(_oracle_prefill_worker, [(c,) for c in chunks]))
+    ntok = n * tokens_per_worker
+    wall = max(secs)
+    return {"value": ntok / wall, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "cpu_model": info["model"],
+            "sample": f"{ntok} of the 2048 prefill tokens ({tokens_per_worker} per process, "
+                      f"{n} processes), {wall:.1f} s"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on every host core: each step is one
+    decode layer call on one token in each of the processes (a bounded
+    sample of the T=1 decode workload); µs per token = step wall / processes."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    info = cpu_info()
+    n = info["cores"]
+    with _pool(n) as ex:
+        list(ex.map(_oracle_decode_worker, [(0.0,)] * n))  # spawn and load every worker
+        for _ in range(args.warmup):
+            list(ex.map(_oracle_decode_worker, [(0.0,)] * n))
+        times = []
+        for _ in range(args.steps):
+            s0 = time.perf_counter()
+            calls = sum(c for c, _ in ex.map(_oracle_decode_worker, [(0.0,)] * n))
+            times.append((time.perf_counter() - s0) / calls)
     us = statistics.mean(times) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "µs/token",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": us * n / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64/int64", "data": "synthetic",
-        "config": {"workload": "decode W4A8 MoE layer, T=1, H=2048, I=768, E=128, top-8",
-                   "parallelism": "single process (CPU oracle)"},
-        "cpu_baseline": {"value": us, "unit": "µs/token", "cores": round(cores, 1),
-                         "kind": "oracle", "sample": f"{args.steps} oracle decode calls, T=1"},
+        "config": {"workload": DECODE_WORKLOAD, "parallelism": f"{n} CPU processes (oracle)"},
+        "cpu_baseline": {"value": us, "unit": "µs/token", "cores": n, "kind": "oracle",
+                         "cpu_model": info["model"],
+                         "sample": f"{args.steps} steps of {n} concurrent oracle decode calls, T=1 "
+                                   "(each process loads the workload once, untimed)"},
         "e2e": {"value": us, "unit": "µs/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -437,6 +474,14 @@ def decode_value(ms_step_max, layers_per_step, world):
     return ms_step_max * 1e3 / (layers_per_step * world)
 
 
+def prefill_roofline(pre, peaks, traffic=None):
+    """The expert GEMMs' throughput against the dense bf16/fp16 peak."""
+    return {"bound": "tensor", "kernel": "grouped_q4_gemm_kernel (gate/up, then down)",
+            "achieved": pre["experts_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": pre["experts_tflops"] / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_source": peaks["source"] + " (burst)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,9 +489,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-stack", action="store_true",
+                    help="leave the 40-layer prefill stack (27 GB of weights) out")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one workload only (short profiling runs)")
     ap.add_argument("--decode-tokens", type=str, default="1,4,16")
+    ap.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
+                    help="layers in the decode chain (fewer: smaller profiling runs)")
     ap.add_argument("--prefill-workload", choices=["prefill", "skewed", "stacked"],
                     default="prefill",
                     help="with --only prefill: the T=2048 layer, the Zipf-skewed T=10240 "
@@ -477,19 +526,29 @@ def main():
     peaks = load_peaks()
     warm = max(args.warmup, 3)
     dec_T = [int(t) for t in args.decode_tokens.split(",")] if args.only != "prefill" else []
-    if args.only != "prefill" and 1 not in dec_T:
-        dec_T = [1] + dec_T
+    if args.only is None and 1 not in dec_T:
+        dec_T = [1] + dec_T  # the headline is the T=1 chain
+    pre = skew = stack = None
     with ClockSampler(local) as clk:
-        dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier) for T in dec_T}
-        if args.no_prefill or args.only == "decode":
-            pre = None
-        elif args.prefill_workload == "stacked":
-            pre = bench_prefill_stack(min(args.steps, 10), warm, torch, moe, device, barrier)
-        else:
-            pre = bench_prefill(args.prefill_workload, args.steps, warm, torch, moe, device,
-                                barrier)
+        dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier,
+                               L=args.decode_layers) for T in dec_T}
+        if args.only == "prefill":
+            if args.prefill_workload == "stacked":
+                pre = bench_prefill_stack(min(args.steps, 10), warm, torch, moe, device, barrier)
+            else:
+                pre = bench_prefill(args.prefill_workload, args.steps, warm, torch, moe, device,
+                                    barrier)
+        elif not (args.no_prefill or args.only == "decode"):
+            pre = bench_prefill("prefill", args.steps, warm, torch, moe, device, barrier)
+            skew = bench_prefill("skewed", min(args.steps, 20), warm, torch, moe, device, barrier)
+            if not args.no_stack:
+                stack = bench_prefill_stack(3, 3, torch, moe, device, barrier)
     if args.only == "prefill":
         print(json.dumps({"prefill": pre, "clocks": clk.summary()}))
+        return 0
+    if args.only == "decode":
+        print(json.dumps({"decode": {f"T{T}": r for T, r in dec.items()}, "clocks": clk.summary(),
+                          "device_status": moe.moe_get_device_status()}))
         return 0
     clocks = clk.summary()
     status = moe.moe_get_device_status()
@@ -498,7 +557,10 @@ def main():
     ms_step = max_over_ranks(d1["ms_per_step"])
     value = decode_value(ms_step, d1["layers_per_step"], world)
     e2e_ms = max_over_ranks(d1["e2e_us_per_token"] * d1["layers_per_step"] / 1e3)
-    roof_gbs = d1["experts_gbs"]
+    # the decode layer (prep + layer kernel) as it runs in the graph: the
+    # per-layer replay time, an upper bound on the two kernels' duration
+    us_layer = ms_step * 1e3 / d1["layers_per_step"]
+    roof_gbs = d1["algorithmic_bytes_per_layer"] / (us_layer * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "µs/token", "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": ms_step,
@@ -506,39 +568,47 @@ def main():
         "dtype": "int4 weights x int8 activations (int32 group dots, fp32 scales)",
         "data": "synthetic",
         "config": {
-            "workload": "decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 "
-                        "(batch-1 decode config); step = CUDA-graph replay of 16 layers with "
-                        "distinct weight copies",
+            "workload": DECODE_WORKLOAD if args.decode_layers == DECODE_LAYERS else
+            DECODE_WORKLOAD.replace("16", str(args.decode_layers)),
             "l2": "inputs larger than L2: each step touches ~360 MB of distinct weights",
             "parallelism": "replicas only" if world > 1 else "single GPU",
         },
-        "roofline": {"bound": "hbm", "kernel": "decode_experts_kernel", "achieved": roof_gbs,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": roof_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_DECODE_EXPERTS_T1,
-                     "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": d1["gateup_bytes"] + d1["down_bytes"] +
-                                                     d1["router_bytes"],
-                     "launch_us": d1["experts_us"]},
+        "roofline": {"bound": "hbm", "kernel": "decode_prep_kernel + decode_layer_kernel",
+                     "achieved": roof_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": roof_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_DECODE_LAYER_T1,
+                     "peak_source": peaks["source"] + " (copy)",
+                     "algorithmic_bytes_per_launch": d1["algorithmic_bytes_per_layer"],
+                     "launch_us": us_layer,
+                     "duration": "per-layer CUDA-graph replay time of the 16-layer chain"},
         "e2e": {"value": e2e_ms * 1e3 / (d1["layers_per_step"] * world), "unit": "µs/token",
                 "h2d_bytes_per_step": d1["h2d_bytes_per_step"],
-                "d2h_bytes_per_step": d1["d2h_bytes_per_step"]},
+                "d2h_bytes_per_step": d1["d2h_bytes_per_step"],
+                "step": "the token's input copied in from pinned host memory, the 16-layer "
+                        "chain, its output copied back"},
         "gpu_launches": args.steps * d1["kernels_per_step"],
         "clocks": clocks,
         "decode": {f"T{T}": r for T, r in dec.items()},
         "device_status": status,
     }
+    for T, r in dec.items():
+        r["hbm_frac"] = r["layer_gbs"] / peaks["hbm_gbs"]
     if pre is not None:
         line["prefill"] = pre
-        line["prefill_roofline"] = {
-            "bound": "tensor", "kernel": "grouped_q4_gemm_kernel (gate/up, then down)",
-            "achieved": pre["experts_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": pre["experts_tflops"] / peaks["bf16_tflops"],
-            "traffic": NCU_TRAFFIC_PREFILL_EXPERTS,
-            "peak_source": peaks["source"]}
+        line["prefill_roofline"] = prefill_roofline(pre, peaks, NCU_TRAFFIC_PREFILL_EXPERTS)
+    if skew is not None:
+        line["prefill_skewed"] = skew
+        line["prefill_skewed"]["roofline"] = prefill_roofline(skew, peaks)
+    if stack is not None:
+        line["prefill_stacked"] = stack
+        line["prefill_stacked"]["roofline"] = {
+            "bound": "tensor", "kernel": "the whole pre-norm layer (40 per step)",
+            "achieved": stack["expert_tflops"], "peak": peaks["bf16_tflops_sustained"],
+            "unit": "TFLOP/s", "frac": stack["expert_tflops"] / peaks["bf16_tflops_sustained"],
+            "traffic": None, "peak_source": peaks["source"] + " (sustained)"}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_decode(1)
+        line["cpu_baseline"] = cpu_baseline_decode()
         if pre is not None:
-            line["prefill"]["cpu_baseline"] = cpu_baseline_prefill(16)
+            line["prefill"]["cpu_baseline"] = cpu_baseline_prefill()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

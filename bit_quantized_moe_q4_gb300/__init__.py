@@ -18,7 +18,7 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "MoeError", "MoeDebug", "load_library", "build",
-    "moe_version", "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk",
+    "moe_version", "moe_q4_packed_bytes", "moe_q4_pack", "moe_q4_quantize", "moe_route_topk",
     "moe_workspace_bytes", "moe_q4_forward_prefill", "moe_w4a8_forward_decode",
     "moe_get_device_status", "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
 ]
@@ -33,6 +33,8 @@ MOE_ERR_TIMEOUT = -6
 MOE_ERR_WORKSPACE = -7
 MOE_Q4_CODES = 0
 MOE_Q4_BLOCK18 = 1
+MOE_SRC_F32 = 0
+MOE_SRC_BF16 = 1
 MOE_OUT_FP32 = 1
 MOE_STACKED_PRENORM = 2
 MOE_MODE_PREFILL = 0
@@ -43,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "moe_version", "moe_last_error_string", "moe_get_device_status", "moe_clear_device_status",
     "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk", "moe_workspace_bytes",
     "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
+    "moe_q4_quantize",
 )
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -86,6 +89,7 @@ def load_library(path: str | None = None):
         "moe_clear_device_status": (_i, [_vp]),
         "moe_q4_packed_bytes": (_sz, [_i, _i, _i]),
         "moe_q4_pack": (_i, [_i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+        "moe_q4_quantize": (_i, [_i, _vp, ctypes.c_longlong, _i, _i, _vp, _vp, _vp]),
         "moe_route_topk": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
         "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
         "moe_q4_forward_prefill": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_uint,
@@ -157,6 +161,31 @@ def moe_q4_pack(src: torch.Tensor, src_scales: torch.Tensor | None, E: int, N: i
     _check(load_library().moe_q4_pack(fmt, _ptr(src), _ptr(src_scales), E, N, K, _ptr(out),
                                       out.numel() * out.element_size(), _stream(stream)))
     return out
+
+
+def moe_q4_quantize(w: torch.Tensor, fmt: int = MOE_Q4_CODES, stream=None):
+    """Encodes float weights [..., K] (fp32 or bf16, K % 32 == 0) as Q4_0
+    blocks on the GPU.  Returns (codes uint8 [..., K], scales fp16 [..., K/32])
+    for MOE_Q4_CODES, or the 18-byte blocks uint8 [..., K/32, 18] for
+    MOE_Q4_BLOCK18."""
+    if w.dtype == torch.float32:
+        src_type = MOE_SRC_F32
+    elif w.dtype == torch.bfloat16:
+        src_type = MOE_SRC_BF16
+    else:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"weights must be float32 or bfloat16, not {w.dtype}")
+    *lead, K = w.shape
+    rows = int(w.numel() // K) if K else 0
+    if fmt == MOE_Q4_CODES:
+        codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        scales = torch.empty((*lead, K // 32), dtype=torch.float16, device=w.device)
+        _check(load_library().moe_q4_quantize(src_type, _ptr(w), rows, K, fmt, _ptr(codes),
+                                              _ptr(scales), _stream(stream)))
+        return codes, scales
+    blocks = torch.empty((*lead, K // 32, 18), dtype=torch.uint8, device=w.device)
+    _check(load_library().moe_q4_quantize(src_type, _ptr(w), rows, K, fmt, _ptr(blocks), None,
+                                          _stream(stream)))
+    return blocks
 
 
 def moe_route_topk(x: torch.Tensor, wr: torch.Tensor, k: int, logits: torch.Tensor | None = None,
@@ -260,7 +289,7 @@ class StageEvents:
 
 def moe_w4a8_forward_decode_noalloc(x, wr, wgu_packed, wd_packed, I: int, k: int, out=None,
                                     out_fp32: bool = True, debug: MoeDebug | None = None,
-                                    stream=None):
+                                    stream=None, prenorm: bool = False):
     """The decode layer with the library's fixed scratch array instead of a
     caller workspace, for callers that cannot allocate device memory (see
     include/moeq4.h).  ``out`` should be preallocated by such callers; this
@@ -270,7 +299,7 @@ def moe_w4a8_forward_decode_noalloc(x, wr, wgu_packed, wd_packed, I: int, k: int
     if out is None:
         out = torch.empty((T, H), dtype=torch.float32 if out_fp32 else torch.bfloat16,
                           device=x.device)
-    flags = MOE_OUT_FP32 if out_fp32 else 0
+    flags = (MOE_OUT_FP32 if out_fp32 else 0) | (MOE_STACKED_PRENORM if prenorm else 0)
     _check(load_library().moe_w4a8_forward_decode_noalloc(
         _ptr(x), _ptr(wr), _ptr(wgu_packed), _ptr(wd_packed), T, H, I, E, k, flags, _ptr(out),
         ctypes.byref(debug) if debug is not None else None, _stream(stream)))

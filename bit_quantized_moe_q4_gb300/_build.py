@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmoeq4.so")
 
 SOURCES = ["api.cu", "pack.cu", "route.cu", "bucket.cu", "misc.cu", "decode.cu",
-           "prefill_gemm.cu", "decode_noalloc.cu"]
+           "prefill_gemm.cu", "decode_noalloc.cu", "quantize.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -165,8 +165,8 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
     w.tile_e = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_n0 = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     w.tile_nn = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
-    w.xn = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
     if (mode == MOE_MODE_PREFILL) {
+        w.xn = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.y = take(Tk * H * 2);
         w.x16 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.route_parts = reinterpret_cast<float*>(take(route_parts_floats(T, H, E) * 4));
@@ -175,15 +175,20 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.tile_done = reinterpret_cast<int32_t*>(take((size_t)max_tiles * 4));
     } else {
         int nsg = 1, nsd = 1;
-        decode_splits(T, H, I, E, k, &nsg, &nsd);
-        w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));
-        w.gu_sum = reinterpret_cast<float*>(take(Tk * 2 * I * 4));
+        decode_split_bounds(T, H, I, E, k, &w.cap_g, &w.cap_d, &nsg, &nsd);
+        // the codes of x and their scales back to back (one contiguous copy)
+        const size_t xq_bytes = (size_t)T * H;
+        w.xq = take(xq_bytes + (size_t)T * (H / kGroup) * 8);
+        w.xs = base ? reinterpret_cast<int2*>(w.xq + xq_bytes) : nullptr;
         w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
+        w.gu_part = reinterpret_cast<float*>(take((size_t)nsg * Tk * 2 * I * 4));
+        w.hq = take(Tk * I);
+        w.hs = reinterpret_cast<int2*>(take(Tk * (I / kGroup) * 8));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
-        w.done = reinterpret_cast<int32_t*>(take((size_t)E * 4));
-        w.gbar = reinterpret_cast<int32_t*>(take(2 * 4));
+        w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));
+        w.sync = reinterpret_cast<int32_t*>(take((size_t)decode_sync_ints(T, H, I, E, k) * 4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;
@@ -204,10 +209,10 @@ int check_layer_shape(int mode, int T, int H, int I, int E, int k) {
     if (big >= (1ll << 31)) return set_err(MOE_ERR_SHAPE, "T*k*max(H,I) = %lld too large", big);
     if (mode == MOE_MODE_DECODE && T > MOE_DECODE_MAX_T)
         return set_err(MOE_ERR_SHAPE, "decode takes at most %d tokens (T=%d)", MOE_DECODE_MAX_T, T);
-    if (mode == MOE_MODE_DECODE && !decode_shape_fits(T, H, I))
+    if (mode == MOE_MODE_DECODE && T > 0 && !decode_shape_fits(T, H, I, E))
         return set_err(MOE_ERR_SHAPE,
-                       "decode with T=%d H=%d I=%d does not fit the on-chip staging "
-                       "(T*(H+I) too large)", T, H, I);
+                       "decode with T=%d H=%d I=%d E=%d does not fit the on-chip staging "
+                       "(T*(H+I) or T*E too large)", T, H, I, E);
     return MOE_OK;
 }
 
@@ -256,23 +261,25 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
         return cuda_check(record_stage(ev[i], s, capturing), "stage event");
     };
     if ((rc = mark(0))) return rc;
-    // the routed and multiplied input: x, or RMSNorm(x) for a stacked layer
-    const uint16_t* xin = x;
-    if (flags & MOE_STACKED_PRENORM) {
-        if ((rc = cuda_check(launch_rmsnorm(x, T, H, 1e-6f, ws.xn, s), "rmsnorm"))) return rc;
-        xin = ws.xn;
-    }
     if (mode == MOE_MODE_DECODE) {
-        // route (+ buckets, x codes), then experts (gate/up, down), then combine
-        if ((rc = cuda_check(launch_decode(xin, x, wr, wgu, wd, T, H, I, E, k,
+        // prep (counters, optional pre-norm, logits, x codes), then the layer
+        // kernel (top-k, buckets, gate/up, h, down, combine)
+        if ((rc = cuda_check(launch_decode(x, wr, wgu, wd, T, H, I, E, k,
+                                           (flags & MOE_STACKED_PRENORM) != 0,
                                            (flags & MOE_OUT_FP32) != 0, out, ws,
                                            dbg ? dbg->dots_gu : nullptr,
                                            dbg ? dbg->dots_d : nullptr,
-                                           dbg != nullptr && dbg->q_h != nullptr, dev->status,
+                                           dbg != nullptr && (dbg->q_h || dbg->d_h), dev->status,
                                            dev->num_sms, ev, capturing, s),
                              "decode")))
             return rc;
     } else {
+        // the routed and multiplied input: x, or RMSNorm(x) for a stacked layer
+        const uint16_t* xin = x;
+        if (flags & MOE_STACKED_PRENORM) {
+            if ((rc = cuda_check(launch_rmsnorm(x, T, H, 1e-6f, ws.xn, s), "rmsnorm"))) return rc;
+            xin = ws.xn;
+        }
         // 1. route (also writes the fp16 copy of x)
         float* logits = dbg ? dbg->logits : nullptr;
         if ((rc = cuda_check(launch_route_gemm(xin, wr, T, H, E, k, ws.route_parts, logits,
@@ -389,6 +396,30 @@ int moe_q4_pack(int fmt, const void* src, const void* src_scales, int E, int N, 
     if (rc) return rc;
     return cuda_check(launch_pack(fmt, src, src_scales, E, N, K, dst, static_cast<cudaStream_t>(stream)),
                       "pack");
+}
+
+int moe_q4_quantize(int src_type, const void* src, long long rows, int K, int fmt, void* dst,
+                    void* dst_scales, void* stream) {
+    if (src_type != MOE_SRC_F32 && src_type != MOE_SRC_BF16)
+        return set_err(MOE_ERR_INVALID_ARG, "unknown source type %d", src_type);
+    if (fmt != MOE_Q4_CODES && fmt != MOE_Q4_BLOCK18)
+        return set_err(MOE_ERR_INVALID_ARG, "unknown output format %d", fmt);
+    if (rows < 0 || K <= 0 || K % kGroup)
+        return set_err(MOE_ERR_SHAPE, "quantize needs rows >= 0 and K %% 32 == 0 (rows=%lld K=%d)",
+                       rows, K);
+    if (rows == 0) return MOE_OK;
+    if (!src || !dst || (fmt == MOE_Q4_CODES && !dst_scales))
+        return set_err(MOE_ERR_INVALID_ARG, "null pointer");
+    if (fmt == MOE_Q4_BLOCK18 && dst_scales)
+        return set_err(MOE_ERR_INVALID_ARG, "18-byte blocks carry their scales; dst_scales must be NULL");
+    if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(dst_scales) & 1u))
+        return set_err(MOE_ERR_ALIGN, "src and dst must be 16-byte aligned, dst_scales 2-byte");
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    return cuda_check(launch_quantize(src_type, src, rows, K, fmt, dst, dst_scales,
+                                      static_cast<cudaStream_t>(stream)),
+                      "quantize");
 }
 
 int moe_route_topk(const uint16_t* x_bf16, const float* wr, int T, int H, int E, int k,

@@ -19,9 +19,8 @@
 // on the GPU (different streams, or different host threads on one device)
 // race on it.  The array keeps the last call's contents; nothing in it needs
 // to start at zero: the decode path writes every scratch value it reads
-// earlier in the same call, except its grid-barrier counter, which the
-// decode call clears the first time it sees this scratch and every call
-// leaves at zero.
+// earlier in the same call, and its first kernel clears the counters the
+// second one synchronises on, whatever shape the previous call had.
 #include <stdio.h>
 
 #include <mutex>

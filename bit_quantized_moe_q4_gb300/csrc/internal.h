@@ -37,16 +37,20 @@ struct Workspace {
     uint16_t* wr_planes;    // [3, E, H] bf16 parts of W_r (prefill, tensor-core router)
     uint16_t* h;            // [T*k, I] fp16 (prefill)
     int32_t* tile_done;     // [max_tiles] (prefill) gate/up epilogue warps done per token tile
-    void* y;                // [T*k, H] weighted expert outputs: fp16
-                            // (prefill) or fp32 (decode)
-    int32_t* done;          // [E]           (decode) finished gate/up tasks per touched expert
-    int32_t* gbar;          // [2]           (decode) grid barrier: arrival count, generation
-    float* gu_sum;          // [T*k, 2I]     (decode) fp32 gate/up row sums, bucket order
-    float* y_part;          // [nsd, T*k, H]  (decode) fp32 partial weighted expert outputs
-    int8_t* q_x;            // [T, H]        (decode)
-    uint16_t* d_x;          // [T, H/32]     (decode)
-    int8_t* q_h;            // [T*k, I]      (decode)
-    uint16_t* d_h;          // [T*k, I/32]   (decode)
+    void* y;                // [T*k, H] (prefill) fp16 weighted expert outputs, bucket order
+    // decode
+    uint8_t* xq;            // [T, H]        int8 codes of x, dp4a order; xs follows directly
+    int2* xs;               // [T, H/32]     {fp32 bits of the scale, -8 * sum of the codes}
+    int8_t* q_x;            // [T, H]        codes of x, column order (stage output)
+    uint16_t* d_x;          // [T, H/32]     fp16 scales of x (stage output)
+    float* gu_part;         // [nsg, T*k, 2I] K parts of the gate/up row sums, bucket order
+    uint8_t* hq;            // [T*k, I]      int8 codes of h, dp4a order
+    int2* hs;               // [T*k, I/32]
+    int8_t* q_h;            // [T*k, I]      (stage output)
+    uint16_t* d_h;          // [T*k, I/32]
+    float* y_part;          // [nsd, T*k, H] K parts of the weighted expert outputs
+    int32_t* sync;          // counters of the layer kernel, cleared by its prep kernel
+    int cap_g, cap_d;       // bounds of the K splits (part buffers hold that many)
     int max_tiles;
     int tile_n;             // tokens per GEMM tile (prefill)
 };
@@ -86,6 +90,8 @@ int record_error(int code, const char* msg);
 // launchers; each returns cudaGetLastError() of its launch
 cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
                         void* dst, cudaStream_t s);
+cudaError_t launch_quantize(int src_type, const void* src, long long rows, int K, int fmt,
+                            void* dst, void* dst_scales, cudaStream_t s);
 cudaError_t launch_route(const uint16_t* x, const float* wr, int T, int H, int E, int k,
                          float* logits, int32_t* idx, float* w, uint16_t* x16, cudaStream_t s);
 // Router as a K-sliced fp32 GEMM into `parts` (route_parts_floats floats; H %
@@ -110,24 +116,29 @@ cudaError_t launch_bucket(const int32_t* idx, const float* w, int T, int E, int 
 // then down x routing weight -> y (bucket order).
 cudaError_t launch_prefill_experts(const void* wgu, const void* wd, const Workspace& ws, int H,
                                    int I, int* status, int num_sms, cudaStream_t s);
-// The whole W4A8 decode layer: one cooperative layer kernel (router, top-k,
-// buckets and x codes in every CTA after one grid barrier, then gate/up and
-// down) and a combine kernel.  `events` is null or the caller's
-// MOE_NUM_STAGE_EVENTS events; boundaries 1..5 are recorded after the layer
-// kernel and 6 after the combine.
-cudaError_t launch_decode(const uint16_t* x, const uint16_t* x_res, const float* wr,
-                          const void* wgu, const void* wd,
-                          int T, int H, int I, int E, int k, bool out_fp32, void* out,
-                          const Workspace& ws, int32_t* dots_gu, int32_t* dots_d, bool write_qh,
-                          int* status, int num_sms, void** events, bool capturing,
+// The whole W4A8 decode layer: a prep kernel (counters cleared, optional
+// pre-norm, router logits, int8 codes of x) and a cooperative layer kernel
+// (top-k and buckets in every CTA, gate/up, h, down, combine).  `events` is
+// null or the caller's MOE_NUM_STAGE_EVENTS events; boundary 1 is recorded
+// after the prep kernel and 2..6 after the layer kernel.
+cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
+                          int T, int H, int I, int E, int k, bool prenorm, bool out_fp32,
+                          void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
+                          bool write_qh, int* status, int num_sms, void** events, bool capturing,
                           cudaStream_t s);
-// Once per device, outside any stream capture: decides how the cooperative
-// expert kernel is launched.
+// Once per device, outside any stream capture: decides whether a cooperative
+// launch may also carry the programmatic-dependent-launch attribute.
 cudaError_t decode_prepare_device(int dev);
-// Whether the decode expert kernel's on-chip staging fits this shape.
-bool decode_shape_fits(int T, int H, int I);
-// K splits (partial-sum count) of the decode gate/up and down tasks.
-void decode_splits(int T, int H, int I, int E, int k, int* nsg, int* nsd);
+// 1: cooperative launches may carry the PDL attribute; 2: they may not.
+int cooperative_pdl_mode(int dev);
+// Whether the decode layer kernel's on-chip staging fits this shape.
+bool decode_shape_fits(int T, int H, int I, int E);
+// Bounds of the decode K splits for a shape: the caps (part-buffer budget)
+// and the largest split any routing can pick (the part buffers' size).
+void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap_d, int* nsg_max,
+                         int* nsd_max);
+// Counters the decode prep kernel clears.
+int decode_sync_ints(int T, int H, int I, int E, int k);
 // xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), one warp per token.
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
                            cudaStream_t s);

@@ -47,8 +47,9 @@
 // reads the h rows of its token tile, so its token loaders wait until the
 // tile's gate/up items have all published theirs (a per-tile count each
 // epilogue warp raises with release semantics after storing its rows; a
-// bounded acquire spin).  Every CTA is resident and every CTA finishes its
-// gate/up items before its down items, so the waits always end; the CTAs
+// bounded acquire spin).  The launch is cooperative, so every CTA is
+// resident, and every CTA finishes its gate/up items before its down items,
+// so the waits always end; the CTAs
 // that finish the gate/up items early go on to down items instead of idling
 // until the last gate/up item is done.  The kernel is launched with
 // programmatic dependent launch:
@@ -571,8 +572,23 @@ cudaError_t launch_prefill_experts(const void* wgu, const void* wd, const Worksp
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    return launch_pdl(grouped_q4_gemm_kernel, dim3(num_sms), dim3(NUM_THREADS), Cfg::SMEM_BYTES, s,
-                      a);
+    // Cooperative: the down items wait on gate/up items of other CTAs, so
+    // every CTA must be resident at once, also when other work holds SMs.
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[2];
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = s;
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = (cooperative_pdl_mode(dev) == 2) ? 1 : 2;
+    return cudaLaunchKernelEx(&cfg, grouped_q4_gemm_kernel, a);
 }
 
 }  // namespace moeq4

@@ -435,9 +435,11 @@ constexpr int TC_MIN_T = 128;
 // bits of what is left).
 __global__ void __launch_bounds__(256) split_wr_kernel(const float* __restrict__ wr, int n4,
                                                        uint16_t* __restrict__ planes) {
-    // Before the wait for the preceding kernel: W_r is the caller's (not
-    // written by the kernel launched just before this call), and the parts
-    // buffer is last read by an earlier call's router, which has finished.
+    // The parts live in the caller's workspace, which the preceding work on
+    // the stream may still be using (a decode call on the same workspace
+    // lets its successor start early): write them only after the wait.
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n4) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(wr) + i);
@@ -457,8 +459,6 @@ __global__ void __launch_bounds__(256) split_wr_kernel(const float* __restrict__
             reinterpret_cast<uint2*>(planes + (size_t)p * n4 * 4)[i] =
                 make_uint2(q[p][0] | ((uint32_t)q[p][1] << 16), q[p][2] | ((uint32_t)q[p][3] << 16));
     }
-    pdl_wait();  // the next kernel may rely on everything before this call
-    pdl_trigger();
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an

@@ -120,12 +120,14 @@ typedef struct moe_debug {
                                   event i at stage boundary i on `stream`
                                   (as external events, so they also work
                                   inside a captured CUDA graph):
-                                  0 start, 1 routed, 2 bucketed,
-                                  3 activations quantised (decode; equal to
-                                  2 in prefill), 4 gate/up done, 5 down
-                                  done (prefill runs both expert GEMMs in
-                                  one launch: 4 and 5 both follow it),
-                                  6 combined (end)                           */
+                                  prefill: 0 start, 1 routed, 2 bucketed,
+                                  3 (= 2), 4 gate/up done, 5 down done
+                                  (both expert GEMMs are one launch: 4 and
+                                  5 both follow it), 6 combined (end);
+                                  decode: 0 start, 1 logits and codes of x
+                                  done (first kernel), 2..6 all after the
+                                  second kernel (routing, experts and
+                                  combine are one launch)                    */
 } moe_debug;
 
 #define MOE_NUM_STAGE_EVENTS 7
@@ -166,6 +168,32 @@ size_t moe_q4_packed_bytes(int E, int N, int K);
 int moe_q4_pack(int fmt, const void* src, const void* src_scales,
                 int E, int N, int K, void* dst, size_t dst_bytes, void* stream);
 
+/* ---- moe_q4_quantize source types ---------------------------------------- */
+#define MOE_SRC_F32  0   /* fp32 weights                                       */
+#define MOE_SRC_BF16 1   /* bf16 weights (their 16-bit patterns)               */
+
+/*
+ * moe_q4_quantize — float weights to Q4_0-family blocks on the GPU (the page,
+ * Methodology 2 "Quantization": group-wise symmetric 4-bit weights of the
+ * Q4_0 family; the page prints no encoder, this is that family's usual
+ * rule).  Per block of 32 consecutive weights of a row: m = the element of
+ * largest magnitude (the first on a tie), sign kept; d = fp16(m / -8), round
+ * to nearest even (d may be negative); q = min(15, max(0, floor(x/d + 8.5)))
+ * against the stored d, taken exactly (the result equals the rounding of the
+ * exact rational); d = 0 gives q = 8.  So w = d (q - 8) decodes it.
+ *   src       [rows, K] fp32 or bf16 (src_type), device pointer
+ *   fmt       MOE_Q4_CODES: dst = uint8 codes [rows, K] (0..15),
+ *                           dst_scales = fp16 [rows, K/32];
+ *             MOE_Q4_BLOCK18: dst = 18-byte blocks [rows, K/32] (the layout
+ *                           above), dst_scales must be NULL
+ * The output is what moe_q4_pack takes.  Limits: rows >= 0, K % 32 == 0,
+ * src and dst 16-byte aligned (dst_scales 2-byte); inputs finite with
+ * |m / 8| <= 65504 (beyond it d overflows to infinity and every code is 8).
+ * One kernel on `stream`; nothing is allocated.
+ */
+int moe_q4_quantize(int src_type, const void* src, long long rows, int K, int fmt, void* dst,
+                    void* dst_scales, void* stream);
+
 /*
  * moe_route_topk — router logits, top-k selection and routing weights.
  *   x_bf16  [T, H] bf16 hidden states       wr [E, H] fp32 router weights
@@ -205,28 +233,26 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
                            moe_debug* dbg, void* stream);
 
 /*
- * moe_w4a8_forward_decode — one MoE layer on the W4A8 integer path: same
- * arguments and layouts as the prefill call, T <= MOE_DECODE_MAX_T, and the
- * on-chip staging must fit: T * (H + I) * 1.25 bytes plus two weight tiles
- * stay under ~170 KB (MOE_ERR_SHAPE otherwise; T = 32 at H = 2048, I = 768
- * fits).  The int32 group dots are exact; the float sums run in fp32.
+ * moe_w4a8_forward_decode — one MoE layer on the W4A8 integer path (the page,
+ * Methodology 1 "Decode (CPU)" and Key Contributions 2: 4-bit weights times
+ * 8-bit activations with integer dot products): same arguments and layouts
+ * as the prefill call, T <= MOE_DECODE_MAX_T, and the on-chip staging must
+ * fit: T * (H + I) * 1.25 bytes plus four weight tiles, and the T x E logits,
+ * stay under ~180 KB (MOE_ERR_SHAPE otherwise; T = 32 at H = 2048, I = 768,
+ * E = 256 fits).  The int32 group dots are exact; the float sums run in fp32
+ * in a fixed order, so repeated calls give the same bits.
  *
  * The call launches two kernels that let their successors start early
- * (programmatic dependent launch): a cooperative layer kernel (one CTA per
- * SM: routing, then gate/up and down) and a combine.  The layer kernel reads
- * `wr` before the work that precedes it on the stream has finished, so `wr`
- * must not be written by the kernel launched immediately before this call
- * on the same stream; x, the output and the workspace are touched only after
- * that work has finished.  The layer kernel's CTAs meet once at a grid
- * barrier whose counter lives in the workspace: it must be zero when a call
- * starts, which the library arranges (it clears it the first time it sees a
- * workspace address on a device, and every call leaves it at zero).  After a
- * MOE_ERR_TIMEOUT, pass a workspace the library has not seen before (or the
- * same one after the next call, whose combine clears the counter).  Routing
- * needs E <= 2 x (number of SMs).
- * When few experts are touched (small T) the K range of the gate/up rows is
- * split and the parts are added in fp32 in the order they arrive, so the
- * last bits of h, and rarely an int8 code of h, may differ between runs.
+ * (programmatic dependent launch): a prep kernel (router logits, int8 codes
+ * of x, and the clearing of the counters the layer kernel synchronises on)
+ * and a cooperative layer kernel (one CTA per SM: top-k, buckets, gate/up,
+ * h, down and the combine).  The prep kernel reads `wr` before the work that
+ * precedes it on the stream has finished, so `wr` must not be written by the
+ * kernel launched immediately before this call on the same stream; x, the
+ * output and the workspace are touched only after that work has finished.
+ * Nothing in the workspace has to survive from one call to the next, and
+ * any other call may use the same workspace in between.  Routing needs
+ * E <= 256 (one prep CTA per expert).
  */
 int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
                             const void* wgu_packed, const void* wd_packed,
@@ -249,14 +275,16 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
  * cudaMalloc, cudaFree or allocating library routine is called.
  *   - Shapes whose workspace (moe_workspace_bytes(MOE_MODE_DECODE, ...)) is
  *     larger than the array are rejected with MOE_ERR_WORKSPACE; 4 MiB covers
- *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8.
+ *     T <= 16 at H = 2048, I = 768, E <= 256, k = 8.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
- *   - All calls share the array and it keeps the last call's contents (no
- *     value in it has to start at zero).  Calls whose work overlaps on the GPU
- *     (several streams or host threads on one device) race on it: serialise
- *     them.
+ *   - All calls share the array and it keeps the last call's contents.  No
+ *     value in it has to start at zero: every call clears the counters it
+ *     synchronises on (in its first kernel) and writes everything else it
+ *     reads earlier in the same call, whatever shape the previous call had.
+ *     Calls whose work overlaps on the GPU (several streams or host threads
+ *     on one device) race on the array: serialise them.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 int moe_w4a8_forward_decode_noalloc(const uint16_t* x_bf16, const float* wr,

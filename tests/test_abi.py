@@ -112,3 +112,16 @@ def test_route_argument_checks(lib):
     assert f(None, FAKE, 4, 256, 8, 2, FAKE, FAKE, None, None) == moe.MOE_ERR_INVALID_ARG
     assert f(FAKE, FAKE, 4, 256, 8, 2, FAKE + 4, FAKE, None, None) == moe.MOE_ERR_ALIGN
     assert f(FAKE, FAKE, 0, 256, 8, 2, FAKE, FAKE, None, None) == moe.MOE_OK
+
+
+def test_quantize_argument_checks(lib):
+    q = lib.moe_q4_quantize
+    assert q(7, FAKE, 4, 64, 0, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG       # source type
+    assert q(0, FAKE, 4, 64, 5, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG       # format
+    assert q(0, FAKE, 4, 40, 0, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE             # K % 32
+    assert q(0, FAKE, -1, 64, 0, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE            # rows < 0
+    assert q(0, None, 4, 64, 0, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG       # null src
+    assert q(0, FAKE, 4, 64, 0, FAKE, None, None) == moe.MOE_ERR_INVALID_ARG       # no scales
+    assert q(0, FAKE, 4, 64, 1, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG       # block18 + scales
+    assert q(0, FAKE + 4, 4, 64, 0, FAKE, FAKE, None) == moe.MOE_ERR_ALIGN
+    assert q(0, FAKE, 0, 64, 0, None, None, None) == moe.MOE_OK                     # nothing to do

@@ -68,11 +68,27 @@ def test_prefill_tiny_bf16_output():
 def test_prefill_full_size_sampled(name, nsample):
     li = workloads.CONFIGS[name]()
     dl = DeviceLayer(li)
-    out = out_to_f64(dl.prefill())
+    d, dbg = moe.make_debug(moe.MOE_MODE_PREFILL, li.T, li.H, li.I, li.E, li.k)
+    out = out_to_f64(dl.prefill(debug=dbg))
     toks = _sample_tokens(li.T, nsample, seed=3)
     ref, r = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k,
                            tokens=toks)
     assert_within_tol(out[toks], ref)
+    # stage: the sampled tokens' rows of h = silu(W_g x) * (W_u x), fp16, in
+    # bucket order, each against the oracle's for the expert of its bucket
+    h = d["h"].cpu().numpy()
+    tok = d["bucket_token"].cpu().numpy()
+    slot = d["bucket_slot"].cpu().numpy()
+    X = O.bf16_bits_to_f64(li.x)
+    got, want = [], []
+    for i, t in enumerate(toks):
+        for p in np.nonzero(tok == t)[0]:
+            e = r["idx"][i, slot[p]]
+            W = O.q4_dequant(li.gu_codes[e], li.gu_scales[e])
+            want.append(O.swiglu(W[: li.I] @ X[t], W[li.I:] @ X[t]))
+            got.append(h[p].astype(np.float64))
+    assert len(got) == len(toks) * li.k
+    assert_within_tol(np.array(got), np.array(want), tol=1e-2, what="h (sampled rows)")
     # every row is finite and the residual dominates nowhere unexpectedly
     assert np.all(np.isfinite(out))
     # deterministic: a second call gives the same bits
@@ -116,6 +132,11 @@ def _decode_check(li, tol=2e-2):
                            keep_dots=True)
     idx = d["topk_idx"].cpu().numpy()
     assert np.array_equal(idx, st["idx"]), "routing differs from the oracle"
+    # bucket membership and order: bit-exact against the oracle's bucketing
+    off_o, tok_o, slot_o = O.bucket(st["idx"], li.E)
+    assert np.array_equal(d["expert_offsets"].cpu().numpy(), off_o)
+    assert np.array_equal(d["bucket_token"].cpu().numpy(), tok_o)
+    assert np.array_equal(d["bucket_slot"].cpu().numpy(), slot_o)
     # int8 activations and their scales: bit-exact
     assert np.array_equal(d["q_x"].cpu().numpy().astype(np.int64), st["qx"])
     assert np.array_equal(d["d_x"].cpu().numpy().view(np.uint16), st["dx"].view(np.uint16))
@@ -177,6 +198,72 @@ def test_decode_adversarial_integer_extremes():
     _decode_check(li)
 
 
+def test_decode_bf16_output():
+    li = workloads.decode(4)
+    dl = DeviceLayer(li)
+    out = out_to_f64(dl.decode(out_fp32=False))
+    ref, _ = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    half_ulp = np.abs(ref) * 2.0 ** -8
+    assert np.all(np.abs(out - ref) <= 2e-2 * O.rms(ref) + half_ulp)
+    # the bf16 output is the fp32 output rounded once
+    out32 = dl.decode(out_fp32=True)
+    assert np.array_equal(out, out_to_f64(out32.to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_prenorm(T):
+    # MOE_STACKED_PRENORM: route and multiply RMSNorm(x), add x itself.  The
+    # norm is taken in fp32 on the GPU and in float64 by the oracle, so an
+    # element of the normalised x can differ by one bf16 ulp and its int8
+    # code by one; the routing follows the contract, the output the layer
+    # tolerance.
+    li = workloads.decode(T)
+    X = O.bf16_bits_to_f64(li.x)
+    li.x = O.f64_to_bf16_bits(X * 7.0 + 3.0)  # an input whose norm is not ~1
+    dl = DeviceLayer(li)
+    d, dbg = moe.make_debug(moe.MOE_MODE_DECODE, li.T, li.H, li.I, li.E, li.k)
+    out = out_to_f64(moe.moe_w4a8_forward_decode(dl.x, dl.wr, dl.wgu, dl.wd, li.I, li.k,
+                                                  debug=dbg, prenorm=True))
+    ref, st = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales,
+                           li.k, prenorm=True)
+    assert np.array_equal(d["topk_idx"].cpu().numpy(), st["idx"])
+    qx = d["q_x"].cpu().numpy().astype(np.int64)
+    assert np.abs(qx - st["qx"]).max() <= 1 and (qx != st["qx"]).mean() < 0.01
+    assert_within_tol(out, ref)
+    # without the flag the same call gives a different layer
+    plain = out_to_f64(dl.decode())
+    assert not np.allclose(plain, out, atol=1e-3)
+
+
+def test_decode_deterministic():
+    # every sum runs in a fixed order: repeated calls give the same bits
+    for T in (1, 16):
+        dl = DeviceLayer(workloads.decode(T))
+        a = out_to_f64(dl.decode())
+        for _ in range(3):
+            assert np.array_equal(out_to_f64(dl.decode()), a)
+
+
+def test_shared_workspace_decode_prefill_decode():
+    # One buffer serves a decode call, then a prefill call, then a decode call
+    # again on the same stream: nothing a call reads may depend on what an
+    # earlier call of the other path left in the buffer.
+    li = workloads.decode(16)
+    dl = DeviceLayer(li)
+    ref_d, _ = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    ref_p, _ = O.moe_prefill(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
+    nb = max(moe.moe_workspace_bytes(m, li.T, li.H, li.I, li.E, li.k)
+             for m in (moe.MOE_MODE_PREFILL, moe.MOE_MODE_DECODE))
+    ws = torch.full((nb,), 0x7F, dtype=torch.uint8, device="cuda")
+    outs = [dl.decode(workspace=ws), dl.prefill(workspace=ws), dl.decode(workspace=ws),
+            dl.prefill(workspace=ws), dl.decode(workspace=ws)]
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+    for i, o in enumerate(outs):
+        assert_within_tol(out_to_f64(o), ref_p if i % 2 else ref_d)
+    assert np.array_equal(out_to_f64(outs[0]), out_to_f64(outs[4]))
+
+
 def test_decode_matches_prefill_closely():
     li = workloads.decode(16)
     dl = DeviceLayer(li)
@@ -187,10 +274,9 @@ def test_decode_matches_prefill_closely():
 
 
 def test_decode_workspace_garbage_and_reuse():
-    # The decode kernel's CTAs meet at a grid barrier whose arrival count
-    # lives in the workspace: a workspace full of garbage is cleared on its
-    # first use, and alternating two workspaces (and the library's default
-    # allocation) keeps every call correct.
+    # Every call clears the counters its kernels synchronise on: a workspace
+    # full of garbage, alternating workspaces and the default allocation all
+    # give the oracle's layer.
     li = workloads.decode(1)
     dl = DeviceLayer(li)
     ref, _ = O.moe_decode(li.x, li.wr, li.gu_codes, li.gu_scales, li.d_codes, li.d_scales, li.k)
@@ -202,3 +288,25 @@ def test_decode_workspace_garbage_and_reuse():
         torch.cuda.synchronize()
         assert moe.moe_get_device_status() == 0
         assert_within_tol(out, ref)
+        if ws is not None:
+            ws.fill_(0x3C)  # garbage again before the next use
+
+
+@pytest.mark.parametrize("path", ["prefill", "decode"])
+def test_layer_while_another_stream_holds_an_sm(path):
+    # The expert kernels of both paths have CTAs that wait on one another, so
+    # they are launched cooperatively: they start only once every CTA can be
+    # resident.  A kernel on another stream that holds one SM for ~2.5 s
+    # (longer than the kernels' 2 s bound on any wait) delays the layer
+    # instead of making it time out.
+    li = workloads.prefill() if path == "prefill" else workloads.decode(16)
+    dl = DeviceLayer(li)
+    ref = out_to_f64(dl.prefill() if path == "prefill" else dl.decode())
+    torch.cuda.synchronize()
+    other = torch.cuda.Stream()
+    with torch.cuda.stream(other):
+        torch.cuda._sleep(int(2.5 * 2.07e9))  # cycles: >= 2.5 s at the 2.07 GHz maximum clock
+    out = out_to_f64(dl.prefill() if path == "prefill" else dl.decode())
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+    assert np.array_equal(out, ref)

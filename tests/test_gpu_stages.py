@@ -194,6 +194,12 @@ def test_bucketing_bit_exact(name):
     assert off[-1] == li.T * li.k
     assert np.array_equal(np.bincount(tok, minlength=li.T), np.full(li.T, li.k))
     if name == "skewed":
+        # the water-filled Zipf(1.1) popularity of the stored histogram (the
+        # oracle's routing; fp32 logits may decide a near tie the other way)
+        import test_workloads_skew as SK
         counts = np.diff(off)
         assert np.all(counts[li.notes["dead_experts"]] == 0)
-        assert counts.max() > 3 * np.median(counts[counts > 0])
+        golden = np.zeros(li.E, np.int64)
+        for _, e, n, _ in SK._golden():
+            golden[e] = n
+        assert np.abs(counts - golden).sum() <= 0.002 * li.T * li.k

@@ -4,19 +4,23 @@ It serves callers that cannot allocate device memory — components hosted by
 an application that owns all device memory, or decode loops that must not call
 cudaMalloc — by running the decode layer on a fixed scratch array inside the
 library.  Checked here through the C ABI: two calls in a row agree with the
-workspace-taking entry point within the layer tolerance, and a shape whose
-scratch would not fit is rejected.  The file is named to be collected last.
+workspace-taking entry point within the layer tolerance; calls of different
+shapes share the array (each call clears what it synchronises on), also when
+a CUDA graph captured at one shape is replayed after an eager call of
+another; the pre-norm flag passes through; a shape whose scratch would not
+fit is rejected.  The file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads
+from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
 
 moe = pytest.importorskip("bit_quantized_moe_q4_gb300")
-from gpu_util import DeviceLayer, TOL_RMS, out_to_f64  # noqa: E402
+from gpu_util import DeviceLayer, TOL_RMS, assert_within_tol, out_to_f64  # noqa: E402
 
 
 def _check_against_workspace_entry(li):
@@ -40,6 +44,62 @@ def test_noalloc_decode_tiny():
 
 def test_noalloc_decode_full_size():
     _check_against_workspace_entry(workloads.decode(4))
+
+
+def _tokens(li, T):
+    li.T = T
+    li.x = li.x[:T].copy()
+    return li
+
+
+def test_noalloc_mixed_token_counts():
+    # T = 1, 4, 1 in a row on the one array: the scratch offsets move with T,
+    # so each call must clear its own counters.
+    base = workloads.decode(16)
+    layers = {T: DeviceLayer(_tokens(workloads.decode(16), T)) for T in (1, 4)}
+    refs = {T: out_to_f64(dl.decode()) for T, dl in layers.items()}
+    for T in (1, 4, 1, 4, 1):
+        dl = layers[T]
+        out = moe.moe_w4a8_forward_decode_noalloc(dl.x, dl.wr, dl.wgu, dl.wd, base.I, base.k)
+        assert np.array_equal(out_to_f64(out), refs[T])  # fixed summation order: same bits
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+
+
+def test_noalloc_graph_replay_after_other_shape():
+    li1 = _tokens(workloads.decode(16), 1)
+    li16 = workloads.decode(16)
+    d1, d16 = DeviceLayer(li1), DeviceLayer(li16)
+    ref1, _ = O.moe_decode(li1.x, li1.wr, li1.gu_codes, li1.gu_scales, li1.d_codes,
+                           li1.d_scales, li1.k)
+    ws_ref1 = out_to_f64(d1.decode())
+    ws_ref16 = out_to_f64(d16.decode())
+    out1 = torch.empty((1, li1.H), dtype=torch.float32, device="cuda")
+    call1 = lambda: moe.moe_w4a8_forward_decode_noalloc(  # noqa: E731
+        d1.x, d1.wr, d1.wgu, d1.wd, li1.I, li1.k, out=out1)
+    call1()  # first call on the device: before the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        call1()
+    out16 = moe.moe_w4a8_forward_decode_noalloc(d16.x, d16.wr, d16.wgu, d16.wd, li16.I, li16.k)
+    out1.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+    assert np.array_equal(out_to_f64(out16), ws_ref16)
+    assert np.array_equal(out_to_f64(out1), ws_ref1)
+    assert_within_tol(out_to_f64(out1), ref1)
+
+
+def test_noalloc_prenorm_flag():
+    li = _tokens(workloads.decode(16), 4)
+    dl = DeviceLayer(li)
+    ref = out_to_f64(moe.moe_w4a8_forward_decode(dl.x, dl.wr, dl.wgu, dl.wd, li.I, li.k,
+                                                 prenorm=True))
+    out = moe.moe_w4a8_forward_decode_noalloc(dl.x, dl.wr, dl.wgu, dl.wd, li.I, li.k,
+                                              prenorm=True)
+    assert np.array_equal(out_to_f64(out), ref)
 
 
 def test_noalloc_rejects_scratch_overflow():
