@@ -34,7 +34,7 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # it is in this tree: the decode expert kernel (T=1) and the prefill expert
 # GEMMs (T=2048).  Set to None when the kernel changes before a new capture.
 NCU_TRAFFIC_DECODE_LAYER_T1 = None  # not yet captured for the prep + layer kernels
-NCU_TRAFFIC_PREFILL_EXPERTS = None  # not yet captured for the single-launch expert GEMMs
+NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch at T=2048
 KERNELS_PER_DECODE_LAYER = 2   # prep (logits, x codes); layer (top-k, buckets, experts, combine)
 DECODE_WORKLOAD = ("decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 (batch-1 decode "
                    "config), in a chain of 16 pre-norm layers with distinct weight copies, "

@@ -183,8 +183,6 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
         w.gu_part = reinterpret_cast<float*>(take((size_t)nsg * Tk * 2 * I * 4));
-        w.hq = take(Tk * I);
-        w.hs = reinterpret_cast<int2*>(take(Tk * (I / kGroup) * 8));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
         w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));

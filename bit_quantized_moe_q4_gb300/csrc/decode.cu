@@ -75,10 +75,14 @@ constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kLayerThreads = kConsumerThreads + kGroups * 32;  // + a producer warp per group
 constexpr int kWarpProducer0 = kConsumerWarps;          // group g's producer: warp kWarpProducer0 + g
-constexpr int kMaxRing = 48;                            // tile slots of both groups' rings
-// Dynamic shared memory of the layer kernel: leaves room on the SM for a
-// prep CTA of the next call (its router row) next to it.
-constexpr int kLayerSmemBudget = 184 * 1024;
+constexpr int kSlotTiles = 4;                           // packed tiles per ring slot (one bulk copy),
+                                                        // fewer when shared memory is short
+constexpr int kMaxSlots = 12;                           // slots of both groups' rings
+constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 32 lanes x 8 floats
+// Dynamic shared memory of the layer kernel: leaves room on the SM (228 KB)
+// for its static part (13.1 KB) and a prep CTA of the next call (its router
+// row, 8 KB at H = 2048) next to it.
+constexpr int kLayerSmemBudget = 200 * 1024;
 constexpr int kPrepThreads = 128;
 constexpr int kMaxTk = MOE_DECODE_MAX_T * MOE_MAX_TOPK;
 // Tasks the K split aims for (gate/up, down); the split depends only on the
@@ -120,15 +124,14 @@ struct LayerArgs {
     int32_t* bucket_token;
     int32_t* bucket_slot;
     float* gu_part;     // [nsg, T*k, 2I] K parts of the gate (0..I-1) and up (I..2I-1) sums
-    uint8_t* hq;        // [T*k, I] int8 codes of h, dp4a order
-    int2* hs;           // [T*k, I/32] {fp32 bits of the scale, -8 * sum}
     int8_t* q_h;        // [T*k, I] stage output (column order), when write_qh
     uint16_t* d_h;      // [T*k, I/32]
     float* y_part;      // [nsd, T*k, H] K parts of the weighted expert outputs
-    int* cnt_h;         // [nslot, I/128] finished gate/up tasks per h block
-    int* done_h;        // [nslot] h blocks done per touched expert
+    int* cnt_h;         // [nslot, I/128] stored gate/up K parts per h block
     int* cnt_y;         // [H/128] finished down tasks per output column block
     int cap_g, cap_d;   // upper bounds of the K splits (size of the part buffers)
+    int ndiv_g, ndiv_d; // divisors of H/64 (resp. I/64) up to the cap, ascending
+    int div_g[16], div_d[16];
     void* out;
     int out_fp32;
     int32_t* dots_gu;   // optional stage outputs
@@ -136,8 +139,9 @@ struct LayerArgs {
     int write_qh;
     int* status;
     // shared-memory plan (bytes from the dynamic base)
-    int ns;             // slots (one tile each) of each group's ring
-    int off_bar, off_ax, off_ah, ah_bytes;
+    int ns;             // slots of each group's ring
+    int st;             // packed tiles per slot (kSlotTiles, or fewer for large T)
+    int off_bar, off_ax, off_ah, ah_bytes, off_red;
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -333,6 +337,11 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
 }
 
 // ----------------------------------------------------------------- layer
+// MAXNT: the most tokens an expert's bucket may hold (T <= MAXNT).  At most
+// 96 registers a thread, which leaves room on the SM for the next call's
+// prep CTA; the MAXNT = 32 variant spills a little instead (it only runs
+// when more than 16 tokens are decoded at once).
+template <int MAXNT>
 __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ int s_idx[kMaxTk];
@@ -343,7 +352,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     __shared__ uint32_t s_mask[kMaxExperts];
     __shared__ int s_off[kMaxExperts + 1];
     __shared__ int s_touched[kMaxExperts];
-    __shared__ int s_slot_tile[kMaxRing];  // the latest tile issued into each slot (both rings)
+    __shared__ int s_slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
     __shared__ int s_nt;
     __shared__ volatile int s_abort;
     __shared__ volatile int s_flag[kGroups];
@@ -360,7 +369,8 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     // group g's ring: slots g*ns .. g*ns + ns - 1
     auto full_bar = [&](int g, int s) { return bar0 + 8u * (g * ns + s); };
     auto empty_bar = [&](int g, int s) { return bar0 + 8u * (2 * ns + g * ns + s); };
-    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * kTileBytes); };
+    const int st = a.st;
+    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
     auto fail = [&]() {
         record_status(a.status, kStatusTimeout);
         s_abort = 1;
@@ -375,13 +385,21 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         s_abort = 0;
         fence_mbar_init();
     }
-    for (int s = tid; s < kMaxRing; s += kLayerThreads) s_slot_tile[s] = -1;
+    for (int s = tid; s < kMaxSlots; s += kLayerThreads) s_slot_chunk[s] = -1;
     __syncthreads();
     pdl_wait();     // the prep kernel's logits, codes and cleared counters
     pdl_trigger();  // the next call's prep may be scheduled; it waits for our end
+    if (warp < kConsumerWarps) {
+        // the int8 codes of x and their scales (written by the prep kernel)
+        // start on their way to shared memory while the CTA routes
+        const int n16 = (T * H + T * Gx * 8) / 16;
+        const uint8_t* src = a.xq;
+        for (int i = tid; i < n16; i += kConsumerThreads)
+            cp_async16(sbase + a.off_ax + 16 * i, src + 16 * (size_t)i);
+    }
 
     // ---------------------------------------------- routing (every CTA)
-    float* s_lg = reinterpret_cast<float*>(dsm);  // [T][E], in the (still unused) ring
+    float* s_lg = reinterpret_cast<float*>(dsm);  // [T][E], in the (still idle) rings and buffers
     for (int i = tid; i < T * E; i += kLayerThreads) s_lg[i] = __ldcg(a.logits + i);
     for (int e = tid; e < E; e += kLayerThreads) s_mask[e] = 0u;
     __syncthreads();
@@ -461,72 +479,115 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     __syncthreads();
 
     // ------------------------------------------------------- work split
-    const int nsg = decode_split_for(nt * RBg, KBg, kTargetGU, a.cap_g);
-    const int nsd = decode_split_for(nt * RBd, KBd, kTargetD, a.cap_d);
+    // K splits: the smallest divisor of the row's 64-column blocks (up to
+    // the cap, listed by the host in ascending order) that gives enough
+    // tasks, else the largest.
+    int nsg = a.div_g[a.ndiv_g - 1], nsd = a.div_d[a.ndiv_d - 1];
+    for (int q = 0; q < a.ndiv_g; ++q)
+        if (nt * RBg * a.div_g[q] >= kTargetGU) { nsg = a.div_g[q]; break; }
+    for (int q = 0; q < a.ndiv_d; ++q)
+        if (nt * RBd * a.div_d[q] >= kTargetD) { nsd = a.div_d[q]; break; }
     const int KCg = KBg / nsg, KCd = KBd / nsd;
-    const int n_gu = nt * RBg * nsg, n_dn = nt * RBd * nsd;
-    const int gu0 = (int)((long long)b * n_gu / G), gu1 = (int)((long long)(b + 1) * n_gu / G);
-    const int dn0 = (int)((long long)b * n_dn / G), dn1 = (int)((long long)(b + 1) * n_dn / G);
+    const int n_gu = nt * RBg * nsg, n_dn = nt * RBd * nsd;  // (x G fits in 32 bits: checked at launch)
+    const int gu0 = b * n_gu / G, gu1 = (b + 1) * n_gu / G;
+    const int dn0 = b * n_dn / G, dn1 = (b + 1) * n_dn / G;
     const int ngl = gu1 - gu0, ndl = dn1 - dn0;  // this CTA's tasks: gate/up, then down
-    // The CTA's task list (local index j: gate/up tasks j < ngl, then down
-    // tasks) is cut in two contiguous halves of about equal tile count, one
-    // per consumer group, so that each group meets runs of tasks that share a
-    // counter (consecutive K parts of one row block) and counts a run once.
-    auto tile0 = [&](int j) { return j < ngl ? j * KCg : ngl * KCg + (j - ngl) * KCd; };
-    const int nloc = ngl + ndl, half = (tile0(nloc) + 1) / 2;
-    int jm = half <= ngl * KCg ? (half + KCg - 1) / KCg
-                               : ngl + (half - ngl * KCg + KCd - 1) / KCd;
-    jm = jm > nloc ? nloc : jm;
-    // the cut nearest the middle: one task earlier if that splits more evenly
-    if (jm > 0 && 2 * tile0(jm - 1) >= 2 * tile0(nloc) - 2 * tile0(jm)) --jm;
-    auto jbeg = [&](int g) { return g == 0 ? 0 : jm; };
-    auto jend = [&](int g) { return g == 0 ? jm : nloc; };
+    // Each group takes a contiguous half of the gate/up tasks, then a
+    // contiguous half of the down tasks, so both groups are in the same
+    // phase and each meets runs of tasks that share a counter.
+    const int gh = (ngl + 1) / 2, dh = ndl / 2;
 
+    // A walk over one group's tasks in order: gate/up tasks (expert slot i,
+    // row block rb, K part kc), then down tasks (i, row block rb, K part kc),
+    // advanced by counting (no division per step).
+    struct Walk {
+        int left_g, left_d;  // tasks left in each phase
+        int i, rb, kc;       // the current task
+        bool gu;
+    };
+    auto walk_start = [&](int g) {
+        Walk w;
+        w.left_g = g == 0 ? gh : ngl - gh;
+        w.left_d = g == 0 ? dh : ndl - dh;
+        w.gu = w.left_g > 0;
+        const int t = w.gu ? gu0 + (g == 0 ? 0 : gh) : dn0 + (g == 0 ? 0 : dh);
+        const int per = w.gu ? RBg * nsg : RBd * nsd, ns_ = w.gu ? nsg : nsd;
+        w.i = t / per;
+        w.rb = (t % per) / ns_;
+        w.kc = t % ns_;
+        return w;
+    };
+    auto walk_next = [&](Walk w, int g) {
+        if (w.gu) {
+            if (--w.left_g > 0) {
+                if (++w.kc == nsg) { w.kc = 0; if (++w.rb == RBg) { w.rb = 0; ++w.i; } }
+            } else if (w.left_d > 0) {  // on to the group's first down task
+                w.gu = false;
+                const int t = dn0 + (g == 0 ? 0 : dh);
+                w.i = t / (RBd * nsd);
+                w.rb = (t % (RBd * nsd)) / nsd;
+                w.kc = t % nsd;
+            }
+        } else {
+            --w.left_d;
+            if (++w.kc == nsd) { w.kc = 0; if (++w.rb == RBd) { w.rb = 0; ++w.i; } }
+        }
+        return w;
+    };
+    auto walk_live = [&](const Walk& w) { return w.gu ? w.left_g > 0 : w.left_d > 0; };
+    auto walk_base = [&](const Walk& w) -> const uint8_t* {
+        return w.gu ? a.wgu + (((size_t)s_touched[w.i] * RBg + w.rb) * KBg + (size_t)w.kc * KCg) * kTileBytes
+                    : a.wd + (((size_t)s_touched[w.i] * RBd + w.rb) * KBd + (size_t)w.kc * KCd) * kTileBytes;
+    };
+
+    // Chunks: the group's tiles, in sequence order, are cut into runs of up
+    // to st tiles that lie back to back in memory (one bulk copy, one ring
+    // slot each).  Producer and consumers apply the same rule to the same
+    // sequence: a tile opens a new chunk unless it directly follows the
+    // open chunk's last tile and the chunk has room.  Slot and phase advance
+    // by counting.
     if (warp >= kWarpProducer0) {
         // ---------------------------------------------------------- producer
-        // The group's tiles in its consumption order: the first ring's worth
-        // by all lanes at once (every slot starts free), then the rest in
-        // order by one lane, each waiting for its slot, which held the tile
-        // ns earlier (already issued), so a parity wait never aliases.
+        // One lane issues the chunks in order; chunk c's slot held chunk
+        // c - ns, issued before it, so a parity wait never aliases.
         const int g = warp - kWarpProducer0;
-        const int t0 = tile0(jbeg(g)), nq = tile0(jend(g)) - t0;
-        auto issue = [&](int q) -> bool {
-            const int t = t0 + q;
-            const uint8_t* src;
-            if (t < ngl * KCg) {
-                const int task = gu0 + t / KCg, u = t % KCg;
-                const int i = task / (RBg * nsg), rem = task % (RBg * nsg);
-                src = a.wgu + (((size_t)s_touched[i] * RBg + rem / nsg) * KBg + (rem % nsg) * KCg + u) *
-                                  kTileBytes;
-            } else {
-                const int td = t - ngl * KCg;
-                const int task = dn0 + td / KCd, u = td % KCd;
-                const int i = task / (RBd * nsd), rem = task % (RBd * nsd);
-                src = a.wd + (((size_t)s_touched[i] * RBd + rem / nsd) * KBd + (rem % nsd) * KCd + u) *
-                                 kTileBytes;
+        if (lane == 0) {
+            int slot = -1, phase = 0, clen = 0, cidx = -1;
+            const uint8_t* caddr = nullptr;
+            bool ok = true;
+            auto issue = [&]() -> bool {
+                if (s_abort || !mbar_wait(empty_bar(g, slot), phase ^ 1) || s_abort) {
+                    fail();
+                    return false;
+                }
+                s_slot_chunk[g * ns + slot] = cidx;
+                mbar_arrive_expect_tx(full_bar(g, slot), (uint32_t)(clen * kTileBytes));
+                bulk_g2s(sbase + slot_addr(g, slot), caddr, (uint32_t)(clen * kTileBytes), full_bar(g, slot));
+                return true;
+            };
+            for (Walk w = walk_start(g); walk_live(w) && ok; w = walk_next(w, g)) {
+                const uint8_t* base = walk_base(w);
+                const int KC = w.gu ? KCg : KCd;
+                for (int u = 0; u < KC; ++u) {
+                    const uint8_t* t = base + (size_t)u * kTileBytes;
+                    if (cidx < 0 || clen == st || t != caddr + (size_t)clen * kTileBytes) {
+                        if (cidx >= 0 && !(ok = issue())) break;
+                        ++cidx;
+                        if (++slot == ns) { slot = 0; phase ^= 1; }
+                        clen = 0;
+                        caddr = t;
+                    }
+                    ++clen;
+                }
             }
-            const int s = q % ns;
-            if (s_abort || !mbar_wait(empty_bar(g, s), ((q / ns) & 1) ^ 1) || s_abort) {
-                fail();
-                return false;
-            }
-            s_slot_tile[g * ns + s] = q;
-            mbar_arrive_expect_tx(full_bar(g, s), (uint32_t)kTileBytes);
-            bulk_g2s(sbase + slot_addr(g, s), src, (uint32_t)kTileBytes, full_bar(g, s));
-            return true;
-        };
-        const int nfirst = nq < ns ? nq : ns;
-        bool ok = true;
-        for (int q = lane; q < nfirst; q += 32) ok = ok && issue(q);
-        if (__all_sync(0xffffffffu, ok) && lane == 0)
-            for (int q = nfirst; q < nq; ++q)
-                if (!issue(q)) break;
+            if (ok && cidx >= 0) issue();
+        }
         // every copy issued lands before the CTA can go away: wait for the
-        // latest use of each slot (earlier uses completed before it)
+        // latest chunk of each slot (earlier ones completed before it)
         __syncwarp();
         for (int s = lane; s < ns; s += 32) {
-            const int q = s_slot_tile[g * ns + s];
-            if (q >= 0) mbar_wait(full_bar(g, s), (q / ns) & 1);
+            const int c = s_slot_chunk[g * ns + s];
+            if (c >= 0) mbar_wait(full_bar(g, s), (c / ns) & 1);
         }
         return;
     }
@@ -539,35 +600,25 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     const int2* ax_s = reinterpret_cast<const int2*>(ax_q + (size_t)T * H);  // [T][Gx]
     uint8_t* ah_q = dsm + a.off_ah + grp * a.ah_bytes;                       // [c][I]
     int2* ah_s = reinterpret_cast<int2*>(ah_q + (size_t)T * I);              // [c][Gh]
-    {
-        // the int8 codes of x (and their scales), written by the prep kernel
-        const int n16 = (T * H + T * Gx * 8) / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(a.xq);
-        uint4* dst = reinterpret_cast<uint4*>(ax_q);
-        for (int i = tid; i < n16; i += kConsumerThreads) dst[i] = __ldcg(src + i);
-        named_sync(1, kConsumerThreads);
-    }
+    uint8_t* red_buf = dsm + a.off_red + grp * kRedBytes;                     // K-part sums of h
+    cp_async_wait_all();  // this thread's copies of the codes of x
+    named_sync(1, kConsumerThreads);
     // Control flow must stay uniform within a group (it shares named
     // barriers): a failed wait only skips work; decisions the group shares
     // are taken by its thread 0 and read after a group barrier.
     bool live = true;  // this warp has not given up
-    auto slot_ready = [&](int q) -> bool {
-        if (!live) return false;
-        if (s_abort || !mbar_wait(full_bar(grp, q % ns), (q / ns) & 1)) {
-            fail();
-            live = false;
-        }
-        return live;
-    };
+    int slot = -1, phase = 0, clen = 0, cidx = -1;  // the open chunk (same walk as the producer)
+    const uint8_t* caddr = nullptr;
     const int r_lane = lane >> 1, h_lane = lane & 1;
     const int lrow = w8 * 16 + r_lane;  // this lane's row in the 128-row block
 
     // One task: rows rb*128 + lrow, 64-column blocks kb0 .. kb0 + KC - 1 of
-    // the current expert (bucket rows off .. off + c - 1, NT >= c), tiles q0 ..
-    // of the group's sequence.  The lane pair's sum for bucket row off + n is stored at
-    // dst[n * ld] (down: times the row's routing weight).
-    auto run_tiles = [&](auto ntc, bool gu, int off, int c, int q0, int kb0, int KC, int row,
-                         float* dst, size_t ld) {
+    // the current expert (bucket rows off .. off + c - 1, NT >= c), packed
+    // tiles base .. base + KC - 1; `next_contig`: the group's next tile lies
+    // right after this task's last.  The lane pair's sum for bucket row
+    // off + n is stored at dst[n * ld] (down: times the row's routing weight).
+    auto run_tiles = [&](auto ntc, bool gu, int off, int c, const uint8_t* base, bool next_contig,
+                         int kb0, int KC, int row, float* dst, size_t ld) {
         constexpr int NT = decltype(ntc)::value;
         const uint8_t* aq = gu ? ax_q : ah_q;
         const int2* as = gu ? ax_s : ah_s;
@@ -578,29 +629,44 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n] = 0.f;
         for (int u = 0; u < KC; ++u) {
-            const int q = q0 + u;
-            if (!slot_ready(q)) continue;
-            const uint8_t* tile = dsm + slot_addr(grp, q % ns);
-            const uint4 wv = *reinterpret_cast<const uint4*>(tile + w8 * 512 + lane * 16);
-            const float dw = half_bits_to_float(
-                *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + w8 * 64 + lane * 2));
-            const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
-                                    wv.w & 0x0F0F0F0Fu};
-            const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
-                                    (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
-            const int g = 2 * (kb0 + u) + h_lane;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                if (n < c) {
-                    const int ar = gu ? s_btok[off + n] : n;
-                    const int2 sc = as[ar * Gk + g];
-                    const int dot = group_dot(wl, wh, aq + (size_t)ar * K + g * kGroup, sc.y);
-                    acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
-                    if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+            const uint8_t* tg = base + (size_t)u * kTileBytes;
+            if (cidx < 0 || clen == st || tg != caddr + (size_t)clen * kTileBytes) {
+                ++cidx;
+                if (++slot == ns) { slot = 0; phase ^= 1; }
+                clen = 0;
+                caddr = tg;
+                if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
+                    fail();
+                    live = false;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(grp, q % ns));  // the tile is consumed
+            const uint8_t* tile = dsm + slot_addr(grp, slot) + clen * kTileBytes;
+            ++clen;
+            if (live) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(tile + w8 * 512 + lane * 16);
+                const float dw = half_bits_to_float(
+                    *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + w8 * 64 + lane * 2));
+                const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
+                                        wv.w & 0x0F0F0F0Fu};
+                const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
+                                        (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                const int g = 2 * (kb0 + u) + h_lane;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    if (n < c) {
+                        const int ar = gu ? s_btok[off + n] : n;
+                        const int2 sc = as[ar * Gk + g];
+                        const int dot = group_dot(wl, wh, aq + (size_t)ar * K + g * kGroup, sc.y);
+                        acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
+                        if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                    }
+                }
+            }
+            // the chunk's last tile frees its slot
+            if (clen == st || (u + 1 == KC && !next_contig)) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(grp, slot));
+            }
         }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
@@ -608,14 +674,14 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
             if (n < c && h_lane == 0 && live) dst[n * ld] = gu ? v : v * s_bsw[off + n];
         }
     };
-    auto dispatch = [&](bool gu, int off, int c, int q0, int kb0, int KC, int row, float* dst,
-                        size_t ld) {
-        if (c <= 1) run_tiles(IntC<1>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
-        else if (c <= 2) run_tiles(IntC<2>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
-        else if (c <= 4) run_tiles(IntC<4>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
-        else if (c <= 8) run_tiles(IntC<8>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
-        else if (c <= 16) run_tiles(IntC<16>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
-        else run_tiles(IntC<MOE_DECODE_MAX_T>{}, gu, off, c, q0, kb0, KC, row, dst, ld);
+    auto dispatch = [&](bool gu, int off, int c, const uint8_t* base, bool next_contig, int kb0,
+                        int KC, int row, float* dst, size_t ld) {
+        if (c <= 1) run_tiles(IntC<1>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+        else if (c <= 2) run_tiles(IntC<2>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+        else if (c <= 4) run_tiles(IntC<4>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+        else if (c <= 8) run_tiles(IntC<8>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+        else if (MAXNT <= 16 || c <= 16) run_tiles(IntC<16>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+        else run_tiles(IntC<MAXNT>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
     };
     // Adds a run's `add` finished tasks to `counter` (one release + acquire
     // atomic by one thread, after the group barrier that orders the run's
@@ -629,47 +695,61 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         return s_flag[grp] != 0;
     };
 
-    const int jb = jbeg(grp), je = jend(grp), qb = tile0(jb);
-    int h_expert = -1;  // touched slot whose h is in this group's buffer
-    int run = 0;        // tasks of the current run counted so far
-    for (int j = jb; j < je; ++j) {
-        if (j < ngl) {
-            // ------------------------------------------ gate/up task
-            const int task = gu0 + j;
-            const int i = task / (RBg * nsg), rem = task % (RBg * nsg);
-            const int rb = rem / nsg, kc = rem % nsg;
-            const int e = s_touched[i], off = s_off[e], c = s_off[e + 1] - off;
-            const int row = rb * kTileRows + lrow;
-            dispatch(true, off, c, tile0(j) - qb, kc * KCg, KCg, row,
-                     a.gu_part + ((size_t)kc * Tk + off) * 2 * I + row, (size_t)2 * I);
-            ++run;
-            // the run goes on while the next task counts toward the same h block
-            const int hb = rb % RBh;
-            if (j + 1 < je && j + 1 < ngl && (task + 1) / (RBg * nsg) == i &&
-                ((task + 1) % (RBg * nsg)) / nsg % RBh == hb)
-                continue;
-            const int add = run;
-            run = 0;
-            if (!flush(&a.cnt_h[i * RBh + hb], add, 2 * nsg)) continue;
-            // the last run of h block hb: h = silu(g) * u over the K parts in
-            // order, int8 per 32 features.  A warp takes four groups at once,
-            // eight lanes a group, four features a lane.
-            const int sub = lane / 8, l8 = lane % 8;
-            for (int q0 = w8 * 4; q0 < 4 * c; q0 += 4 * kGroupWarps) {
-                const int q = q0 + sub;
-                const bool ok = q < 4 * c;
-                const int n = ok ? q / 4 : 0, gg = ok ? q % 4 : 0;
-                const int f0 = hb * kTileRows + gg * kGroup + l8 * 4;
-                float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
-                if (ok) {
-                    for (int p = 0; p < nsg; ++p) {
-                        const float* src = a.gu_part + ((size_t)p * Tk + off + n) * 2 * I + f0;
-                        const float4 g4 = __ldcg(reinterpret_cast<const float4*>(src));
-                        const float4 u4 = __ldcg(reinterpret_cast<const float4*>(src + I));
+    // The h of a down task's K range, from the gate/up K parts of its expert:
+    // features f0 .. f0 + nf - 1 of bucket rows off .. off + c - 1, into this
+    // group's buffer (int8 codes in dp4a order, {scale, -8 * sum} per 32).
+    // The group's warps split the K parts (ps subsets) and the feature
+    // quads, two K parts in flight a lane; the subsets' sums meet in shared
+    // memory and are added in subset order.  Every down task of the range
+    // computes the same codes.
+    auto compute_h = [&](int off, int c, int f0, int nf, int nsg_, bool store) {
+        const int ps = nsg_ >= 8 ? 8 : nsg_ >= 4 ? 4 : nsg_ >= 2 ? 2 : 1;
+        const int sub = w8 % ps, blk = w8 / ps, nblk = kGroupWarps / ps;
+        const int nq4 = c * nf / 4, q4_per_tok = nf / 4;
+        float4* red = reinterpret_cast<float4*>(red_buf);  // [8 warps][32 lanes][2]
+        for (int qb = 0; qb < nq4; qb += 32 * nblk) {
+            const int quad = qb + blk * 32 + lane;
+            const bool ok = quad < nq4;
+            const int n = ok ? quad / q4_per_tok : 0, f = f0 + (ok ? quad % q4_per_tok : 0) * 4;
+            float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (ok) {
+                for (int p0 = sub; p0 < nsg_; p0 += 2 * ps) {
+                    float4 g4[2], u4[2];
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        const int p = p0 + z * ps;
+                        if (p < nsg_) {
+                            const float* src = a.gu_part + ((size_t)p * Tk + off + n) * 2 * I + f;
+                            g4[z] = __ldcg(reinterpret_cast<const float4*>(src));
+                            u4[z] = __ldcg(reinterpret_cast<const float4*>(src + I));
+                        }
+                    }
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        if (p0 + z * ps < nsg_) {
+                            gv[0] += g4[z].x; gv[1] += g4[z].y; gv[2] += g4[z].z; gv[3] += g4[z].w;
+                            uv[0] += u4[z].x; uv[1] += u4[z].y; uv[2] += u4[z].z; uv[3] += u4[z].w;
+                        }
+                    }
+                }
+            }
+            if (ps > 1) {
+                red[(w8 * 32 + lane) * 2] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                red[(w8 * 32 + lane) * 2 + 1] = make_float4(uv[0], uv[1], uv[2], uv[3]);
+                group_sync();
+            }
+            if (sub == 0) {  // whole warps: the first warp of each quad block
+                if (ps > 1) {
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) gv[z] = uv[z] = 0.f;
+                    for (int s = 0; s < ps; ++s) {
+                        const float4 g4 = red[((w8 + s) * 32 + lane) * 2];
+                        const float4 u4 = red[((w8 + s) * 32 + lane) * 2 + 1];
                         gv[0] += g4.x; gv[1] += g4.y; gv[2] += g4.z; gv[3] += g4.w;
                         uv[0] += u4.x; uv[1] += u4.y; uv[2] += u4.z; uv[3] += u4.w;
                     }
                 }
+                // h = silu(g) * u; eight lanes hold one 32-feature group
                 float h[4], amax = 0.f;
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
@@ -694,34 +774,65 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
                 // the group: the even lane stores the chunk in dp4a order
                 const uint32_t w4o = __shfl_xor_sync(0xffffffffu, w4, 1);
                 if (ok) {
-                    const size_t prow = (size_t)(off + n);
-                    if ((l8 & 1) == 0)
-                        *reinterpret_cast<uint2*>(a.hq + prow * I + f0) = permute_chunk(w4, w4o);
-                    if (l8 == 0) a.hs[prow * Gh + f0 / kGroup] = make_int2(__float_as_int(d), -8 * sum);
-                    if (a.write_qh) {
-                        *reinterpret_cast<uint32_t*>(a.q_h + prow * I + f0) = w4;
-                        if (l8 == 0) a.d_h[prow * Gh + f0 / kGroup] = db;
+                    if ((lane & 1) == 0)
+                        *reinterpret_cast<uint2*>(ah_q + (size_t)n * I + f) = permute_chunk(w4, w4o);
+                    if ((lane & 7) == 0) ah_s[n * Gh + f / kGroup] = make_int2(__float_as_int(d), -8 * sum);
+                    if (store) {
+                        const size_t prow = (size_t)(off + n);
+                        *reinterpret_cast<uint32_t*>(a.q_h + prow * I + f) = w4;
+                        if ((lane & 7) == 0) a.d_h[prow * Gh + f / kGroup] = db;
                     }
                 }
             }
+            if (ps > 1) group_sync();  // the sums buffer is reused
+        }
+    };
+
+    int h_key = -1;  // (touched slot, K part) whose h is in this group's buffer
+    int run = 0;     // tasks of the current run counted so far
+    Walk w = walk_start(grp);
+    while (walk_live(w)) {
+        const Walk nx = walk_next(w, grp);
+        const bool has_next = walk_live(nx);
+        const uint8_t* base = walk_base(w);
+        const int KC = w.gu ? KCg : KCd;
+        const bool next_contig = has_next && walk_base(nx) == base + (size_t)KC * kTileBytes;
+        const int i = w.i, rb = w.rb, kc = w.kc;
+        const Walk cur = w;
+        w = nx;
+        const int e = s_touched[i], off = s_off[e], c = s_off[e + 1] - off;
+        if (cur.gu) {
+            // ------------------------------------------ gate/up task
+            const int row = rb * kTileRows + lrow;
+            dispatch(true, off, c, base, next_contig, kc * KCg, KCg, row,
+                     a.gu_part + ((size_t)kc * Tk + off) * 2 * I + row, (size_t)2 * I);
+            ++run;
+            // the run goes on while the next task counts toward the same h
+            // block (gate rows rb and up rows rb + RBh feed h block rb % RBh)
+            const int hb = rb < RBh ? rb : rb - RBh;
+            if (has_next && nx.gu && nx.i == i && (nx.rb < RBh ? nx.rb : nx.rb - RBh) == hb) continue;
+            // count the run's K parts of h block hb (they are stored)
             group_sync();
-            if (gtid == 0) red_release_add(&a.done_h[i], 1);
+            if (gtid == 0) red_release_add(&a.cnt_h[i * RBh + hb], run);
+            run = 0;
         } else {
             // --------------------------------------------- down task
-            const int task = dn0 + (j - ngl);
-            const int i = task / (RBd * nsd), rem = task % (RBd * nsd);
-            const int rbd = rem / nsd, kc = rem % nsd;
-            const int e = s_touched[i], off = s_off[e], c = s_off[e + 1] - off;
-            if (i != h_expert) {
-                // wait until every h block of the expert is done, then load h
+            const int rbd = rb;
+            if (i * nsd + kc != h_key) {
+                // wait until every gate/up K part of the h blocks this K range
+                // overlaps is stored, then form h for the range
+                const int f0 = kc * KCd * kTileK, nf = KCd * kTileK;
                 if (gtid == 0) {
                     bool got = !s_abort;
-                    if (got && ld_acquire(&a.done_h[i]) < RBh) {
-                        const unsigned long long t0 = globaltimer_ns();
-                        while (ld_acquire(&a.done_h[i]) < RBh) {
-                            if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
-                                got = false;
-                                break;
+                    for (int hb = f0 / kTileRows; hb <= (f0 + nf - 1) / kTileRows && got; ++hb) {
+                        const int* cnt = &a.cnt_h[i * RBh + hb];
+                        if (ld_acquire(cnt) < 2 * nsg) {
+                            const unsigned long long t0 = globaltimer_ns();
+                            while (ld_acquire(cnt) < 2 * nsg) {
+                                if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+                                    got = false;
+                                    break;
+                                }
                             }
                         }
                     }
@@ -730,38 +841,43 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
                 }
                 group_sync();
                 if (s_flag[grp]) {
-                    const int nq = c * I / 16, ns16 = c * Gh * 8 / 16;
-                    const uint4* srcq = reinterpret_cast<const uint4*>(a.hq + (size_t)off * I);
-                    const uint4* srcs = reinterpret_cast<const uint4*>(a.hs + (size_t)off * Gh);
-                    for (int z = gtid; z < nq; z += kGroupThreads)
-                        reinterpret_cast<uint4*>(ah_q)[z] = __ldcg(srcq + z);
-                    for (int z = gtid; z < ns16; z += kGroupThreads)
-                        reinterpret_cast<uint4*>(ah_s)[z] = __ldcg(srcs + z);
+                    compute_h(off, c, f0, nf, nsg, a.write_qh && rbd == 0);
                 } else {
                     live = false;  // nothing valid to multiply: skip the rest
                 }
                 group_sync();
-                h_expert = i;
+                h_key = i * nsd + kc;
             }
             const int row = rbd * kTileRows + lrow;
-            dispatch(false, off, c, tile0(j) - qb, kc * KCd, KCd, row,
+            dispatch(false, off, c, base, next_contig, kc * KCd, KCd, row,
                      a.y_part + ((size_t)kc * Tk + off) * H + row, (size_t)H);
             ++run;
             // the run goes on while the next task counts toward the same columns
-            if (j + 1 < je && (task + 1) % (RBd * nsd) / nsd == rbd && (task + 1) / (RBd * nsd) == i)
-                continue;
+            if (has_next && nx.i == i && nx.rb == rbd) continue;
             const int add = run;
             run = 0;
             if (!flush(&a.cnt_y[rbd], add, nt * nsd)) continue;
             // the last run of output columns rbd*128 .. +127: residual plus
-            // every slot's parts, slots in order, K parts in order
+            // every slot's parts, slots in order, K parts in order (loaded
+            // eight at a time before they are added)
             const int c0 = rbd * kTileRows;
             for (int it = gtid; it < kTileRows * T; it += kGroupThreads) {
                 const int t = it / kTileRows, col = c0 + it % kTileRows;
                 float v = bf16_bits_to_float(a.x_res[(size_t)t * H + col]);
-                for (int jj = 0; jj < k; ++jj) {
-                    const int p = s_slotpos[t * k + jj];
-                    for (int kp = 0; kp < nsd; ++kp) v += __ldcg(a.y_part + ((size_t)kp * Tk + p) * H + col);
+                const float* yc = a.y_part + col;
+                int jj = 0, kp = 0;  // slot and K part of the next load
+                for (int q0 = 0; q0 < k * nsd; q0 += 8) {
+                    float part[8];
+#pragma unroll
+                    for (int z = 0; z < 8; ++z) {
+                        part[z] = 0.f;
+                        if (jj < k) {
+                            part[z] = __ldcg(yc + ((size_t)kp * Tk + s_slotpos[t * k + jj]) * H);
+                            if (++kp == nsd) { kp = 0; ++jj; }
+                        }
+                    }
+#pragma unroll
+                    for (int z = 0; z < 8; ++z) v += part[z];  // (the padding adds 0)
                 }
                 if (a.out_fp32)
                     static_cast<float*>(a.out)[(size_t)t * H + col] = v;
@@ -776,28 +892,36 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 int g_layer_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
 
 struct Plan {
-    int ns, off_bar, off_ax, off_ah, ah_bytes, smem;
+    int ns, st, off_bar, off_ax, off_ah, ah_bytes, off_red, smem;
 };
 
 int al128(long long v) { return (int)((v + 127) & ~127ll); }
 
 // Shared-memory plan of the layer kernel; false if it does not fit.
+// Layout: the two rings, the two groups' h buffers and K-part sum buffers
+// (all idle while the CTA routes, when they hold the logits), then the
+// codes of x (filled by cp.async during routing) and the ring barriers.
 bool plan_layer(int T, int H, int I, int E, Plan* p) {
     const long long ax = al128((long long)T * H + (long long)T * (H / kGroup) * 8);
     const long long ah = al128((long long)T * I + (long long)T * (I / kGroup) * 8);
-    const long long rest = kLayerSmemBudget - ax - 2 * ah - 2 * kMaxRing * 8 - 128;
-    if (rest < 2ll * kGroups * kTileBytes) return false;
-    int ns = (int)(rest / kTileBytes) / kGroups;  // slots of each group's ring
-    ns = ns > kMaxRing / kGroups ? kMaxRing / kGroups : ns;
-    // the routing phase keeps all T x E logits in the rings
-    if ((long long)T * E * 4 > (long long)kGroups * ns * kTileBytes) return false;
+    const long long rest = kLayerSmemBudget - ax - 2 * ah - 2 * kRedBytes - 2 * kMaxSlots * 8 - 256;
+    // the largest slot (up to kSlotTiles tiles) that still gives each group's
+    // ring two slots, else one
+    int st = kSlotTiles;
+    while (st > 1 && rest < (long long)kGroups * 2 * st * kTileBytes) st /= 2;
+    int ns = (int)(rest / ((long long)st * kTileBytes)) / kGroups;  // slots of each group's ring
+    ns = ns > kMaxSlots / kGroups ? kMaxSlots / kGroups : ns;
+    if (ns < 1) return false;
     p->ns = ns;
-    p->off_bar = kGroups * ns * kTileBytes;
-    p->off_ax = al128(p->off_bar + 2 * kGroups * ns * 8);
-    p->off_ah = p->off_ax + (int)ax;
+    p->st = st;
+    p->off_ah = kGroups * ns * st * kTileBytes;
     p->ah_bytes = (int)ah;
-    p->smem = p->off_ah + 2 * (int)ah;
-    return true;
+    p->off_red = p->off_ah + 2 * (int)ah;
+    p->off_ax = al128(p->off_red + 2 * kRedBytes);
+    p->off_bar = al128(p->off_ax + ax);
+    p->smem = p->off_bar + 2 * kGroups * ns * 8;
+    // the routing phase keeps all T x E logits below the codes of x
+    return (long long)T * E * 4 <= p->off_ax;
 }
 
 __global__ void coop_pdl_probe_kernel(int* p) {
@@ -864,7 +988,7 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
 
 int decode_sync_ints(int T, int H, int I, int E, int k) {
     const int nslot = std::min(E, T * k);
-    return nslot * (I / kTileRows) + nslot + H / kTileRows;
+    return nslot * (I / kTileRows) + H / kTileRows;
 }
 
 cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
@@ -903,8 +1027,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
         (err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     psmem)) != cudaSuccess)
         return err;
-    if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess)
+    if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess) {
+        cudaGetLastError();
         return err;
+    }
     if ((err = mark(1)) != cudaSuccess) return err;
     // ---- layer ----
     LayerArgs a{};
@@ -927,16 +1053,24 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.bucket_token = ws.bucket_token;
     a.bucket_slot = ws.bucket_slot;
     a.gu_part = ws.gu_part;
-    a.hq = ws.hq;
-    a.hs = ws.hs;
     a.q_h = ws.q_h;
     a.d_h = ws.d_h;
     a.y_part = ws.y_part;
     a.cnt_h = ws.sync;
-    a.done_h = ws.sync + nslot * (I / kTileRows);
-    a.cnt_y = a.done_h + nslot;
+    a.cnt_y = ws.sync + nslot * (I / kTileRows);
     a.cap_g = ws.cap_g;
     a.cap_d = ws.cap_d;
+    for (int d = 1; d <= H / kTileK && d <= ws.cap_g && a.ndiv_g < 16; ++d)
+        if ((H / kTileK) % d == 0) a.div_g[a.ndiv_g++] = d;
+    for (int d = 1; d <= I / kTileK && d <= ws.cap_d && a.ndiv_d < 16; ++d)
+        if ((I / kTileK) % d == 0) a.div_d[a.ndiv_d++] = d;
+    // 32-bit task indices: b x (tasks) must fit
+    {
+        const long long nt_max = std::min(E, T * k);
+        const long long per = std::max((long long)(2 * I / kTileRows) * a.div_g[a.ndiv_g - 1],
+                                       (long long)(H / kTileRows) * a.div_d[a.ndiv_d - 1]);
+        if ((long long)(num_sms + 1) * nt_max * per >= (1ll << 31)) return cudaErrorInvalidValue;
+    }
     a.out = out;
     a.out_fp32 = out_fp32 ? 1 : 0;
     a.dots_gu = dots_gu;
@@ -944,14 +1078,14 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.write_qh = write_qh ? 1 : 0;
     a.status = status;
     a.ns = plan.ns;
+    a.st = plan.st;
     a.off_bar = plan.off_bar;
     a.off_ax = plan.off_ax;
     a.off_ah = plan.off_ah;
     a.ah_bytes = plan.ah_bytes;
-    // (32-bit task indices: the api checks T * k * max(H, I) < 2^31, which
-    // bounds touched experts x row blocks x splits far below it)
-    err = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               plan.smem);
+    a.off_red = plan.off_red;
+    void (*kern)(LayerArgs) = T <= 16 ? decode_layer_kernel<16> : decode_layer_kernel<MOE_DECODE_MAX_T>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute at[2];
@@ -965,7 +1099,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = (g_layer_pdl[dev & 63] == 2) ? 1 : 2;
-    if ((err = cudaLaunchKernelEx(&cfg, decode_layer_kernel, a)) != cudaSuccess) return err;
+    if ((err = cudaLaunchKernelEx(&cfg, kern, a)) != cudaSuccess) {
+        cudaGetLastError();  // a refused launch: clear it, the context is intact
+        return err;
+    }
     for (int i = 2; i <= 6; ++i)
         if ((err = mark(i)) != cudaSuccess) return err;
     return cudaGetLastError();

@@ -44,8 +44,6 @@ struct Workspace {
     int8_t* q_x;            // [T, H]        codes of x, column order (stage output)
     uint16_t* d_x;          // [T, H/32]     fp16 scales of x (stage output)
     float* gu_part;         // [nsg, T*k, 2I] K parts of the gate/up row sums, bucket order
-    uint8_t* hq;            // [T*k, I]      int8 codes of h, dp4a order
-    int2* hs;               // [T*k, I/32]
     int8_t* q_h;            // [T*k, I]      (stage output)
     uint16_t* d_h;          // [T*k, I/32]
     float* y_part;          // [nsd, T*k, H] K parts of the weighted expert outputs
