@@ -47,7 +47,7 @@ EXPORTED_SYMBOLS = (
     "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
     "moe_q4_quantize",
 )
-MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):

@@ -75,9 +75,9 @@ constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kLayerThreads = kConsumerThreads + kGroups * 32;  // + a producer warp per group
 constexpr int kWarpProducer0 = kConsumerWarps;          // group g's producer: warp kWarpProducer0 + g
-constexpr int kSlotTiles = 4;                           // packed tiles per ring slot (one bulk copy),
+constexpr int kSlotTiles = 2;                           // packed tiles per ring slot (one bulk copy),
                                                         // fewer when shared memory is short
-constexpr int kMaxSlots = 12;                           // slots of both groups' rings
+constexpr int kMaxSlots = 24;                           // slots of both groups' rings
 constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 32 lanes x 8 floats
 // Dynamic shared memory of the layer kernel: leaves room on the SM (228 KB)
 // for its static part (13.1 KB) and a prep CTA of the next call (its router
@@ -85,14 +85,21 @@ constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 
 constexpr int kLayerSmemBudget = 200 * 1024;
 constexpr int kPrepThreads = 128;
 constexpr int kMaxTk = MOE_DECODE_MAX_T * MOE_MAX_TOPK;
-// Tasks the K split aims for (gate/up, down); the split depends only on the
-// number of touched experts and the shape, so results are reproducible.
-constexpr int kTargetGU = 152 * 8;
-constexpr int kTargetD = 152 * 4;
+// Tasks the K split aims for (gate/up and down alike): the split depends only
+// on the number of touched experts and the shape, so results are
+// reproducible.  A task keeps at least two tiles.
+constexpr int kTargetTasks = 152 * 16;
 constexpr int kMaxSplit = 16;
-// Bytes of K-part sums (each of gate/up and down) the split may use; beyond
-// it the split is capped.
-constexpr size_t kPartBudget = 1u << 20;
+// Bytes of K-part sums the split may use (gate/up, down); beyond them the
+// split is capped.
+constexpr size_t kPartBudgetGU = 4u << 20;
+constexpr size_t kPartBudgetD = 2u << 20;
+// Cost of a tile in the work split, in units of one bucket row's group dot
+// products: streaming it weighs as much as this many rows.
+constexpr int kTileCost = 3;
+// Routing ranks the logits with every thread when a token's E logits times
+// its T x E elements need at most this many comparisons a thread.
+constexpr int kRankCompares = 128;
 
 struct PrepArgs {
     const uint16_t* x;
@@ -185,14 +192,20 @@ template <int N>
 struct IntC {
     static constexpr int value = N;
 };
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
+};
 
 }  // namespace
 
-// Smallest divisor d of KB (d <= cap) with units * d >= target; if there is
-// none, the largest divisor <= cap.  Non-increasing in `units`.
+// Smallest divisor d of KB (d <= cap, d <= KB / 2 unless KB = 1) with
+// units * d >= target; if there is none, the largest such divisor.
+// Non-increasing in `units`.
 __host__ __device__ inline int decode_split_for(int units, int KB, int target, int cap) {
     int best = 1;
-    for (int d = 1; d <= KB && d <= cap; ++d) {
+    const int dmax = KB > 1 ? KB / 2 : 1;
+    for (int d = 1; d <= dmax && d <= cap; ++d) {
         if (KB % d) continue;
         best = d;
         if ((long long)units * d >= target) return d;
@@ -258,9 +271,12 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
         if (one) prep_load(xr, 0, H8, lane, cur);
         float r = 1.0f;
         if (a.prenorm) {
-            // the same order and rounding as the prefill RMSNorm: each lane
-            // over its columns in order, then a butterfly
-            float ss = 0.f;
+            // each lane over its columns, one partial sum per unit slot (in
+            // column order within a unit), the slots in order, then a
+            // butterfly
+            float ssu[kPrepUnits];
+#pragma unroll
+            for (int i = 0; i < kPrepUnits; ++i) ssu[i] = 0.f;
             for (int ch = 0; ch < nchunk; ++ch) {
                 if (!one) prep_load(xr, ch * kChunkUnits, H8, lane, cur);
 #pragma unroll
@@ -268,14 +284,18 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                     float xf[8];
                     unpack8(cur[i], xf);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) ss = fmaf(xf[q], xf[q], ss);
+                    for (int q = 0; q < 8; ++q) ssu[i] = fmaf(xf[q], xf[q], ssu[i]);
                 }
             }
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPrepUnits; ++i) ss += ssu[i];
             ss = warp_sum(ss);
             r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + 1e-6f));
         }
-        const bool duty = (t % (int)gridDim.x) == e;  // this CTA writes token t's codes
-        float acc = 0.f;
+        float accu[kPrepUnits];  // the logit's partial sums, one per unit slot
+#pragma unroll
+        for (int i = 0; i < kPrepUnits; ++i) accu[i] = 0.f;
         for (int ch = 0; ch < nchunk; ++ch) {
             if (!one) prep_load(xr, ch * kChunkUnits, H8, lane, cur);
 #pragma unroll
@@ -291,6 +311,7 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                 if (valid) {
                     const float4 w0 = *reinterpret_cast<const float4*>(w + u * 8);
                     const float4 w1 = *reinterpret_cast<const float4*>(w + u * 8 + 4);
+                    float acc = accu[i];
                     acc = fmaf(xf[0], w0.x, acc);
                     acc = fmaf(xf[1], w0.y, acc);
                     acc = fmaf(xf[2], w0.z, acc);
@@ -299,18 +320,23 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                     acc = fmaf(xf[5], w1.y, acc);
                     acc = fmaf(xf[6], w1.z, acc);
                     acc = fmaf(xf[7], w1.w, acc);
+                    accu[i] = acc;
                 }
-                if (duty) {
-                    // int8 codes per 32 columns: lanes 4m..4m+3 hold one group
-                    float amax = 0.f;
+                // int8 codes per 32 columns (lanes 4m..4m+3 hold one group):
+                // group g of token t is coded by CTA (t * H/32 + g) % grid
+                float amax = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                    const uint16_t db = act_scale_bits(amax);
-                    const float d = half_bits_to_float(db);
-                    uint32_t lo = 0u, hi = 0u;
-                    int gsum = 0;
+                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const bool duty = (unsigned)(t * G32 + u / 4) % gridDim.x == (unsigned)e;
+                uint32_t lo = 0u, hi = 0u;
+                int gsum = 0;
+                uint16_t db = 0;
+                float d = 0.f;
+                if (duty) {
+                    db = act_scale_bits(amax);
+                    d = half_bits_to_float(db);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int qc = act_code(xf[q], d);
@@ -318,25 +344,57 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                         if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
                         else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
                     }
-                    gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
-                    gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
-                    if (valid) {
-                        *reinterpret_cast<uint2*>(a.xq + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
-                        *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
-                        if ((lane & 3) == 0) {
-                            a.xs[t * G32 + u / 4] = make_int2(__float_as_int(d), -8 * gsum);
-                            a.d_x[t * G32 + u / 4] = db;
-                        }
+                }
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
+                gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+                if (duty && valid) {
+                    *reinterpret_cast<uint2*>(a.xq + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
+                    *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
+                    if ((lane & 3) == 0) {
+                        a.xs[t * G32 + u / 4] = make_int2(__float_as_int(d), -8 * gsum);
+                        a.d_x[t * G32 + u / 4] = db;
                     }
                 }
             }
         }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPrepUnits; ++i) acc += accu[i];
         acc = warp_sum(acc);
         if (lane == 0) a.logits[(size_t)t * a.E + e] = acc;
     }
 }
 
 // ----------------------------------------------------------------- layer
+// The first task of worker v of V when the `per` tasks of touched slot i
+// (KC tiles each) cost KC * (kTileCost + c_i) each, c_i = toff[i + 1] -
+// toff[i] bucket rows: the task whose cost range holds the position
+// floor(v * total / V).  Monotone in v; bound(0) = 0 and bound(V) = nt * per.
+// The whole warp calls it: a ballot over the slots finds the one whose cost
+// range holds the position (the prefixes rise with i), one division places
+// the position within that slot.
+__device__ __forceinline__ int split_bound_warp(int v, int V, int nt, int Tk, int per, int KC,
+                                                const int* toff, int lane) {
+    using u64 = unsigned long long;
+    const u64 U = (u64)per * KC;  // tiles of a touched slot
+    const u64 tot = U * ((u64)kTileCost * nt + Tk);
+    const u64 vt = (u64)v * tot;  // V times the position
+    // slots 0..nt whose prefix U * (kTileCost * i + toff[i]) <= the position
+    int cnt = 0;
+    for (int i0 = 0; i0 <= nt; i0 += 32) {
+        const int i = i0 + lane;
+        const bool le = i <= nt && (u64)V * U * ((u64)kTileCost * i + toff[i]) <= vt;
+        cnt += __popc(__ballot_sync(0xffffffffu, le));
+    }
+    const int lo = cnt - 1;
+    if (lo >= nt) return nt * per;
+    // floor((position - prefix) / (KC * w)), w = kTileCost + c_lo, scaled by V
+    const u64 num = vt - (u64)V * U * ((u64)kTileCost * lo + toff[lo]);
+    const u64 den = (u64)V * KC * (kTileCost + toff[lo + 1] - toff[lo]);
+    const u64 j = (num >> 32) == 0 && (den >> 32) == 0 ? (u64)((unsigned)num / (unsigned)den) : num / den;
+    return lo * per + (int)(j < (u64)per ? j : (u64)per);
+}
+
 // MAXNT: the most tokens an expert's bucket may hold (T <= MAXNT).  At most
 // 96 registers a thread, which leaves room on the SM for the next call's
 // prep CTA; the MAXNT = 32 variant spills a little instead (it only runs
@@ -352,8 +410,10 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     __shared__ uint32_t s_mask[kMaxExperts];
     __shared__ int s_off[kMaxExperts + 1];
     __shared__ int s_touched[kMaxExperts];
+    __shared__ int s_toff[kMaxExperts + 1];  // touched slot -> its first bucket row (+ total)
     __shared__ int s_slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
-    __shared__ int s_nt;
+    __shared__ int s_nt, s_nsg, s_nsd;
+    __shared__ int s_bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
     __shared__ volatile int s_abort;
     __shared__ volatile int s_flag[kGroups];
 
@@ -399,28 +459,69 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     }
 
     // ---------------------------------------------- routing (every CTA)
-    float* s_lg = reinterpret_cast<float*>(dsm);  // [T][E], in the (still idle) rings and buffers
-    for (int i = tid; i < T * E; i += kLayerThreads) s_lg[i] = __ldcg(a.logits + i);
+    // Every CTA takes the same decisions from the same logits: each token's
+    // top k (larger logit first, the lower expert index on a tie) with
+    // softmax weights over them, a token bitmask per expert, the buckets and
+    // the work split.
+    float* s_lg = reinterpret_cast<float*>(dsm);                  // [T][E] logits, and
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(s_lg + T * E);  // their order keys, in
+    for (int i = tid; i < T * E; i += kLayerThreads) {            // the still idle ring
+        const float v = __ldcg(a.logits + i);
+        s_lg[i] = v;
+        s_key[i] = float_order_key(v);
+    }
     for (int e = tid; e < E; e += kLayerThreads) s_mask[e] = 0u;
     __syncthreads();
-    if (warp < kConsumerWarps) {
-        for (int t = warp; t < T; t += kConsumerWarps) {
-            int si;
-            float sw;
-            warp_topk(s_lg + t * E, E, k, si, sw);
-            if (lane < k) {
-                s_idx[t * k + lane] = si;
-                s_w[t * k + lane] = sw;
+    if ((long long)T * E * E <= (long long)kLayerThreads * kRankCompares) {
+        // few tokens: every thread ranks (t, e) against a share of the
+        // token's keys (nsub threads an element, interleaved), the shares
+        // are added; rank < k places e in t's choices
+        int nsub = 1;
+        while (nsub < 32 && T * E * 2 * nsub <= kLayerThreads) nsub *= 2;
+        const int el = tid / nsub, sub = tid % nsub;
+        const bool mine = el < T * E;
+        const int t = mine ? el / E : 0, e = mine ? el - t * E : 0;
+        int rank = 0;
+        if (mine) {
+            const uint32_t* kr = s_key + t * E;
+            const uint32_t mk = kr[e];
+            for (int q = sub; q < E; q += nsub) {
+                const uint32_t kq = kr[q];
+                rank += (kq > mk || (kq == mk && q < e)) ? 1 : 0;
             }
         }
+        for (int o = 1; o < nsub; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (mine && sub == 0 && rank < k) {
+            s_idx[t * k + rank] = e;
+            atomicOr(&s_mask[e], 1u << t);
+        }
+    } else {
+        if (warp < kConsumerWarps) {
+            for (int t = warp; t < T; t += kConsumerWarps) {
+                int si;
+                float sw;
+                warp_topk(s_lg + t * E, E, k, si, sw);
+                if (lane < k) s_idx[t * k + lane] = si;
+            }
+        }
+        __syncthreads();
+        // token t's bit in the mask of each expert it chose (T <= 32)
+        for (int p = tid; p < Tk; p += kLayerThreads) atomicOr(&s_mask[s_idx[p]], 1u << (p / k));
     }
     __syncthreads();
-    // token t's bit in the mask of each expert it chose (T <= 32)
-    for (int p = tid; p < Tk; p += kLayerThreads) atomicOr(&s_mask[s_idx[p]], 1u << (p / k));
-    __syncthreads();
-    if (warp == 0) {
-        // experts 8*lane .. 8*lane+7 (E <= 256): bucket offsets and the
-        // touched list (ascending expert order) by a warp scan
+    if (warp < kConsumerWarps) {
+        // the softmax weights over each token's k choices
+        for (int t = warp; t < T; t += kConsumerWarps) {
+            const float v = lane < k ? s_lg[t * E + s_idx[t * k + lane]] : 0.f;
+            const float m = __shfl_sync(0xffffffffu, v, 0);  // the largest
+            const float z = lane < k ? expf(v - m) : 0.f;
+            const float zs = warp_sum(z);
+            if (lane < k) s_w[t * k + lane] = z / zs;
+        }
+    } else if (warp == kWarpProducer0) {
+        // experts 8*lane .. 8*lane+7 (E <= 256): bucket offsets, the touched
+        // list (ascending expert order) and its offsets by a warp scan; the
+        // K splits
         int cnt[8], tot = 0, tch = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -445,76 +546,103 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
             const int e = 8 * lane + i;
             if (e < E) {
                 s_off[e] = off;
-                if (cnt[i] > 0) s_touched[pos++] = e;
+                if (cnt[i] > 0) {
+                    s_toff[pos] = off;
+                    s_touched[pos++] = e;
+                }
                 off += cnt[i];
             }
         }
+        const int nt_ = __shfl_sync(0xffffffffu, itch, 31);
+        // K splits: the smallest divisor of the row's 64-column blocks (listed
+        // by the host, ascending, within the caps) that gives enough tasks,
+        // else the largest
+        const unsigned okg = __ballot_sync(
+            0xffffffffu, lane < a.ndiv_g && nt_ * RBg * a.div_g[lane < a.ndiv_g ? lane : 0] >= kTargetTasks);
+        const unsigned okd = __ballot_sync(
+            0xffffffffu, lane < a.ndiv_d && nt_ * RBd * a.div_d[lane < a.ndiv_d ? lane : 0] >= kTargetTasks);
         if (lane == 31) {
             s_off[E] = itot;
             s_nt = itch;
+            s_toff[itch] = itot;
+            s_nsg = okg ? a.div_g[__ffs(okg) - 1] : a.div_g[a.ndiv_g - 1];
+            s_nsd = okd ? a.div_d[__ffs(okd) - 1] : a.div_d[a.ndiv_d - 1];
         }
     }
     __syncthreads();
     const int nt = s_nt;
-    for (int p = tid; p < Tk; p += kLayerThreads) {
-        const int t = p / k, e = s_idx[p];
-        const int pos = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
-        s_btok[pos] = t;
-        s_bsw[pos] = s_w[p];
-        s_slotpos[p] = pos;
-        if (b == 0) {
-            a.topk_idx[p] = e;
-            a.topk_w[p] = s_w[p];
-            a.bucket_token[pos] = t;
-            a.bucket_slot[pos] = p % k;
+    if (warp < 4 * kGroups) {
+        // Tasks are shared out by cost, a tile of touched slot i weighing
+        // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
+        // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
+        // likewise.  Warp 4g + j finds group g's bound j.
+        const int g = warp >> 2, j = warp & 3;
+        const bool gu = j < 2;
+        const int nsg_ = s_nsg, nsd_ = s_nsd;
+        const int per = gu ? RBg * nsg_ : RBd * nsd_;
+        const int KC = gu ? KBg / nsg_ : KBd / nsd_;
+        const int bnd = split_bound_warp(2 * b + g + (j & 1), 2 * G, nt, Tk, per, KC, s_toff, lane);
+        if (lane == 0) s_bnd[g][j] = bnd;
+    } else {
+        const int tid2 = tid - 4 * kGroups * 32, nthr2 = kLayerThreads - 4 * kGroups * 32;
+        for (int p = tid2; p < Tk; p += nthr2) {
+            const int t = p / k, e = s_idx[p];
+            const int pos = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
+            s_btok[pos] = t;
+            s_bsw[pos] = s_w[p];
+            s_slotpos[p] = pos;
+            if (b == 0) {
+                a.topk_idx[p] = e;
+                a.topk_w[p] = s_w[p];
+                a.bucket_token[pos] = t;
+                a.bucket_slot[pos] = p % k;
+            }
         }
-    }
-    if (b == 0) {
-        for (int i = tid; i <= E; i += kLayerThreads) a.offsets[i] = s_off[i];
-        for (int i = tid; i < nt; i += kLayerThreads) a.touched[i] = s_touched[i];
-        if (tid == 0) a.counters[kCntTouched] = nt;
+        if (b == 0) {
+            for (int i = tid2; i <= E; i += nthr2) a.offsets[i] = s_off[i];
+            for (int i = tid2; i < nt; i += nthr2) a.touched[i] = s_touched[i];
+            if (tid2 == 0) a.counters[kCntTouched] = nt;
+        }
     }
     // the ring held the logits through generic accesses; bulk copies refill it
     fence_proxy_async_smem();
     __syncthreads();
 
     // ------------------------------------------------------- work split
-    // K splits: the smallest divisor of the row's 64-column blocks (up to
-    // the cap, listed by the host in ascending order) that gives enough
-    // tasks, else the largest.
-    int nsg = a.div_g[a.ndiv_g - 1], nsd = a.div_d[a.ndiv_d - 1];
-    for (int q = 0; q < a.ndiv_g; ++q)
-        if (nt * RBg * a.div_g[q] >= kTargetGU) { nsg = a.div_g[q]; break; }
-    for (int q = 0; q < a.ndiv_d; ++q)
-        if (nt * RBd * a.div_d[q] >= kTargetD) { nsd = a.div_d[q]; break; }
+    const int nsg = s_nsg, nsd = s_nsd;
     const int KCg = KBg / nsg, KCd = KBd / nsd;
-    const int n_gu = nt * RBg * nsg, n_dn = nt * RBd * nsd;  // (x G fits in 32 bits: checked at launch)
-    const int gu0 = b * n_gu / G, gu1 = (b + 1) * n_gu / G;
-    const int dn0 = b * n_dn / G, dn1 = (b + 1) * n_dn / G;
-    const int ngl = gu1 - gu0, ndl = dn1 - dn0;  // this CTA's tasks: gate/up, then down
-    // Each group takes a contiguous half of the gate/up tasks, then a
-    // contiguous half of the down tasks, so both groups are in the same
-    // phase and each meets runs of tasks that share a counter.
-    const int gh = (ngl + 1) / 2, dh = ndl / 2;
+    const int per_g = RBg * nsg, per_d = RBd * nsd;  // tasks of a touched slot
 
     // A walk over one group's tasks in order: gate/up tasks (expert slot i,
-    // row block rb, K part kc), then down tasks (i, row block rb, K part kc),
+    // row block rb, K part kc: kc fastest), then down tasks (i, K part kc,
+    // row block rb: rb fastest, so that a run of down tasks shares its h),
     // advanced by counting (no division per step).
     struct Walk {
         int left_g, left_d;  // tasks left in each phase
         int i, rb, kc;       // the current task
         bool gu;
     };
+    auto walk_down_at = [&](Walk& w, int t) {
+        w.gu = false;
+        w.i = t / per_d;
+        const int r = t - w.i * per_d;
+        w.kc = r / RBd;
+        w.rb = r - w.kc * RBd;
+    };
     auto walk_start = [&](int g) {
         Walk w;
-        w.left_g = g == 0 ? gh : ngl - gh;
-        w.left_d = g == 0 ? dh : ndl - dh;
-        w.gu = w.left_g > 0;
-        const int t = w.gu ? gu0 + (g == 0 ? 0 : gh) : dn0 + (g == 0 ? 0 : dh);
-        const int per = w.gu ? RBg * nsg : RBd * nsd, ns_ = w.gu ? nsg : nsd;
-        w.i = t / per;
-        w.rb = (t % per) / ns_;
-        w.kc = t % ns_;
+        w.left_g = s_bnd[g][1] - s_bnd[g][0];
+        w.left_d = s_bnd[g][3] - s_bnd[g][2];
+        if (w.left_g > 0) {
+            w.gu = true;
+            const int t = s_bnd[g][0];
+            w.i = t / per_g;
+            const int r = t - w.i * per_g;
+            w.rb = r / nsg;
+            w.kc = r - w.rb * nsg;
+        } else {
+            walk_down_at(w, s_bnd[g][2]);
+        }
         return w;
     };
     auto walk_next = [&](Walk w, int g) {
@@ -522,15 +650,11 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
             if (--w.left_g > 0) {
                 if (++w.kc == nsg) { w.kc = 0; if (++w.rb == RBg) { w.rb = 0; ++w.i; } }
             } else if (w.left_d > 0) {  // on to the group's first down task
-                w.gu = false;
-                const int t = dn0 + (g == 0 ? 0 : dh);
-                w.i = t / (RBd * nsd);
-                w.rb = (t % (RBd * nsd)) / nsd;
-                w.kc = t % nsd;
+                walk_down_at(w, s_bnd[g][2]);
             }
         } else {
             --w.left_d;
-            if (++w.kc == nsd) { w.kc = 0; if (++w.rb == RBd) { w.rb = 0; ++w.i; } }
+            if (++w.rb == RBd) { w.rb = 0; if (++w.kc == nsd) { w.kc = 0; ++w.i; } }
         }
         return w;
     };
@@ -540,47 +664,39 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
                     : a.wd + (((size_t)s_touched[w.i] * RBd + w.rb) * KBd + (size_t)w.kc * KCd) * kTileBytes;
     };
 
-    // Chunks: the group's tiles, in sequence order, are cut into runs of up
-    // to st tiles that lie back to back in memory (one bulk copy, one ring
-    // slot each).  Producer and consumers apply the same rule to the same
-    // sequence: a tile opens a new chunk unless it directly follows the
-    // open chunk's last tile and the chunk has room.  Slot and phase advance
-    // by counting.
+    // Chunks: each task's tiles are cut into runs of up to st tiles (one bulk
+    // copy, one ring slot each), chunk after chunk in the group's task order.
+    // Producer and consumers walk the same chunks; slot and phase advance by
+    // counting.
     if (warp >= kWarpProducer0) {
         // ---------------------------------------------------------- producer
         // One lane issues the chunks in order; chunk c's slot held chunk
         // c - ns, issued before it, so a parity wait never aliases.
         const int g = warp - kWarpProducer0;
         if (lane == 0) {
-            int slot = -1, phase = 0, clen = 0, cidx = -1;
-            const uint8_t* caddr = nullptr;
+            int slot = -1, phase = 0, cidx = -1;
             bool ok = true;
-            auto issue = [&]() -> bool {
-                if (s_abort || !mbar_wait(empty_bar(g, slot), phase ^ 1) || s_abort) {
-                    fail();
-                    return false;
-                }
-                s_slot_chunk[g * ns + slot] = cidx;
-                mbar_arrive_expect_tx(full_bar(g, slot), (uint32_t)(clen * kTileBytes));
-                bulk_g2s(sbase + slot_addr(g, slot), caddr, (uint32_t)(clen * kTileBytes), full_bar(g, slot));
-                return true;
-            };
             for (Walk w = walk_start(g); walk_live(w) && ok; w = walk_next(w, g)) {
                 const uint8_t* base = walk_base(w);
                 const int KC = w.gu ? KCg : KCd;
-                for (int u = 0; u < KC; ++u) {
-                    const uint8_t* t = base + (size_t)u * kTileBytes;
-                    if (cidx < 0 || clen == st || t != caddr + (size_t)clen * kTileBytes) {
-                        if (cidx >= 0 && !(ok = issue())) break;
-                        ++cidx;
-                        if (++slot == ns) { slot = 0; phase ^= 1; }
-                        clen = 0;
-                        caddr = t;
+                for (int u0 = 0; u0 < KC; u0 += st) {
+                    const int n = KC - u0 < st ? KC - u0 : st;
+                    ++cidx;
+                    if (++slot == ns) {
+                        slot = 0;
+                        phase ^= 1;
                     }
-                    ++clen;
+                    if (s_abort || !mbar_wait(empty_bar(g, slot), phase ^ 1) || s_abort) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    s_slot_chunk[g * ns + slot] = cidx;
+                    mbar_arrive_expect_tx(full_bar(g, slot), (uint32_t)(n * kTileBytes));
+                    bulk_g2s(sbase + slot_addr(g, slot), base + (size_t)u0 * kTileBytes,
+                             (uint32_t)(n * kTileBytes), full_bar(g, slot));
                 }
             }
-            if (ok && cidx >= 0) issue();
         }
         // every copy issued lands before the CTA can go away: wait for the
         // latest chunk of each slot (earlier ones completed before it)
@@ -607,105 +723,93 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     // barriers): a failed wait only skips work; decisions the group shares
     // are taken by its thread 0 and read after a group barrier.
     bool live = true;  // this warp has not given up
-    int slot = -1, phase = 0, clen = 0, cidx = -1;  // the open chunk (same walk as the producer)
-    const uint8_t* caddr = nullptr;
+    int slot = -1, phase = 0;  // the current chunk's slot (same walk as the producer)
     const int r_lane = lane >> 1, h_lane = lane & 1;
     const int lrow = w8 * 16 + r_lane;  // this lane's row in the 128-row block
 
     // One task: rows rb*128 + lrow, 64-column blocks kb0 .. kb0 + KC - 1 of
     // the current expert (bucket rows off .. off + c - 1, NT >= c), packed
-    // tiles base .. base + KC - 1; `next_contig`: the group's next tile lies
-    // right after this task's last.  The lane pair's sum for bucket row
-    // off + n is stored at dst[n * ld] (down: times the row's routing weight).
-    auto run_tiles = [&](auto ntc, bool gu, int off, int c, const uint8_t* base, bool next_contig,
-                         int kb0, int KC, int row, float* dst, size_t ld) {
+    // tiles base .. base + KC - 1, which arrive in chunks of up to st tiles.
+    // The lane pair's sum for bucket row off + n is stored at dst[n * ld]
+    // (down: times the row's routing weight).  GU: gate/up (activations x,
+    // bucket row -> token) or down (activations h, one row per bucket row).
+    auto run_tiles = [&](auto ntc, auto guc, int off, int c, int kb0, int KC, int row, float* dst,
+                         size_t ld) {
         constexpr int NT = decltype(ntc)::value;
-        const uint8_t* aq = gu ? ax_q : ah_q;
-        const int2* as = gu ? ax_s : ah_s;
-        const int K = gu ? H : I, Gk = gu ? Gx : Gh;
-        int32_t* dots = gu ? a.dots_gu : a.dots_d;
-        const size_t dots_ld = gu ? (size_t)2 * I : (size_t)H;
+        constexpr bool GU = decltype(guc)::value;
+        const uint8_t* aq = GU ? ax_q : ah_q;
+        const int2* as = GU ? ax_s : ah_s;
+        const int K = GU ? H : I, Gk = GU ? Gx : Gh;
+        int32_t* dots = GU ? a.dots_gu : a.dots_d;
+        const size_t dots_ld = GU ? (size_t)2 * I : (size_t)H;
+        const int code_off = w8 * 512 + lane * 16;                  // this lane's 16 code bytes
+        const int scale_off = kTileCodeBytes + w8 * 64 + lane * 2;  // and its group's scale
         float acc[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[n] = 0.f;
-        for (int u = 0; u < KC; ++u) {
-            const uint8_t* tg = base + (size_t)u * kTileBytes;
-            if (cidx < 0 || clen == st || tg != caddr + (size_t)clen * kTileBytes) {
-                ++cidx;
-                if (++slot == ns) { slot = 0; phase ^= 1; }
-                clen = 0;
-                caddr = tg;
-                if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
-                    fail();
-                    live = false;
-                }
+        for (int u0 = 0; u0 < KC; u0 += st) {
+            const int nu = KC - u0 < st ? KC - u0 : st;
+            if (++slot == ns) {
+                slot = 0;
+                phase ^= 1;
             }
-            const uint8_t* tile = dsm + slot_addr(grp, slot) + clen * kTileBytes;
-            ++clen;
+            if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
+                fail();
+                live = false;
+            }
+            const uint8_t* chunk = dsm + slot_addr(grp, slot);
             if (live) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(tile + w8 * 512 + lane * 16);
-                const float dw = half_bits_to_float(
-                    *reinterpret_cast<const uint16_t*>(tile + kTileCodeBytes + w8 * 64 + lane * 2));
-                const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
-                                        wv.w & 0x0F0F0F0Fu};
-                const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
-                                        (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
-                const int g = 2 * (kb0 + u) + h_lane;
+                for (int uu = 0; uu < nu; ++uu) {
+                    const uint8_t* tile = chunk + uu * kTileBytes;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
+                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
+                                            wv.w & 0x0F0F0F0Fu};
+                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
+                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                    const int g = 2 * (kb0 + u0 + uu) + h_lane;
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    if (n < c) {
-                        const int ar = gu ? s_btok[off + n] : n;
-                        const int2 sc = as[ar * Gk + g];
-                        const int dot = group_dot(wl, wh, aq + (size_t)ar * K + g * kGroup, sc.y);
-                        acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
-                        if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                    for (int n = 0; n < NT; ++n) {
+                        if (n < c) {
+                            const int ar = GU ? s_btok[off + n] : n;
+                            const int2 sc = as[ar * Gk + g];
+                            const int dot = group_dot(wl, wh, aq + ar * K + g * kGroup, sc.y);
+                            acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
+                            if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                        }
                     }
                 }
             }
-            // the chunk's last tile frees its slot
-            if (clen == st || (u + 1 == KC && !next_contig)) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(grp, slot));
-            }
+            // the chunk's slot is free again
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(grp, slot));
         }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             const float v = acc[n] + __shfl_xor_sync(0xffffffffu, acc[n], 1);
-            if (n < c && h_lane == 0 && live) dst[n * ld] = gu ? v : v * s_bsw[off + n];
+            if (n < c && h_lane == 0 && live) dst[n * ld] = GU ? v : v * s_bsw[off + n];
         }
     };
-    auto dispatch = [&](bool gu, int off, int c, const uint8_t* base, bool next_contig, int kb0,
-                        int KC, int row, float* dst, size_t ld) {
-        if (c <= 1) run_tiles(IntC<1>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
-        else if (c <= 2) run_tiles(IntC<2>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
-        else if (c <= 4) run_tiles(IntC<4>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
-        else if (c <= 8) run_tiles(IntC<8>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
-        else if (MAXNT <= 16 || c <= 16) run_tiles(IntC<16>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
-        else run_tiles(IntC<MAXNT>{}, gu, off, c, base, next_contig, kb0, KC, row, dst, ld);
+    auto dispatch = [&](auto guc, int off, int c, int kb0, int KC, int row, float* dst, size_t ld) {
+        if (c <= 1) run_tiles(IntC<1>{}, guc, off, c, kb0, KC, row, dst, ld);
+        else if (c <= 2) run_tiles(IntC<2>{}, guc, off, c, kb0, KC, row, dst, ld);
+        else if (c <= 4) run_tiles(IntC<4>{}, guc, off, c, kb0, KC, row, dst, ld);
+        else if (c <= 8) run_tiles(IntC<8>{}, guc, off, c, kb0, KC, row, dst, ld);
+        else if (MAXNT <= 16 || c <= 16) run_tiles(IntC<16>{}, guc, off, c, kb0, KC, row, dst, ld);
+        else run_tiles(IntC<MAXNT>{}, guc, off, c, kb0, KC, row, dst, ld);
     };
-    // Adds a run's `add` finished tasks to `counter` (one release + acquire
-    // atomic by one thread, after the group barrier that orders the run's
-    // stores) and tells the group whether the run completed the `target`:
-    // then the group goes on with the follow-up work, reading what the other
-    // tasks stored.
-    auto flush = [&](int* counter, int add, int target) -> bool {
-        group_sync();
-        if (gtid == 0) s_flag[grp] = (atom_add_acq_rel_gpu(counter, add) + add == target) ? 1 : 0;
-        group_sync();
-        return s_flag[grp] != 0;
-    };
-
-    // The h of a down task's K range, from the gate/up K parts of its expert:
+    // The h of a run of down tasks, from the gate/up K parts of its expert:
     // features f0 .. f0 + nf - 1 of bucket rows off .. off + c - 1, into this
     // group's buffer (int8 codes in dp4a order, {scale, -8 * sum} per 32).
-    // The group's warps split the K parts (ps subsets) and the feature
-    // quads, two K parts in flight a lane; the subsets' sums meet in shared
-    // memory and are added in subset order.  Every down task of the range
-    // computes the same codes.
+    // The group's warps split the K parts into ps subsets (as many as still
+    // cover every feature quad in one pass) and the quads; a lane keeps two
+    // K parts in flight, the subsets' sums meet in shared memory and are
+    // added in subset order.
     auto compute_h = [&](int off, int c, int f0, int nf, int nsg_, bool store) {
-        const int ps = nsg_ >= 8 ? 8 : nsg_ >= 4 ? 4 : nsg_ >= 2 ? 2 : 1;
-        const int sub = w8 % ps, blk = w8 / ps, nblk = kGroupWarps / ps;
         const int nq4 = c * nf / 4, q4_per_tok = nf / 4;
+        int ps = 1;
+        while (ps < kGroupWarps && 2 * ps <= nsg_ && 32 * (kGroupWarps / (2 * ps)) >= nq4) ps *= 2;
+        const int sub = w8 % ps, blk = w8 / ps, nblk = kGroupWarps / ps;
         float4* red = reinterpret_cast<float4*>(red_buf);  // [8 warps][32 lanes][2]
         for (int qb = 0; qb < nq4; qb += 32 * nblk) {
             const int quad = qb + blk * 32 + lane;
@@ -788,15 +892,84 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         }
     };
 
-    int h_key = -1;  // (touched slot, K part) whose h is in this group's buffer
-    int run = 0;     // tasks of the current run counted so far
+    // Items it0 .. it1 - 1 (item = token * 128 + column) of output columns
+    // rbd*128 .. +127, once every down task of the block is stored: residual
+    // plus every slot's parts, slots in order, K parts in order.  sp threads
+    // share an item when the piece has fewer items than the group has
+    // threads; each takes a contiguous range of the parts (the first also
+    // the residual) and the ranges' sums are added in order.  A thread walks
+    // its items x parts in order, sixteen loads in flight.
+    auto combine = [&](int rbd, int it0, int it1) {
+        const int c0 = rbd * kTileRows, n_it = it1 - it0, P = k * nsd;
+        int sp = 1;
+        while (sp < 4 && n_it * 2 * sp <= kGroupThreads && 2 * sp <= P) sp *= 2;
+        const int sub = gtid % sp, istride = kGroupThreads / sp;
+        const int pa = P * sub / sp, pb = P * (sub + 1) / sp;
+        const int ne = pb - pa + (sub == 0 ? 1 : 0);  // loads of an item (+ the residual)
+        const int ja = pa / nsd, kpa = pa % nsd;
+        float* cred = reinterpret_cast<float*>(red_buf);  // [n_it][sp] range sums (sp > 1)
+        auto store_out = [&](int it, float v) {
+            const size_t o = (size_t)(it / kTileRows) * H + c0 + it % kTileRows;
+            if (a.out_fp32) static_cast<float*>(a.out)[o] = v;
+            else static_cast<uint16_t*>(a.out)[o] = float_to_bf16_bits(v);
+        };
+        // load walker (item, entry, slot j, K part kp) and sum walker (item, entry)
+        int it_l = it0 + gtid / sp, e_l = 0, j = ja, kp = kpa;
+        int it_c = it_l, e_c = 0;
+        float v = 0.f;
+        while (it_c < it1) {
+            float part[16];
+#pragma unroll
+            for (int z = 0; z < 16; ++z) {
+                part[z] = 0.f;
+                if (it_l < it1) {
+                    const int t = it_l / kTileRows, col = c0 + it_l % kTileRows;
+                    if (sub == 0 && e_l == 0) {
+                        part[z] = bf16_bits_to_float(a.x_res[(size_t)t * H + col]);
+                    } else {
+                        part[z] = __ldcg(a.y_part + ((size_t)kp * Tk + s_slotpos[t * k + j]) * H + col);
+                        if (++kp == nsd) { kp = 0; ++j; }
+                    }
+                    if (++e_l == ne) {
+                        e_l = 0;
+                        j = ja;
+                        kp = kpa;
+                        it_l += istride;
+                    }
+                }
+            }
+#pragma unroll
+            for (int z = 0; z < 16; ++z) {
+                if (it_c < it1) {
+                    v += part[z];
+                    if (++e_c == ne) {
+                        if (sp > 1) cred[(it_c - it0) * sp + sub] = v;
+                        else store_out(it_c, v);
+                        v = 0.f;
+                        e_c = 0;
+                        it_c += istride;
+                    }
+                }
+            }
+        }
+        if (sp > 1) {
+            group_sync();
+            for (int it = it0 + gtid; it < it1; it += kGroupThreads) {
+                float w = cred[(it - it0) * sp];
+                for (int q = 1; q < sp; ++q) w += cred[(it - it0) * sp + q];
+                store_out(it, w);
+            }
+            group_sync();  // the buffer is shared with compute_h
+        }
+    };
+
+    int h_key = -1;    // (touched slot, K part) whose h is in this group's buffer
+    int rb_first = 0;  // the first row block of the current run of down tasks
+    int run = 0;       // gate/up tasks of the current run counted so far
     Walk w = walk_start(grp);
     while (walk_live(w)) {
         const Walk nx = walk_next(w, grp);
         const bool has_next = walk_live(nx);
-        const uint8_t* base = walk_base(w);
-        const int KC = w.gu ? KCg : KCd;
-        const bool next_contig = has_next && walk_base(nx) == base + (size_t)KC * kTileBytes;
         const int i = w.i, rb = w.rb, kc = w.kc;
         const Walk cur = w;
         w = nx;
@@ -804,7 +977,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         if (cur.gu) {
             // ------------------------------------------ gate/up task
             const int row = rb * kTileRows + lrow;
-            dispatch(true, off, c, base, next_contig, kc * KCg, KCg, row,
+            dispatch(BoolC<true>{}, off, c, kc * KCg, KCg, row,
                      a.gu_part + ((size_t)kc * Tk + off) * 2 * I + row, (size_t)2 * I);
             ++run;
             // the run goes on while the next task counts toward the same h
@@ -817,9 +990,9 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
             run = 0;
         } else {
             // --------------------------------------------- down task
-            const int rbd = rb;
             if (i * nsd + kc != h_key) {
-                // wait until every gate/up K part of the h blocks this K range
+                // a new run (same slot and K part, row blocks rb, rb + 1, ...):
+                // wait until every gate/up K part of the h blocks its K range
                 // overlaps is stored, then form h for the range
                 const int f0 = kc * KCd * kTileK, nf = KCd * kTileK;
                 if (gtid == 0) {
@@ -841,55 +1014,68 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
                 }
                 group_sync();
                 if (s_flag[grp]) {
-                    compute_h(off, c, f0, nf, nsg, a.write_qh && rbd == 0);
+                    compute_h(off, c, f0, nf, nsg, a.write_qh && rb == 0);
                 } else {
                     live = false;  // nothing valid to multiply: skip the rest
                 }
                 group_sync();
                 h_key = i * nsd + kc;
+                rb_first = rb;
             }
-            const int row = rbd * kTileRows + lrow;
-            dispatch(false, off, c, base, next_contig, kc * KCd, KCd, row,
+            const int row = rb * kTileRows + lrow;
+            dispatch(BoolC<false>{}, off, c, kc * KCd, KCd, row,
                      a.y_part + ((size_t)kc * Tk + off) * H + row, (size_t)H);
-            ++run;
-            // the run goes on while the next task counts toward the same columns
-            if (has_next && nx.i == i && nx.rb == rbd) continue;
-            const int add = run;
-            run = 0;
-            if (!flush(&a.cnt_y[rbd], add, nt * nsd)) continue;
-            // the last run of output columns rbd*128 .. +127: residual plus
-            // every slot's parts, slots in order, K parts in order (loaded
-            // eight at a time before they are added)
-            const int c0 = rbd * kTileRows;
-            for (int it = gtid; it < kTileRows * T; it += kGroupThreads) {
-                const int t = it / kTileRows, col = c0 + it % kTileRows;
-                float v = bf16_bits_to_float(a.x_res[(size_t)t * H + col]);
-                const float* yc = a.y_part + col;
-                int jj = 0, kp = 0;  // slot and K part of the next load
-                for (int q0 = 0; q0 < k * nsd; q0 += 8) {
-                    float part[8];
-#pragma unroll
-                    for (int z = 0; z < 8; ++z) {
-                        part[z] = 0.f;
-                        if (jj < k) {
-                            part[z] = __ldcg(yc + ((size_t)kp * Tk + s_slotpos[t * k + jj]) * H);
-                            if (++kp == nsd) { kp = 0; ++jj; }
+            // the run goes on while the next task shares its slot and K part
+            if (has_next && !nx.gu && nx.i == i && nx.kc == kc) continue;
+            // count the run's tasks (one per column block rb_first .. rb): a
+            // release add per block after the barrier that orders the run's
+            // stores
+            const int nrb = rb - rb_first + 1;
+            group_sync();
+            for (int r = gtid; r < nrb; r += kGroupThreads) red_release_add(&a.cnt_y[rb_first + r], 1);
+        }
+    }
+
+    // ------------------------------------------------------------ combine
+    // The items of each output column block are cut into np pieces; piece q
+    // of block r (unit u = r * np + q) belongs to worker u * V / (RBd * np),
+    // which combines it after its own tasks, once the block's count shows
+    // every down task stored.  With no more blocks than workers, no worker
+    // holds more than one unit.
+    {
+        const int V = 2 * G, v = 2 * b + grp, items = kTileRows * T;
+        int np = V / RBd;
+        np = np < items / 64 ? np : items / 64;
+        np = np > 1 ? np : 1;
+        const int nu = RBd * np;
+        const int u0 = (v * nu + V - 1) / V, u1 = ((v + 1) * nu + V - 1) / V;
+        for (int u = u0; u < u1; ++u) {
+            const int r = u / np, q = u - r * np;
+            if (gtid == 0) {
+                const int* cnt = &a.cnt_y[r];
+                bool got = !s_abort;
+                if (got && ld_acquire(cnt) < nt * nsd) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (ld_acquire(cnt) < nt * nsd) {
+                        if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            got = false;
+                            break;
                         }
                     }
-#pragma unroll
-                    for (int z = 0; z < 8; ++z) v += part[z];  // (the padding adds 0)
                 }
-                if (a.out_fp32)
-                    static_cast<float*>(a.out)[(size_t)t * H + col] = v;
-                else
-                    static_cast<uint16_t*>(a.out)[(size_t)t * H + col] = float_to_bf16_bits(v);
+                if (!got) fail();
+                s_flag[grp] = got ? 1 : 0;
             }
+            group_sync();
+            if (s_flag[grp]) combine(r, q * items / np, (q + 1) * items / np);
+            group_sync();  // s_flag is reused
         }
     }
 }
 
 // ---------------------------------------------------------------- launch
 int g_layer_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
+int g_prep_carveout[64] = {};
 
 struct Plan {
     int ns, st, off_bar, off_ax, off_ah, ah_bytes, off_red, smem;
@@ -920,8 +1106,9 @@ bool plan_layer(int T, int H, int I, int E, Plan* p) {
     p->off_ax = al128(p->off_red + 2 * kRedBytes);
     p->off_bar = al128(p->off_ax + ax);
     p->smem = p->off_bar + 2 * kGroups * ns * 8;
-    // the routing phase keeps all T x E logits below the codes of x
-    return (long long)T * E * 4 <= p->off_ax;
+    // the routing phase keeps all T x E logits and their order keys below
+    // the codes of x
+    return (long long)T * E * 8 <= p->off_ax;
 }
 
 __global__ void coop_pdl_probe_kernel(int* p) {
@@ -974,16 +1161,16 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
                          int* nsd_max) {
     const size_t Tk = (size_t)T * k;
     const int KBg = H / kTileK, KBd = I / kTileK;
-    auto cap = [](size_t row_bytes) {
-        size_t c = row_bytes ? kPartBudget / row_bytes : kMaxSplit;
+    auto cap = [](size_t budget, size_t part_bytes) {
+        size_t c = part_bytes ? budget / part_bytes : kMaxSplit;
         return (int)std::max<size_t>(1, std::min<size_t>(c, kMaxSplit));
     };
-    *cap_g = cap(Tk * 2 * I * 4);
-    *cap_d = cap(Tk * H * 4);
+    *cap_g = cap(kPartBudgetGU, Tk * 2 * I * 4);
+    *cap_d = cap(kPartBudgetD, Tk * H * 4);
     // the split only shrinks as more experts are touched, and at least k are
     const int nt_min = std::max(1, std::min(k, E));
-    *nsg_max = decode_split_for(nt_min * (2 * I / kTileRows), KBg, kTargetGU, *cap_g);
-    *nsd_max = decode_split_for(nt_min * (H / kTileRows), KBd, kTargetD, *cap_d);
+    *nsg_max = decode_split_for(nt_min * (2 * I / kTileRows), KBg, kTargetTasks, *cap_g);
+    *nsd_max = decode_split_for(nt_min * (H / kTileRows), KBd, kTargetTasks, *cap_d);
 }
 
 int decode_sync_ints(int T, int H, int I, int E, int k) {
@@ -1027,6 +1214,14 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
         (err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     psmem)) != cudaSuccess)
         return err;
+    // the SM's largest shared-memory split for the prep kernel too, so that a
+    // layer CTA of the same call can be placed beside a running prep CTA
+    if (!g_prep_carveout[dev & 63]) {
+        if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return err;
+        g_prep_carveout[dev & 63] = 1;
+    }
     if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess) {
         cudaGetLastError();
         return err;
@@ -1060,17 +1255,16 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.cnt_y = ws.sync + nslot * (I / kTileRows);
     a.cap_g = ws.cap_g;
     a.cap_d = ws.cap_d;
-    for (int d = 1; d <= H / kTileK && d <= ws.cap_g && a.ndiv_g < 16; ++d)
-        if ((H / kTileK) % d == 0) a.div_g[a.ndiv_g++] = d;
-    for (int d = 1; d <= I / kTileK && d <= ws.cap_d && a.ndiv_d < 16; ++d)
-        if ((I / kTileK) % d == 0) a.div_d[a.ndiv_d++] = d;
-    // 32-bit task indices: b x (tasks) must fit
-    {
-        const long long nt_max = std::min(E, T * k);
-        const long long per = std::max((long long)(2 * I / kTileRows) * a.div_g[a.ndiv_g - 1],
-                                       (long long)(H / kTileRows) * a.div_d[a.ndiv_d - 1]);
-        if ((long long)(num_sms + 1) * nt_max * per >= (1ll << 31)) return cudaErrorInvalidValue;
-    }
+    // the K splits the kernel may choose: divisors of the row's 64-column
+    // blocks within the cap, at least two tiles a task (the rule of
+    // decode_split_for)
+    auto divisors = [](int KB, int cap, int* list, int* n) {
+        const int dmax = KB > 1 ? KB / 2 : 1;
+        for (int d = 1; d <= dmax && d <= cap && *n < 16; ++d)
+            if (KB % d == 0) list[(*n)++] = d;
+    };
+    divisors(H / kTileK, ws.cap_g, a.div_g, &a.ndiv_g);
+    divisors(I / kTileK, ws.cap_d, a.div_d, &a.ndiv_d);
     a.out = out;
     a.out_fp32 = out_fp32 ? 1 : 0;
     a.dots_gu = dots_gu;

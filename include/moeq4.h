@@ -274,8 +274,8 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
  * library holds it until the process exits).  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library routine is called.
  *   - Shapes whose workspace (moe_workspace_bytes(MOE_MODE_DECODE, ...)) is
- *     larger than the array are rejected with MOE_ERR_WORKSPACE; 4 MiB covers
- *     T <= 16 at H = 2048, I = 768, E <= 256, k = 8.
+ *     larger than the array are rejected with MOE_ERR_WORKSPACE; 8 MiB covers
+ *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8 (5.4 MiB at T = 32).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -286,7 +286,7 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
  *     Calls whose work overlaps on the GPU (several streams or host threads
  *     on one device) race on the array: serialise them.
  */
-#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int moe_w4a8_forward_decode_noalloc(const uint16_t* x_bf16, const float* wr,
                                     const void* wgu_packed, const void* wd_packed,
                                     int T, int H, int I, int E, int k, unsigned flags,

@@ -103,10 +103,10 @@ def test_noalloc_prenorm_flag():
 
 
 def test_noalloc_rejects_scratch_overflow():
-    # T = 32, H = 4096, I = 1536, E = 256, k = 8 needs ~4.8 MB of scratch, more
-    # than the 4 MiB array; the call is refused before any weight is read, so
-    # small placeholder weight buffers suffice.
-    T, H, I, E, k = 32, 4096, 1536, 256, 8
+    # T = 16, H = 4096, I = 2048, E = 256, k = 16 fits the on-chip staging but
+    # needs ~8.7 MiB of scratch, more than the 8 MiB array; the call is refused
+    # before any weight is read, so small placeholder weight buffers suffice.
+    T, H, I, E, k = 16, 4096, 2048, 256, 16
     assert moe.moe_workspace_bytes(moe.MOE_MODE_DECODE, T, H, I, E, k) > moe.MOE_NOALLOC_SCRATCH_BYTES
     x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
     wr = torch.zeros((E, H), dtype=torch.float32, device="cuda")
