@@ -216,24 +216,17 @@ __host__ __device__ inline int decode_split_for(int units, int KB, int target, i
 namespace {
 
 // ------------------------------------------------------------------ prep
-// One warp per token (tokens w, w + 4, ...), no block barriers after the
-// router row has landed.  Lane l holds the row's 8-column units u0 + l +
-// 32 i, i < 8, of a 2048-column chunk; with one chunk (H <= 2048) the row is
-// read once, otherwise each chunk is read in turn (twice with the pre-norm:
-// once for the norm).  At most 80 registers a thread: next to a layer kernel
-// of the previous call (576 threads x 96) the SM has 128 x 80 left, so the
-// next layer's prep can stage its router row while that kernel runs.
-constexpr int kPrepUnits = 8;            // units per lane per chunk
-constexpr int kChunkUnits = kPrepUnits * 32;
-
-__device__ __forceinline__ void prep_load(const uint16_t* xr, int u0, int H8, int lane,
-                                          uint4 (&v)[kPrepUnits]) {
-#pragma unroll
-    for (int i = 0; i < kPrepUnits; ++i) {
-        const int u = u0 + lane + 32 * i;
-        v[i] = u < H8 ? __ldcg(reinterpret_cast<const uint4*>(xr) + u) : make_uint4(0u, 0u, 0u, 0u);
-    }
-}
+// Each token has tpt = 128 >> ceil(log2 T) threads (4 <= tpt <= 128); thread
+// `sub` of token t holds the 8-column units sub, sub + tpt, ... of its row,
+// eight at a time.  Its partial sums (one per unit slot mod 8, in column
+// order within a unit) are added in slot order, then across the token's
+// threads by a butterfly (and across its warps in warp order, through
+// shared memory, when tpt > 32).  A quad of threads holds one 32-column
+// group, whose int8 codes one CTA writes: CTA (t * H/32 + g) % grid.  At
+// most 80 registers a thread: next to a layer kernel of the previous call
+// (576 threads x 96) the SM has 128 x 80 left, so the next layer's prep can
+// stage its router row while that kernel runs.
+constexpr int kPrepBatch = 8;  // units a thread loads at once
 
 __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -247,6 +240,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
 __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     extern __shared__ __align__(128) uint8_t psm[];  // this CTA's router row [H] fp32
     __shared__ __align__(8) uint64_t s_bar;
+    __shared__ float s_red[kPrepThreads / 32];
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int e = blockIdx.x, H = a.H, T = a.T;
     const uint32_t bar = smem_u32(&s_bar);
@@ -261,49 +255,79 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     pdl_trigger();  // the layer kernel may be scheduled; it waits for our end
     for (int i = e * kPrepThreads + tid; i < a.nsync; i += gridDim.x * kPrepThreads) a.sync[i] = 0;
     const int H8 = H / 8, G32 = H / kGroup;
-    const int nw = kPrepThreads / 32, nchunk = (H8 + kChunkUnits - 1) / kChunkUnits;
-    const bool one = nchunk == 1;
-    uint4 cur[kPrepUnits];
+    int tpt = kPrepThreads;
+    while (tpt > 4 && kPrepThreads / tpt < T) tpt >>= 1;  // T <= 32
+    const int t = tid / tpt, sub = tid % tpt;
+    const bool act = t < T;
+    const int nm = (H8 + tpt - 1) / tpt;  // unit slots of a thread (the last ones may be past the row)
+    const uint16_t* xr = a.x + (size_t)(act ? t : 0) * H;
+    uint4 v[kPrepBatch];
+    auto load = [&](int m0) {
+#pragma unroll
+        for (int z = 0; z < kPrepBatch; ++z) {
+            const int u = sub + tpt * (m0 + z);
+            v[z] = act && m0 + z < nm && u < H8 ? __ldcg(reinterpret_cast<const uint4*>(xr) + u)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // the sum over the token's threads: butterfly within the warp, then the
+    // token's warps in order
+    auto token_sum = [&](float x) -> float {
+        for (int o = 1; o < 32 && o < tpt; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (tpt > 32) {
+            __syncthreads();  // s_red is free
+            if (lane == 0) s_red[warp] = x;
+            __syncthreads();
+            const int w0 = (t * tpt) / 32;
+            x = 0.f;
+            for (int q = 0; q < tpt / 32; ++q) x += s_red[w0 + q];
+        }
+        return x;
+    };
     if (!mbar_wait(bar, 0)) record_status(a.status, kStatusTimeout);
     const float* w = reinterpret_cast<const float*>(psm);
-    for (int t = warp; t < T; t += nw) {
-        const uint16_t* xr = a.x + (size_t)t * H;
-        if (one) prep_load(xr, 0, H8, lane, cur);
-        float r = 1.0f;
-        if (a.prenorm) {
-            // each lane over its columns, one partial sum per unit slot (in
-            // column order within a unit), the slots in order, then a
-            // butterfly
-            float ssu[kPrepUnits];
+    float r = 1.0f;
+    const bool one_batch = nm <= kPrepBatch;
+    if (a.prenorm) {
+        // RMSNorm of the token, in fp32
+        float ssu[kPrepBatch];
 #pragma unroll
-            for (int i = 0; i < kPrepUnits; ++i) ssu[i] = 0.f;
-            for (int ch = 0; ch < nchunk; ++ch) {
-                if (!one) prep_load(xr, ch * kChunkUnits, H8, lane, cur);
+        for (int z = 0; z < kPrepBatch; ++z) ssu[z] = 0.f;
+        for (int m0 = 0; m0 < nm; m0 += kPrepBatch) {
+            load(m0);
 #pragma unroll
-                for (int i = 0; i < kPrepUnits; ++i) {
+            for (int z = 0; z < kPrepBatch; ++z) {
+                if (m0 + z < nm) {  // (uniform)
                     float xf[8];
-                    unpack8(cur[i], xf);
+                    unpack8(v[z], xf);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) ssu[i] = fmaf(xf[q], xf[q], ssu[i]);
+                    for (int q = 0; q < 8; ++q) ssu[z] = fmaf(xf[q], xf[q], ssu[z]);
                 }
             }
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < kPrepUnits; ++i) ss += ssu[i];
-            ss = warp_sum(ss);
-            r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + 1e-6f));
         }
-        float accu[kPrepUnits];  // the logit's partial sums, one per unit slot
+        float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < kPrepUnits; ++i) accu[i] = 0.f;
-        for (int ch = 0; ch < nchunk; ++ch) {
-            if (!one) prep_load(xr, ch * kChunkUnits, H8, lane, cur);
+        for (int z = 0; z < kPrepBatch; ++z) ss += ssu[z];
+        ss = token_sum(ss);
+        r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + 1e-6f));
+    }
+    float accu[kPrepBatch];  // the logit's partial sums, one per unit slot
 #pragma unroll
-            for (int i = 0; i < kPrepUnits; ++i) {
-                const int u = ch * kChunkUnits + lane + 32 * i;
-                const bool valid = u < H8;
+    for (int z = 0; z < kPrepBatch; ++z) accu[z] = 0.f;
+    // duty: CTA (t * H/32 + g) % grid codes group g of token t; this quad's
+    // group advances by tpt/4 a unit slot
+    const unsigned grid = gridDim.x, gstep = (unsigned)(tpt / 4) % grid;
+    unsigned gd = (unsigned)(t * G32 + sub / 4) % grid;
+    const unsigned qmask = 0xFu << (lane & ~3);  // this thread's quad
+    for (int m0 = 0; m0 < nm; m0 += kPrepBatch) {
+        if (!(a.prenorm && one_batch)) load(m0);  // one batch: still held from the norm
+#pragma unroll
+        for (int z = 0; z < kPrepBatch; ++z) {
+            if (m0 + z < nm) {  // (uniform)
+                const int u = sub + tpt * (m0 + z);
+                const bool valid = act && u < H8;
                 float xf[8];
-                unpack8(cur[i], xf);
+                unpack8(v[z], xf);
                 if (a.prenorm) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) xf[q] = bf16_bits_to_float(float_to_bf16_bits(xf[q] * r));
@@ -311,7 +335,7 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                 if (valid) {
                     const float4 w0 = *reinterpret_cast<const float4*>(w + u * 8);
                     const float4 w1 = *reinterpret_cast<const float4*>(w + u * 8 + 4);
-                    float acc = accu[i];
+                    float acc = accu[z];
                     acc = fmaf(xf[0], w0.x, acc);
                     acc = fmaf(xf[1], w0.y, acc);
                     acc = fmaf(xf[2], w0.z, acc);
@@ -320,23 +344,18 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                     acc = fmaf(xf[5], w1.y, acc);
                     acc = fmaf(xf[6], w1.z, acc);
                     acc = fmaf(xf[7], w1.w, acc);
-                    accu[i] = acc;
+                    accu[z] = acc;
                 }
-                // int8 codes per 32 columns (lanes 4m..4m+3 hold one group):
-                // group g of token t is coded by CTA (t * H/32 + g) % grid
-                float amax = 0.f;
+                if (valid && gd == (unsigned)e) {  // the whole quad: one group, one decision
+                    float amax = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const bool duty = (unsigned)(t * G32 + u / 4) % gridDim.x == (unsigned)e;
-                uint32_t lo = 0u, hi = 0u;
-                int gsum = 0;
-                uint16_t db = 0;
-                float d = 0.f;
-                if (duty) {
-                    db = act_scale_bits(amax);
-                    d = half_bits_to_float(db);
+                    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
+                    amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
+                    const uint16_t db = act_scale_bits(amax);
+                    const float d = half_bits_to_float(db);
+                    uint32_t lo = 0u, hi = 0u;
+                    int gsum = 0;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int qc = act_code(xf[q], d);
@@ -344,10 +363,8 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                         if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
                         else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
                     }
-                }
-                gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
-                gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
-                if (duty && valid) {
+                    gsum += __shfl_xor_sync(qmask, gsum, 1);
+                    gsum += __shfl_xor_sync(qmask, gsum, 2);
                     *reinterpret_cast<uint2*>(a.xq + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
                     *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
                     if ((lane & 3) == 0) {
@@ -356,13 +373,15 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                     }
                 }
             }
+            gd += gstep;
+            if (gd >= grid) gd -= grid;
         }
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < kPrepUnits; ++i) acc += accu[i];
-        acc = warp_sum(acc);
-        if (lane == 0) a.logits[(size_t)t * a.E + e] = acc;
     }
+    float acc = 0.f;
+#pragma unroll
+    for (int z = 0; z < kPrepBatch; ++z) acc += accu[z];
+    acc = token_sum(acc);
+    if (act && sub == 0) a.logits[(size_t)t * a.E + e] = acc;
 }
 
 // ----------------------------------------------------------------- layer
@@ -727,76 +746,92 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     const int r_lane = lane >> 1, h_lane = lane & 1;
     const int lrow = w8 * 16 + r_lane;  // this lane's row in the 128-row block
 
-    // One task: rows rb*128 + lrow, 64-column blocks kb0 .. kb0 + KC - 1 of
-    // the current expert (bucket rows off .. off + c - 1, NT >= c), packed
-    // tiles base .. base + KC - 1, which arrive in chunks of up to st tiles.
-    // The lane pair's sum for bucket row off + n is stored at dst[n * ld]
-    // (down: times the row's routing weight).  GU: gate/up (activations x,
-    // bucket row -> token) or down (activations h, one row per bucket row).
-    auto run_tiles = [&](auto ntc, auto guc, int off, int c, int kb0, int KC, int row, float* dst,
-                         size_t ld) {
+    // One run: the group's consecutive tasks of touched slot i that share a
+    // row block (gate/up: so one h block) or a K part (down: so one h
+    // range), from w on; returns the number of tasks and leaves w at the
+    // next one.  Bucket rows off .. off + c - 1 (NT >= c).  A task is rows
+    // rb*128 + lrow and the K part's KC 64-column blocks; its tiles arrive
+    // in chunks of up to st tiles.  At its end the lane pair's sum for bucket
+    // row off + n is stored in the K part's slot (down: times the row's
+    // routing weight).  GU: gate/up (activations x, bucket row -> token) or
+    // down (activations h, one row per bucket row).
+    auto run_tasks = [&](auto ntc, auto guc, int off, int c, Walk& w) -> int {
         constexpr int NT = decltype(ntc)::value;
         constexpr bool GU = decltype(guc)::value;
         const uint8_t* aq = GU ? ax_q : ah_q;
         const int2* as = GU ? ax_s : ah_s;
-        const int K = GU ? H : I, Gk = GU ? Gx : Gh;
+        const int K = GU ? H : I, Gk = GU ? Gx : Gh, KC = GU ? KCg : KCd;
         int32_t* dots = GU ? a.dots_gu : a.dots_d;
         const size_t dots_ld = GU ? (size_t)2 * I : (size_t)H;
+        const size_t ld = GU ? (size_t)2 * I : (size_t)H;
         const int code_off = w8 * 512 + lane * 16;                  // this lane's 16 code bytes
         const int scale_off = kTileCodeBytes + w8 * 64 + lane * 2;  // and its group's scale
-        float acc[NT];
+        const int i = w.i;
+        int ntask = 0;
+        while (true) {
+            const int rb = w.rb, kc = w.kc, kb0 = kc * KC, row = rb * kTileRows + lrow;
+            float acc[NT];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) acc[n] = 0.f;
-        for (int u0 = 0; u0 < KC; u0 += st) {
-            const int nu = KC - u0 < st ? KC - u0 : st;
-            if (++slot == ns) {
-                slot = 0;
-                phase ^= 1;
-            }
-            if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
-                fail();
-                live = false;
-            }
-            const uint8_t* chunk = dsm + slot_addr(grp, slot);
-            if (live) {
-                for (int uu = 0; uu < nu; ++uu) {
-                    const uint8_t* tile = chunk + uu * kTileBytes;
-                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
-                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
-                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
-                                            wv.w & 0x0F0F0F0Fu};
-                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
-                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
-                    const int g = 2 * (kb0 + u0 + uu) + h_lane;
+            for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+            for (int u0 = 0; u0 < KC; u0 += st) {
+                const int nu = KC - u0 < st ? KC - u0 : st;
+                if (++slot == ns) {
+                    slot = 0;
+                    phase ^= 1;
+                }
+                if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
+                    fail();
+                    live = false;
+                }
+                const uint8_t* chunk = dsm + slot_addr(grp, slot);
+                if (live) {
+                    for (int uu = 0; uu < nu; ++uu) {
+                        const uint8_t* tile = chunk + uu * kTileBytes;
+                        const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                        const float dw =
+                            half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
+                        const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
+                                                wv.w & 0x0F0F0F0Fu};
+                        const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
+                                                (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                        const int g = 2 * (kb0 + u0 + uu) + h_lane;
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        if (n < c) {
-                            const int ar = GU ? s_btok[off + n] : n;
-                            const int2 sc = as[ar * Gk + g];
-                            const int dot = group_dot(wl, wh, aq + ar * K + g * kGroup, sc.y);
-                            acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
-                            if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                        for (int n = 0; n < NT; ++n) {
+                            if (n < c) {
+                                const int ar = GU ? s_btok[off + n] : n;
+                                const int2 sc = as[ar * Gk + g];
+                                const int dot = group_dot(wl, wh, aq + ar * K + g * kGroup, sc.y);
+                                acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
+                                if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                            }
                         }
                     }
                 }
+                // the chunk's slot is free again
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(grp, slot));
             }
-            // the chunk's slot is free again
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(grp, slot));
-        }
+            float* dst = (GU ? a.gu_part + ((size_t)kc * Tk + off) * 2 * I
+                             : a.y_part + ((size_t)kc * Tk + off) * H) + row;
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const float v = acc[n] + __shfl_xor_sync(0xffffffffu, acc[n], 1);
-            if (n < c && h_lane == 0 && live) dst[n * ld] = GU ? v : v * s_bsw[off + n];
+            for (int n = 0; n < NT; ++n) {
+                const float v = acc[n] + __shfl_xor_sync(0xffffffffu, acc[n], 1);
+                if (n < c && h_lane == 0 && live) dst[n * ld] = GU ? v : v * s_bsw[off + n];
+            }
+            ++ntask;
+            const Walk nx = walk_next(w, grp);
+            const bool more = walk_live(nx) && nx.gu == GU && nx.i == i && (GU ? nx.rb == rb : nx.kc == kc);
+            w = nx;
+            if (!more) return ntask;
         }
     };
-    auto dispatch = [&](auto guc, int off, int c, int kb0, int KC, int row, float* dst, size_t ld) {
-        if (c <= 1) run_tiles(IntC<1>{}, guc, off, c, kb0, KC, row, dst, ld);
-        else if (c <= 2) run_tiles(IntC<2>{}, guc, off, c, kb0, KC, row, dst, ld);
-        else if (c <= 4) run_tiles(IntC<4>{}, guc, off, c, kb0, KC, row, dst, ld);
-        else if (c <= 8) run_tiles(IntC<8>{}, guc, off, c, kb0, KC, row, dst, ld);
-        else if (MAXNT <= 16 || c <= 16) run_tiles(IntC<16>{}, guc, off, c, kb0, KC, row, dst, ld);
-        else run_tiles(IntC<MAXNT>{}, guc, off, c, kb0, KC, row, dst, ld);
+    auto dispatch = [&](auto guc, int off, int c, Walk& w) -> int {
+        if (c <= 1) return run_tasks(IntC<1>{}, guc, off, c, w);
+        if (c <= 2) return run_tasks(IntC<2>{}, guc, off, c, w);
+        if (c <= 4) return run_tasks(IntC<4>{}, guc, off, c, w);
+        if (c <= 8) return run_tasks(IntC<8>{}, guc, off, c, w);
+        if (MAXNT <= 16 || c <= 16) return run_tasks(IntC<16>{}, guc, off, c, w);
+        return run_tasks(IntC<MAXNT>{}, guc, off, c, w);
     };
     // The h of a run of down tasks, from the gate/up K parts of its expert:
     // features f0 .. f0 + nf - 1 of bucket rows off .. off + c - 1, into this
@@ -897,15 +932,14 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     // plus every slot's parts, slots in order, K parts in order.  sp threads
     // share an item when the piece has fewer items than the group has
     // threads; each takes a contiguous range of the parts (the first also
-    // the residual) and the ranges' sums are added in order.  A thread walks
-    // its items x parts in order, sixteen loads in flight.
+    // the residual), loading eight at a time, and the ranges' sums are added
+    // in order.
     auto combine = [&](int rbd, int it0, int it1) {
         const int c0 = rbd * kTileRows, n_it = it1 - it0, P = k * nsd;
         int sp = 1;
-        while (sp < 4 && n_it * 2 * sp <= kGroupThreads && 2 * sp <= P) sp *= 2;
-        const int sub = gtid % sp, istride = kGroupThreads / sp;
+        while (sp < 8 && n_it * 2 * sp <= kGroupThreads && 2 * sp <= P) sp *= 2;
+        const int sub = gtid % sp;
         const int pa = P * sub / sp, pb = P * (sub + 1) / sp;
-        const int ne = pb - pa + (sub == 0 ? 1 : 0);  // loads of an item (+ the residual)
         const int ja = pa / nsd, kpa = pa % nsd;
         float* cred = reinterpret_cast<float*>(red_buf);  // [n_it][sp] range sums (sp > 1)
         auto store_out = [&](int it, float v) {
@@ -913,126 +947,93 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
             if (a.out_fp32) static_cast<float*>(a.out)[o] = v;
             else static_cast<uint16_t*>(a.out)[o] = float_to_bf16_bits(v);
         };
-        // load walker (item, entry, slot j, K part kp) and sum walker (item, entry)
-        int it_l = it0 + gtid / sp, e_l = 0, j = ja, kp = kpa;
-        int it_c = it_l, e_c = 0;
-        float v = 0.f;
-        while (it_c < it1) {
-            float part[16];
+#pragma unroll 1
+        for (int it = it0 + gtid / sp; it < it1; it += kGroupThreads / sp) {
+            const int t = it / kTileRows, col = c0 + it % kTileRows;
+            float v = sub == 0 ? bf16_bits_to_float(a.x_res[(size_t)t * H + col]) : 0.f;
+            const float* yc = a.y_part + col;
+            const int* sp_t = s_slotpos + t * k;
+            int j = ja, kp = kpa;
+#pragma unroll 1
+            for (int p0 = pa; p0 < pb; p0 += 8) {
+                float part[8];
 #pragma unroll
-            for (int z = 0; z < 16; ++z) {
-                part[z] = 0.f;
-                if (it_l < it1) {
-                    const int t = it_l / kTileRows, col = c0 + it_l % kTileRows;
-                    if (sub == 0 && e_l == 0) {
-                        part[z] = bf16_bits_to_float(a.x_res[(size_t)t * H + col]);
-                    } else {
-                        part[z] = __ldcg(a.y_part + ((size_t)kp * Tk + s_slotpos[t * k + j]) * H + col);
-                        if (++kp == nsd) { kp = 0; ++j; }
-                    }
-                    if (++e_l == ne) {
-                        e_l = 0;
-                        j = ja;
-                        kp = kpa;
-                        it_l += istride;
+                for (int z = 0; z < 8; ++z) {
+                    part[z] = 0.f;
+                    if (p0 + z < pb) {
+                        part[z] = __ldcg(yc + ((size_t)kp * Tk + sp_t[j]) * H);
+                        if (++kp == nsd) {
+                            kp = 0;
+                            ++j;
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int z = 0; z < 16; ++z) {
-                if (it_c < it1) {
-                    v += part[z];
-                    if (++e_c == ne) {
-                        if (sp > 1) cred[(it_c - it0) * sp + sub] = v;
-                        else store_out(it_c, v);
-                        v = 0.f;
-                        e_c = 0;
-                        it_c += istride;
-                    }
-                }
+                for (int z = 0; z < 8; ++z) v += part[z];  // (the padding adds 0)
             }
+            if (sp > 1) cred[(it - it0) * sp + sub] = v;
+            else store_out(it, v);
         }
         if (sp > 1) {
             group_sync();
+#pragma unroll 1
             for (int it = it0 + gtid; it < it1; it += kGroupThreads) {
-                float w = cred[(it - it0) * sp];
-                for (int q = 1; q < sp; ++q) w += cred[(it - it0) * sp + q];
-                store_out(it, w);
+                float v = cred[(it - it0) * sp];
+                for (int q = 1; q < sp; ++q) v += cred[(it - it0) * sp + q];
+                store_out(it, v);
             }
             group_sync();  // the buffer is shared with compute_h
         }
     };
 
-    int h_key = -1;    // (touched slot, K part) whose h is in this group's buffer
-    int rb_first = 0;  // the first row block of the current run of down tasks
-    int run = 0;       // gate/up tasks of the current run counted so far
     Walk w = walk_start(grp);
     while (walk_live(w)) {
-        const Walk nx = walk_next(w, grp);
-        const bool has_next = walk_live(nx);
         const int i = w.i, rb = w.rb, kc = w.kc;
-        const Walk cur = w;
-        w = nx;
         const int e = s_touched[i], off = s_off[e], c = s_off[e + 1] - off;
-        if (cur.gu) {
-            // ------------------------------------------ gate/up task
-            const int row = rb * kTileRows + lrow;
-            dispatch(BoolC<true>{}, off, c, kc * KCg, KCg, row,
-                     a.gu_part + ((size_t)kc * Tk + off) * 2 * I + row, (size_t)2 * I);
-            ++run;
-            // the run goes on while the next task counts toward the same h
-            // block (gate rows rb and up rows rb + RBh feed h block rb % RBh)
+        if (w.gu) {
+            // ------------------------------------------ gate/up run
+            const int n = dispatch(BoolC<true>{}, off, c, w);
+            // count the run's K parts of h block rb % RBh (gate rows rb and
+            // up rows rb + RBh feed it) once they are stored
             const int hb = rb < RBh ? rb : rb - RBh;
-            if (has_next && nx.gu && nx.i == i && (nx.rb < RBh ? nx.rb : nx.rb - RBh) == hb) continue;
-            // count the run's K parts of h block hb (they are stored)
             group_sync();
-            if (gtid == 0) red_release_add(&a.cnt_h[i * RBh + hb], run);
-            run = 0;
+            if (gtid == 0) red_release_add(&a.cnt_h[i * RBh + hb], n);
         } else {
-            // --------------------------------------------- down task
-            if (i * nsd + kc != h_key) {
-                // a new run (same slot and K part, row blocks rb, rb + 1, ...):
-                // wait until every gate/up K part of the h blocks its K range
-                // overlaps is stored, then form h for the range
-                const int f0 = kc * KCd * kTileK, nf = KCd * kTileK;
-                if (gtid == 0) {
-                    bool got = !s_abort;
-                    for (int hb = f0 / kTileRows; hb <= (f0 + nf - 1) / kTileRows && got; ++hb) {
-                        const int* cnt = &a.cnt_h[i * RBh + hb];
-                        if (ld_acquire(cnt) < 2 * nsg) {
-                            const unsigned long long t0 = globaltimer_ns();
-                            while (ld_acquire(cnt) < 2 * nsg) {
-                                if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
-                                    got = false;
-                                    break;
-                                }
+            // --------------------------------------------- down run
+            // (slot i, K part kc, row blocks rb, rb + 1, ...): wait until
+            // every gate/up K part of the h blocks the K range overlaps is
+            // stored, then form h for the range
+            const int f0 = kc * KCd * kTileK, nf = KCd * kTileK;
+            if (gtid == 0) {
+                bool got = !s_abort;
+                for (int hb = f0 / kTileRows; hb <= (f0 + nf - 1) / kTileRows && got; ++hb) {
+                    const int* cnt = &a.cnt_h[i * RBh + hb];
+                    if (ld_acquire(cnt) < 2 * nsg) {
+                        const unsigned long long t0 = globaltimer_ns();
+                        while (ld_acquire(cnt) < 2 * nsg) {
+                            if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+                                got = false;
+                                break;
                             }
                         }
                     }
-                    if (!got) fail();
-                    s_flag[grp] = got ? 1 : 0;
                 }
-                group_sync();
-                if (s_flag[grp]) {
-                    compute_h(off, c, f0, nf, nsg, a.write_qh && rb == 0);
-                } else {
-                    live = false;  // nothing valid to multiply: skip the rest
-                }
-                group_sync();
-                h_key = i * nsd + kc;
-                rb_first = rb;
+                if (!got) fail();
+                s_flag[grp] = got ? 1 : 0;
             }
-            const int row = rb * kTileRows + lrow;
-            dispatch(BoolC<false>{}, off, c, kc * KCd, KCd, row,
-                     a.y_part + ((size_t)kc * Tk + off) * H + row, (size_t)H);
-            // the run goes on while the next task shares its slot and K part
-            if (has_next && !nx.gu && nx.i == i && nx.kc == kc) continue;
-            // count the run's tasks (one per column block rb_first .. rb): a
-            // release add per block after the barrier that orders the run's
-            // stores
-            const int nrb = rb - rb_first + 1;
             group_sync();
-            for (int r = gtid; r < nrb; r += kGroupThreads) red_release_add(&a.cnt_y[rb_first + r], 1);
+            if (s_flag[grp]) {
+                compute_h(off, c, f0, nf, nsg, a.write_qh && rb == 0);
+            } else {
+                live = false;  // nothing valid to multiply: skip the rest
+            }
+            group_sync();
+            const int n = dispatch(BoolC<false>{}, off, c, w);
+            // count the run's tasks (one per column block rb .. rb + n - 1):
+            // a release add per block after the barrier that orders the
+            // run's stores
+            group_sync();
+            for (int r = gtid; r < n; r += kGroupThreads) red_release_add(&a.cnt_y[rb + r], 1);
         }
     }
 
@@ -1043,10 +1044,12 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     // every down task stored.  With no more blocks than workers, no worker
     // holds more than one unit.
     {
-        const int V = 2 * G, v = 2 * b + grp, items = kTileRows * T;
-        int np = V / RBd;
-        np = np < items / 64 ? np : items / 64;
-        np = np > 1 ? np : 1;
+        // np: enough pieces that a thread loads at most eight parts (sp
+        // threads an item), while there are workers for them and a piece
+        // keeps 32 items
+        const int V = 2 * G, v = 2 * b + grp, items = kTileRows * T, P = k * nsd;
+        int np = 1;
+        while (np * 2 <= items / 32 && RBd * np * 2 <= V && (long long)items * P > 2048ll * np) np *= 2;
         const int nu = RBd * np;
         const int u0 = (v * nu + V - 1) / V, u1 = ((v + 1) * nu + V - 1) / V;
         for (int u = u0; u < u1; ++u) {
