@@ -183,6 +183,41 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / steps
+    # the same L layers in one launch (moe_w4a8_forward_decode_stack): its
+    # output must carry the chain's bits
+    out_stack = torch.empty((T, li.H), dtype=torch.bfloat16, device=device)
+
+    def run_stack():
+        moe.moe_w4a8_forward_decode_stack(x, layers, li.I, li.k, out=out_stack, out_fp32=False,
+                                          workspace=ws, prenorm=True)
+
+    run_stack()
+    run_chain()
+    torch.cuda.synchronize()
+    stack_same = bool(torch.equal(out_stack.view(torch.int16), outs[-1].view(torch.int16)))
+    gs = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs, capture_error_mode="relaxed"):
+        run_stack()
+    for _ in range(max(warmup, 3)):
+        gs.replay()
+    torch.cuda.synchronize()
+    barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(steps):
+        gs.replay()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ms_stack = s0.elapsed_time(s1) / steps
+    barrier()
+    s0.record(stream)
+    for _ in range(steps):
+        x.copy_(x_host, non_blocking=True)
+        gs.replay()
+        out_host.copy_(out_stack, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_stack_ms = s0.elapsed_time(s1) / steps
     expert_bytes = GU_BYTES_PER_EXPERT + D_BYTES_PER_EXPERT
     # algorithmic bytes of each layer: its touched experts' packed weights,
     # the router, x in and the output out (bf16)
@@ -197,8 +232,15 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
         "e2e_us_per_token": e2e_ms * 1e3 / (L * T),
         "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 2,
         "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
+        "stack": {
+            "entry": "moe_w4a8_forward_decode_stack (the L layers in one cooperative launch)",
+            "equals_chain_bits": stack_same, "ms_per_step": ms_stack,
+            "us_per_layer": ms_stack * 1e3 / L, "us_per_token": ms_stack * 1e3 / (L * T),
+            "layer_gbs": statistics.mean(layer_bytes) / (ms_stack * 1e3 / L * 1e-6) / 1e9,
+            "e2e_us_per_token": e2e_stack_ms * 1e3 / (L * T), "kernels_per_step": 2,
+        },
     }
-    del layers, outs, ws, g
+    del layers, outs, ws, g, gs
     torch.cuda.empty_cache()
     return res
 

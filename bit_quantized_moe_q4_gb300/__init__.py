@@ -20,7 +20,7 @@ __all__ = [
     "MoeError", "MoeDebug", "load_library", "build",
     "moe_version", "moe_q4_packed_bytes", "moe_q4_pack", "moe_q4_quantize", "moe_route_topk",
     "moe_workspace_bytes", "moe_q4_forward_prefill", "moe_w4a8_forward_decode",
-    "moe_get_device_status", "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
+    "moe_w4a8_forward_decode_stack", "moe_get_device_status", "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -45,8 +45,9 @@ EXPORTED_SYMBOLS = (
     "moe_version", "moe_last_error_string", "moe_get_device_status", "moe_clear_device_status",
     "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk", "moe_workspace_bytes",
     "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
-    "moe_q4_quantize",
+    "moe_q4_quantize", "moe_w4a8_forward_decode_stack",
 )
+MOE_DECODE_MAX_LAYERS = 64
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -99,6 +100,8 @@ def load_library(path: str | None = None):
         "moe_w4a8_forward_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                                  ctypes.c_uint, _vp, ctypes.POINTER(MoeDebug),
                                                  _vp]),
+        "moe_w4a8_forward_decode_stack": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                               ctypes.c_uint, _vp, _vp, _sz, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -268,6 +271,29 @@ def moe_w4a8_forward_decode(x, wr, wgu_packed, wd_packed, I: int, k: int, out=No
     """One decode MoE layer on the W4A8 integer path (T <= 32)."""
     return _forward("moe_w4a8_forward_decode", x, wr, wgu_packed, wd_packed, I, k, out, out_fp32,
                     workspace, debug, stream, prenorm)
+
+
+def moe_w4a8_forward_decode_stack(x, layers, I: int, k: int, out=None, out_fp32: bool = True,
+                                  workspace=None, stream=None, prenorm: bool = True):
+    """L stacked decode layers in one launch.  ``layers``: a sequence of
+    (wr, wgu_packed, wd_packed) per layer; layer l + 1 reads layer l's output
+    rounded to bf16.  Returns the last layer's output [T, H]."""
+    T, H = x.shape
+    L = len(layers)
+    E = layers[0][0].shape[0] if L else 0
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_bytes(MOE_MODE_DECODE, T, H, I, E, k), 1),
+                                dtype=torch.uint8, device=x.device)
+    arrs = [(ctypes.c_void_p * max(L, 1))(*[_ptr(layer[j]).value for layer in layers])
+            for j in range(3)]
+    flags = (MOE_OUT_FP32 if out_fp32 else 0) | (MOE_STACKED_PRENORM if prenorm else 0)
+    _check(load_library().moe_w4a8_forward_decode_stack(
+        _ptr(x), L, arrs[0], arrs[1], arrs[2], T, H, I, E, k, flags, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
 
 
 class StageEvents:

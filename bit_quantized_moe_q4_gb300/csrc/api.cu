@@ -187,6 +187,9 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
         w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));
         w.sync = reinterpret_cast<int32_t*>(take((size_t)decode_sync_ints(T, H, I, E, k) * 4));
+        w.xbuf0 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
+        w.xbuf1 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
+        w.gbar = reinterpret_cast<int32_t*>(take(4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;
@@ -459,6 +462,47 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void*
                             moe_debug* dbg, void* stream) {
     return forward(MOE_MODE_DECODE, x_bf16, wr, wgu_packed, wd_packed, T, H, I, E, k, flags, out,
                    workspace, ws_bytes, dbg, stream);
+}
+
+int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* const* wr,
+                                  const void* const* wgu_packed, const void* const* wd_packed,
+                                  int T, int H, int I, int E, int k, unsigned flags, void* out,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+    int rc = check_layer_shape(MOE_MODE_DECODE, T, H, I, E, k);
+    if (rc) return rc;
+    if (flags & ~(MOE_OUT_FP32 | MOE_STACKED_PRENORM))
+        return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (L < 1 || L > MOE_DECODE_MAX_LAYERS)
+        return set_err(MOE_ERR_SHAPE, "L=%d must satisfy 1 <= L <= %d", L, MOE_DECODE_MAX_LAYERS);
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !wr || !wgu_packed || !wd_packed || !out)
+        return set_err(MOE_ERR_INVALID_ARG, "null argument");
+    for (int l = 0; l < L; ++l) {
+        if (!wr[l] || !wgu_packed[l] || !wd_packed[l])
+            return set_err(MOE_ERR_INVALID_ARG, "null weight pointer of layer %d", l);
+        if (!aligned16(wr[l]) || !aligned16(wgu_packed[l]) || !aligned16(wd_packed[l]))
+            return set_err(MOE_ERR_ALIGN, "weights of layer %d must be 16-byte aligned", l);
+    }
+    if (!aligned16(x_bf16) || !aligned16(out) || !aligned16(workspace))
+        return set_err(MOE_ERR_ALIGN, "tensor arguments must be 16-byte aligned");
+    if (out == static_cast<const void*>(x_bf16))
+        return set_err(MOE_ERR_INVALID_ARG, "out may not alias x");
+    const size_t need = carve(MOE_MODE_DECODE, T, H, I, E, k, nullptr, nullptr);
+    if (!workspace || ws_bytes < need)
+        return set_err(MOE_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    if (!decode_stack_fits(T, H, I, E, dev->num_sms))
+        return set_err(MOE_ERR_SHAPE,
+                       "decode stack with T=%d H=%d I=%d E=%d does not fit the on-chip staging", T, H,
+                       I, E);
+    Workspace ws{};
+    carve(MOE_MODE_DECODE, T, H, I, E, k, static_cast<uint8_t*>(workspace), &ws);
+    return cuda_check(launch_decode_stack(x_bf16, L, wr, wgu_packed, wd_packed, T, H, I, E, k,
+                                          (flags & MOE_STACKED_PRENORM) != 0,
+                                          (flags & MOE_OUT_FP32) != 0, out, ws, dev->status,
+                                          dev->num_sms, static_cast<cudaStream_t>(stream)),
+                      "decode stack");
 }
 
 }  // extern "C"

@@ -237,30 +237,24 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
     }
 }
 
-__global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
-    extern __shared__ __align__(128) uint8_t psm[];  // this CTA's router row [H] fp32
-    __shared__ __align__(8) uint64_t s_bar;
-    __shared__ float s_red[kPrepThreads / 32];
+constexpr int kPrepBarId = 4;  // named barrier of the row's 128 threads
+
+// Router row e (staged in shared memory at w) of every token of x, by
+// threads 0..127: the optional RMSNorm, the logit, and the int8 codes of the
+// 32-column groups g of token t with (t * H/32 + g) % nrow == e (nrow: the
+// number of router rows).  s_red: 4 floats, s_r: MOE_DECODE_MAX_T floats of
+// shared memory.
+__device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, int e, int nrow,
+                                         const float* w, float* s_red, float* s_r) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-    const int e = blockIdx.x, H = a.H, T = a.T;
-    const uint32_t bar = smem_u32(&s_bar);
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(bar, (uint32_t)(H * 4));
-        bulk_g2s(smem_u32(psm), a.wr + (size_t)e * H, (uint32_t)(H * 4), bar);
-    }
-    __syncthreads();
-    pdl_wait();     // x and the workspace belong to this call from here on
-    pdl_trigger();  // the layer kernel may be scheduled; it waits for our end
-    for (int i = e * kPrepThreads + tid; i < a.nsync; i += gridDim.x * kPrepThreads) a.sync[i] = 0;
+    const int H = a.H, T = a.T;
     const int H8 = H / 8, G32 = H / kGroup;
     int tpt = kPrepThreads;
     while (tpt > 4 && kPrepThreads / tpt < T) tpt >>= 1;  // T <= 32
     const int t = tid / tpt, sub = tid % tpt;
     const bool act = t < T;
     const int nm = (H8 + tpt - 1) / tpt;  // unit slots of a thread (the last ones may be past the row)
-    const uint16_t* xr = a.x + (size_t)(act ? t : 0) * H;
+    const uint16_t* xr = x + (size_t)(act ? t : 0) * H;
     uint4 v[kPrepBatch];
     auto load = [&](int m0) {
 #pragma unroll
@@ -275,17 +269,15 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     auto token_sum = [&](float x) -> float {
         for (int o = 1; o < 32 && o < tpt; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         if (tpt > 32) {
-            __syncthreads();  // s_red is free
+            named_sync(kPrepBarId, kPrepThreads);  // s_red is free
             if (lane == 0) s_red[warp] = x;
-            __syncthreads();
+            named_sync(kPrepBarId, kPrepThreads);
             const int w0 = (t * tpt) / 32;
             x = 0.f;
             for (int q = 0; q < tpt / 32; ++q) x += s_red[w0 + q];
         }
         return x;
     };
-    if (!mbar_wait(bar, 0)) record_status(a.status, kStatusTimeout);
-    const float* w = reinterpret_cast<const float*>(psm);
     float r = 1.0f;
     const bool one_batch = nm <= kPrepBatch;
     if (a.prenorm) {
@@ -310,15 +302,11 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
         for (int z = 0; z < kPrepBatch; ++z) ss += ssu[z];
         ss = token_sum(ss);
         r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + 1e-6f));
+        if (act && sub == 0) s_r[t] = r;  // for the coding pass
     }
     float accu[kPrepBatch];  // the logit's partial sums, one per unit slot
 #pragma unroll
     for (int z = 0; z < kPrepBatch; ++z) accu[z] = 0.f;
-    // duty: CTA (t * H/32 + g) % grid codes group g of token t; this quad's
-    // group advances by tpt/4 a unit slot
-    const unsigned grid = gridDim.x, gstep = (unsigned)(tpt / 4) % grid;
-    unsigned gd = (unsigned)(t * G32 + sub / 4) % grid;
-    const unsigned qmask = 0xFu << (lane & ~3);  // this thread's quad
     for (int m0 = 0; m0 < nm; m0 += kPrepBatch) {
         if (!(a.prenorm && one_batch)) load(m0);  // one batch: still held from the norm
 #pragma unroll
@@ -346,35 +334,7 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
                     acc = fmaf(xf[7], w1.w, acc);
                     accu[z] = acc;
                 }
-                if (valid && gd == (unsigned)e) {  // the whole quad: one group, one decision
-                    float amax = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
-                    amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
-                    amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
-                    const uint16_t db = act_scale_bits(amax);
-                    const float d = half_bits_to_float(db);
-                    uint32_t lo = 0u, hi = 0u;
-                    int gsum = 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int qc = act_code(xf[q], d);
-                        gsum += qc;
-                        if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
-                        else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
-                    }
-                    gsum += __shfl_xor_sync(qmask, gsum, 1);
-                    gsum += __shfl_xor_sync(qmask, gsum, 2);
-                    *reinterpret_cast<uint2*>(a.xq + (size_t)t * H + u * 8) = permute_chunk(lo, hi);
-                    *reinterpret_cast<uint2*>(a.q_x + (size_t)t * H + u * 8) = make_uint2(lo, hi);
-                    if ((lane & 3) == 0) {
-                        a.xs[t * G32 + u / 4] = make_int2(__float_as_int(d), -8 * gsum);
-                        a.d_x[t * G32 + u / 4] = db;
-                    }
-                }
             }
-            gd += gstep;
-            if (gd >= grid) gd -= grid;
         }
     }
     float acc = 0.f;
@@ -382,6 +342,73 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     for (int z = 0; z < kPrepBatch; ++z) acc += accu[z];
     acc = token_sum(acc);
     if (act && sub == 0) a.logits[(size_t)t * a.E + e] = acc;
+    // int8 codes per 32 columns: this row's groups (t, g), (t * H/32 + g) %
+    // nrow == e, one quad of threads each (quad j takes the j-th, j + 32-th,
+    // ...), from x (and the token's norm factor) again
+    if (a.prenorm) named_sync(kPrepBarId, kPrepThreads);  // s_r is stored
+    const int quad = tid / 4, ql = tid % 4;
+    const unsigned qmask = 0xFu << (lane & ~3);
+    int idx = 0;
+    for (int t2 = 0; t2 < T; ++t2) {
+        int g = (e - t2 * G32) % nrow;  // (|t2 * G32| < 2^31)
+        if (g < 0) g += nrow;
+        for (; g < G32; g += nrow, ++idx) {
+            if (idx % (kPrepThreads / 4) != quad) continue;
+            const int u = g * 4 + ql;  // this lane's 8 columns
+            float xf[8];
+            unpack8(__ldcg(reinterpret_cast<const uint4*>(x + (size_t)t2 * H) + u), xf);
+            if (a.prenorm) {
+                const float r2 = s_r[t2];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) xf[q] = bf16_bits_to_float(float_to_bf16_bits(xf[q] * r2));
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
+            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
+            const uint16_t db = act_scale_bits(amax);
+            const float d = half_bits_to_float(db);
+            uint32_t lo = 0u, hi = 0u;
+            int gsum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int qc = act_code(xf[q], d);
+                gsum += qc;
+                if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
+                else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
+            }
+            gsum += __shfl_xor_sync(qmask, gsum, 1);
+            gsum += __shfl_xor_sync(qmask, gsum, 2);
+            *reinterpret_cast<uint2*>(a.xq + (size_t)t2 * H + u * 8) = permute_chunk(lo, hi);
+            *reinterpret_cast<uint2*>(a.q_x + (size_t)t2 * H + u * 8) = make_uint2(lo, hi);
+            if (ql == 0) {
+                a.xs[t2 * G32 + g] = make_int2(__float_as_int(d), -8 * gsum);
+                a.d_x[t2 * G32 + g] = db;
+            }
+        }
+    }
+}
+
+__global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
+    extern __shared__ __align__(128) uint8_t psm[];  // this CTA's router row [H] fp32
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ float s_red[kPrepThreads / 32];
+    __shared__ float s_r[MOE_DECODE_MAX_T];
+    const int tid = threadIdx.x, e = blockIdx.x, H = a.H;
+    const uint32_t bar = smem_u32(&s_bar);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, (uint32_t)(H * 4));
+        bulk_g2s(smem_u32(psm), a.wr + (size_t)e * H, (uint32_t)(H * 4), bar);
+    }
+    __syncthreads();
+    pdl_wait();     // x and the workspace belong to this call from here on
+    pdl_trigger();  // the layer kernel may be scheduled; it waits for our end
+    for (int i = e * kPrepThreads + tid; i < a.nsync; i += gridDim.x * kPrepThreads) a.sync[i] = 0;
+    if (!mbar_wait(bar, 0)) record_status(a.status, kStatusTimeout);
+    prep_row(a, a.x, e, gridDim.x, reinterpret_cast<const float*>(psm), s_red, s_r);
 }
 
 // ----------------------------------------------------------------- layer
@@ -414,27 +441,96 @@ __device__ __forceinline__ int split_bound_warp(int v, int V, int nt, int Tk, in
     return lo * per + (int)(j < (u64)per ? j : (u64)per);
 }
 
-// MAXNT: the most tokens an expert's bucket may hold (T <= MAXNT).  At most
-// 96 registers a thread, which leaves room on the SM for the next call's
-// prep CTA; the MAXNT = 32 variant spills a little instead (it only runs
-// when more than 16 tokens are decoded at once).
+// The layer's shared state outside the dynamic plan.
+struct LayerShared {
+    int idx[kMaxTk];
+    float w[kMaxTk];
+    int btok[kMaxTk];    // bucket row -> token
+    float bsw[kMaxTk];   // bucket row -> routing weight
+    int slotpos[kMaxTk]; // (t, j) -> bucket row
+    uint32_t mask[kMaxExperts];
+    int off[kMaxExperts + 1];
+    int touched[kMaxExperts];
+    int toff[kMaxExperts + 1];  // touched slot -> its first bucket row (+ total)
+    int slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
+    int nt, nsg, nsd;
+    int bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
+    volatile int abort;
+    volatile int flag[kGroups];
+};
+
+// A thread's position in its group's ring (the chunk sequence continues
+// from layer to layer within a launch).
+struct Pipe {
+    int slot, phase, cidx;
+};
+
+// What changes from layer to layer: the input (also the residual), the
+// expert weights and the output.
+struct LayerIO {
+    const uint16_t* x_res;
+    const uint8_t* wgu;
+    const uint8_t* wd;
+    void* out;
+    int out_fp32;
+};
+
+__device__ __forceinline__ uint32_t ring_bar(const LayerArgs& a, uint32_t sbase, bool full, int g, int s) {
+    return sbase + a.off_bar + 8u * ((full ? 0 : 2 * a.ns) + g * a.ns + s);
+}
+
+// Once per launch: the ring barriers, no chunk issued yet, no failure.
+__device__ __forceinline__ void ring_init(const LayerArgs& a, LayerShared& S, uint8_t* dsm) {
+    const uint32_t sbase = smem_u32(dsm);
+    if (threadIdx.x == 0) {
+        for (int g = 0; g < kGroups; ++g) {
+            for (int s = 0; s < a.ns; ++s) {
+                mbar_init(ring_bar(a, sbase, true, g, s), 1);
+                mbar_init(ring_bar(a, sbase, false, g, s), kGroupWarps);
+            }
+        }
+        S.abort = 0;
+        fence_mbar_init();
+    }
+    for (int s = threadIdx.x; s < kMaxSlots; s += kLayerThreads) S.slot_chunk[s] = -1;
+}
+
+// Before the CTA exits, every copy it issued has landed: the producer warps
+// wait for the latest chunk of each slot (earlier ones completed before it).
+__device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, uint8_t* dsm) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp < kWarpProducer0) return;
+    const int g = warp - kWarpProducer0;
+    const uint32_t sbase = smem_u32(dsm);
+    __syncwarp();
+    for (int s = lane; s < a.ns; s += 32) {
+        const int c = S.slot_chunk[g * a.ns + s];
+        if (c >= 0) mbar_wait(ring_bar(a, sbase, true, g, s), (c / a.ns) & 1);
+    }
+}
+
+// One decode layer (everything after the prep kernel's work) by one CTA of
+// the cooperative grid.  MAXNT: the most tokens an expert's bucket may hold
+// (T <= MAXNT).
 template <int MAXNT>
-__global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ int s_idx[kMaxTk];
-    __shared__ float s_w[kMaxTk];
-    __shared__ int s_btok[kMaxTk];    // bucket row -> token
-    __shared__ float s_bsw[kMaxTk];   // bucket row -> routing weight
-    __shared__ int s_slotpos[kMaxTk]; // (t, j) -> bucket row
-    __shared__ uint32_t s_mask[kMaxExperts];
-    __shared__ int s_off[kMaxExperts + 1];
-    __shared__ int s_touched[kMaxExperts];
-    __shared__ int s_toff[kMaxExperts + 1];  // touched slot -> its first bucket row (+ total)
-    __shared__ int s_slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
-    __shared__ int s_nt, s_nsg, s_nsd;
-    __shared__ int s_bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
-    __shared__ volatile int s_abort;
-    __shared__ volatile int s_flag[kGroups];
+__device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
+                                           uint8_t* dsm, Pipe& pp) {
+    int* s_idx = S.idx;
+    float* s_w = S.w;
+    int* s_btok = S.btok;
+    float* s_bsw = S.bsw;
+    int* s_slotpos = S.slotpos;
+    uint32_t* s_mask = S.mask;
+    int* s_off = S.off;
+    int* s_touched = S.touched;
+    int* s_toff = S.toff;
+    int* s_slot_chunk = S.slot_chunk;
+    int& s_nt = S.nt;
+    int& s_nsg = S.nsg;
+    int& s_nsd = S.nsd;
+    auto& s_bnd = S.bnd;
+    volatile int& s_abort = S.abort;
+    volatile int* s_flag = S.flag;
 
     const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k;
     const int KBg = H / kTileK, KBd = I / kTileK;
@@ -444,30 +540,15 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
     const uint32_t sbase = smem_u32(dsm);
-    const uint32_t bar0 = sbase + a.off_bar;
     // group g's ring: slots g*ns .. g*ns + ns - 1
-    auto full_bar = [&](int g, int s) { return bar0 + 8u * (g * ns + s); };
-    auto empty_bar = [&](int g, int s) { return bar0 + 8u * (2 * ns + g * ns + s); };
+    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
+    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
     const int st = a.st;
     auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
     auto fail = [&]() {
         record_status(a.status, kStatusTimeout);
         s_abort = 1;
     };
-    if (tid == 0) {
-        for (int g = 0; g < kGroups; ++g) {
-            for (int s = 0; s < ns; ++s) {
-                mbar_init(full_bar(g, s), 1);
-                mbar_init(empty_bar(g, s), kGroupWarps);
-            }
-        }
-        s_abort = 0;
-        fence_mbar_init();
-    }
-    for (int s = tid; s < kMaxSlots; s += kLayerThreads) s_slot_chunk[s] = -1;
-    __syncthreads();
-    pdl_wait();     // the prep kernel's logits, codes and cleared counters
-    pdl_trigger();  // the next call's prep may be scheduled; it waits for our end
     if (warp < kConsumerWarps) {
         // the int8 codes of x and their scales (written by the prep kernel)
         // start on their way to shared memory while the CTA routes
@@ -679,8 +760,8 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     };
     auto walk_live = [&](const Walk& w) { return w.gu ? w.left_g > 0 : w.left_d > 0; };
     auto walk_base = [&](const Walk& w) -> const uint8_t* {
-        return w.gu ? a.wgu + (((size_t)s_touched[w.i] * RBg + w.rb) * KBg + (size_t)w.kc * KCg) * kTileBytes
-                    : a.wd + (((size_t)s_touched[w.i] * RBd + w.rb) * KBd + (size_t)w.kc * KCd) * kTileBytes;
+        return w.gu ? io.wgu + (((size_t)s_touched[w.i] * RBg + w.rb) * KBg + (size_t)w.kc * KCg) * kTileBytes
+                    : io.wd + (((size_t)s_touched[w.i] * RBd + w.rb) * KBd + (size_t)w.kc * KCd) * kTileBytes;
     };
 
     // Chunks: each task's tiles are cut into runs of up to st tiles (one bulk
@@ -693,8 +774,10 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         // c - ns, issued before it, so a parity wait never aliases.
         const int g = warp - kWarpProducer0;
         if (lane == 0) {
-            int slot = -1, phase = 0, cidx = -1;
-            bool ok = true;
+            int& slot = pp.slot;
+            int& phase = pp.phase;
+            int& cidx = pp.cidx;
+            bool ok = !s_abort;
             for (Walk w = walk_start(g); walk_live(w) && ok; w = walk_next(w, g)) {
                 const uint8_t* base = walk_base(w);
                 const int KC = w.gu ? KCg : KCd;
@@ -717,13 +800,6 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
                 }
             }
         }
-        // every copy issued lands before the CTA can go away: wait for the
-        // latest chunk of each slot (earlier ones completed before it)
-        __syncwarp();
-        for (int s = lane; s < ns; s += 32) {
-            const int c = s_slot_chunk[g * ns + s];
-            if (c >= 0) mbar_wait(full_bar(g, s), (c / ns) & 1);
-        }
         return;
     }
 
@@ -741,8 +817,9 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     // Control flow must stay uniform within a group (it shares named
     // barriers): a failed wait only skips work; decisions the group shares
     // are taken by its thread 0 and read after a group barrier.
-    bool live = true;  // this warp has not given up
-    int slot = -1, phase = 0;  // the current chunk's slot (same walk as the producer)
+    bool live = !s_abort;  // this warp has not given up
+    int& slot = pp.slot;   // the current chunk's slot (same walk as the producer)
+    int& phase = pp.phase;
     const int r_lane = lane >> 1, h_lane = lane & 1;
     const int lrow = w8 * 16 + r_lane;  // this lane's row in the 128-row block
 
@@ -944,13 +1021,13 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
         float* cred = reinterpret_cast<float*>(red_buf);  // [n_it][sp] range sums (sp > 1)
         auto store_out = [&](int it, float v) {
             const size_t o = (size_t)(it / kTileRows) * H + c0 + it % kTileRows;
-            if (a.out_fp32) static_cast<float*>(a.out)[o] = v;
-            else static_cast<uint16_t*>(a.out)[o] = float_to_bf16_bits(v);
+            if (io.out_fp32) static_cast<float*>(io.out)[o] = v;
+            else static_cast<uint16_t*>(io.out)[o] = float_to_bf16_bits(v);
         };
 #pragma unroll 1
         for (int it = it0 + gtid / sp; it < it1; it += kGroupThreads / sp) {
             const int t = it / kTileRows, col = c0 + it % kTileRows;
-            float v = sub == 0 ? bf16_bits_to_float(a.x_res[(size_t)t * H + col]) : 0.f;
+            float v = sub == 0 ? bf16_bits_to_float(io.x_res[(size_t)t * H + col]) : 0.f;
             const float* yc = a.y_part + col;
             const int* sp_t = s_slotpos + t * k;
             int j = ja, kp = kpa;
@@ -1076,6 +1153,123 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     }
 }
 
+// One decode layer: one CTA per SM, launched cooperatively (all CTAs
+// resident: they wait on one another's results).  At most 96 registers a
+// thread, which leaves room on the SM for the next call's prep CTA; the
+// MAXNT = 32 variant spills a little instead (it only runs when more than
+// 16 tokens are decoded at once).
+template <int MAXNT>
+__global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ LayerShared S;
+    ring_init(a, S, dsm);
+    __syncthreads();
+    pdl_wait();     // the prep kernel's logits, codes and cleared counters
+    pdl_trigger();  // the next call's prep may be scheduled; it waits for our end
+    Pipe pp{-1, 0, -1};
+    const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
+    layer_body<MAXNT>(a, io, S, dsm, pp);
+    ring_drain(a, S, dsm);
+}
+
+// A stack of L decode layers in one cooperative launch: layer l + 1 reads
+// layer l's output.  Per layer: the prep work (CTA b holds router rows b,
+// b + grid, ..., staged in shared memory during the layer before, and runs
+// the prep kernel's arithmetic on its first 128 threads; every CTA clears a
+// share of the layer's counters), a grid barrier, the layer itself, a grid
+// barrier.  The code stays resident in the SMs' instruction caches from
+// layer to layer and no kernel boundary separates them.
+struct StackArgs {
+    LayerArgs la;  // shape, workspace and shared-memory plan (not x, weights, output)
+    PrepArgs pa;   // shape and the prep outputs (not x, router rows)
+    const float* wr[MOE_DECODE_MAX_LAYERS];
+    const uint8_t* wgu[MOE_DECODE_MAX_LAYERS];
+    const uint8_t* wd[MOE_DECODE_MAX_LAYERS];
+    int L;
+    const uint16_t* x0;     // the stack's input [T, H] bf16
+    uint16_t* xbuf[2];      // layer outputs inside the stack [T, H] bf16 (ping-pong)
+    void* out;              // the last layer's output
+    int out_fp32;
+    int* gbar;              // grid barrier arrivals, zero at launch
+    int off_wr;             // staged router rows [rows][H] fp32 in dynamic shared memory
+};
+
+// 96 registers a thread: the SM's four register files (16,384 each) hold
+// five of the 18 warps at most at that size.
+template <int MAXNT>
+__global__ void __maxnreg__(96) decode_stack_kernel(const __grid_constant__ StackArgs A) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ LayerShared S;
+    __shared__ __align__(8) uint64_t s_wrbar;
+    __shared__ float s_red[kPrepThreads / 32];
+    __shared__ float s_r[MOE_DECODE_MAX_T];
+    const LayerArgs& a = A.la;
+    const int tid = threadIdx.x, b = blockIdx.x, G = gridDim.x, H = a.H, E = a.E;
+    const uint32_t wrbar = smem_u32(&s_wrbar);
+    float* wrow = reinterpret_cast<float*>(dsm + A.off_wr);
+    const int nrows = b < E ? (E - 1 - b) / G + 1 : 0;  // router rows b, b + G, ...
+    // (thread 0) this CTA's router rows of layer l into shared memory
+    auto stage_rows = [&](int l) {
+        fence_proxy_async_smem();  // after the generic reads of the layer before
+        mbar_arrive_expect_tx(wrbar, (uint32_t)(nrows * H * 4));
+        for (int j = 0; j < nrows; ++j)
+            bulk_g2s(smem_u32(wrow + (size_t)j * H), A.wr[l] + (size_t)(b + j * G) * H, (uint32_t)(H * 4),
+                     wrbar);
+    };
+    ring_init(a, S, dsm);
+    if (tid == 0) {
+        mbar_init(wrbar, 1);
+        fence_mbar_init();
+        if (nrows) stage_rows(0);
+    }
+    __syncthreads();
+    pdl_wait();  // the cleared barrier counter
+    pdl_trigger();
+    // grid barrier n (counting from 1): every CTA has arrived n times
+    int nbar = 0;
+    auto grid_sync = [&]() {
+        __syncthreads();
+        ++nbar;
+        if (tid == 0) {
+            red_release_add(A.gbar, 1);
+            const int target = nbar * G;
+            bool ok = !S.abort;
+            if (ok && ld_acquire(A.gbar) < target) {
+                const unsigned long long t0 = globaltimer_ns();
+                while (ld_acquire(A.gbar) < target) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) {
+                record_status(a.status, kStatusTimeout);
+                S.abort = 1;
+            }
+        }
+        __syncthreads();
+    };
+    Pipe pp{-1, 0, -1};
+    for (int l = 0; l < A.L; ++l) {
+        const uint16_t* xin = l == 0 ? A.x0 : A.xbuf[(l - 1) & 1];
+        const bool last = l == A.L - 1;
+        const LayerIO io{xin, A.wgu[l], A.wd[l], last ? A.out : (void*)A.xbuf[l & 1], last ? A.out_fp32 : 0};
+        // prep: the counters of this layer (nobody reads the last layer's
+        // any more), then this CTA's router rows
+        for (int i = b * kLayerThreads + tid; i < A.pa.nsync; i += G * kLayerThreads) A.pa.sync[i] = 0;
+        if (tid < kPrepThreads && nrows) {
+            if (!mbar_wait(wrbar, l & 1)) record_status(a.status, kStatusTimeout);
+            for (int j = 0; j < nrows; ++j) prep_row(A.pa, xin, b + j * G, E, wrow + (size_t)j * H, s_red, s_r);
+        }
+        grid_sync();
+        if (tid == 0 && nrows && l + 1 < A.L) stage_rows(l + 1);  // its rows are read
+        layer_body<MAXNT>(a, io, S, dsm, pp);
+        grid_sync();
+    }
+    ring_drain(a, S, dsm);
+}
+
 // ---------------------------------------------------------------- launch
 int g_layer_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
 int g_prep_carveout[64] = {};
@@ -1090,10 +1284,10 @@ int al128(long long v) { return (int)((v + 127) & ~127ll); }
 // Layout: the two rings, the two groups' h buffers and K-part sum buffers
 // (all idle while the CTA routes, when they hold the logits), then the
 // codes of x (filled by cp.async during routing) and the ring barriers.
-bool plan_layer(int T, int H, int I, int E, Plan* p) {
+bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
     const long long ax = al128((long long)T * H + (long long)T * (H / kGroup) * 8);
     const long long ah = al128((long long)T * I + (long long)T * (I / kGroup) * 8);
-    const long long rest = kLayerSmemBudget - ax - 2 * ah - 2 * kRedBytes - 2 * kMaxSlots * 8 - 256;
+    const long long rest = budget - ax - 2 * ah - 2 * kRedBytes - 2 * kMaxSlots * 8 - 256;
     // the largest slot (up to kSlotTiles tiles) that still gives each group's
     // ring two slots, else one
     int st = kSlotTiles;
@@ -1157,7 +1351,7 @@ int cooperative_pdl_mode(int dev) { return g_layer_pdl[dev & 63]; }
 
 bool decode_shape_fits(int T, int H, int I, int E) {
     Plan p;
-    return plan_layer(T, H, I, E, &p);
+    return plan_layer(T, H, I, E, kLayerSmemBudget, &p);
 }
 
 void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap_d, int* nsg_max,
@@ -1181,25 +1375,11 @@ int decode_sync_ints(int T, int H, int I, int E, int k) {
     return nslot * (I / kTileRows) + H / kTileRows;
 }
 
-cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
-                          int T, int H, int I, int E, int k, bool prenorm, bool out_fp32,
-                          void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
-                          bool write_qh, int* status, int num_sms, void** ev, bool capturing,
-                          cudaStream_t s) {
-    if (T == 0) return cudaSuccess;
-    Plan plan;
-    if (!plan_layer(T, H, I, E, &plan)) return cudaErrorInvalidValue;
-    cudaError_t err;
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    auto mark = [&](int i) -> cudaError_t {
-        return (ev && ev[i]) ? record_stage(ev[i], s, capturing) : cudaSuccess;
-    };
-    const int nslot = std::min(E, T * k);
-    // ---- prep ----
+namespace {
+
+PrepArgs make_prep_args(int T, int H, int I, int E, int k, bool prenorm, const Workspace& ws,
+                        int* status) {
     PrepArgs p{};
-    p.x = x;
-    p.wr = wr;
     p.T = T;
     p.H = H;
     p.E = E;
@@ -1212,29 +1392,12 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     p.sync = ws.sync;
     p.nsync = decode_sync_ints(T, H, I, E, k);
     p.status = status;
-    const int psmem = H * 4;
-    if (psmem > 48 * 1024 &&
-        (err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    psmem)) != cudaSuccess)
-        return err;
-    // the SM's largest shared-memory split for the prep kernel too, so that a
-    // layer CTA of the same call can be placed beside a running prep CTA
-    if (!g_prep_carveout[dev & 63]) {
-        if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                        (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-            return err;
-        g_prep_carveout[dev & 63] = 1;
-    }
-    if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess) {
-        cudaGetLastError();
-        return err;
-    }
-    if ((err = mark(1)) != cudaSuccess) return err;
-    // ---- layer ----
+    return p;
+}
+
+LayerArgs make_layer_args(int T, int H, int I, int E, int k, const Workspace& ws, const Plan& plan,
+                          int* status) {
     LayerArgs a{};
-    a.x_res = x;
-    a.wgu = static_cast<const uint8_t*>(wgu);
-    a.wd = static_cast<const uint8_t*>(wd);
     a.T = T;
     a.H = H;
     a.I = I;
@@ -1254,6 +1417,7 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.q_h = ws.q_h;
     a.d_h = ws.d_h;
     a.y_part = ws.y_part;
+    const int nslot = std::min(E, T * k);
     a.cnt_h = ws.sync;
     a.cnt_y = ws.sync + nslot * (I / kTileRows);
     a.cap_g = ws.cap_g;
@@ -1268,11 +1432,6 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     };
     divisors(H / kTileK, ws.cap_g, a.div_g, &a.ndiv_g);
     divisors(I / kTileK, ws.cap_d, a.div_d, &a.ndiv_d);
-    a.out = out;
-    a.out_fp32 = out_fp32 ? 1 : 0;
-    a.dots_gu = dots_gu;
-    a.dots_d = dots_d;
-    a.write_qh = write_qh ? 1 : 0;
     a.status = status;
     a.ns = plan.ns;
     a.st = plan.st;
@@ -1281,14 +1440,21 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.off_ah = plan.off_ah;
     a.ah_bytes = plan.ah_bytes;
     a.off_red = plan.off_red;
-    void (*kern)(LayerArgs) = T <= 16 ? decode_layer_kernel<16> : decode_layer_kernel<MOE_DECODE_MAX_T>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
+    return a;
+}
+
+// A cooperative launch of one CTA per SM, with programmatic dependent launch
+// where the device accepts both.
+template <typename Args>
+cudaError_t launch_coop(void (*kern)(Args), const Args& args, int num_sms, int smem, int dev,
+                        cudaStream_t s) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute at[2];
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(kLayerThreads);
-    cfg.dynamicSmemBytes = plan.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     at[0].id = cudaLaunchAttributeCooperative;
     at[0].val.cooperative = 1;
@@ -1296,12 +1462,121 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = (g_layer_pdl[dev & 63] == 2) ? 1 : 2;
-    if ((err = cudaLaunchKernelEx(&cfg, kern, a)) != cudaSuccess) {
+    if ((err = cudaLaunchKernelEx(&cfg, kern, args)) != cudaSuccess) {
         cudaGetLastError();  // a refused launch: clear it, the context is intact
         return err;
     }
+    return cudaSuccess;
+}
+
+__global__ void decode_stack_clear_kernel(int* gbar) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) *gbar = 0;
+}
+
+// Dynamic shared memory the stack kernel may use (its static part, ~14.7 KB,
+// and this stay within the 227 KB a CTA may have).
+constexpr long long kStackSmemMax = 212 * 1024;
+
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, const void* wd,
+                          int T, int H, int I, int E, int k, bool prenorm, bool out_fp32,
+                          void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
+                          bool write_qh, int* status, int num_sms, void** ev, bool capturing,
+                          cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    Plan plan;
+    if (!plan_layer(T, H, I, E, kLayerSmemBudget, &plan)) return cudaErrorInvalidValue;
+    cudaError_t err;
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    auto mark = [&](int i) -> cudaError_t {
+        return (ev && ev[i]) ? record_stage(ev[i], s, capturing) : cudaSuccess;
+    };
+    // ---- prep ----
+    PrepArgs p = make_prep_args(T, H, I, E, k, prenorm, ws, status);
+    p.x = x;
+    p.wr = wr;
+    const int psmem = H * 4;
+    if (psmem > 48 * 1024 &&
+        (err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    psmem)) != cudaSuccess)
+        return err;
+    // the SM's largest shared-memory split for the prep kernel too, so that a
+    // layer CTA of the same call can be placed beside a running prep CTA
+    if (!g_prep_carveout[dev & 63]) {
+        if ((err = cudaFuncSetAttribute(decode_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return err;
+        g_prep_carveout[dev & 63] = 1;
+    }
+    if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess) {
+        cudaGetLastError();
+        return err;
+    }
+    if ((err = mark(1)) != cudaSuccess) return err;
+    // ---- layer ----
+    LayerArgs a = make_layer_args(T, H, I, E, k, ws, plan, status);
+    a.x_res = x;
+    a.wgu = static_cast<const uint8_t*>(wgu);
+    a.wd = static_cast<const uint8_t*>(wd);
+    a.out = out;
+    a.out_fp32 = out_fp32 ? 1 : 0;
+    a.dots_gu = dots_gu;
+    a.dots_d = dots_d;
+    a.write_qh = write_qh ? 1 : 0;
+    void (*kern)(LayerArgs) = T <= 16 ? decode_layer_kernel<16> : decode_layer_kernel<MOE_DECODE_MAX_T>;
+    if ((err = launch_coop(kern, a, num_sms, plan.smem, dev, s)) != cudaSuccess) return err;
     for (int i = 2; i <= 6; ++i)
         if ((err = mark(i)) != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+bool decode_stack_fits(int T, int H, int I, int E, int num_sms) {
+    if (num_sms <= 0) return false;
+    Plan plan;
+    const long long rows = (E + num_sms - 1) / num_sms;
+    return plan_layer(T, H, I, E, kStackSmemMax - al128(rows * H * 4) - 128, &plan);
+}
+
+cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr,
+                                const void* const* wgu, const void* const* wd, int T, int H, int I,
+                                int E, int k, bool prenorm, bool out_fp32, void* out,
+                                const Workspace& ws, int* status, int num_sms, cudaStream_t s) {
+    if (T == 0 || L == 0) return cudaSuccess;
+    if (L > MOE_DECODE_MAX_LAYERS) return cudaErrorInvalidValue;
+    const long long rows = (E + num_sms - 1) / num_sms;
+    const long long wr_bytes = al128(rows * H * 4);
+    Plan plan;
+    if (!plan_layer(T, H, I, E, kStackSmemMax - wr_bytes - 128, &plan)) return cudaErrorInvalidValue;
+    cudaError_t err;
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    StackArgs A{};
+    A.la = make_layer_args(T, H, I, E, k, ws, plan, status);
+    A.pa = make_prep_args(T, H, I, E, k, prenorm, ws, status);
+    for (int l = 0; l < L; ++l) {
+        A.wr[l] = wr[l];
+        A.wgu[l] = static_cast<const uint8_t*>(wgu[l]);
+        A.wd[l] = static_cast<const uint8_t*>(wd[l]);
+    }
+    A.L = L;
+    A.x0 = x;
+    A.xbuf[0] = ws.xbuf0;
+    A.xbuf[1] = ws.xbuf1;
+    A.out = out;
+    A.out_fp32 = out_fp32 ? 1 : 0;
+    A.gbar = ws.gbar;
+    A.off_wr = al128(plan.smem);
+    const int smem = A.off_wr + (int)wr_bytes;
+    if ((err = launch_pdl(decode_stack_clear_kernel, dim3(1), dim3(32), 0, s, ws.gbar)) != cudaSuccess) {
+        cudaGetLastError();
+        return err;
+    }
+    void (*kern)(StackArgs) = T <= 16 ? decode_stack_kernel<16> : decode_stack_kernel<MOE_DECODE_MAX_T>;
+    if ((err = launch_coop(kern, A, num_sms, smem, dev, s)) != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -48,6 +48,9 @@ struct Workspace {
     uint16_t* d_h;          // [T*k, I/32]
     float* y_part;          // [nsd, T*k, H] K parts of the weighted expert outputs
     int32_t* sync;          // counters of the layer kernel, cleared by its prep kernel
+    uint16_t* xbuf0;        // [T, H] decode stack: layer outputs inside the stack (ping-pong)
+    uint16_t* xbuf1;
+    int32_t* gbar;          // decode stack: grid barrier arrivals
     int cap_g, cap_d;       // bounds of the K splits (part buffers hold that many)
     int max_tiles;
     int tile_n;             // tokens per GEMM tile (prefill)
@@ -124,6 +127,15 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
                           void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
                           bool write_qh, int* status, int num_sms, void** events, bool capturing,
                           cudaStream_t s);
+// L stacked decode layers in one cooperative launch (after a kernel that
+// zeroes the grid barrier counter): layer l + 1 reads layer l's bf16 output,
+// the last writes `out`.  wr/wgu/wd: host arrays of L device pointers.
+cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr,
+                                const void* const* wgu, const void* const* wd, int T, int H, int I,
+                                int E, int k, bool prenorm, bool out_fp32, void* out,
+                                const Workspace& ws, int* status, int num_sms, cudaStream_t s);
+// Whether the decode stack kernel's on-chip staging fits this shape.
+bool decode_stack_fits(int T, int H, int I, int E, int num_sms);
 // Once per device, outside any stream capture: decides whether a cooperative
 // launch may also carry the programmatic-dependent-launch attribute.
 cudaError_t decode_prepare_device(int dev);

@@ -64,6 +64,7 @@ extern "C" {
 #define MOE_MAX_EXPERTS   256
 #define MOE_MAX_TOPK      16
 #define MOE_DECODE_MAX_T  32     /* decode path: tokens per call            */
+#define MOE_DECODE_MAX_LAYERS 64 /* decode stack: layers per call           */
 
 /* ---- moe_q4_pack formats ------------------------------------------------- */
 /* MOE_Q4_CODES:   src = uint8 codes [E, N, K] (values 0..15, one per byte),
@@ -259,6 +260,32 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
                             int T, int H, int I, int E, int k, unsigned flags,
                             void* out, void* workspace, size_t ws_bytes,
                             moe_debug* dbg, void* stream);
+
+/*
+ * moe_w4a8_forward_decode_stack — L consecutive decode layers (each adds its
+ * expert output to its input, the residual stream) in one cooperative
+ * launch: the pages' per-token decode loop over the MoE layers.  Layer l + 1
+ * reads layer l's output rounded to bf16; the result equals, bit for bit, L
+ * moe_w4a8_forward_decode calls chained through bf16 outputs with the same
+ * flags (MOE_OUT_FP32 applies to the last layer only).
+ *   x_bf16     [T, H] input of layer 0 (not written)
+ *   L          1 <= L <= MOE_DECODE_MAX_LAYERS
+ *   wr, wgu_packed, wd_packed
+ *              HOST arrays of L device pointers, one layer each, layouts as in
+ *              moe_w4a8_forward_decode (the arrays are read during the call)
+ *   out        the last layer's output; may not alias x
+ *   workspace  >= moe_workspace_bytes(MOE_MODE_DECODE, T, H, I, E, k) bytes
+ * Each layer clears its own counters inside the launch and a small kernel
+ * before it zeroes the grid barrier, so nothing in the workspace has to
+ * survive between calls.  Shapes must fit the decode staging (as for
+ * moe_w4a8_forward_decode, with the CTA's router rows, E / SMs rounded up,
+ * also staged: MOE_ERR_SHAPE otherwise).  Routing, codes and sums follow
+ * the single-layer call exactly; no stage outputs are written.
+ */
+int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* const* wr,
+                                  const void* const* wgu_packed, const void* const* wd_packed,
+                                  int T, int H, int I, int E, int k, unsigned flags, void* out,
+                                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * moe_w4a8_forward_decode_noalloc — the same decode layer as

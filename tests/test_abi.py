@@ -88,6 +88,32 @@ def test_forward_argument_checks(lib, fn):
         assert _prefill(lib, fn=fn, T=33) == moe.MOE_ERR_SHAPE       # decode takes <= 32 tokens
 
 
+def _stack(lib, L=2, T=1, H=256, I=128, E=8, k=2, flags=1, x=FAKE, layer=(FAKE, FAKE, FAKE),
+           bad_layer=None, out=FAKE * 2, ws=FAKE * 3, ws_bytes=1 << 40):
+    ptrs = [list(layer) for _ in range(max(L, 1))]
+    if bad_layer is not None:
+        ptrs[bad_layer[0]][bad_layer[1]] = bad_layer[2]
+    arrs = [(ctypes.c_void_p * len(ptrs))(*[p[j] for p in ptrs]) for j in range(3)]
+    return lib.moe_w4a8_forward_decode_stack(x, L, arrs[0], arrs[1], arrs[2], T, H, I, E, k, flags,
+                                             out, ws, ws_bytes, None)
+
+
+def test_decode_stack_argument_checks(lib):
+    assert _stack(lib, L=0) == moe.MOE_ERR_SHAPE
+    assert _stack(lib, L=moe.MOE_DECODE_MAX_LAYERS + 1) == moe.MOE_ERR_SHAPE
+    assert b"L=" in lib.moe_last_error_string()
+    assert _stack(lib, T=33) == moe.MOE_ERR_SHAPE
+    assert _stack(lib, H=200) == moe.MOE_ERR_SHAPE
+    assert _stack(lib, flags=4) == moe.MOE_ERR_INVALID_ARG
+    assert _stack(lib, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert _stack(lib, bad_layer=(1, 2, None)) == moe.MOE_ERR_INVALID_ARG   # layer 1's wd
+    assert b"layer 1" in lib.moe_last_error_string()
+    assert _stack(lib, bad_layer=(0, 1, FAKE + 8)) == moe.MOE_ERR_ALIGN
+    assert _stack(lib, out=FAKE) == moe.MOE_ERR_INVALID_ARG                 # out aliases x
+    assert _stack(lib, ws_bytes=16) == moe.MOE_ERR_WORKSPACE
+    assert _stack(lib, T=0) == moe.MOE_OK                                   # empty input: no-op
+
+
 def test_error_string_names_the_problem(lib):
     assert _prefill(lib, H=200) == moe.MOE_ERR_SHAPE
     assert b"128" in lib.moe_last_error_string()
