@@ -31,9 +31,10 @@ DECODE_LAYERS = 16          # distinct weight copies per decode step
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel as
-# it is in this tree: the decode expert kernel (T=1) and the prefill expert
-# GEMMs (T=2048).  Set to None when the kernel changes before a new capture.
-NCU_TRAFFIC_DECODE_LAYER_T1 = None  # not yet captured for the prep + layer kernels
+# it is in this tree: the decode prep and layer kernels (T=1) and the prefill
+# expert GEMMs (T=2048).  Set to None when a kernel changes before a new
+# capture.
+NCU_TRAFFIC_DECODE_LAYER_T1 = 21_346_560 + 1_086_976  # layer + prep kernel, ncu, one launch each at T=1
 NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch at T=2048
 KERNELS_PER_DECODE_LAYER = 2   # prep (logits, x codes); layer (top-k, buckets, experts, combine)
 DECODE_WORKLOAD = ("decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 (batch-1 decode "
