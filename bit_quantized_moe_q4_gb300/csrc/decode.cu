@@ -412,6 +412,19 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
 }
 
 // ----------------------------------------------------------------- layer
+// The first task of worker v of V when every touched slot has the same
+// bucket size and there are no more runs (nruns, P consecutive tasks each)
+// than workers: run r is shared by workers ceil(rV/nruns) ..
+// ceil((r+1)V/nruns) - 1 (at least one), each taking an equal part of its
+// tasks, so no worker's share crosses a run.
+__device__ __forceinline__ int run_bound(int v, int V, int nruns, int P) {
+    if (v >= V) return nruns * P;
+    const int r = (int)((long long)v * nruns / V);
+    const int w0 = (int)(((long long)r * V + nruns - 1) / nruns);
+    const int w1 = (int)(((long long)(r + 1) * V + nruns - 1) / nruns);
+    return r * P + (int)((long long)(v - w0) * P / (w1 - w0));
+}
+
 // The first task of worker v of V when the `per` tasks of touched slot i
 // (KC tiles each) cost KC * (kTileCost + c_i) each, c_i = toff[i + 1] -
 // toff[i] bucket rows: the task whose cost range holds the position
@@ -454,6 +467,7 @@ struct LayerShared {
     int toff[kMaxExperts + 1];  // touched slot -> its first bucket row (+ total)
     int slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
     int nt, nsg, nsd;
+    int eqc;                    // every touched slot has the same bucket size
     int bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
     volatile int abort;
     volatile int flag[kGroups];
@@ -528,6 +542,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     int& s_nt = S.nt;
     int& s_nsg = S.nsg;
     int& s_nsd = S.nsd;
+    int& s_eqc = S.eqc;
     auto& s_bnd = S.bnd;
     volatile int& s_abort = S.abort;
     volatile int* s_flag = S.flag;
@@ -661,12 +676,18 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
             0xffffffffu, lane < a.ndiv_g && nt_ * RBg * a.div_g[lane < a.ndiv_g ? lane : 0] >= kTargetTasks);
         const unsigned okd = __ballot_sync(
             0xffffffffu, lane < a.ndiv_d && nt_ * RBd * a.div_d[lane < a.ndiv_d ? lane : 0] >= kTargetTasks);
+        const int ceq = Tk / nt_;  // every bucket of this size?
+        bool eq_l = Tk % nt_ == 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) eq_l = eq_l && (cnt[i] == 0 || cnt[i] == ceq);
+        const bool eqc = __all_sync(0xffffffffu, eq_l);
         if (lane == 31) {
             s_off[E] = itot;
             s_nt = itch;
             s_toff[itch] = itot;
             s_nsg = okg ? a.div_g[__ffs(okg) - 1] : a.div_g[a.ndiv_g - 1];
             s_nsd = okd ? a.div_d[__ffs(okd) - 1] : a.div_d[a.ndiv_d - 1];
+            s_eqc = eqc ? 1 : 0;
         }
     }
     __syncthreads();
@@ -675,13 +696,18 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
         // Tasks are shared out by cost, a tile of touched slot i weighing
         // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
         // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
-        // likewise.  Warp 4g + j finds group g's bound j.
+        // likewise.  With equal buckets and no more runs (gate/up: slot and
+        // row block; down: slot and K part) than workers, the shares follow
+        // the runs instead (run_bound).  Warp 4g + j finds group g's bound j.
         const int g = warp >> 2, j = warp & 3;
         const bool gu = j < 2;
         const int nsg_ = s_nsg, nsd_ = s_nsd;
         const int per = gu ? RBg * nsg_ : RBd * nsd_;
         const int KC = gu ? KBg / nsg_ : KBd / nsd_;
-        const int bnd = split_bound_warp(2 * b + g + (j & 1), 2 * G, nt, Tk, per, KC, s_toff, lane);
+        const int nruns = gu ? nt * RBg : nt * nsd_, P = gu ? nsg_ : RBd;
+        const int v = 2 * b + g + (j & 1);
+        const int bnd = s_eqc && nruns <= 2 * G ? run_bound(v, 2 * G, nruns, P)
+                                                 : split_bound_warp(v, 2 * G, nt, Tk, per, KC, s_toff, lane);
         if (lane == 0) s_bnd[g][j] = bnd;
     } else {
         const int tid2 = tid - 4 * kGroups * 32, nthr2 = kLayerThreads - 4 * kGroups * 32;
