@@ -239,13 +239,18 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
 
 constexpr int kPrepBarId = 4;  // named barrier of the row's 128 threads
 
-// Router row e (staged in shared memory at w) of every token of x, by
-// threads 0..127: the optional RMSNorm, the logit, and the int8 codes of the
-// 32-column groups g of token t with (t * H/32 + g) % nrow == e (nrow: the
-// number of router rows).  s_red: 4 floats, s_r: MOE_DECODE_MAX_T floats of
-// shared memory.
+// The prep work of one CTA on threads 0..127, for every token of x: the
+// optional RMSNorm factor, then by `mode`
+//   0: router row e's logit (row staged in shared memory at w) and the int8
+//      codes of the 32-column groups g of token t with (t * H/32 + g) % nrow
+//      == e (nrow: the number of router rows);
+//   1: router row e's logit only;
+//   2: the int8 codes of the groups cb*32 .. cb*32 + 31 in (token, group)
+//      order, one quad of threads each (a CTA beside the logit CTAs).
+// s_red: 4 floats, s_r: MOE_DECODE_MAX_T floats of shared memory.
 __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, int e, int nrow,
-                                         const float* w, float* s_red, float* s_r) {
+                                         const float* w, float* s_red, float* s_r, int mode = 0,
+                                         int cb = 0) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int H = a.H, T = a.T;
     const int H8 = H / 8, G32 = H / kGroup;
@@ -304,6 +309,7 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, i
         r = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, (float)H) + 1e-6f));
         if (act && sub == 0) s_r[t] = r;  // for the coding pass
     }
+    if (mode != 2) {
     float accu[kPrepBatch];  // the logit's partial sums, one per unit slot
 #pragma unroll
     for (int z = 0; z < kPrepBatch; ++z) accu[z] = 0.f;
@@ -342,9 +348,12 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, i
     for (int z = 0; z < kPrepBatch; ++z) acc += accu[z];
     acc = token_sum(acc);
     if (act && sub == 0) a.logits[(size_t)t * a.E + e] = acc;
-    // int8 codes per 32 columns: this row's groups (t, g), (t * H/32 + g) %
-    // nrow == e, one quad of threads each (quad j takes the j-th, j + 32-th,
-    // ...), from x (and the token's norm factor) again
+    }
+    if (mode == 1) return;
+    // int8 codes per 32 columns, one quad of threads a group, from x (and
+    // the token's norm factor) again: mode 0, this row's groups (t, g),
+    // (t * H/32 + g) % nrow == e (quad j takes the j-th, j + 32-th, ...);
+    // mode 2, the block's groups
     if (a.prenorm) named_sync(kPrepBarId, kPrepThreads);  // s_r is stored
     const int quad = tid / 4, ql = tid % 4;
     const unsigned qmask = 0xFu << (lane & ~3);
@@ -352,8 +361,15 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, i
     for (int t2 = 0; t2 < T; ++t2) {
         int g = (e - t2 * G32) % nrow;  // (|t2 * G32| < 2^31)
         if (g < 0) g += nrow;
-        for (; g < G32; g += nrow, ++idx) {
-            if (idx % (kPrepThreads / 4) != quad) continue;
+        int gstep = nrow;
+        if (mode == 2) {  // this quad's group of the block, in token t2 = its token
+            const int fi = cb * (kPrepThreads / 4) + quad;
+            if (t2 != fi / G32) continue;
+            g = fi % G32;
+            gstep = G32;  // one group
+        }
+        for (; g < G32; g += gstep, ++idx) {
+            if (mode == 0 && idx % (kPrepThreads / 4) != quad) continue;
             const int u = g * 4 + ql;  // this lane's 8 columns
             float xf[8];
             unpack8(__ldcg(reinterpret_cast<const uint4*>(x + (size_t)t2 * H) + u), xf);
@@ -390,14 +406,17 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, i
     }
 }
 
+// CTAs 0..E-1: router row e (its logits); CTAs E..: blocks of 32 int8-coded
+// groups of x.
 __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     extern __shared__ __align__(128) uint8_t psm[];  // this CTA's router row [H] fp32
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ float s_red[kPrepThreads / 32];
     __shared__ float s_r[MOE_DECODE_MAX_T];
     const int tid = threadIdx.x, e = blockIdx.x, H = a.H;
+    const bool coder = e >= a.E;
     const uint32_t bar = smem_u32(&s_bar);
-    if (tid == 0) {
+    if (tid == 0 && !coder) {
         mbar_init(bar, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(bar, (uint32_t)(H * 4));
@@ -407,8 +426,12 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     pdl_wait();     // x and the workspace belong to this call from here on
     pdl_trigger();  // the layer kernel may be scheduled; it waits for our end
     for (int i = e * kPrepThreads + tid; i < a.nsync; i += gridDim.x * kPrepThreads) a.sync[i] = 0;
+    if (coder) {
+        prep_row(a, a.x, 0, a.E, nullptr, s_red, s_r, 2, e - a.E);
+        return;
+    }
     if (!mbar_wait(bar, 0)) record_status(a.status, kStatusTimeout);
-    prep_row(a, a.x, e, gridDim.x, reinterpret_cast<const float*>(psm), s_red, s_r);
+    prep_row(a, a.x, e, a.E, reinterpret_cast<const float*>(psm), s_red, s_r, 1);
 }
 
 // ----------------------------------------------------------------- layer
@@ -1538,7 +1561,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
             return err;
         g_prep_carveout[dev & 63] = 1;
     }
-    if ((err = launch_pdl(decode_prep_kernel, dim3(E), dim3(kPrepThreads), psmem, s, p)) != cudaSuccess) {
+    // E router-row CTAs and the CTAs coding x, 32 groups each
+    const int ncode = (T * (H / kGroup) + kPrepThreads / 4 - 1) / (kPrepThreads / 4);
+    if ((err = launch_pdl(decode_prep_kernel, dim3(E + ncode), dim3(kPrepThreads), psmem, s, p)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return err;
     }
