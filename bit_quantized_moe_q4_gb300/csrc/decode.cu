@@ -489,6 +489,8 @@ struct LayerShared {
     int touched[kMaxExperts];
     int toff[kMaxExperts + 1];  // touched slot -> its first bucket row (+ total)
     int slot_chunk[kMaxSlots];  // the latest chunk issued into each slot (both rings)
+    const uint8_t* ctab_p[kGroups][32];  // producer: the next chunks' sources
+    int ctab_n[kGroups][32];             // and sizes in tiles
     int nt, nsg, nsd;
     int eqc;                    // every touched slot has the same bucket size
     int bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
@@ -808,10 +810,6 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
         return w;
     };
     auto walk_live = [&](const Walk& w) { return w.gu ? w.left_g > 0 : w.left_d > 0; };
-    auto walk_base = [&](const Walk& w) -> const uint8_t* {
-        return w.gu ? io.wgu + (((size_t)s_touched[w.i] * RBg + w.rb) * KBg + (size_t)w.kc * KCg) * kTileBytes
-                    : io.wd + (((size_t)s_touched[w.i] * RBd + w.rb) * KBd + (size_t)w.kc * KCd) * kTileBytes;
-    };
 
     // Chunks: each task's tiles are cut into runs of up to st tiles (one bulk
     // copy, one ring slot each), chunk after chunk in the group's task order.
@@ -819,35 +817,61 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     // counting.
     if (warp >= kWarpProducer0) {
         // ---------------------------------------------------------- producer
-        // One lane issues the chunks in order; chunk c's slot held chunk
-        // c - ns, issued before it, so a parity wait never aliases.
+        // The group's chunks, 32 at a time: each lane finds one chunk's
+        // source from its index (task = index / chunks a task, in the walk's
+        // order), then lane 0 issues them in order; chunk c's slot held
+        // chunk c - ns, issued before it, so a parity wait never aliases.
         const int g = warp - kWarpProducer0;
-        if (lane == 0) {
-            int& slot = pp.slot;
-            int& phase = pp.phase;
-            int& cidx = pp.cidx;
-            bool ok = !s_abort;
-            for (Walk w = walk_start(g); walk_live(w) && ok; w = walk_next(w, g)) {
-                const uint8_t* base = walk_base(w);
-                const int KC = w.gu ? KCg : KCd;
-                for (int u0 = 0; u0 < KC; u0 += st) {
-                    const int n = KC - u0 < st ? KC - u0 : st;
+        const int ngu = s_bnd[g][1] - s_bnd[g][0], ndn = s_bnd[g][3] - s_bnd[g][2];
+        const int cptg = (KCg + st - 1) / st, cptd = (KCd + st - 1) / st;  // chunks a task
+        const int nch = ngu * cptg + ndn * cptd;
+        bool ok = !s_abort;
+        for (int c0 = 0; c0 < nch && ok; c0 += 32) {
+            const int c = c0 + lane;
+            if (c < nch) {
+                const uint8_t* src;
+                int n;
+                if (c < ngu * cptg) {
+                    const int tl = c / cptg, u0 = (c - tl * cptg) * st;
+                    const int t = s_bnd[g][0] + tl;
+                    const int i = t / per_g, r = t - i * per_g, rb = r / nsg, kc = r - rb * nsg;
+                    src = io.wgu + (((size_t)s_touched[i] * RBg + rb) * KBg + (size_t)kc * KCg + u0) * kTileBytes;
+                    n = KCg - u0 < st ? KCg - u0 : st;
+                } else {
+                    const int c2 = c - ngu * cptg, tl = c2 / cptd, u0 = (c2 - tl * cptd) * st;
+                    const int t = s_bnd[g][2] + tl;
+                    const int i = t / per_d, r = t - i * per_d, kc = r / RBd, rb = r - kc * RBd;
+                    src = io.wd + (((size_t)s_touched[i] * RBd + rb) * KBd + (size_t)kc * KCd + u0) * kTileBytes;
+                    n = KCd - u0 < st ? KCd - u0 : st;
+                }
+                S.ctab_p[g][lane] = src;
+                S.ctab_n[g][lane] = n;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                int& slot = pp.slot;
+                int& phase = pp.phase;
+                int& cidx = pp.cidx;
+                const int m = nch - c0 < 32 ? nch - c0 : 32;
+                for (int j = 0; j < m; ++j) {
                     ++cidx;
                     if (++slot == ns) {
                         slot = 0;
                         phase ^= 1;
                     }
-                    if (s_abort || !mbar_wait(empty_bar(g, slot), phase ^ 1) || s_abort) {
+                    // (the first ns chunks of the launch go to slots never used)
+                    if (s_abort || (cidx >= ns && !mbar_wait(empty_bar(g, slot), phase ^ 1)) || s_abort) {
                         fail();
                         ok = false;
                         break;
                     }
+                    const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * kTileBytes);
                     s_slot_chunk[g * ns + slot] = cidx;
-                    mbar_arrive_expect_tx(full_bar(g, slot), (uint32_t)(n * kTileBytes));
-                    bulk_g2s(sbase + slot_addr(g, slot), base + (size_t)u0 * kTileBytes,
-                             (uint32_t)(n * kTileBytes), full_bar(g, slot));
+                    mbar_arrive_expect_tx(full_bar(g, slot), bytes);
+                    bulk_g2s(sbase + slot_addr(g, slot), S.ctab_p[g][j], bytes, full_bar(g, slot));
                 }
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);  // (the table is rewritten next round)
         }
         return;
     }
