@@ -550,8 +550,9 @@ __device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, u
 
 // One decode layer (everything after the prep kernel's work) by one CTA of
 // the cooperative grid.  MAXNT: the most tokens an expert's bucket may hold
-// (T <= MAXNT).
-template <int MAXNT>
+// (T <= MAXNT).  DOTS: also store every int32 group dot (stage outputs; the
+// variant that does not is the one calls run without them).
+template <int MAXNT, bool DOTS>
 __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
                                            uint8_t* dsm, Pipe& pp) {
     int* s_idx = S.idx;
@@ -911,12 +912,22 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
         const uint8_t* aq = GU ? ax_q : ah_q;
         const int2* as = GU ? ax_s : ah_s;
         const int K = GU ? H : I, Gk = GU ? Gx : Gh, KC = GU ? KCg : KCd;
-        int32_t* dots = GU ? a.dots_gu : a.dots_d;
+        int32_t* dots = DOTS ? (GU ? a.dots_gu : a.dots_d) : nullptr;
         const size_t dots_ld = GU ? (size_t)2 * I : (size_t)H;
         const size_t ld = GU ? (size_t)2 * I : (size_t)H;
         const int code_off = w8 * 512 + lane * 16;                  // this lane's 16 code bytes
         const int scale_off = kTileCodeBytes + w8 * 64 + lane * 2;  // and its group's scale
         const int i = w.i;
+        // the bucket rows' activation rows and scale rows (fixed for the run;
+        // held in registers for small buckets)
+        constexpr int NH = NT <= 4 ? NT : 1;
+        int arow[NH], srow[NH];
+#pragma unroll
+        for (int n = 0; n < NH; ++n) {
+            const int ar = GU ? s_btok[off + (n < c ? n : 0)] : n;
+            arow[n] = ar * K;
+            srow[n] = ar * Gk;
+        }
         int ntask = 0;
         while (true) {
             const int rb = w.rb, kc = w.kc, kb0 = kc * KC, row = rb * kTileRows + lrow;
@@ -948,11 +959,19 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {
                             if (n < c) {
-                                const int ar = GU ? s_btok[off + n] : n;
-                                const int2 sc = as[ar * Gk + g];
-                                const int dot = group_dot(wl, wh, aq + ar * K + g * kGroup, sc.y);
+                                int ao, so;
+                                if constexpr (NT <= 4) {
+                                    ao = arow[n];
+                                    so = srow[n];
+                                } else {
+                                    const int ar = GU ? s_btok[off + n] : n;
+                                    ao = ar * K;
+                                    so = ar * Gk;
+                                }
+                                const int2 sc = as[so + g];
+                                const int dot = group_dot(wl, wh, aq + ao + g * kGroup, sc.y);
                                 acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
-                                if (dots) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
+                                if (DOTS) dots[((size_t)(off + n) * dots_ld + row) * Gk + g] = dot;
                             }
                         }
                     }
@@ -1231,7 +1250,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
 // thread, which leaves room on the SM for the next call's prep CTA; the
 // MAXNT = 32 variant spills a little instead (it only runs when more than
 // 16 tokens are decoded at once).
-template <int MAXNT>
+template <int MAXNT, bool DOTS>
 __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ LayerShared S;
@@ -1241,7 +1260,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     pdl_trigger();  // the next call's prep may be scheduled; it waits for our end
     Pipe pp{-1, 0, -1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
-    layer_body<MAXNT>(a, io, S, dsm, pp);
+    layer_body<MAXNT, DOTS>(a, io, S, dsm, pp);
     ring_drain(a, S, dsm);
 }
 
@@ -1337,7 +1356,7 @@ __global__ void __maxnreg__(96) decode_stack_kernel(const __grid_constant__ Stac
         }
         grid_sync();
         if (tid == 0 && nrows && l + 1 < A.L) stage_rows(l + 1);  // its rows are read
-        layer_body<MAXNT>(a, io, S, dsm, pp);
+        layer_body<MAXNT, false>(a, io, S, dsm, pp);
         grid_sync();
     }
     ring_drain(a, S, dsm);
@@ -1603,7 +1622,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.dots_gu = dots_gu;
     a.dots_d = dots_d;
     a.write_qh = write_qh ? 1 : 0;
-    void (*kern)(LayerArgs) = T <= 16 ? decode_layer_kernel<16> : decode_layer_kernel<MOE_DECODE_MAX_T>;
+    const bool dots = dots_gu || dots_d;
+    void (*kern)(LayerArgs) =
+        T <= 16 ? (dots ? decode_layer_kernel<16, true> : decode_layer_kernel<16, false>)
+                : (dots ? decode_layer_kernel<MOE_DECODE_MAX_T, true> : decode_layer_kernel<MOE_DECODE_MAX_T, false>);
     if ((err = launch_coop(kern, a, num_sms, plan.smem, dev, s)) != cudaSuccess) return err;
     for (int i = 2; i <= 6; ++i)
         if ((err = mark(i)) != cudaSuccess) return err;
