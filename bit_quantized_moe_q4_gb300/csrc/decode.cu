@@ -75,7 +75,7 @@ constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kLayerThreads = kConsumerThreads + kGroups * 32;  // + a producer warp per group
 constexpr int kWarpProducer0 = kConsumerWarps;          // group g's producer: warp kWarpProducer0 + g
-constexpr int kSlotTiles = 2;                           // packed tiles per ring slot (one bulk copy),
+constexpr int kSlotTiles = 4;                           // packed tiles per ring slot (one bulk copy),
                                                         // fewer when shared memory is short
 constexpr int kMaxSlots = 24;                           // slots of both groups' rings
 constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 32 lanes x 8 floats
@@ -1380,9 +1380,11 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
     const long long ax = al128((long long)T * H + (long long)T * (H / kGroup) * 8);
     const long long ah = al128((long long)T * I + (long long)T * (I / kGroup) * 8);
     const long long rest = budget - ax - 2 * ah - 2 * kRedBytes - 2 * kMaxSlots * 8 - 256;
-    // the largest slot (up to kSlotTiles tiles) that still gives each group's
-    // ring two slots, else one
-    int st = kSlotTiles;
+    // slots of four tiles for several tokens while each group's ring keeps
+    // three of them (fewer chunk hand-offs), else two-tile slots (one token:
+    // short tasks, deeper ring), else the largest slot that still gives each
+    // group's ring two slots, else one
+    int st = T >= 4 && rest >= (long long)kGroups * 3 * 4 * kTileBytes ? 4 : 2;
     while (st > 1 && rest < (long long)kGroups * 2 * st * kTileBytes) st /= 2;
     int ns = (int)(rest / ((long long)st * kTileBytes)) / kGroups;  // slots of each group's ring
     ns = ns > kMaxSlots / kGroups ? kMaxSlots / kGroups : ns;
