@@ -184,7 +184,7 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / steps
-    # the same L layers in one launch (moe_w4a8_forward_decode_stack): its
+    # the same L layers from one call (moe_w4a8_forward_decode_stack): its
     # output must carry the chain's bits
     out_stack = torch.empty((T, li.H), dtype=torch.bfloat16, device=device)
 
@@ -234,11 +234,11 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
         "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 2,
         "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
         "stack": {
-            "entry": "moe_w4a8_forward_decode_stack (the L layers in one cooperative launch)",
+            "entry": "moe_w4a8_forward_decode_stack (one call: the L layers' 2L kernels, chained by PDL)",
             "equals_chain_bits": stack_same, "ms_per_step": ms_stack,
             "us_per_layer": ms_stack * 1e3 / L, "us_per_token": ms_stack * 1e3 / (L * T),
             "layer_gbs": statistics.mean(layer_bytes) / (ms_stack * 1e3 / L * 1e-6) / 1e9,
-            "e2e_us_per_token": e2e_stack_ms * 1e3 / (L * T), "kernels_per_step": 2,
+            "e2e_us_per_token": e2e_stack_ms * 1e3 / (L * T), "kernels_per_step": 2 * L,
         },
     }
     del layers, outs, ws, g, gs

@@ -275,7 +275,7 @@ def moe_w4a8_forward_decode(x, wr, wgu_packed, wd_packed, I: int, k: int, out=No
 
 def moe_w4a8_forward_decode_stack(x, layers, I: int, k: int, out=None, out_fp32: bool = True,
                                   workspace=None, stream=None, prenorm: bool = True):
-    """L stacked decode layers in one launch.  ``layers``: a sequence of
+    """L stacked decode layers from one call.  ``layers``: a sequence of
     (wr, wgu_packed, wd_packed) per layer; layer l + 1 reads layer l's output
     rounded to bf16.  Returns the last layer's output [T, H]."""
     T, H = x.shape

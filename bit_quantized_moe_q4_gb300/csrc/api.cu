@@ -185,11 +185,10 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.gu_part = reinterpret_cast<float*>(take((size_t)nsg * Tk * 2 * I * 4));
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
-        w.y_part = reinterpret_cast<float*>(take((size_t)nsd * Tk * H * 4));
+        w.y_part = reinterpret_cast<float*>(take((size_t)decode_y_parts(T, H, I, E, k) * Tk * H * 4));
         w.sync = reinterpret_cast<int32_t*>(take((size_t)decode_sync_ints(T, H, I, E, k) * 4));
         w.xbuf0 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.xbuf1 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
-        w.gbar = reinterpret_cast<int32_t*>(take(4));
     }
     w.max_tiles = max_tiles;
     w.tile_n = tile_n;
@@ -492,10 +491,6 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
         return set_err(MOE_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev))) return rc;
-    if (!decode_stack_fits(T, H, I, E, dev->num_sms))
-        return set_err(MOE_ERR_SHAPE,
-                       "decode stack with T=%d H=%d I=%d E=%d does not fit the on-chip staging", T, H,
-                       I, E);
     Workspace ws{};
     carve(MOE_MODE_DECODE, T, H, I, E, k, static_cast<uint8_t*>(workspace), &ws);
     return cuda_check(launch_decode_stack(x_bf16, L, wr, wgu_packed, wd_packed, T, H, I, E, k,

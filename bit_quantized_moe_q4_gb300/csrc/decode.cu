@@ -149,6 +149,10 @@ struct LayerArgs {
     int ns;             // slots of each group's ring
     int st;             // packed tiles per slot (kSlotTiles, or fewer for large T)
     int off_bar, off_ax, off_ah, ah_bytes, off_red;
+    // clustered layer kernel: tickets [T, H/128] (cleared by the prep kernel),
+    // the K-part exchange buffers and the groups' h buffers
+    int* ticket;
+    int off_p, off_h, h_bytes;
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -221,9 +225,10 @@ namespace {
 // eight at a time.  Its partial sums (one per unit slot mod 8, in column
 // order within a unit) are added in slot order, then across the token's
 // threads by a butterfly (and across its warps in warp order, through
-// shared memory, when tpt > 32).  A quad of threads holds one 32-column
-// group, whose int8 codes one CTA writes: CTA (t * H/32 + g) % grid.  At
-// most 80 registers a thread: next to a layer kernel of the previous call
+// shared memory, when tpt > 32).  mode 1: the norm, then router row e's
+// logits; mode 2: the norm, then the int8 codes of block cb of the token
+// groups (a quad of threads a 32-column group).  At most 80 registers a
+// thread: next to a layer kernel of the previous call
 // (576 threads x 96) the SM has 128 x 80 left, so the next layer's prep can
 // stage its router row while that kernel runs.
 constexpr int kPrepBatch = 8;  // units a thread loads at once
@@ -248,9 +253,8 @@ constexpr int kPrepBarId = 4;  // named barrier of the row's 128 threads
 //   2: the int8 codes of the groups cb*32 .. cb*32 + 31 in (token, group)
 //      order, one quad of threads each (a CTA beside the logit CTAs).
 // s_red: 4 floats, s_r: MOE_DECODE_MAX_T floats of shared memory.
-__device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, int e, int nrow,
-                                         const float* w, float* s_red, float* s_r, int mode = 0,
-                                         int cb = 0) {
+__device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, int e, const float* w,
+                                         float* s_red, float* s_r, int mode, int cb = 0) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int H = a.H, T = a.T;
     const int H8 = H / 8, G32 = H / kGroup;
@@ -350,58 +354,44 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const uint16_t* x, i
     if (act && sub == 0) a.logits[(size_t)t * a.E + e] = acc;
     }
     if (mode == 1) return;
-    // int8 codes per 32 columns, one quad of threads a group, from x (and
-    // the token's norm factor) again: mode 0, this row's groups (t, g),
-    // (t * H/32 + g) % nrow == e (quad j takes the j-th, j + 32-th, ...);
-    // mode 2, the block's groups
+    // mode 2: the int8 codes of block cb of the T * H/32 groups (32 groups,
+    // one quad of threads each), from x and the token's norm factor again
     if (a.prenorm) named_sync(kPrepBarId, kPrepThreads);  // s_r is stored
     const int quad = tid / 4, ql = tid % 4;
     const unsigned qmask = 0xFu << (lane & ~3);
-    int idx = 0;
-    for (int t2 = 0; t2 < T; ++t2) {
-        int g = (e - t2 * G32) % nrow;  // (|t2 * G32| < 2^31)
-        if (g < 0) g += nrow;
-        int gstep = nrow;
-        if (mode == 2) {  // this quad's group of the block, in token t2 = its token
-            const int fi = cb * (kPrepThreads / 4) + quad;
-            if (t2 != fi / G32) continue;
-            g = fi % G32;
-            gstep = G32;  // one group
+    const int fi = cb * (kPrepThreads / 4) + quad, t2 = fi / G32, g = fi - t2 * G32;
+    if (t2 < T) {  // (uniform in the quad)
+        const int u = g * 4 + ql;  // this lane's 8 columns
+        float xf[8];
+        unpack8(__ldcg(reinterpret_cast<const uint4*>(x + (size_t)t2 * H) + u), xf);
+        if (a.prenorm) {
+            const float r2 = s_r[t2];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xf[q] = bf16_bits_to_float(float_to_bf16_bits(xf[q] * r2));
         }
-        for (; g < G32; g += gstep, ++idx) {
-            if (mode == 0 && idx % (kPrepThreads / 4) != quad) continue;
-            const int u = g * 4 + ql;  // this lane's 8 columns
-            float xf[8];
-            unpack8(__ldcg(reinterpret_cast<const uint4*>(x + (size_t)t2 * H) + u), xf);
-            if (a.prenorm) {
-                const float r2 = s_r[t2];
+        float amax = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) xf[q] = bf16_bits_to_float(float_to_bf16_bits(xf[q] * r2));
-            }
-            float amax = 0.f;
+        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
+        amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
+        const uint16_t db = act_scale_bits(amax);
+        const float d = half_bits_to_float(db);
+        uint32_t lo = 0u, hi = 0u;
+        int gsum = 0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(xf[q]));
-            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
-            const uint16_t db = act_scale_bits(amax);
-            const float d = half_bits_to_float(db);
-            uint32_t lo = 0u, hi = 0u;
-            int gsum = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int qc = act_code(xf[q], d);
-                gsum += qc;
-                if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
-                else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
-            }
-            gsum += __shfl_xor_sync(qmask, gsum, 1);
-            gsum += __shfl_xor_sync(qmask, gsum, 2);
-            *reinterpret_cast<uint2*>(a.xq + (size_t)t2 * H + u * 8) = permute_chunk(lo, hi);
-            *reinterpret_cast<uint2*>(a.q_x + (size_t)t2 * H + u * 8) = make_uint2(lo, hi);
-            if (ql == 0) {
-                a.xs[t2 * G32 + g] = make_int2(__float_as_int(d), -8 * gsum);
-                a.d_x[t2 * G32 + g] = db;
-            }
+        for (int q = 0; q < 8; ++q) {
+            const int qc = act_code(xf[q], d);
+            gsum += qc;
+            if (q < 4) lo |= ((uint32_t)qc & 0xffu) << (8 * q);
+            else hi |= ((uint32_t)qc & 0xffu) << (8 * (q - 4));
+        }
+        gsum += __shfl_xor_sync(qmask, gsum, 1);
+        gsum += __shfl_xor_sync(qmask, gsum, 2);
+        *reinterpret_cast<uint2*>(a.xq + (size_t)t2 * H + u * 8) = permute_chunk(lo, hi);
+        *reinterpret_cast<uint2*>(a.q_x + (size_t)t2 * H + u * 8) = make_uint2(lo, hi);
+        if (ql == 0) {
+            a.xs[t2 * G32 + g] = make_int2(__float_as_int(d), -8 * gsum);
+            a.d_x[t2 * G32 + g] = db;
         }
     }
 }
@@ -427,11 +417,11 @@ __global__ void __maxnreg__(80) decode_prep_kernel(const PrepArgs a) {
     pdl_trigger();  // the layer kernel may be scheduled; it waits for our end
     for (int i = e * kPrepThreads + tid; i < a.nsync; i += gridDim.x * kPrepThreads) a.sync[i] = 0;
     if (coder) {
-        prep_row(a, a.x, 0, a.E, nullptr, s_red, s_r, 2, e - a.E);
+        prep_row(a, a.x, 0, nullptr, s_red, s_r, 2, e - a.E);
         return;
     }
     if (!mbar_wait(bar, 0)) record_status(a.status, kStatusTimeout);
-    prep_row(a, a.x, e, a.E, reinterpret_cast<const float*>(psm), s_red, s_r, 1);
+    prep_row(a, a.x, e, reinterpret_cast<const float*>(psm), s_red, s_r, 1);
 }
 
 // ----------------------------------------------------------------- layer
@@ -548,13 +538,16 @@ __device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, u
     }
 }
 
-// One decode layer (everything after the prep kernel's work) by one CTA of
-// the cooperative grid.  MAXNT: the most tokens an expert's bucket may hold
-// (T <= MAXNT).  DOTS: also store every int32 group dot (stage outputs; the
-// variant that does not is the one calls run without them).
-template <int MAXNT, bool DOTS>
-__device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
-                                           uint8_t* dsm, Pipe& pp) {
+// Routing, taken by every CTA from the same logits: each token's top k
+// (larger logit first, the lower expert index on a tie) with softmax weights
+// over them, a token bitmask per expert, the buckets (a scan over experts),
+// the K splits of the task kernel.  CTA 0 stores the routing results.  The
+// logits and their order keys sit in the still idle dynamic shared memory
+// below the codes of x.  split(warp, lane) runs on warps 0 .. 4*kGroups - 1
+// (the work split of the caller) while the other warps fill the buckets.
+template <typename Split>
+__device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, uint8_t* dsm,
+                                            Split&& split) {
     int* s_idx = S.idx;
     float* s_w = S.w;
     int* s_btok = S.btok;
@@ -564,46 +557,15 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     int* s_off = S.off;
     int* s_touched = S.touched;
     int* s_toff = S.toff;
-    int* s_slot_chunk = S.slot_chunk;
     int& s_nt = S.nt;
     int& s_nsg = S.nsg;
     int& s_nsd = S.nsd;
     int& s_eqc = S.eqc;
-    auto& s_bnd = S.bnd;
-    volatile int& s_abort = S.abort;
-    volatile int* s_flag = S.flag;
-
     const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k;
-    const int KBg = H / kTileK, KBd = I / kTileK;
-    const int RBg = 2 * I / kTileRows, RBd = H / kTileRows, RBh = I / kTileRows;
-    const int Gx = H / kGroup, Gh = I / kGroup;
-    const int Tk = T * k, ns = a.ns;
+    const int RBg = 2 * I / kTileRows, RBd = H / kTileRows;
+    const int Tk = T * k;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int G = gridDim.x, b = blockIdx.x;
-    const uint32_t sbase = smem_u32(dsm);
-    // group g's ring: slots g*ns .. g*ns + ns - 1
-    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
-    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
-    const int st = a.st;
-    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
-    auto fail = [&]() {
-        record_status(a.status, kStatusTimeout);
-        s_abort = 1;
-    };
-    if (warp < kConsumerWarps) {
-        // the int8 codes of x and their scales (written by the prep kernel)
-        // start on their way to shared memory while the CTA routes
-        const int n16 = (T * H + T * Gx * 8) / 16;
-        const uint8_t* src = a.xq;
-        for (int i = tid; i < n16; i += kConsumerThreads)
-            cp_async16(sbase + a.off_ax + 16 * i, src + 16 * (size_t)i);
-    }
-
-    // ---------------------------------------------- routing (every CTA)
-    // Every CTA takes the same decisions from the same logits: each token's
-    // top k (larger logit first, the lower expert index on a tie) with
-    // softmax weights over them, a token bitmask per expert, the buckets and
-    // the work split.
+    const int b = blockIdx.x;
     float* s_lg = reinterpret_cast<float*>(dsm);                  // [T][E] logits, and
     uint32_t* s_key = reinterpret_cast<uint32_t*>(s_lg + T * E);  // their order keys, in
     for (int i = tid; i < T * E; i += kLayerThreads) {            // the still idle ring
@@ -719,22 +681,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     __syncthreads();
     const int nt = s_nt;
     if (warp < 4 * kGroups) {
-        // Tasks are shared out by cost, a tile of touched slot i weighing
-        // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
-        // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
-        // likewise.  With equal buckets and no more runs (gate/up: slot and
-        // row block; down: slot and K part) than workers, the shares follow
-        // the runs instead (run_bound).  Warp 4g + j finds group g's bound j.
-        const int g = warp >> 2, j = warp & 3;
-        const bool gu = j < 2;
-        const int nsg_ = s_nsg, nsd_ = s_nsd;
-        const int per = gu ? RBg * nsg_ : RBd * nsd_;
-        const int KC = gu ? KBg / nsg_ : KBd / nsd_;
-        const int nruns = gu ? nt * RBg : nt * nsd_, P = gu ? nsg_ : RBd;
-        const int v = 2 * b + g + (j & 1);
-        const int bnd = s_eqc && nruns <= 2 * G ? run_bound(v, 2 * G, nruns, P)
-                                                 : split_bound_warp(v, 2 * G, nt, Tk, per, KC, s_toff, lane);
-        if (lane == 0) s_bnd[g][j] = bnd;
+        split(warp, lane);
     } else {
         const int tid2 = tid - 4 * kGroups * 32, nthr2 = kLayerThreads - 4 * kGroups * 32;
         for (int p = tid2; p < Tk; p += nthr2) {
@@ -756,9 +703,82 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
             if (tid2 == 0) a.counters[kCntTouched] = nt;
         }
     }
-    // the ring held the logits through generic accesses; bulk copies refill it
+    // the logits were held through generic accesses; bulk copies refill
+    // that memory
     fence_proxy_async_smem();
     __syncthreads();
+
+}
+
+// One decode layer (everything after the prep kernel's work) by one CTA of
+// the cooperative grid.  MAXNT: the most tokens an expert's bucket may hold
+// (T <= MAXNT).  DOTS: also store every int32 group dot (stage outputs; the
+// variant that does not is the one calls run without them).
+template <int MAXNT, bool DOTS>
+__device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
+                                           uint8_t* dsm, Pipe& pp) {
+    int* s_btok = S.btok;
+    float* s_bsw = S.bsw;
+    int* s_slotpos = S.slotpos;
+    int* s_off = S.off;
+    int* s_touched = S.touched;
+    int* s_toff = S.toff;
+    int* s_slot_chunk = S.slot_chunk;
+    int& s_nt = S.nt;
+    int& s_nsg = S.nsg;
+    int& s_nsd = S.nsd;
+    int& s_eqc = S.eqc;
+    auto& s_bnd = S.bnd;
+    volatile int& s_abort = S.abort;
+    volatile int* s_flag = S.flag;
+
+    const int T = a.T, H = a.H, I = a.I, k = a.k;
+    const int KBg = H / kTileK, KBd = I / kTileK;
+    const int RBg = 2 * I / kTileRows, RBd = H / kTileRows, RBh = I / kTileRows;
+    const int Gx = H / kGroup, Gh = I / kGroup;
+    const int Tk = T * k, ns = a.ns;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int G = gridDim.x, b = blockIdx.x;
+    const uint32_t sbase = smem_u32(dsm);
+    // group g's ring: slots g*ns .. g*ns + ns - 1
+    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
+    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
+    const int st = a.st;
+    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
+    auto fail = [&]() {
+        record_status(a.status, kStatusTimeout);
+        s_abort = 1;
+    };
+    if (warp < kConsumerWarps) {
+        // the int8 codes of x and their scales (written by the prep kernel)
+        // start on their way to shared memory while the CTA routes
+        const int n16 = (T * H + T * Gx * 8) / 16;
+        const uint8_t* src = a.xq;
+        for (int i = tid; i < n16; i += kConsumerThreads)
+            cp_async16(sbase + a.off_ax + 16 * i, src + 16 * (size_t)i);
+    }
+
+    // ---------------------------------------------- routing (every CTA)
+    route_layer(a, S, dsm, [&](int warp, int lane) {
+        // Tasks are shared out by cost, a tile of touched slot i weighing
+        // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
+        // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
+        // likewise.  With equal buckets and no more runs (gate/up: slot and
+        // row block; down: slot and K part) than workers, the shares follow
+        // the runs instead (run_bound).  Warp 4g + j finds group g's bound j.
+        const int nt = s_nt;
+        const int g = warp >> 2, j = warp & 3;
+        const bool gu = j < 2;
+        const int nsg_ = s_nsg, nsd_ = s_nsd;
+        const int per = gu ? RBg * nsg_ : RBd * nsd_;
+        const int KC = gu ? KBg / nsg_ : KBd / nsd_;
+        const int nruns = gu ? nt * RBg : nt * nsd_, P = gu ? nsg_ : RBd;
+        const int v = 2 * b + g + (j & 1);
+        const int bnd = s_eqc && nruns <= 2 * G ? run_bound(v, 2 * G, nruns, P)
+                                                 : split_bound_warp(v, 2 * G, nt, Tk, per, KC, s_toff, lane);
+        if (lane == 0) s_bnd[g][j] = bnd;
+    });
+    const int nt = s_nt;
 
     // ------------------------------------------------------- work split
     const int nsg = s_nsg, nsd = s_nsd;
@@ -1264,110 +1284,491 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     ring_drain(a, S, dsm);
 }
 
-// A stack of L decode layers in one cooperative launch: layer l + 1 reads
-// layer l's output.  Per layer: the prep work (CTA b holds router rows b,
-// b + grid, ..., staged in shared memory during the layer before, and runs
-// the prep kernel's arithmetic on its first 128 threads; every CTA clears a
-// share of the layer's counters), a grid barrier, the layer itself, a grid
-// barrier.  The code stays resident in the SMs' instruction caches from
-// layer to layer and no kernel boundary separates them.
-struct StackArgs {
-    LayerArgs la;  // shape, workspace and shared-memory plan (not x, weights, output)
-    PrepArgs pa;   // shape and the prep outputs (not x, router rows)
-    const float* wr[MOE_DECODE_MAX_LAYERS];
-    const uint8_t* wgu[MOE_DECODE_MAX_LAYERS];
-    const uint8_t* wd[MOE_DECODE_MAX_LAYERS];
-    int L;
-    const uint16_t* x0;     // the stack's input [T, H] bf16
-    uint16_t* xbuf[2];      // layer outputs inside the stack [T, H] bf16 (ping-pong)
-    void* out;              // the last layer's output
-    int out_fp32;
-    int* gbar;              // grid barrier arrivals, zero at launch
-    int off_wr;             // staged router rows [rows][H] fp32 in dynamic shared memory
-};
+// ------------------------------------------------------ clustered layer
+// A second form of the layer kernel for a few tokens.  Pairs of CTAs form
+// thread-block clusters; a cluster's kUnitWorkers consumer groups share each
+// unit = (touched slot i, 128-feature block hb of h), so that a unit's h
+// never leaves the cluster:
+//   gate/up  worker w = 2 * rank + g (CTA rank of the cluster, group g):
+//            rows of block hb of the gate (g = 0) or up (g = 1) half of
+//            W_gu, K part `rank` of kClusterCTAs; its per-token row sums go
+//            to every CTA of the cluster (st.async into distributed shared
+//            memory, counted as transaction bytes on the receiver's mbarrier)
+//   h        each group adds the K parts of gate and of up (part order),
+//            h = silu(g) * u, int8 codes per 32 features
+//   down     worker w: row blocks w, w + kUnitWorkers, ... of W_d over the
+//            block's 128 columns: routing weight * row sums, the parts hb of
+//            y (one per h block)
+//   combine  a count per (token, 128-column block of the output) of the
+//            parts stored (k * I/128 of them); the block's items are cut into
+//            pieces, each owned by a fixed group of the grid, which waits for
+//            the count after its own units and adds the residual and the
+//            parts (slot order, then block order).
+// Units go to clusters in contiguous ranges of equal cost (a unit of slot i
+// weighs kTileCost + c_i per tile, all units have the same tiles).  The
+// combine waits on other clusters, so the launch is cooperative as well.
+constexpr int kClusterCTAs = 2;
+constexpr int kUnitWorkers = kClusterCTAs * kGroups;
+constexpr int kClusterMaxT = 8;   // tokens per call of the clustered kernel
 
-// 96 registers a thread: the SM's four register files (16,384 each) hold
-// five of the 18 warps at most at that size.
-template <int MAXNT>
-__global__ void __maxnreg__(96) decode_stack_kernel(const __grid_constant__ StackArgs A) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ LayerShared S;
-    __shared__ __align__(8) uint64_t s_wrbar;
-    __shared__ float s_red[kPrepThreads / 32];
-    __shared__ float s_r[MOE_DECODE_MAX_T];
-    const LayerArgs& a = A.la;
-    const int tid = threadIdx.x, b = blockIdx.x, G = gridDim.x, H = a.H, E = a.E;
-    const uint32_t wrbar = smem_u32(&s_wrbar);
-    float* wrow = reinterpret_cast<float*>(dsm + A.off_wr);
-    const int nrows = b < E ? (E - 1 - b) / G + 1 : 0;  // router rows b, b + G, ...
-    // (thread 0) this CTA's router rows of layer l into shared memory
-    auto stage_rows = [&](int l) {
-        fence_proxy_async_smem();  // after the generic reads of the layer before
-        mbar_arrive_expect_tx(wrbar, (uint32_t)(nrows * H * 4));
-        for (int j = 0; j < nrows; ++j)
-            bulk_g2s(smem_u32(wrow + (size_t)j * H), A.wr[l] + (size_t)(b + j * G) * H, (uint32_t)(H * 4),
-                     wrbar);
-    };
-    ring_init(a, S, dsm);
-    if (tid == 0) {
-        mbar_init(wrbar, 1);
-        fence_mbar_init();
-        if (nrows) stage_rows(0);
+// The first unit of cluster q of NC: the unit whose cost range holds the
+// position q * total / NC (units of touched slot i, RBh of them, weigh
+// kTileCost + c_i each, c_i = toff[i + 1] - toff[i]).  Monotone in q;
+// bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp calls it.
+__device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
+                                               int lane) {
+    using u64 = unsigned long long;
+    const u64 tot = (u64)RBh * ((u64)kTileCost * nt + Tk);
+    const u64 qt = (u64)q * tot;  // NC times the position
+    int cnt = 0;                  // slots whose first unit starts before it
+    for (int i0 = 0; i0 <= nt; i0 += 32) {
+        const int i = i0 + lane;
+        const bool lt = i <= nt && (u64)NC * RBh * ((u64)kTileCost * i + toff[i]) < qt;
+        cnt += __popc(__ballot_sync(0xffffffffu, lt));
     }
-    __syncthreads();
-    pdl_wait();  // the cleared barrier counter
-    pdl_trigger();
-    // grid barrier n (counting from 1): every CTA has arrived n times
-    int nbar = 0;
-    auto grid_sync = [&]() {
-        __syncthreads();
-        ++nbar;
-        if (tid == 0) {
-            red_release_add(A.gbar, 1);
-            const int target = nbar * G;
-            bool ok = !S.abort;
-            if (ok && ld_acquire(A.gbar) < target) {
-                const unsigned long long t0 = globaltimer_ns();
-                while (ld_acquire(A.gbar) < target) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (cnt == 0) return 0;
+    const int i = cnt - 1;
+    if (i >= nt) return nt * RBh;
+    const u64 base = (u64)NC * RBh * ((u64)kTileCost * i + toff[i]);
+    const u64 wn = (u64)NC * (kTileCost + toff[i + 1] - toff[i]);
+    const u64 j = (qt - base + wn - 1) / wn;
+    return i * RBh + (int)(j < (u64)RBh ? j : (u64)RBh);
+}
+
+template <int MAXNT, bool DOTS>
+__device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
+                                             uint8_t* dsm, Pipe& pp) {
+    volatile int& s_abort = S.abort;
+    const int T = a.T, H = a.H, I = a.I, k = a.k;
+    const int KBg = H / kTileK, KBd = I / kTileK;
+    const int RBg = 2 * I / kTileRows, RBd = H / kTileRows, RBh = I / kTileRows;
+    const int Gx = H / kGroup, Gh = I / kGroup;
+    const int Tk = T * k, ns = a.ns, st = a.st;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int rank = (int)cluster_ctarank(), cq = (int)cluster_id_x(), NC = (int)cluster_count_x();
+    const uint32_t sbase = smem_u32(dsm);
+    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
+    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
+    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
+    auto pbar = [&](int pb) { return sbase + a.off_bar + 8u * (4 * ns + pb); };
+    auto fail = [&]() {
+        record_status(a.status, kStatusTimeout);
+        s_abort = 1;
+    };
+    if (warp < kConsumerWarps) {
+        const int n16 = (T * H + T * Gx * 8) / 16;
+        for (int i = tid; i < n16; i += kConsumerThreads)
+            cp_async16(sbase + a.off_ax + 16 * i, a.xq + 16 * (size_t)i);
+    }
+    route_layer(a, S, dsm, [&](int warp, int lane) {
+        if (warp == 0) {
+            const int nt = S.nt;
+            const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane);
+            const int u1 = unit_bound_warp(cq + 1, NC, nt, Tk, RBh, S.toff, lane);
+            if (lane == 0) {
+                S.bnd[0][0] = u0;
+                S.bnd[0][1] = u1;
+            }
+        }
+    });
+    const int ub0 = S.bnd[0][0], nu = S.bnd[0][1] - ub0;
+    const int KCg = KBg / kClusterCTAs, kb0 = rank * KCg;  // this CTA's K part of gate/up
+    const int cptg = (KCg + st - 1) / st;                    // gate/up chunks of a unit
+
+    if (warp >= kWarpProducer0) {
+        // ---------------------------------------------------------- producer
+        // Worker w's chunks in its consumers' order: per unit, the gate/up
+        // K part in runs of st tiles, then its down row blocks (two tiles
+        // each: the block's 128 columns).
+        const int g = warp - kWarpProducer0, w = 2 * rank + g;
+        const int ndn = w < RBd ? (RBd - w + kUnitWorkers - 1) / kUnitWorkers : 0;
+        const int cpu = cptg + ndn, nch = nu * cpu;
+        bool ok = !s_abort;
+        for (int c0 = 0; c0 < nch && ok; c0 += 32) {
+            const int c = c0 + lane;
+            if (c < nch) {
+                const int ul = c / cpu, j = c - ul * cpu;
+                const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;
+                const size_t e = (size_t)S.touched[i];
+                const uint8_t* src;
+                int n;
+                if (j < cptg) {
+                    const int rb = g ? RBh + hb : hb, u0 = j * st;
+                    src = io.wgu + ((e * RBg + rb) * KBg + kb0 + u0) * kTileBytes;
+                    n = KCg - u0 < st ? KCg - u0 : st;
+                } else {
+                    const int rbd = w + (j - cptg) * kUnitWorkers;
+                    src = io.wd + ((e * RBd + rbd) * KBd + 2 * hb) * kTileBytes;
+                    n = 2;
+                }
+                S.ctab_p[g][lane] = src;
+                S.ctab_n[g][lane] = n;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                int& slot = pp.slot;
+                int& phase = pp.phase;
+                int& cidx = pp.cidx;
+                const int m = nch - c0 < 32 ? nch - c0 : 32;
+                for (int j = 0; j < m; ++j) {
+                    ++cidx;
+                    if (++slot == ns) {
+                        slot = 0;
+                        phase ^= 1;
+                    }
+                    if (s_abort || (cidx >= ns && !mbar_wait(empty_bar(g, slot), phase ^ 1)) || s_abort) {
+                        fail();
                         ok = false;
                         break;
                     }
+                    const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * kTileBytes);
+                    S.slot_chunk[g * ns + slot] = cidx;
+                    mbar_arrive_expect_tx(full_bar(g, slot), bytes);
+                    bulk_g2s(sbase + slot_addr(g, slot), S.ctab_p[g][j], bytes, full_bar(g, slot));
                 }
             }
-            if (!ok) {
-                record_status(a.status, kStatusTimeout);
-                S.abort = 1;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int grp = warp / kGroupWarps, w8 = warp % kGroupWarps;
+    const int gtid = tid - grp * kGroupThreads, w = 2 * rank + grp;
+    const int ndn = w < RBd ? (RBd - w + kUnitWorkers - 1) / kUnitWorkers : 0;
+    auto group_sync = [&]() { named_sync(2 + grp, kGroupThreads); };
+    const uint8_t* ax_q = dsm + a.off_ax;                                    // [T][H]
+    const int2* ax_s = reinterpret_cast<const int2*>(ax_q + (size_t)T * H);  // [T][Gx]
+    uint8_t* hq = dsm + a.off_h + grp * a.h_bytes;                           // [T][128] codes
+    int2* hs = reinterpret_cast<int2*>(hq + (size_t)T * kTileRows);          // [T][4]
+    const float* pbuf = reinterpret_cast<const float*>(dsm + a.off_p);      // [2][workers][T][128]
+    cp_async_wait_all();
+    named_sync(1, kConsumerThreads);
+    bool live = !s_abort;
+    // warp 0 of group 0 keeps this CTA's exchange barriers armed (its lane 0
+    // arms them); it waits on every phase, even after a failure elsewhere,
+    // so that it never arms a phase twice.  armok is uniform in the warp.
+    const bool arm_warp = grp == 0 && w8 == 0;
+    bool armok = true;
+    int& slot = pp.slot;
+    int& phase = pp.phase;
+    const int r_lane = lane >> 1, h_lane = lane & 1;
+    const int lrow = w8 * 16 + r_lane;
+    const int code_off = w8 * 512 + lane * 16;
+    const int scale_off = kTileCodeBytes + w8 * 64 + lane * 2;
+    auto next_chunk = [&]() -> const uint8_t* {
+        if (++slot == ns) {
+            slot = 0;
+            phase ^= 1;
+        }
+        if (live && (s_abort || !mbar_wait(full_bar(grp, slot), phase))) {
+            fail();
+            live = false;
+        }
+        return dsm + slot_addr(grp, slot);
+    };
+    auto free_chunk = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(grp, slot));
+    };
+
+    // Items i0 .. i1 - 1 of output columns rbd*128 .. +127 of token t: the
+    // residual plus the k slots' parts (slot order, then h-block order).  sp
+    // threads share an item, each a contiguous range of the parts (the first
+    // also the residual), the ranges' sums added by a butterfly.
+    auto combine_piece = [&](int t, int rbd, int i0, int i1) {
+        const int n_it = i1 - i0, P = k * RBh;
+        int sp = 1;
+        while (sp < 8 && n_it * 2 * sp <= kGroupThreads && 2 * sp <= P) sp *= 2;
+        const int sub = gtid % sp, it = i0 + gtid / sp;
+        const int pa = P * sub / sp, pe = P * (sub + 1) / sp;
+        const bool mine = it < i1;
+        const int col = rbd * kTileRows + (mine ? it : i0);
+        float v = mine && sub == 0 ? bf16_bits_to_float(io.x_res[(size_t)t * H + col]) : 0.f;
+        const int* sp_t = S.slotpos + t * k;
+        int j = pa / RBh, hb2 = pa - (pa / RBh) * RBh;
+#pragma unroll 1
+        for (int p0 = pa; p0 < pe; p0 += 8) {
+            float part[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) {
+                part[z] = 0.f;
+                if (mine && p0 + z < pe) {
+                    part[z] = __ldcg(a.y_part + ((size_t)hb2 * Tk + sp_t[j]) * H + col);
+                    if (++hb2 == RBh) {
+                        hb2 = 0;
+                        ++j;
+                    }
+                }
+            }
+#pragma unroll
+            for (int z = 0; z < 8; ++z) v += part[z];
+        }
+        for (int o = 1; o < sp; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (mine && sub == 0) {
+            const size_t o = (size_t)t * H + col;
+            if (io.out_fp32) static_cast<float*>(io.out)[o] = v;
+            else static_cast<uint16_t*>(io.out)[o] = float_to_bf16_bits(v);
+        }
+    };
+
+    auto unit = [&](auto ntc, int ul) {
+        constexpr int NT = decltype(ntc)::value;
+        const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;
+        const int e = S.touched[i], off = S.off[e], c = S.off[e + 1] - off;
+        const int pb = ul & 1;
+        const uint32_t ppar = (uint32_t)((ul >> 1) & 1);
+        if (arm_warp && armok && lane == 0)
+            mbar_arrive_expect_tx(pbar(pb), (uint32_t)(kUnitWorkers * c * kTileRows * 4));
+        // ------------------------------------------------ gate/up K part
+        const int rb = grp ? RBh + hb : hb;
+        const int row = rb * kTileRows + lrow;
+        constexpr int NH = NT <= 4 ? NT : 1;
+        int arow[NH], srow[NH];
+#pragma unroll
+        for (int n = 0; n < NH; ++n) {
+            const int ar = S.btok[off + (n < c ? n : 0)];
+            arow[n] = ar * H;
+            srow[n] = ar * Gx;
+        }
+        float acc[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+        for (int jc = 0; jc < cptg; ++jc) {
+            const int u0 = jc * st, nuj = KCg - u0 < st ? KCg - u0 : st;
+            const uint8_t* chunk = next_chunk();
+            if (live) {
+                for (int uu = 0; uu < nuj; ++uu) {
+                    const uint8_t* tile = chunk + uu * kTileBytes;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
+                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
+                                            wv.w & 0x0F0F0F0Fu};
+                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
+                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                    const int g = 2 * (kb0 + u0 + uu) + h_lane;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        if (n < c) {
+                            int ao, so;
+                            if constexpr (NT <= 4) {
+                                ao = arow[n];
+                                so = srow[n];
+                            } else {
+                                const int ar = S.btok[off + n];
+                                ao = ar * H;
+                                so = ar * Gx;
+                            }
+                            const int2 sc = ax_s[so + g];
+                            const int dot = group_dot(wl, wh, ax_q + ao + g * kGroup, sc.y);
+                            acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
+                            if (DOTS) a.dots_gu[((size_t)(off + n) * 2 * I + row) * Gx + g] = dot;
+                        }
+                    }
+                }
+            }
+            free_chunk();
+        }
+        // the K part's row sums to every CTA of the cluster: lane 8q sends
+        // rows 4q' .. 4q' + 3 of its warp (the lane pairs' sums)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            if (n < c) {
+                const float v = acc[n] + __shfl_xor_sync(0xffffffffu, acc[n], 1);
+                const float v1 = __shfl_down_sync(0xffffffffu, v, 2);
+                const float v2 = __shfl_down_sync(0xffffffffu, v, 4);
+                const float v3 = __shfl_down_sync(0xffffffffu, v, 6);
+                if ((lane & 7) == 0) {
+                    const uint32_t la =
+                        sbase + a.off_p + 4u * ((((pb * kUnitWorkers + w) * T + n) * kTileRows) + lrow);
+#pragma unroll
+                    for (int d = 0; d < kClusterCTAs; ++d)
+                        st_async_v4(mapa_shared(la, d), v, v1, v2, v3, mapa_shared(pbar(pb), d));
+                }
             }
         }
-        __syncthreads();
-    };
-    Pipe pp{-1, 0, -1};
-    for (int l = 0; l < A.L; ++l) {
-        const uint16_t* xin = l == 0 ? A.x0 : A.xbuf[(l - 1) & 1];
-        const bool last = l == A.L - 1;
-        const LayerIO io{xin, A.wgu[l], A.wd[l], last ? A.out : (void*)A.xbuf[l & 1], last ? A.out_fp32 : 0};
-        // prep: the counters of this layer (nobody reads the last layer's
-        // any more), then this CTA's router rows
-        for (int i = b * kLayerThreads + tid; i < A.pa.nsync; i += G * kLayerThreads) A.pa.sync[i] = 0;
-        if (tid < kPrepThreads && nrows) {
-            if (!mbar_wait(wrbar, l & 1)) record_status(a.status, kStatusTimeout);
-            for (int j = 0; j < nrows; ++j) prep_row(A.pa, xin, b + j * G, E, wrow + (size_t)j * H, s_red, s_r);
+        // ------------------------------------- h (every K part has arrived)
+        if (arm_warp ? armok : live) {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(pbar(pb), ppar));
+            if (!ok) {
+                armok = false;
+                if (live) fail();
+                live = false;
+            } else if (live && s_abort) {
+                live = false;
+            }
         }
-        grid_sync();
-        if (tid == 0 && nrows && l + 1 < A.L) stage_rows(l + 1);  // its rows are read
-        layer_body<MAXNT, false>(a, io, S, dsm, pp);
-        grid_sync();
+        for (int n = w8; n < c; n += kGroupWarps) {  // warp n: bucket row n, lane: 4 features
+            const int f = 4 * lane;
+            float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < kClusterCTAs; ++r) {
+                const float4 g4 = *reinterpret_cast<const float4*>(
+                    pbuf + (((pb * kUnitWorkers + 2 * r) * T + n) * kTileRows + f));
+                const float4 u4 = *reinterpret_cast<const float4*>(
+                    pbuf + (((pb * kUnitWorkers + 2 * r + 1) * T + n) * kTileRows + f));
+                gv[0] += g4.x; gv[1] += g4.y; gv[2] += g4.z; gv[3] += g4.w;
+                uv[0] += u4.x; uv[1] += u4.y; uv[2] += u4.z; uv[3] += u4.w;
+            }
+            float h[4], amax = 0.f;
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                h[z] = gv[z] / (1.0f + __expf(-gv[z])) * uv[z];
+                amax = fmaxf(amax, fabsf(h[z]));
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const uint16_t db = act_scale_bits(amax);
+            const float d = half_bits_to_float(db);
+            uint32_t w4 = 0u;
+            int sum = 0;
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const int qv = act_code(h[z], d);
+                sum += qv;
+                w4 |= ((uint32_t)qv & 0xffu) << (8 * z);
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const uint32_t w4o = __shfl_xor_sync(0xffffffffu, w4, 1);
+            if ((lane & 1) == 0) *reinterpret_cast<uint2*>(hq + n * kTileRows + f) = permute_chunk(w4, w4o);
+            if ((lane & 7) == 0) hs[n * 4 + lane / 8] = make_int2(__float_as_int(d), -8 * sum);
+            if (a.write_qh && w == 0) {
+                const size_t prow = (size_t)(off + n);
+                *reinterpret_cast<uint32_t*>(a.q_h + prow * I + hb * kTileRows + f) = w4;
+                if ((lane & 7) == 0) a.d_h[prow * Gh + hb * 4 + lane / 8] = db;
+            }
+        }
+        group_sync();
+        // ------------------------------------------- down row blocks
+        for (int dd = 0; dd < ndn; ++dd) {
+            const int rbd = w + dd * kUnitWorkers;
+            const uint8_t* chunk = next_chunk();
+            float accd[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) accd[n] = 0.f;
+            if (live) {
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint8_t* tile = chunk + kt * kTileBytes;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
+                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
+                                            wv.w & 0x0F0F0F0Fu};
+                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
+                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                    const int gl = 2 * kt + h_lane;
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        if (n < c) {
+                            const int2 sc = hs[n * 4 + gl];
+                            const int dot = group_dot(wl, wh, hq + n * kTileRows + gl * kGroup, sc.y);
+                            accd[n] = fmaf((float)dot, dw * __int_as_float(sc.x), accd[n]);
+                            if (DOTS)
+                                a.dots_d[((size_t)(off + n) * H + rbd * kTileRows + lrow) * Gh + hb * 4 + gl] = dot;
+                        }
+                    }
+                }
+            }
+            free_chunk();
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const float v = accd[n] + __shfl_xor_sync(0xffffffffu, accd[n], 1);
+                if (n < c && h_lane == 0 && live)
+                    a.y_part[((size_t)hb * Tk + off + n) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
+            }
+        }
+        // ------------------------------------- counts of the parts stored
+        group_sync();  // the group's stores of y come before its counts
+        for (int r = gtid; r < ndn * c; r += kGroupThreads) {
+            const int dd = r / c, n = r - dd * c;
+            red_release_add(&a.ticket[S.btok[off + n] * RBd + w + dd * kUnitWorkers], 1);
+        }
+    };
+
+    for (int ul = 0; ul < nu; ++ul) {
+        const int u = ub0 + ul, i = u / RBh;
+        const int e = S.touched[i], c = S.off[e + 1] - S.off[e];
+        if (c <= 1) unit(IntC<1>{}, ul);
+        else if (c <= 2) unit(IntC<2>{}, ul);
+        else if (c <= 4 || MAXNT <= 4) unit(IntC<4 < MAXNT ? 4 : MAXNT>{}, ul);
+        else unit(IntC<MAXNT>{}, ul);
     }
+    // every byte sent to this CTA has arrived before it may leave (the
+    // arming warp waited on every phase unless one ran out of time)
+    if (arm_warp && !armok && lane == 0) fail();
+
+    // ------------------------------------------------------------ combine
+    // Block (t, rbd) = token t's output columns rbd*128 .. +127, cut into np
+    // pieces; piece pc of the T * RBd * np belongs to worker pc * V / pieces
+    // (at most one each), which takes it after its own units once the
+    // block's count shows all k * RBh parts stored.
+    {
+        const int V = 2 * gridDim.x, v = 2 * blockIdx.x + grp, P = k * RBh, nb = T * RBd;
+        int np = 1;
+        while (np * 2 <= kTileRows / 32 && nb * np * 2 <= V && kTileRows * P > 2048 * np) np *= 2;
+        const int npc = nb * np;
+        const int p0 = (int)(((long long)v * npc + V - 1) / V);
+        const int p1 = (int)(((long long)(v + 1) * npc + V - 1) / V);
+        for (int pc = p0; pc < p1; ++pc) {
+            const int blk = pc / np, q = pc - blk * np;
+            if (gtid == 0) {
+                const int* cnt = &a.ticket[blk];
+                bool got = !s_abort;
+                if (got && ld_acquire(cnt) < P) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (ld_acquire(cnt) < P) {
+                        if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            got = false;
+                            break;
+                        }
+                    }
+                }
+                if (!got) fail();
+                S.flag[grp] = got ? 1 : 0;
+            }
+            group_sync();
+            if (S.flag[grp])
+                combine_piece(blk / RBd, blk - (blk / RBd) * RBd, q * kTileRows / np, (q + 1) * kTileRows / np);
+            group_sync();  // the flag is reused
+        }
+    }
+}
+
+// One decode layer by clusters of kClusterCTAs CTAs, one CTA per SM,
+// launched cooperatively (the combine waits on other clusters).  MAXNT: the
+// most tokens a bucket may hold (T <= MAXNT).
+template <int MAXNT, bool DOTS>
+__global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ LayerShared S;
+    if (threadIdx.x == 0) {
+        const uint32_t sbase = smem_u32(dsm);
+        for (int pb = 0; pb < 2; ++pb) mbar_init(sbase + a.off_bar + 8u * (4 * a.ns + pb), 1);
+    }
+    ring_init(a, S, dsm);  // (its thread 0 fences the barrier inits for the cluster)
+    __syncthreads();
+    cluster_sync_all();  // the peers' exchange barriers exist before anyone sends
+    pdl_wait();          // the prep kernel's logits, codes and cleared tickets
+    pdl_trigger();
+    Pipe pp{-1, 0, -1};
+    const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
+    cluster_body<MAXNT, DOTS>(a, io, S, dsm, pp);
     ring_drain(a, S, dsm);
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while its peer may still address it
 }
 
 // ---------------------------------------------------------------- launch
 int g_layer_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
+// clustered kernel: 0 unknown, 1 cluster + cooperative + PDL accepted, 2 without
+// PDL, 3 not accepted (the task kernel runs instead)
+int g_cluster_mode[64] = {};
 int g_prep_carveout[64] = {};
 
 struct Plan {
     int ns, st, off_bar, off_ax, off_ah, ah_bytes, off_red, smem;
+    int off_p, off_h, h_bytes;  // clustered kernel
 };
 
 int al128(long long v) { return (int)((v + 127) & ~127ll); }
@@ -1384,7 +1785,7 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
     // three of them (fewer chunk hand-offs), else two-tile slots (one token:
     // short tasks, deeper ring), else the largest slot that still gives each
     // group's ring two slots, else one
-    int st = T >= 4 && rest >= (long long)kGroups * 3 * 4 * kTileBytes ? 4 : 2;
+    int st = T >= 4 && rest >= (long long)kGroups * 3 * kSlotTiles * kTileBytes ? kSlotTiles : 2;
     while (st > 1 && rest < (long long)kGroups * 2 * st * kTileBytes) st /= 2;
     int ns = (int)(rest / ((long long)st * kTileBytes)) / kGroups;  // slots of each group's ring
     ns = ns > kMaxSlots / kGroups ? kMaxSlots / kGroups : ns;
@@ -1402,7 +1803,43 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
     return (long long)T * E * 8 <= p->off_ax;
 }
 
+// Shared-memory plan of the clustered layer kernel; false if it does not
+// fit (or T exceeds kClusterMaxT).  Layout: the two rings, the K-part
+// exchange buffers [2][workers][T][128] fp32, the groups' h buffers, the
+// codes of x, the barriers (rings, then the two exchange barriers).
+bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p) {
+    (void)I;
+    if (T < 1 || T > kClusterMaxT) return false;
+    if ((H / kTileK) % kClusterCTAs) return false;
+    const long long ax = al128((long long)T * H + (long long)T * (H / kGroup) * 8);
+    const long long pbytes = al128(2ll * kUnitWorkers * T * kTileRows * 4);
+    const long long hbytes = al128((long long)T * kTileRows + (long long)T * 4 * 8);
+    const long long rest = budget - ax - pbytes - 2 * hbytes - (4ll * kMaxSlots + 2) * 8 - 256;
+    const int st = T >= 4 && rest >= (long long)kGroups * 3 * kSlotTiles * kTileBytes ? kSlotTiles : 2;
+    int ns = (int)(rest / ((long long)st * kTileBytes)) / kGroups;
+    ns = ns > kMaxSlots / kGroups ? kMaxSlots / kGroups : ns;
+    if (ns < 2) return false;
+    p->ns = ns;
+    p->st = st;
+    p->off_p = kGroups * ns * st * kTileBytes;
+    p->off_h = p->off_p + (int)pbytes;
+    p->h_bytes = (int)hbytes;
+    p->off_ax = al128(p->off_h + 2 * hbytes);
+    p->off_bar = al128(p->off_ax + ax);
+    p->smem = p->off_bar + (4 * ns + 2) * 8;
+    p->off_ah = p->off_red = p->ah_bytes = 0;
+    // the routing scratch (logits and keys) stays below the exchange
+    // buffers, which a peer may fill while this CTA still routes
+    return (long long)T * E * 8 <= p->off_p;
+}
+
 __global__ void coop_pdl_probe_kernel(int* p) {
+    pdl_wait();
+    if (p && threadIdx.x == 0 && blockIdx.x == 0) *p = 1;
+}
+
+__global__ void cluster_probe_kernel(int* p) {
+    cluster_sync_all();
     pdl_wait();
     if (p && threadIdx.x == 0 && blockIdx.x == 0) *p = 1;
 }
@@ -1437,6 +1874,26 @@ cudaError_t decode_prepare_device(int dev) {
         cudaGetLastError();  // refused: a launch error only, the context is intact
         mode = 2;
     }
+    // a cooperative launch in clusters of kClusterCTAs, with PDL, else without
+    cudaLaunchAttribute ac[3];
+    ac[0].id = cudaLaunchAttributeClusterDimension;
+    ac[0].val.clusterDim.x = kClusterCTAs;
+    ac[0].val.clusterDim.y = 1;
+    ac[0].val.clusterDim.z = 1;
+    ac[1] = at[0];
+    ac[2] = at[1];
+    cfg.gridDim = dim3(2 * kClusterCTAs);
+    cfg.attrs = ac;
+    int& cm = g_cluster_mode[dev & 63];
+    for (int na = 3; na >= 2 && cm == 0; --na) {
+        cfg.numAttrs = na;
+        err = cudaLaunchKernelEx(&cfg, cluster_probe_kernel, (int*)nullptr);
+        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, cluster_probe_kernel, (int*)nullptr);
+        if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+        if (err == cudaSuccess) cm = na == 3 ? 1 : 2;
+        else cudaGetLastError();
+    }
+    if (cm == 0) cm = 3;
     cudaStreamDestroy(st);
     return cudaSuccess;
 }
@@ -1466,7 +1923,16 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
 
 int decode_sync_ints(int T, int H, int I, int E, int k) {
     const int nslot = std::min(E, T * k);
-    return nslot * (I / kTileRows) + H / kTileRows;
+    // the task kernel's counters, or the clustered kernel's tickets
+    return std::max(nslot * (I / kTileRows) + H / kTileRows, T * (H / kTileRows));
+}
+
+int decode_y_parts(int T, int H, int I, int E, int k) {
+    int cap_g, cap_d, nsg, nsd;
+    decode_split_bounds(T, H, I, E, k, &cap_g, &cap_d, &nsg, &nsd);
+    Plan p;
+    const int ncl = plan_cluster(T, H, I, E, kLayerSmemBudget, &p) ? I / kTileRows : 0;
+    return std::max(nsd, ncl);
 }
 
 namespace {
@@ -1514,6 +1980,7 @@ LayerArgs make_layer_args(int T, int H, int I, int E, int k, const Workspace& ws
     const int nslot = std::min(E, T * k);
     a.cnt_h = ws.sync;
     a.cnt_y = ws.sync + nslot * (I / kTileRows);
+    a.ticket = ws.sync;
     a.cap_g = ws.cap_g;
     a.cap_d = ws.cap_d;
     // the K splits the kernel may choose: divisors of the row's 64-column
@@ -1563,15 +2030,52 @@ cudaError_t launch_coop(void (*kern)(Args), const Args& args, int num_sms, int s
     return cudaSuccess;
 }
 
-__global__ void decode_stack_clear_kernel(int* gbar) {
-    pdl_wait();
-    pdl_trigger();
-    if (threadIdx.x == 0) *gbar = 0;
-}
+int g_cluster_max[64] = {};  // co-resident clusters of the clustered kernel (0: not asked yet)
 
-// Dynamic shared memory the stack kernel may use (its static part, ~14.7 KB,
-// and this stay within the 227 KB a CTA may have).
-constexpr long long kStackSmemMax = 212 * 1024;
+// A cooperative launch of the clustered layer kernel: clusters of
+// kClusterCTAs CTAs, as many as the device holds at once (at most one CTA per
+// SM), with programmatic dependent launch where the device accepts it.
+cudaError_t launch_cluster(void (*kern)(LayerArgs), const LayerArgs& args, int num_sms, int smem, int dev,
+                           cudaStream_t s) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute at[3];
+    cfg.blockDim = dim3(kLayerThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kClusterCTAs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    at[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[2].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    int ncl = num_sms / kClusterCTAs;
+    int& mx = g_cluster_max[dev & 63];
+    if (mx == 0) {
+        cfg.gridDim = dim3(ncl * kClusterCTAs);
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+            mx = n;
+        } else {
+            cudaGetLastError();
+            mx = ncl;
+        }
+    }
+    ncl = std::min(ncl, mx);
+    if (ncl < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(ncl * kClusterCTAs);
+    cfg.numAttrs = g_cluster_mode[dev & 63] == 1 ? 3 : 2;
+    if ((err = cudaLaunchKernelEx(&cfg, kern, args)) != cudaSuccess) {
+        cudaGetLastError();
+        return err;
+    }
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -1625,6 +2129,22 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.dots_d = dots_d;
     a.write_qh = write_qh ? 1 : 0;
     const bool dots = dots_gu || dots_d;
+    Plan cplan;
+    if (g_cluster_mode[dev & 63] <= 2 && plan_cluster(T, H, I, E, kLayerSmemBudget, &cplan)) {
+        a.ns = cplan.ns;
+        a.st = cplan.st;
+        a.off_bar = cplan.off_bar;
+        a.off_ax = cplan.off_ax;
+        a.off_p = cplan.off_p;
+        a.off_h = cplan.off_h;
+        a.h_bytes = cplan.h_bytes;
+        void (*kern)(LayerArgs) = dots ? decode_cluster_kernel<kClusterMaxT, true>
+                                       : decode_cluster_kernel<kClusterMaxT, false>;
+        if ((err = launch_cluster(kern, a, num_sms, cplan.smem, dev, s)) != cudaSuccess) return err;
+        for (int i = 2; i <= 6; ++i)
+            if ((err = mark(i)) != cudaSuccess) return err;
+        return cudaGetLastError();
+    }
     void (*kern)(LayerArgs) =
         T <= 16 ? (dots ? decode_layer_kernel<16, true> : decode_layer_kernel<16, false>)
                 : (dots ? decode_layer_kernel<MOE_DECODE_MAX_T, true> : decode_layer_kernel<MOE_DECODE_MAX_T, false>);
@@ -1634,50 +2154,24 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     return cudaGetLastError();
 }
 
-bool decode_stack_fits(int T, int H, int I, int E, int num_sms) {
-    if (num_sms <= 0) return false;
-    Plan plan;
-    const long long rows = (E + num_sms - 1) / num_sms;
-    return plan_layer(T, H, I, E, kStackSmemMax - al128(rows * H * 4) - 128, &plan);
-}
-
 cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr,
                                 const void* const* wgu, const void* const* wd, int T, int H, int I,
                                 int E, int k, bool prenorm, bool out_fp32, void* out,
                                 const Workspace& ws, int* status, int num_sms, cudaStream_t s) {
     if (T == 0 || L == 0) return cudaSuccess;
     if (L > MOE_DECODE_MAX_LAYERS) return cudaErrorInvalidValue;
-    const long long rows = (E + num_sms - 1) / num_sms;
-    const long long wr_bytes = al128(rows * H * 4);
-    Plan plan;
-    if (!plan_layer(T, H, I, E, kStackSmemMax - wr_bytes - 128, &plan)) return cudaErrorInvalidValue;
-    cudaError_t err;
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    StackArgs A{};
-    A.la = make_layer_args(T, H, I, E, k, ws, plan, status);
-    A.pa = make_prep_args(T, H, I, E, k, prenorm, ws, status);
+    // layer l reads layer l - 1's bf16 output from one workspace buffer and
+    // writes the other; each layer's prep kernel waits for the layer before
+    const uint16_t* cur = x;
     for (int l = 0; l < L; ++l) {
-        A.wr[l] = wr[l];
-        A.wgu[l] = static_cast<const uint8_t*>(wgu[l]);
-        A.wd[l] = static_cast<const uint8_t*>(wd[l]);
+        const bool last = l == L - 1;
+        void* dst = last ? out : static_cast<void*>(l % 2 ? ws.xbuf1 : ws.xbuf0);
+        cudaError_t err = launch_decode(cur, wr[l], wgu[l], wd[l], T, H, I, E, k, prenorm, last && out_fp32,
+                                        dst, ws, nullptr, nullptr, false, status, num_sms, nullptr, false, s);
+        if (err != cudaSuccess) return err;
+        cur = static_cast<const uint16_t*>(dst);
     }
-    A.L = L;
-    A.x0 = x;
-    A.xbuf[0] = ws.xbuf0;
-    A.xbuf[1] = ws.xbuf1;
-    A.out = out;
-    A.out_fp32 = out_fp32 ? 1 : 0;
-    A.gbar = ws.gbar;
-    A.off_wr = al128(plan.smem);
-    const int smem = A.off_wr + (int)wr_bytes;
-    if ((err = launch_pdl(decode_stack_clear_kernel, dim3(1), dim3(32), 0, s, ws.gbar)) != cudaSuccess) {
-        cudaGetLastError();
-        return err;
-    }
-    void (*kern)(StackArgs) = T <= 16 ? decode_stack_kernel<16> : decode_stack_kernel<MOE_DECODE_MAX_T>;
-    if ((err = launch_coop(kern, A, num_sms, smem, dev, s)) != cudaSuccess) return err;
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace moeq4

@@ -46,11 +46,10 @@ struct Workspace {
     float* gu_part;         // [nsg, T*k, 2I] K parts of the gate/up row sums, bucket order
     int8_t* q_h;            // [T*k, I]      (stage output)
     uint16_t* d_h;          // [T*k, I/32]
-    float* y_part;          // [nsd, T*k, H] K parts of the weighted expert outputs
+    float* y_part;          // [parts, T*k, H] parts of the weighted expert outputs
     int32_t* sync;          // counters of the layer kernel, cleared by its prep kernel
     uint16_t* xbuf0;        // [T, H] decode stack: layer outputs inside the stack (ping-pong)
     uint16_t* xbuf1;
-    int32_t* gbar;          // decode stack: grid barrier arrivals
     int cap_g, cap_d;       // bounds of the K splits (part buffers hold that many)
     int max_tiles;
     int tile_n;             // tokens per GEMM tile (prefill)
@@ -127,15 +126,12 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
                           void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
                           bool write_qh, int* status, int num_sms, void** events, bool capturing,
                           cudaStream_t s);
-// L stacked decode layers in one cooperative launch (after a kernel that
-// zeroes the grid barrier counter): layer l + 1 reads layer l's bf16 output,
-// the last writes `out`.  wr/wgu/wd: host arrays of L device pointers.
+// L chained decode layers: per layer the prep and layer kernels, linked by
+// programmatic dependent launch; layer l + 1 reads layer l's bf16 output.
 cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr,
                                 const void* const* wgu, const void* const* wd, int T, int H, int I,
                                 int E, int k, bool prenorm, bool out_fp32, void* out,
                                 const Workspace& ws, int* status, int num_sms, cudaStream_t s);
-// Whether the decode stack kernel's on-chip staging fits this shape.
-bool decode_stack_fits(int T, int H, int I, int E, int num_sms);
 // Once per device, outside any stream capture: decides whether a cooperative
 // launch may also carry the programmatic-dependent-launch attribute.
 cudaError_t decode_prepare_device(int dev);
@@ -149,6 +145,9 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
                          int* nsd_max);
 // Counters the decode prep kernel clears.
 int decode_sync_ints(int T, int H, int I, int E, int k);
+// Parts of the weighted expert outputs the decode layer may store (the
+// y_part buffer holds that many [T*k, H] planes).
+int decode_y_parts(int T, int H, int I, int E, int k);
 // xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), one warp per token.
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
                            cudaStream_t s);

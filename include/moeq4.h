@@ -247,7 +247,10 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
  * (programmatic dependent launch): a prep kernel (router logits, int8 codes
  * of x, and the clearing of the counters the layer kernel synchronises on)
  * and a cooperative layer kernel (one CTA per SM: top-k, buckets, gate/up,
- * h, down and the combine).  The prep kernel reads `wr` before the work that
+ * h, down and the combine).  For T <= 8 the layer kernel runs in clusters
+ * of two CTAs that share each (expert, 128-feature block of h) unit through
+ * distributed shared memory; for larger T it splits the experts' rows and K
+ * ranges over all CTAs.  The prep kernel reads `wr` before the work that
  * precedes it on the stream has finished, so `wr` must not be written by the
  * kernel launched immediately before this call on the same stream; x, the
  * output and the workspace are touched only after that work has finished.
@@ -263,11 +266,14 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
 
 /*
  * moe_w4a8_forward_decode_stack — L consecutive decode layers (each adds its
- * expert output to its input, the residual stream) in one cooperative
- * launch: the pages' per-token decode loop over the MoE layers.  Layer l + 1
- * reads layer l's output rounded to bf16; the result equals, bit for bit, L
- * moe_w4a8_forward_decode calls chained through bf16 outputs with the same
- * flags (MOE_OUT_FP32 applies to the last layer only).
+ * expert output to its input, the residual stream) from one call: the
+ * pages' per-token decode loop over the MoE layers.  The call enqueues each
+ * layer's two kernels on the stream, every kernel linked to the one before
+ * by programmatic dependent launch (the next layer's router row is staged
+ * while the layer before still runs).  Layer l + 1 reads layer l's output
+ * rounded to bf16; the result equals, bit for bit, L moe_w4a8_forward_decode
+ * calls chained through bf16 outputs with the same flags (MOE_OUT_FP32
+ * applies to the last layer only).
  *   x_bf16     [T, H] input of layer 0 (not written)
  *   L          1 <= L <= MOE_DECODE_MAX_LAYERS
  *   wr, wgu_packed, wd_packed
@@ -275,12 +281,11 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr,
  *              moe_w4a8_forward_decode (the arrays are read during the call)
  *   out        the last layer's output; may not alias x
  *   workspace  >= moe_workspace_bytes(MOE_MODE_DECODE, T, H, I, E, k) bytes
- * Each layer clears its own counters inside the launch and a small kernel
- * before it zeroes the grid barrier, so nothing in the workspace has to
- * survive between calls.  Shapes must fit the decode staging (as for
- * moe_w4a8_forward_decode, with the CTA's router rows, E / SMs rounded up,
- * also staged: MOE_ERR_SHAPE otherwise).  Routing, codes and sums follow
- * the single-layer call exactly; no stage outputs are written.
+ * Each layer clears its own counters in its first kernel, so nothing in the
+ * workspace has to survive between calls; the layers' intermediate outputs
+ * live in the workspace.  Shapes as for moe_w4a8_forward_decode.  Routing,
+ * codes and sums follow the single-layer call exactly; no stage outputs are
+ * written.
  */
 int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* const* wr,
                                   const void* const* wgu_packed, const void* const* wd_packed,
@@ -302,7 +307,8 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
  * cudaMalloc, cudaFree or allocating library routine is called.
  *   - Shapes whose workspace (moe_workspace_bytes(MOE_MODE_DECODE, ...)) is
  *     larger than the array are rejected with MOE_ERR_WORKSPACE; 8 MiB covers
- *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8 (5.4 MiB at T = 32).
+ *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8 (6.2 MiB at most, at
+ *     T = 8).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.

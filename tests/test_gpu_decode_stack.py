@@ -1,18 +1,18 @@
-"""GPU: the stacked decode kernel (moe_w4a8_forward_decode_stack) through the
+"""GPU: the stacked decode entry (moe_w4a8_forward_decode_stack) through the
 C ABI, against the chain of single-layer decode calls, bit for bit.
 
 The per-token decode loop of the page "A 35B Hybrid-Attention Mixture-of-
 Experts Model on a 6GB 2011 GPU" (Methodology 1, "Decode (CPU)"): every
 generated token runs through every layer's experts.  The stack runs the same
-arithmetic as the single-layer call (the same prep and layer code, layer
+kernels as the single-layer call, one call enqueueing all layers (layer
 l + 1 reading layer l's output rounded to bf16), so its output must equal the
 chained calls' bits; the single-layer path is pinned to the oracle by the
 layer tests and along the oracle's own chain (the decode-chain test), and one
 case here also follows the oracle's chain directly.
 
-Cases: the first 8 layers of the stacked workload (E = 256, so some CTAs hold
-two router rows) at T = 1, 4, 16 and 32 (the T > 16 variant); three E = 128
-layers (some CTAs hold none); fp32 and bf16 last outputs, with and without
+Cases: the first 8 layers of the stacked workload (E = 256) at T = 1, 4
+(clustered layer kernel), 16 and 32 (the task kernel and its T > 16
+variant); three E = 128 layers; fp32 and bf16 last outputs, with and without
 the pre-norm; a stack of one; repeated calls, a garbage-filled workspace and
 a captured graph replay.
 """
