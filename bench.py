@@ -34,9 +34,19 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # it is in this tree: the decode prep and layer kernels (T=1) and the prefill
 # expert GEMMs (T=2048).  Set to None when a kernel changes before a new
 # capture.
-NCU_TRAFFIC_DECODE_LAYER_T1 = 21_346_560 + 1_086_976  # layer + prep kernel, ncu, one launch each at T=1
+# DRAM bytes (read + write) of one decode layer at T=1 (prep, clustered and
+# combine kernels, one launch each under ncu); None until captured for the
+# current kernels
+NCU_TRAFFIC_DECODE_LAYER_T1 = None
 NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch at T=2048
-KERNELS_PER_DECODE_LAYER = 2   # prep (logits, x codes); layer (top-k, buckets, experts, combine)
+# kernels of one decode layer: prep (logits, x codes) and, for T <= 8, the
+# clustered expert kernel and the combine kernel; else the task kernel (top-k,
+# buckets, experts, combine)
+
+
+def kernels_per_decode_layer(T):
+    return 3 if T <= 8 else 2
+
 DECODE_WORKLOAD = ("decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 (batch-1 decode "
                    "config), in a chain of 16 pre-norm layers with distinct weight copies, "
                    "each layer decoding the previous one's bf16 output")
@@ -232,13 +242,14 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
         "layer_gbs": statistics.mean(layer_bytes) / (us_layer * 1e-6) / 1e9,
         "e2e_us_per_token": e2e_ms * 1e3 / (L * T),
         "h2d_bytes_per_step": T * li.H * 2, "d2h_bytes_per_step": T * li.H * 2,
-        "kernels_per_step": L * KERNELS_PER_DECODE_LAYER,
+        "kernels_per_step": L * kernels_per_decode_layer(T),
         "stack": {
-            "entry": "moe_w4a8_forward_decode_stack (one call: the L layers' 2L kernels, chained by PDL)",
+            "entry": "moe_w4a8_forward_decode_stack (one call: the L layers' kernels, chained by PDL)",
             "equals_chain_bits": stack_same, "ms_per_step": ms_stack,
             "us_per_layer": ms_stack * 1e3 / L, "us_per_token": ms_stack * 1e3 / (L * T),
             "layer_gbs": statistics.mean(layer_bytes) / (ms_stack * 1e3 / L * 1e-6) / 1e9,
-            "e2e_us_per_token": e2e_stack_ms * 1e3 / (L * T), "kernels_per_step": 2 * L,
+            "e2e_us_per_token": e2e_stack_ms * 1e3 / (L * T),
+            "kernels_per_step": L * kernels_per_decode_layer(T),
         },
     }
     del layers, outs, ws, g, gs
@@ -616,7 +627,8 @@ def main():
             "l2": "inputs larger than L2: each step touches ~360 MB of distinct weights",
             "parallelism": "replicas only" if world > 1 else "single GPU",
         },
-        "roofline": {"bound": "hbm", "kernel": "decode_prep_kernel + decode_layer_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_prep_kernel + decode_cluster_kernel + decode_combine_kernel",
                      "achieved": roof_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": roof_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC_DECODE_LAYER_T1,
                      "peak_source": peaks["source"] + " (copy)",

@@ -149,9 +149,9 @@ struct LayerArgs {
     int ns;             // slots of each group's ring
     int st;             // packed tiles per slot (kSlotTiles, or fewer for large T)
     int off_bar, off_ax, off_ah, ah_bytes, off_red;
-    // clustered layer kernel: tickets [T, H/128] (cleared by the prep kernel),
-    // the K-part exchange buffers and the groups' h buffers
-    int* ticket;
+    int32_t* slot_pos;  // [T*k] bucket row of (t, j) (CTA 0 stores it)
+    // clustered layer kernel: the K-part exchange buffers and the groups' h
+    // buffers
     int off_p, off_h, h_bytes;
 };
 
@@ -243,6 +243,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
 }
 
 constexpr int kPrepBarId = 4;  // named barrier of the row's 128 threads
+constexpr int kRouteBarId = 5; // named barrier of the four warps routing one token
 
 // The prep work of one CTA on threads 0..127, for every token of x: the
 // optional RMSNorm factor, then by `mode`
@@ -545,7 +546,8 @@ __device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, u
 // logits and their order keys sit in the still idle dynamic shared memory
 // below the codes of x.  split(warp, lane) runs on warps 0 .. 4*kGroups - 1
 // (the work split of the caller) while the other warps fill the buckets.
-template <typename Split>
+// ONE_TOKEN_PATH: a single token is routed by one warp instead.
+template <bool ONE_TOKEN_PATH, typename Split>
 __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, uint8_t* dsm,
                                             Split&& split) {
     int* s_idx = S.idx;
@@ -566,6 +568,96 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     const int Tk = T * k;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int b = blockIdx.x;
+    if (ONE_TOKEN_PATH && T == 1) {
+        // One token: warps 0..3 (expert e on thread e % 128) rank every
+        // expert's logit against all E (larger first, the lower index on a
+        // tie: the order of the general path); rank < k places it.  Warp 0
+        // then forms the softmax weights over the k choices exactly as the
+        // general path, and each choice's bucket row (the choices of lower
+        // index); every thread of the four warps forms the offsets of its
+        // experts (the choices below them).
+        if (warp < 4) {
+            float* s_lg = reinterpret_cast<float*>(dsm);
+            uint32_t* s_key = reinterpret_cast<uint32_t*>(s_lg + kMaxExperts);
+            uint32_t mk[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = tid + 128 * r;
+                const float v = e < E ? __ldcg(a.logits + e) : 0.f;
+                mk[r] = float_order_key(v);
+                if (e < E) {
+                    s_lg[e] = v;
+                    s_key[e] = mk[r];
+                } else if (e < ((E + 3) & ~3)) {
+                    s_key[e] = 0u;  // padding: never greater, never ranked before e < E
+                }
+            }
+            named_sync(kRouteBarId, 128);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = tid + 128 * r;
+                if (e < E) {
+                    int rank = 0;
+                    for (int q = 0; q < E; q += 4) {
+                        const uint4 kq = *reinterpret_cast<const uint4*>(s_key + q);
+                        rank += (kq.x > mk[r] || (kq.x == mk[r] && q < e)) ? 1 : 0;
+                        rank += (kq.y > mk[r] || (kq.y == mk[r] && q + 1 < e)) ? 1 : 0;
+                        rank += (kq.z > mk[r] || (kq.z == mk[r] && q + 2 < e)) ? 1 : 0;
+                        rank += (kq.w > mk[r] || (kq.w == mk[r] && q + 3 < e)) ? 1 : 0;
+                    }
+                    if (rank < k) s_idx[rank] = e;
+                }
+            }
+            named_sync(kRouteBarId, 128);
+            if (warp == 0) {
+                const int si = lane < k ? s_idx[lane] : 0;
+                const float v = lane < k ? s_lg[si] : 0.f;
+                const float m = __shfl_sync(0xffffffffu, v, 0);  // the largest
+                const float z = lane < k ? expf(v - m) : 0.f;
+                const float zs = warp_sum(z);
+                int pos = 0;  // choice j's bucket row: the choices of lower index
+                for (int q = 0; q < k; ++q) pos += __shfl_sync(0xffffffffu, si, q) < si ? 1 : 0;
+                if (lane < k) {
+                    const float sw = z / zs;
+                    s_w[lane] = sw;
+                    s_slotpos[lane] = pos;
+                    s_btok[pos] = 0;
+                    s_bsw[pos] = sw;
+                    s_touched[pos] = si;
+                    s_toff[pos] = pos;
+                    if (b == 0) {
+                        a.topk_idx[lane] = si;
+                        a.topk_w[lane] = sw;
+                        a.slot_pos[lane] = pos;
+                        a.bucket_token[pos] = 0;
+                        a.bucket_slot[pos] = lane;
+                        a.touched[pos] = si;
+                    }
+                }
+                if (lane == 0) {
+                    s_off[E] = k;
+                    s_toff[k] = k;
+                    s_nt = k;
+                    s_eqc = 1;
+                    if (b == 0) {
+                        a.offsets[E] = k;
+                        a.counters[kCntTouched] = k;
+                    }
+                }
+            }
+            for (int e = tid; e < E; e += 128) {
+                int c = 0;
+                for (int q = 0; q < k; ++q) c += s_idx[q] < e ? 1 : 0;
+                s_off[e] = c;
+                if (b == 0) a.offsets[e] = c;
+            }
+        }
+        __syncthreads();
+        if (warp < 4 * kGroups) split(warp, lane);
+        fence_proxy_async_smem();
+        __syncthreads();
+        return;
+    }
     float* s_lg = reinterpret_cast<float*>(dsm);                  // [T][E] logits, and
     uint32_t* s_key = reinterpret_cast<uint32_t*>(s_lg + T * E);  // their order keys, in
     for (int i = tid; i < T * E; i += kLayerThreads) {            // the still idle ring
@@ -693,6 +785,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
             if (b == 0) {
                 a.topk_idx[p] = e;
                 a.topk_w[p] = s_w[p];
+                a.slot_pos[p] = pos;
                 a.bucket_token[pos] = t;
                 a.bucket_slot[pos] = p % k;
             }
@@ -759,7 +852,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     }
 
     // ---------------------------------------------- routing (every CTA)
-    route_layer(a, S, dsm, [&](int warp, int lane) {
+    route_layer<false>(a, S, dsm, [&](int warp, int lane) {
         // Tasks are shared out by cost, a tile of touched slot i weighing
         // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
         // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
@@ -1299,14 +1392,13 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 //   down     worker w: row blocks w, w + kUnitWorkers, ... of W_d over the
 //            block's 128 columns: routing weight * row sums, the parts hb of
 //            y (one per h block)
-//   combine  a count per (token, 128-column block of the output) of the
-//            parts stored (k * I/128 of them); the block's items are cut into
-//            pieces, each owned by a fixed group of the grid, which waits for
-//            the count after its own units and adds the residual and the
-//            parts (slot order, then block order).
+// and a third kernel (decode_combine_kernel) adds, per output element, the
+// residual and the k * I/128 parts (slot order, then block order).
 // Units go to clusters in contiguous ranges of equal cost (a unit of slot i
-// weighs kTileCost + c_i per tile, all units have the same tiles).  The
-// combine waits on other clusters, so the launch is cooperative as well.
+// weighs kTileCost + c_i per tile, all units have the same tiles).  No CTA
+// waits for a CTA outside its cluster, so the launch need not be
+// cooperative (a cooperative launch would not start before the prep kernel
+// has drained, and costs ~3 us a layer).
 constexpr int kClusterCTAs = 2;
 constexpr int kUnitWorkers = kClusterCTAs * kGroups;
 constexpr int kClusterMaxT = 8;   // tokens per call of the clustered kernel
@@ -1316,7 +1408,8 @@ constexpr int kClusterMaxT = 8;   // tokens per call of the clustered kernel
 // kTileCost + c_i each, c_i = toff[i + 1] - toff[i]).  Monotone in q;
 // bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp calls it.
 __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
-                                               int lane) {
+                                               int lane, bool equal) {
+    if (equal) return (int)(((long long)q * nt * RBh + NC - 1) / NC);  // (all units weigh the same)
     using u64 = unsigned long long;
     const u64 tot = (u64)RBh * ((u64)kTileCost * nt + Tk);
     const u64 qt = (u64)q * tot;  // NC times the position
@@ -1360,11 +1453,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
         for (int i = tid; i < n16; i += kConsumerThreads)
             cp_async16(sbase + a.off_ax + 16 * i, a.xq + 16 * (size_t)i);
     }
-    route_layer(a, S, dsm, [&](int warp, int lane) {
+    route_layer<true>(a, S, dsm, [&](int warp, int lane) {
         if (warp == 0) {
             const int nt = S.nt;
-            const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane);
-            const int u1 = unit_bound_warp(cq + 1, NC, nt, Tk, RBh, S.toff, lane);
+            const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
+            const int u1 = unit_bound_warp(cq + 1, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
             if (lane == 0) {
                 S.bnd[0][0] = u0;
                 S.bnd[0][1] = u1;
@@ -1434,7 +1527,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 
     // ---------------------------------------------------------- consumers
     const int grp = warp / kGroupWarps, w8 = warp % kGroupWarps;
-    const int gtid = tid - grp * kGroupThreads, w = 2 * rank + grp;
+    const int w = 2 * rank + grp;
     const int ndn = w < RBd ? (RBd - w + kUnitWorkers - 1) / kUnitWorkers : 0;
     auto group_sync = [&]() { named_sync(2 + grp, kGroupThreads); };
     const uint8_t* ax_q = dsm + a.off_ax;                                    // [T][H]
@@ -1470,46 +1563,6 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     auto free_chunk = [&]() {
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(grp, slot));
-    };
-
-    // Items i0 .. i1 - 1 of output columns rbd*128 .. +127 of token t: the
-    // residual plus the k slots' parts (slot order, then h-block order).  sp
-    // threads share an item, each a contiguous range of the parts (the first
-    // also the residual), the ranges' sums added by a butterfly.
-    auto combine_piece = [&](int t, int rbd, int i0, int i1) {
-        const int n_it = i1 - i0, P = k * RBh;
-        int sp = 1;
-        while (sp < 8 && n_it * 2 * sp <= kGroupThreads && 2 * sp <= P) sp *= 2;
-        const int sub = gtid % sp, it = i0 + gtid / sp;
-        const int pa = P * sub / sp, pe = P * (sub + 1) / sp;
-        const bool mine = it < i1;
-        const int col = rbd * kTileRows + (mine ? it : i0);
-        float v = mine && sub == 0 ? bf16_bits_to_float(io.x_res[(size_t)t * H + col]) : 0.f;
-        const int* sp_t = S.slotpos + t * k;
-        int j = pa / RBh, hb2 = pa - (pa / RBh) * RBh;
-#pragma unroll 1
-        for (int p0 = pa; p0 < pe; p0 += 8) {
-            float part[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z) {
-                part[z] = 0.f;
-                if (mine && p0 + z < pe) {
-                    part[z] = __ldcg(a.y_part + ((size_t)hb2 * Tk + sp_t[j]) * H + col);
-                    if (++hb2 == RBh) {
-                        hb2 = 0;
-                        ++j;
-                    }
-                }
-            }
-#pragma unroll
-            for (int z = 0; z < 8; ++z) v += part[z];
-        }
-        for (int o = 1; o < sp; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (mine && sub == 0) {
-            const size_t o = (size_t)t * H + col;
-            if (io.out_fp32) static_cast<float*>(io.out)[o] = v;
-            else static_cast<uint16_t*>(io.out)[o] = float_to_bf16_bits(v);
-        }
     };
 
     auto unit = [&](auto ntc, int ul) {
@@ -1678,12 +1731,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                     a.y_part[((size_t)hb * Tk + off + n) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
             }
         }
-        // ------------------------------------- counts of the parts stored
-        group_sync();  // the group's stores of y come before its counts
-        for (int r = gtid; r < ndn * c; r += kGroupThreads) {
-            const int dd = r / c, n = r - dd * c;
-            red_release_add(&a.ticket[S.btok[off + n] * RBd + w + dd * kUnitWorkers], 1);
-        }
+        group_sync();  // the h buffer is rewritten by the next unit
     };
 
     for (int ul = 0; ul < nu; ++ul) {
@@ -1697,47 +1745,10 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     // every byte sent to this CTA has arrived before it may leave (the
     // arming warp waited on every phase unless one ran out of time)
     if (arm_warp && !armok && lane == 0) fail();
-
-    // ------------------------------------------------------------ combine
-    // Block (t, rbd) = token t's output columns rbd*128 .. +127, cut into np
-    // pieces; piece pc of the T * RBd * np belongs to worker pc * V / pieces
-    // (at most one each), which takes it after its own units once the
-    // block's count shows all k * RBh parts stored.
-    {
-        const int V = 2 * gridDim.x, v = 2 * blockIdx.x + grp, P = k * RBh, nb = T * RBd;
-        int np = 1;
-        while (np * 2 <= kTileRows / 32 && nb * np * 2 <= V && kTileRows * P > 2048 * np) np *= 2;
-        const int npc = nb * np;
-        const int p0 = (int)(((long long)v * npc + V - 1) / V);
-        const int p1 = (int)(((long long)(v + 1) * npc + V - 1) / V);
-        for (int pc = p0; pc < p1; ++pc) {
-            const int blk = pc / np, q = pc - blk * np;
-            if (gtid == 0) {
-                const int* cnt = &a.ticket[blk];
-                bool got = !s_abort;
-                if (got && ld_acquire(cnt) < P) {
-                    const unsigned long long t0 = globaltimer_ns();
-                    while (ld_acquire(cnt) < P) {
-                        if (s_abort || globaltimer_ns() - t0 > kWaitLimitNs) {
-                            got = false;
-                            break;
-                        }
-                    }
-                }
-                if (!got) fail();
-                S.flag[grp] = got ? 1 : 0;
-            }
-            group_sync();
-            if (S.flag[grp])
-                combine_piece(blk / RBd, blk - (blk / RBd) * RBd, q * kTileRows / np, (q + 1) * kTileRows / np);
-            group_sync();  // the flag is reused
-        }
-    }
 }
 
-// One decode layer by clusters of kClusterCTAs CTAs, one CTA per SM,
-// launched cooperatively (the combine waits on other clusters).  MAXNT: the
-// most tokens a bucket may hold (T <= MAXNT).
+// The experts of one decode layer by clusters of kClusterCTAs CTAs, one CTA
+// per SM.  MAXNT: the most tokens a bucket may hold (T <= MAXNT).
 template <int MAXNT, bool DOTS>
 __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -1759,9 +1770,64 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     cluster_sync_all();  // no CTA leaves while its peer may still address it
 }
 
+// ------------------------------------------------------------- combine
+// After the clustered layer kernel: out[t][col] = x[t][col] plus the k
+// slots' parts (slot j = 0 .. k-1, then h block 0 .. nparts-1, in that
+// order).  A CTA takes 32 consecutive columns of one token; warp w adds the
+// w-th eighth of the parts (warp 0 starting from the residual), the eighths
+// are added in warp order.
+constexpr int kCombineWarps = 8;
+struct CombineArgs {
+    const uint16_t* x_res;
+    const float* y_part;     // [nparts][T*k][H]
+    const int32_t* slot_pos; // [T*k]
+    int T, H, k, nparts;
+    void* out;
+    int out_fp32;
+};
+
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const CombineArgs c) {
+    __shared__ float s_part[kCombineWarps][32];
+    pdl_wait();  // the layer kernel's parts
+    pdl_trigger();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int it = blockIdx.x * 32 + lane;  // (H is a multiple of 32)
+    const int t = it / c.H, col = it - t * c.H;
+    const int Tk = c.T * c.k, P = c.k * c.nparts;
+    const int pa = P * warp / kCombineWarps, pe = P * (warp + 1) / kCombineWarps;
+    const bool mine = t < c.T;
+    float v = mine && warp == 0 ? bf16_bits_to_float(c.x_res[(size_t)t * c.H + col]) : 0.f;
+    int j = pa / c.nparts, hb = pa - (pa / c.nparts) * c.nparts;
+#pragma unroll 1
+    for (int p0 = pa; p0 < pe; p0 += 8) {
+        float part[8];
+#pragma unroll
+        for (int z = 0; z < 8; ++z) {
+            part[z] = 0.f;
+            if (mine && p0 + z < pe) {
+                part[z] = __ldcg(c.y_part + ((size_t)hb * Tk + c.slot_pos[t * c.k + j]) * c.H + col);
+                if (++hb == c.nparts) {
+                    hb = 0;
+                    ++j;
+                }
+            }
+        }
+#pragma unroll
+        for (int z = 0; z < 8; ++z) v += part[z];
+    }
+    s_part[warp][lane] = v;
+    __syncthreads();
+    if (warp == 0 && mine) {
+        for (int w = 1; w < kCombineWarps; ++w) v += s_part[w][lane];
+        const size_t o = (size_t)t * c.H + col;
+        if (c.out_fp32) static_cast<float*>(c.out)[o] = v;
+        else static_cast<uint16_t*>(c.out)[o] = float_to_bf16_bits(v);
+    }
+}
+
 // ---------------------------------------------------------------- launch
 int g_layer_pdl[64] = {};  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
-// clustered kernel: 0 unknown, 1 cluster + cooperative + PDL accepted, 2 without
+// clustered kernel: 0 unknown, 1 clusters + PDL accepted, 2 clusters without
 // PDL, 3 not accepted (the task kernel runs instead)
 int g_cluster_mode[64] = {};
 int g_prep_carveout[64] = {};
@@ -1874,23 +1940,22 @@ cudaError_t decode_prepare_device(int dev) {
         cudaGetLastError();  // refused: a launch error only, the context is intact
         mode = 2;
     }
-    // a cooperative launch in clusters of kClusterCTAs, with PDL, else without
-    cudaLaunchAttribute ac[3];
+    // a launch in clusters of kClusterCTAs, with PDL, else without
+    cudaLaunchAttribute ac[2];
     ac[0].id = cudaLaunchAttributeClusterDimension;
     ac[0].val.clusterDim.x = kClusterCTAs;
     ac[0].val.clusterDim.y = 1;
     ac[0].val.clusterDim.z = 1;
-    ac[1] = at[0];
-    ac[2] = at[1];
+    ac[1] = at[1];
     cfg.gridDim = dim3(2 * kClusterCTAs);
     cfg.attrs = ac;
     int& cm = g_cluster_mode[dev & 63];
-    for (int na = 3; na >= 2 && cm == 0; --na) {
+    for (int na = 2; na >= 1 && cm == 0; --na) {
         cfg.numAttrs = na;
         err = cudaLaunchKernelEx(&cfg, cluster_probe_kernel, (int*)nullptr);
         if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, cluster_probe_kernel, (int*)nullptr);
         if (err == cudaSuccess) err = cudaStreamSynchronize(st);
-        if (err == cudaSuccess) cm = na == 3 ? 1 : 2;
+        if (err == cudaSuccess) cm = na == 2 ? 1 : 2;
         else cudaGetLastError();
     }
     if (cm == 0) cm = 3;
@@ -1923,8 +1988,7 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
 
 int decode_sync_ints(int T, int H, int I, int E, int k) {
     const int nslot = std::min(E, T * k);
-    // the task kernel's counters, or the clustered kernel's tickets
-    return std::max(nslot * (I / kTileRows) + H / kTileRows, T * (H / kTileRows));
+    return nslot * (I / kTileRows) + H / kTileRows;
 }
 
 int decode_y_parts(int T, int H, int I, int E, int k) {
@@ -1980,7 +2044,7 @@ LayerArgs make_layer_args(int T, int H, int I, int E, int k, const Workspace& ws
     const int nslot = std::min(E, T * k);
     a.cnt_h = ws.sync;
     a.cnt_y = ws.sync + nslot * (I / kTileRows);
-    a.ticket = ws.sync;
+    a.slot_pos = ws.slot_pos;
     a.cap_g = ws.cap_g;
     a.cap_d = ws.cap_d;
     // the K splits the kernel may choose: divisors of the row's 64-column
@@ -2032,15 +2096,15 @@ cudaError_t launch_coop(void (*kern)(Args), const Args& args, int num_sms, int s
 
 int g_cluster_max[64] = {};  // co-resident clusters of the clustered kernel (0: not asked yet)
 
-// A cooperative launch of the clustered layer kernel: clusters of
-// kClusterCTAs CTAs, as many as the device holds at once (at most one CTA per
-// SM), with programmatic dependent launch where the device accepts it.
+// A launch of the clustered layer kernel: clusters of kClusterCTAs CTAs, as
+// many as the device holds at once (at most one CTA per SM), with
+// programmatic dependent launch where the device accepts it.
 cudaError_t launch_cluster(void (*kern)(LayerArgs), const LayerArgs& args, int num_sms, int smem, int dev,
                            cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute at[3];
+    cudaLaunchAttribute at[2];
     cfg.blockDim = dim3(kLayerThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -2048,10 +2112,8 @@ cudaError_t launch_cluster(void (*kern)(LayerArgs), const LayerArgs& args, int n
     at[0].val.clusterDim.x = kClusterCTAs;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeCooperative;
-    at[1].val.cooperative = 1;
-    at[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[2].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     int ncl = num_sms / kClusterCTAs;
     int& mx = g_cluster_max[dev & 63];
@@ -2069,7 +2131,7 @@ cudaError_t launch_cluster(void (*kern)(LayerArgs), const LayerArgs& args, int n
     ncl = std::min(ncl, mx);
     if (ncl < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(ncl * kClusterCTAs);
-    cfg.numAttrs = g_cluster_mode[dev & 63] == 1 ? 3 : 2;
+    cfg.numAttrs = g_cluster_mode[dev & 63] == 1 ? 2 : 1;
     if ((err = cudaLaunchKernelEx(&cfg, kern, args)) != cudaSuccess) {
         cudaGetLastError();
         return err;
@@ -2141,8 +2203,15 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
         void (*kern)(LayerArgs) = dots ? decode_cluster_kernel<kClusterMaxT, true>
                                        : decode_cluster_kernel<kClusterMaxT, false>;
         if ((err = launch_cluster(kern, a, num_sms, cplan.smem, dev, s)) != cudaSuccess) return err;
-        for (int i = 2; i <= 6; ++i)
+        for (int i = 2; i <= 5; ++i)
             if ((err = mark(i)) != cudaSuccess) return err;
+        CombineArgs c{x, a.y_part, a.slot_pos, T, H, k, I / kTileRows, out, out_fp32 ? 1 : 0};
+        if ((err = launch_pdl(decode_combine_kernel, dim3((T * H) / 32), dim3(kCombineWarps * 32), 0, s, c)) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return err;
+        }
+        if ((err = mark(6)) != cudaSuccess) return err;
         return cudaGetLastError();
     }
     void (*kern)(LayerArgs) =
