@@ -149,7 +149,6 @@ struct LayerArgs {
     int ns;             // slots of each group's ring
     int st;             // packed tiles per slot (kSlotTiles, or fewer for large T)
     int off_bar, off_ax, off_ah, ah_bytes, off_red;
-    int32_t* slot_pos;  // [T*k] bucket row of (t, j) (CTA 0 stores it)
     // clustered layer kernel: the K-part exchange buffers and the groups' h
     // buffers
     int off_p, off_h, h_bytes;
@@ -244,6 +243,8 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&xf)[8]) {
 
 constexpr int kPrepBarId = 4;  // named barrier of the row's 128 threads
 constexpr int kRouteBarId = 5; // named barrier of the four warps routing one token
+constexpr int kCombineBarId = 6;  // named barrier of the eight combine warps
+enum { kRouteGeneral = 0, kRouteOneTokenFast = 1, kRouteOneTokenOnly = 2 };
 
 // The prep work of one CTA on threads 0..127, for every token of x: the
 // optional RMSNorm factor, then by `mode`
@@ -473,6 +474,7 @@ struct LayerShared {
     int idx[kMaxTk];
     float w[kMaxTk];
     int btok[kMaxTk];    // bucket row -> token
+    uint8_t bslot[kMaxTk];  // bucket row -> the token's choice (0 .. k-1)
     float bsw[kMaxTk];   // bucket row -> routing weight
     int slotpos[kMaxTk]; // (t, j) -> bucket row
     uint32_t mask[kMaxExperts];
@@ -493,6 +495,8 @@ struct LayerShared {
 // from layer to layer within a launch).
 struct Pipe {
     int slot, phase, cidx;
+    int units;  // clustered kernel: units exchanged so far (the exchange barriers' phases)
+    int armok;  // clustered kernel: the arming warp has met every phase in time
 };
 
 // What changes from layer to layer: the input (also the residual), the
@@ -546,10 +550,13 @@ __device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, u
 // logits and their order keys sit in the still idle dynamic shared memory
 // below the codes of x.  split(warp, lane) runs on warps 0 .. 4*kGroups - 1
 // (the work split of the caller) while the other warps fill the buckets.
-// ONE_TOKEN_PATH: a single token is routed by one warp instead.
-template <bool ONE_TOKEN_PATH, typename Split>
+// ROUTE: kRouteGeneral, kRouteOneTokenFast (a single token is routed by four
+// warps instead) or kRouteOneTokenOnly (T == 1 always: only that path is
+// built).
+template <int ROUTE, typename Split>
 __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, uint8_t* dsm,
                                             Split&& split) {
+    constexpr bool ONE_TOKEN_PATH = ROUTE != kRouteGeneral;
     int* s_idx = S.idx;
     float* s_w = S.w;
     int* s_btok = S.btok;
@@ -568,7 +575,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     const int Tk = T * k;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int b = blockIdx.x;
-    if (ONE_TOKEN_PATH && T == 1) {
+    if (ROUTE == kRouteOneTokenOnly || (ONE_TOKEN_PATH && T == 1)) {
         // One token: warps 0..3 (expert e on thread e % 128) rank every
         // expert's logit against all E (larger first, the lower index on a
         // tie: the order of the general path); rank < k places it.  Warp 0
@@ -622,13 +629,13 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
                     s_w[lane] = sw;
                     s_slotpos[lane] = pos;
                     s_btok[pos] = 0;
+                    S.bslot[pos] = lane;
                     s_bsw[pos] = sw;
                     s_touched[pos] = si;
                     s_toff[pos] = pos;
                     if (b == 0) {
                         a.topk_idx[lane] = si;
                         a.topk_w[lane] = sw;
-                        a.slot_pos[lane] = pos;
                         a.bucket_token[pos] = 0;
                         a.bucket_slot[pos] = lane;
                         a.touched[pos] = si;
@@ -658,6 +665,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
         __syncthreads();
         return;
     }
+    if constexpr (ROUTE != kRouteOneTokenOnly) {
     float* s_lg = reinterpret_cast<float*>(dsm);                  // [T][E] logits, and
     uint32_t* s_key = reinterpret_cast<uint32_t*>(s_lg + T * E);  // their order keys, in
     for (int i = tid; i < T * E; i += kLayerThreads) {            // the still idle ring
@@ -780,12 +788,12 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
             const int t = p / k, e = s_idx[p];
             const int pos = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
             s_btok[pos] = t;
+            S.bslot[pos] = p % k;
             s_bsw[pos] = s_w[p];
             s_slotpos[p] = pos;
             if (b == 0) {
                 a.topk_idx[p] = e;
                 a.topk_w[p] = s_w[p];
-                a.slot_pos[p] = pos;
                 a.bucket_token[pos] = t;
                 a.bucket_slot[pos] = p % k;
             }
@@ -800,7 +808,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     // that memory
     fence_proxy_async_smem();
     __syncthreads();
-
+    }
 }
 
 // One decode layer (everything after the prep kernel's work) by one CTA of
@@ -852,7 +860,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
     }
 
     // ---------------------------------------------- routing (every CTA)
-    route_layer<false>(a, S, dsm, [&](int warp, int lane) {
+    route_layer<kRouteGeneral>(a, S, dsm, [&](int warp, int lane) {
         // Tasks are shared out by cost, a tile of touched slot i weighing
         // kTileCost + c_i: worker v = 2b + g (consumer group g of CTA b)
         // runs the gate/up tasks [bound(v), bound(v + 1)) and the down tasks
@@ -1371,7 +1379,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     __syncthreads();
     pdl_wait();     // the prep kernel's logits, codes and cleared counters
     pdl_trigger();  // the next call's prep may be scheduled; it waits for our end
-    Pipe pp{-1, 0, -1};
+    Pipe pp{-1, 0, -1, 0, 1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
     layer_body<MAXNT, DOTS>(a, io, S, dsm, pp);
     ring_drain(a, S, dsm);
@@ -1453,7 +1461,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
         for (int i = tid; i < n16; i += kConsumerThreads)
             cp_async16(sbase + a.off_ax + 16 * i, a.xq + 16 * (size_t)i);
     }
-    route_layer<true>(a, S, dsm, [&](int warp, int lane) {
+    route_layer<MAXNT == 1 ? kRouteOneTokenOnly : kRouteOneTokenFast>(a, S, dsm, [&](int warp, int lane) {
         if (warp == 0) {
             const int nt = S.nt;
             const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
@@ -1542,7 +1550,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     // arms them); it waits on every phase, even after a failure elsewhere,
     // so that it never arms a phase twice.  armok is uniform in the warp.
     const bool arm_warp = grp == 0 && w8 == 0;
-    bool armok = true;
+    int& armok = pp.armok;
     int& slot = pp.slot;
     int& phase = pp.phase;
     const int r_lane = lane >> 1, h_lane = lane & 1;
@@ -1569,8 +1577,9 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
         constexpr int NT = decltype(ntc)::value;
         const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;
         const int e = S.touched[i], off = S.off[e], c = S.off[e + 1] - off;
-        const int pb = ul & 1;
-        const uint32_t ppar = (uint32_t)((ul >> 1) & 1);
+        const int ux = pp.units + ul;  // the exchange's ordinal in the launch
+        const int pb = ux & 1;
+        const uint32_t ppar = (uint32_t)((ux >> 1) & 1);
         if (arm_warp && armok && lane == 0)
             mbar_arrive_expect_tx(pbar(pb), (uint32_t)(kUnitWorkers * c * kTileRows * 4));
         // ------------------------------------------------ gate/up K part
@@ -1644,7 +1653,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
         if (arm_warp ? armok : live) {
             const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(pbar(pb), ppar));
             if (!ok) {
-                armok = false;
+                armok = 0;
                 if (live) fail();
                 live = false;
             } else if (live && s_abort) {
@@ -1727,21 +1736,28 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const float v = accd[n] + __shfl_xor_sync(0xffffffffu, accd[n], 1);
-                if (n < c && h_lane == 0 && live)
-                    a.y_part[((size_t)hb * Tk + off + n) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
+                if (n < c && h_lane == 0 && live) {
+                    const int tj = S.btok[off + n] * k + S.bslot[off + n];  // (token, choice)
+                    a.y_part[((size_t)hb * Tk + tj) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
+                }
             }
         }
         group_sync();  // the h buffer is rewritten by the next unit
     };
 
     for (int ul = 0; ul < nu; ++ul) {
-        const int u = ub0 + ul, i = u / RBh;
-        const int e = S.touched[i], c = S.off[e + 1] - S.off[e];
-        if (c <= 1) unit(IntC<1>{}, ul);
-        else if (c <= 2) unit(IntC<2>{}, ul);
-        else if (c <= 4 || MAXNT <= 4) unit(IntC<4 < MAXNT ? 4 : MAXNT>{}, ul);
-        else unit(IntC<MAXNT>{}, ul);
+        if constexpr (MAXNT == 1) {
+            unit(IntC<1>{}, ul);
+        } else {
+            const int u = ub0 + ul, i = u / RBh;
+            const int e = S.touched[i], c = S.off[e + 1] - S.off[e];
+            if (c <= 1) unit(IntC<1>{}, ul);
+            else if (c <= 2) unit(IntC<2>{}, ul);
+            else if (c <= 4 || MAXNT <= 4) unit(IntC<4 < MAXNT ? 4 : MAXNT>{}, ul);
+            else unit(IntC<MAXNT>{}, ul);
+        }
     }
+    pp.units += nu;
     // every byte sent to this CTA has arrived before it may leave (the
     // arming warp waited on every phase unless one ran out of time)
     if (arm_warp && !armok && lane == 0) fail();
@@ -1762,7 +1778,7 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     cluster_sync_all();  // the peers' exchange barriers exist before anyone sends
     pdl_wait();          // the prep kernel's logits, codes and cleared tickets
     pdl_trigger();
-    Pipe pp{-1, 0, -1};
+    Pipe pp{-1, 0, -1, 0, 1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
     cluster_body<MAXNT, DOTS>(a, io, S, dsm, pp);
     ring_drain(a, S, dsm);
@@ -1772,26 +1788,24 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
 
 // ------------------------------------------------------------- combine
 // After the clustered layer kernel: out[t][col] = x[t][col] plus the k
-// slots' parts (slot j = 0 .. k-1, then h block 0 .. nparts-1, in that
-// order).  A CTA takes 32 consecutive columns of one token; warp w adds the
+// choices' parts (choice j = 0 .. k-1, then h block 0 .. nparts-1, in that
+// order; the parts are stored by (token, choice)).  A CTA takes 32 consecutive columns of one token; warp w adds the
 // w-th eighth of the parts (warp 0 starting from the residual), the eighths
 // are added in warp order.
 constexpr int kCombineWarps = 8;
 struct CombineArgs {
     const uint16_t* x_res;
-    const float* y_part;     // [nparts][T*k][H]
-    const int32_t* slot_pos; // [T*k]
+    const float* y_part;     // [nparts][T*k][H], row t*k + j
     int T, H, k, nparts;
     void* out;
     int out_fp32;
 };
 
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const CombineArgs c) {
-    __shared__ float s_part[kCombineWarps][32];
-    pdl_wait();  // the layer kernel's parts
-    pdl_trigger();
+// Output columns 32*blk .. +31 (of the T x H output, row-major) by warps
+// 0 .. kCombineWarps-1 of the calling CTA.
+__device__ __forceinline__ void combine_cols32(const CombineArgs& c, int blk, float (*s_part)[32]) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int it = blockIdx.x * 32 + lane;  // (H is a multiple of 32)
+    const int it = blk * 32 + lane;  // (H is a multiple of 32)
     const int t = it / c.H, col = it - t * c.H;
     const int Tk = c.T * c.k, P = c.k * c.nparts;
     const int pa = P * warp / kCombineWarps, pe = P * (warp + 1) / kCombineWarps;
@@ -1805,7 +1819,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         for (int z = 0; z < 8; ++z) {
             part[z] = 0.f;
             if (mine && p0 + z < pe) {
-                part[z] = __ldcg(c.y_part + ((size_t)hb * Tk + c.slot_pos[t * c.k + j]) * c.H + col);
+                part[z] = __ldcg(c.y_part + ((size_t)hb * Tk + t * c.k + j) * c.H + col);
                 if (++hb == c.nparts) {
                     hb = 0;
                     ++j;
@@ -1816,13 +1830,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         for (int z = 0; z < 8; ++z) v += part[z];
     }
     s_part[warp][lane] = v;
-    __syncthreads();
+    named_sync(kCombineBarId, kCombineWarps * 32);
     if (warp == 0 && mine) {
         for (int w = 1; w < kCombineWarps; ++w) v += s_part[w][lane];
         const size_t o = (size_t)t * c.H + col;
         if (c.out_fp32) static_cast<float*>(c.out)[o] = v;
         else static_cast<uint16_t*>(c.out)[o] = float_to_bf16_bits(v);
     }
+    named_sync(kCombineBarId, kCombineWarps * 32);  // s_part is reused
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const CombineArgs c) {
+    __shared__ float s_part[kCombineWarps][32];
+    pdl_wait();  // the layer kernel's parts
+    pdl_trigger();
+    combine_cols32(c, blockIdx.x, s_part);
 }
 
 // ---------------------------------------------------------------- launch
@@ -2044,7 +2066,6 @@ LayerArgs make_layer_args(int T, int H, int I, int E, int k, const Workspace& ws
     const int nslot = std::min(E, T * k);
     a.cnt_h = ws.sync;
     a.cnt_y = ws.sync + nslot * (I / kTileRows);
-    a.slot_pos = ws.slot_pos;
     a.cap_g = ws.cap_g;
     a.cap_d = ws.cap_d;
     // the K splits the kernel may choose: divisors of the row's 64-column
@@ -2205,7 +2226,7 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
         if ((err = launch_cluster(kern, a, num_sms, cplan.smem, dev, s)) != cudaSuccess) return err;
         for (int i = 2; i <= 5; ++i)
             if ((err = mark(i)) != cudaSuccess) return err;
-        CombineArgs c{x, a.y_part, a.slot_pos, T, H, k, I / kTileRows, out, out_fp32 ? 1 : 0};
+        CombineArgs c{x, a.y_part, T, H, k, I / kTileRows, out, out_fp32 ? 1 : 0};
         if ((err = launch_pdl(decode_combine_kernel, dim3((T * H) / 32), dim3(kCombineWarps * 32), 0, s, c)) !=
             cudaSuccess) {
             cudaGetLastError();
@@ -2229,6 +2250,7 @@ cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr
                                 const Workspace& ws, int* status, int num_sms, cudaStream_t s) {
     if (T == 0 || L == 0) return cudaSuccess;
     if (L > MOE_DECODE_MAX_LAYERS) return cudaErrorInvalidValue;
+
     // layer l reads layer l - 1's bf16 output from one workspace buffer and
     // writes the other; each layer's prep kernel waits for the layer before
     const uint16_t* cur = x;
