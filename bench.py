@@ -45,7 +45,7 @@ NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch 
 
 
 def kernels_per_decode_layer(T):
-    return 3 if T <= 8 else 2
+    return 3 if T <= 16 else 2
 
 DECODE_WORKLOAD = ("decode W4A8 MoE layer: T=1, H=2048, I=768, E=128, top-8 (batch-1 decode "
                    "config), in a chain of 16 pre-norm layers with distinct weight copies, "

@@ -7,6 +7,8 @@
 #include <mutex>
 
 #include "common.cuh"
+#include <algorithm>
+
 #include "internal.h"
 
 namespace moeq4 {
@@ -182,10 +184,16 @@ size_t carve(int mode, int T, int H, int I, int E, int k, uint8_t* base, Workspa
         w.xs = base ? reinterpret_cast<int2*>(w.xq + xq_bytes) : nullptr;
         w.q_x = reinterpret_cast<int8_t*>(take((size_t)T * H));
         w.d_x = reinterpret_cast<uint16_t*>(take((size_t)T * (H / kGroup) * 2));
-        w.gu_part = reinterpret_cast<float*>(take((size_t)nsg * Tk * 2 * I * 4));
+        // one region for the parts: the task kernel's gate/up K parts and
+        // down K parts, or the clustered kernel's per-h-block parts
+        const size_t gu_bytes = (size_t)nsg * Tk * 2 * I * 4, yd_bytes = (size_t)nsd * Tk * H * 4;
+        const size_t yc_bytes = (size_t)decode_cluster_parts(T, H, I, E) * Tk * H * 4;
+        uint8_t* parts = take(std::max(gu_bytes + yd_bytes, yc_bytes));
+        w.gu_part = reinterpret_cast<float*>(parts);
+        w.y_part = base ? reinterpret_cast<float*>(parts + gu_bytes) : nullptr;
+        w.y_unit = reinterpret_cast<float*>(parts);
         w.q_h = reinterpret_cast<int8_t*>(take(Tk * I));
         w.d_h = reinterpret_cast<uint16_t*>(take(Tk * (I / kGroup) * 2));
-        w.y_part = reinterpret_cast<float*>(take((size_t)decode_y_parts(T, H, I, E, k) * Tk * H * 4));
         w.sync = reinterpret_cast<int32_t*>(take((size_t)decode_sync_ints(T, H, I, E, k) * 4));
         w.xbuf0 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
         w.xbuf1 = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));

@@ -77,7 +77,8 @@ constexpr int kLayerThreads = kConsumerThreads + kGroups * 32;  // + a producer 
 constexpr int kWarpProducer0 = kConsumerWarps;          // group g's producer: warp kWarpProducer0 + g
 constexpr int kSlotTiles = 4;                           // packed tiles per ring slot (one bulk copy),
                                                         // fewer when shared memory is short
-constexpr int kMaxSlots = 24;                           // slots of both groups' rings
+constexpr int kMaxSlots = 32;                           // slots of both groups' rings
+constexpr int kRingStride = kMaxSlots / 2;              // barrier and slot stride of a group's ring
 constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 32 lanes x 8 floats
 // Dynamic shared memory of the layer kernel: leaves room on the SM (228 KB)
 // for its static part (13.1 KB) and a prep CTA of the next call (its router
@@ -149,9 +150,10 @@ struct LayerArgs {
     int ns;             // slots of each group's ring
     int st;             // packed tiles per slot (kSlotTiles, or fewer for large T)
     int off_bar, off_ax, off_ah, ah_bytes, off_red;
-    // clustered layer kernel: the K-part exchange buffers and the groups' h
-    // buffers
-    int off_p, off_h, h_bytes;
+    // clustered layer kernel: bytes of the rings and the K-part exchange
+    // buffers (laid out in the kernel once the largest bucket is known),
+    // and the groups' h buffers
+    int ring_bytes, off_h, h_bytes;
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -487,6 +489,8 @@ struct LayerShared {
     int nt, nsg, nsd;
     int eqc;                    // every touched slot has the same bucket size
     int bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
+    int cmax;                   // clustered kernel: the largest bucket
+    int rns;                    // clustered kernel: slots of each group's ring
     volatile int abort;
     volatile int flag[kGroups];
 };
@@ -509,8 +513,10 @@ struct LayerIO {
     int out_fp32;
 };
 
+// Full and empty barriers of slot s of group g's ring: kMaxSlots of each
+// at off_bar, kRingStride a group, whatever number of slots a launch uses.
 __device__ __forceinline__ uint32_t ring_bar(const LayerArgs& a, uint32_t sbase, bool full, int g, int s) {
-    return sbase + a.off_bar + 8u * ((full ? 0 : 2 * a.ns) + g * a.ns + s);
+    return sbase + a.off_bar + 8u * ((full ? 0 : kMaxSlots) + g * kRingStride + s);
 }
 
 // Once per launch: the ring barriers, no chunk issued yet, no failure.
@@ -518,7 +524,7 @@ __device__ __forceinline__ void ring_init(const LayerArgs& a, LayerShared& S, ui
     const uint32_t sbase = smem_u32(dsm);
     if (threadIdx.x == 0) {
         for (int g = 0; g < kGroups; ++g) {
-            for (int s = 0; s < a.ns; ++s) {
+            for (int s = 0; s < kRingStride; ++s) {
                 mbar_init(ring_bar(a, sbase, true, g, s), 1);
                 mbar_init(ring_bar(a, sbase, false, g, s), kGroupWarps);
             }
@@ -531,15 +537,15 @@ __device__ __forceinline__ void ring_init(const LayerArgs& a, LayerShared& S, ui
 
 // Before the CTA exits, every copy it issued has landed: the producer warps
 // wait for the latest chunk of each slot (earlier ones completed before it).
-__device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, uint8_t* dsm) {
+__device__ __forceinline__ void ring_drain(const LayerArgs& a, LayerShared& S, uint8_t* dsm, int ns) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp < kWarpProducer0) return;
     const int g = warp - kWarpProducer0;
     const uint32_t sbase = smem_u32(dsm);
     __syncwarp();
-    for (int s = lane; s < a.ns; s += 32) {
-        const int c = S.slot_chunk[g * a.ns + s];
-        if (c >= 0) mbar_wait(ring_bar(a, sbase, true, g, s), (c / a.ns) & 1);
+    for (int s = lane; s < ns; s += 32) {
+        const int c = S.slot_chunk[g * kRingStride + s];
+        if (c >= 0) mbar_wait(ring_bar(a, sbase, true, g, s), (c / ns) & 1);
     }
 }
 
@@ -988,7 +994,7 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a, const LayerIO& io
                         break;
                     }
                     const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * kTileBytes);
-                    s_slot_chunk[g * ns + slot] = cidx;
+                    s_slot_chunk[g * kRingStride + slot] = cidx;
                     mbar_arrive_expect_tx(full_bar(g, slot), bytes);
                     bulk_g2s(sbase + slot_addr(g, slot), S.ctab_p[g][j], bytes, full_bar(g, slot));
                 }
@@ -1382,7 +1388,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
     Pipe pp{-1, 0, -1, 0, 1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
     layer_body<MAXNT, DOTS>(a, io, S, dsm, pp);
-    ring_drain(a, S, dsm);
+    ring_drain(a, S, dsm, a.ns);
 }
 
 // ------------------------------------------------------ clustered layer
@@ -1409,7 +1415,7 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 // has drained, and costs ~3 us a layer).
 constexpr int kClusterCTAs = 2;
 constexpr int kUnitWorkers = kClusterCTAs * kGroups;
-constexpr int kClusterMaxT = 8;   // tokens per call of the clustered kernel
+constexpr int kClusterMaxT = 16;  // tokens per call of the clustered kernel
 
 // The first unit of cluster q of NC: the unit whose cost range holds the
 // position q * total / NC (units of touched slot i, RBh of them, weigh
@@ -1444,35 +1450,59 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     const int KBg = H / kTileK, KBd = I / kTileK;
     const int RBg = 2 * I / kTileRows, RBd = H / kTileRows, RBh = I / kTileRows;
     const int Gx = H / kGroup, Gh = I / kGroup;
-    const int Tk = T * k, ns = a.ns, st = a.st;
+    const int Tk = T * k;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int rank = (int)cluster_ctarank(), cq = (int)cluster_id_x(), NC = (int)cluster_count_x();
+    const int Hh = H / kClusterCTAs, Gxh = Gx / kClusterCTAs;  // this CTA's K part of x
     const uint32_t sbase = smem_u32(dsm);
-    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
-    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
-    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
-    auto pbar = [&](int pb) { return sbase + a.off_bar + 8u * (4 * ns + pb); };
     auto fail = [&]() {
         record_status(a.status, kStatusTimeout);
         s_abort = 1;
     };
     if (warp < kConsumerWarps) {
-        const int n16 = (T * H + T * Gx * 8) / 16;
-        for (int i = tid; i < n16; i += kConsumerThreads)
-            cp_async16(sbase + a.off_ax + 16 * i, a.xq + 16 * (size_t)i);
+        // the codes of x and their scales over this CTA's K part: [T][H/2]
+        // codes, then [T][Gx/2] scales
+        const int nc16 = Hh / 16, ns16 = Gxh * 8 / 16, per = nc16 + ns16;
+        const uint8_t* xs_g = a.xq + (size_t)T * H;
+        for (int i = tid; i < T * per; i += kConsumerThreads) {
+            const int t = i / per, j = i - t * per;
+            if (j < nc16)
+                cp_async16(sbase + a.off_ax + t * Hh + 16 * j, a.xq + (size_t)t * H + rank * Hh + 16 * j);
+            else
+                cp_async16(sbase + a.off_ax + T * Hh + t * Gxh * 8 + 16 * (j - nc16),
+                           xs_g + ((size_t)t * Gx + rank * Gxh) * 8 + 16 * (j - nc16));
+        }
     }
     route_layer<MAXNT == 1 ? kRouteOneTokenOnly : kRouteOneTokenFast>(a, S, dsm, [&](int warp, int lane) {
         if (warp == 0) {
             const int nt = S.nt;
             const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
             const int u1 = unit_bound_warp(cq + 1, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
+            int cm = 0;  // the largest bucket
+            for (int i = lane; i < nt; i += 32) cm = max(cm, S.toff[i + 1] - S.toff[i]);
+            cm = __reduce_max_sync(0xffffffffu, cm);
             if (lane == 0) {
                 S.bnd[0][0] = u0;
                 S.bnd[0][1] = u1;
+                S.cmax = cm;
             }
         }
     });
     const int ub0 = S.bnd[0][0], nu = S.bnd[0][1] - ub0;
+    // The rings and the exchange buffers share ring_bytes: the exchange
+    // buffers take what the largest bucket needs, the rings the rest (every
+    // CTA lays them out alike from the same routing).
+    const int cmax = S.cmax;
+    const int pbytes = (2 * kUnitWorkers * cmax * kTileRows * 4 + 127) & ~127;
+    const int rbytes = a.ring_bytes - pbytes;
+    const int st = T >= 4 && rbytes >= kGroups * 3 * kSlotTiles * kTileBytes ? kSlotTiles : 2;
+    const int ns = min(kRingStride, rbytes / (st * kTileBytes) / kGroups);
+    const int off_p = kGroups * ns * st * kTileBytes;
+    S.rns = ns;  // (every thread stores the same value)
+    auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
+    auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
+    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
+    auto pbar = [&](int pb) { return sbase + a.off_bar + 8u * (2 * kMaxSlots + pb); };
     const int KCg = KBg / kClusterCTAs, kb0 = rank * KCg;  // this CTA's K part of gate/up
     const int cptg = (KCg + st - 1) / st;                    // gate/up chunks of a unit
 
@@ -1523,7 +1553,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                         break;
                     }
                     const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * kTileBytes);
-                    S.slot_chunk[g * ns + slot] = cidx;
+                    S.slot_chunk[g * kRingStride + slot] = cidx;
                     mbar_arrive_expect_tx(full_bar(g, slot), bytes);
                     bulk_g2s(sbase + slot_addr(g, slot), S.ctab_p[g][j], bytes, full_bar(g, slot));
                 }
@@ -1538,11 +1568,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     const int w = 2 * rank + grp;
     const int ndn = w < RBd ? (RBd - w + kUnitWorkers - 1) / kUnitWorkers : 0;
     auto group_sync = [&]() { named_sync(2 + grp, kGroupThreads); };
-    const uint8_t* ax_q = dsm + a.off_ax;                                    // [T][H]
-    const int2* ax_s = reinterpret_cast<const int2*>(ax_q + (size_t)T * H);  // [T][Gx]
+    const uint8_t* ax_q = dsm + a.off_ax;                                     // [T][H/2]
+    const int2* ax_s = reinterpret_cast<const int2*>(ax_q + (size_t)T * Hh);  // [T][Gx/2]
     uint8_t* hq = dsm + a.off_h + grp * a.h_bytes;                           // [T][128] codes
     int2* hs = reinterpret_cast<int2*>(hq + (size_t)T * kTileRows);          // [T][4]
-    const float* pbuf = reinterpret_cast<const float*>(dsm + a.off_p);      // [2][workers][T][128]
+    const float* pbuf = reinterpret_cast<const float*>(dsm + off_p);  // [2][workers][cmax][128]
     cp_async_wait_all();
     named_sync(1, kConsumerThreads);
     bool live = !s_abort;
@@ -1590,8 +1620,8 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 #pragma unroll
         for (int n = 0; n < NH; ++n) {
             const int ar = S.btok[off + (n < c ? n : 0)];
-            arow[n] = ar * H;
-            srow[n] = ar * Gx;
+            arow[n] = ar * Hh;
+            srow[n] = ar * Gxh;
         }
         float acc[NT];
 #pragma unroll
@@ -1608,7 +1638,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                                             wv.w & 0x0F0F0F0Fu};
                     const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
                                             (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
-                    const int g = 2 * (kb0 + u0 + uu) + h_lane;
+                    const int gl = 2 * (u0 + uu) + h_lane, g = 2 * kb0 + gl;  // (local, absolute)
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         if (n < c) {
@@ -1618,11 +1648,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                                 so = srow[n];
                             } else {
                                 const int ar = S.btok[off + n];
-                                ao = ar * H;
-                                so = ar * Gx;
+                                ao = ar * Hh;
+                                so = ar * Gxh;
                             }
-                            const int2 sc = ax_s[so + g];
-                            const int dot = group_dot(wl, wh, ax_q + ao + g * kGroup, sc.y);
+                            const int2 sc = ax_s[so + gl];
+                            const int dot = group_dot(wl, wh, ax_q + ao + gl * kGroup, sc.y);
                             acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
                             if (DOTS) a.dots_gu[((size_t)(off + n) * 2 * I + row) * Gx + g] = dot;
                         }
@@ -1642,7 +1672,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                 const float v3 = __shfl_down_sync(0xffffffffu, v, 6);
                 if ((lane & 7) == 0) {
                     const uint32_t la =
-                        sbase + a.off_p + 4u * ((((pb * kUnitWorkers + w) * T + n) * kTileRows) + lrow);
+                        sbase + off_p + 4u * ((((pb * kUnitWorkers + w) * cmax + n) * kTileRows) + lrow);
 #pragma unroll
                     for (int d = 0; d < kClusterCTAs; ++d)
                         st_async_v4(mapa_shared(la, d), v, v1, v2, v3, mapa_shared(pbar(pb), d));
@@ -1666,9 +1696,9 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 #pragma unroll
             for (int r = 0; r < kClusterCTAs; ++r) {
                 const float4 g4 = *reinterpret_cast<const float4*>(
-                    pbuf + (((pb * kUnitWorkers + 2 * r) * T + n) * kTileRows + f));
+                    pbuf + (((pb * kUnitWorkers + 2 * r) * cmax + n) * kTileRows + f));
                 const float4 u4 = *reinterpret_cast<const float4*>(
-                    pbuf + (((pb * kUnitWorkers + 2 * r + 1) * T + n) * kTileRows + f));
+                    pbuf + (((pb * kUnitWorkers + 2 * r + 1) * cmax + n) * kTileRows + f));
                 gv[0] += g4.x; gv[1] += g4.y; gv[2] += g4.z; gv[3] += g4.w;
                 uv[0] += u4.x; uv[1] += u4.y; uv[2] += u4.z; uv[3] += u4.w;
             }
@@ -1771,7 +1801,7 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     __shared__ LayerShared S;
     if (threadIdx.x == 0) {
         const uint32_t sbase = smem_u32(dsm);
-        for (int pb = 0; pb < 2; ++pb) mbar_init(sbase + a.off_bar + 8u * (4 * a.ns + pb), 1);
+        for (int pb = 0; pb < 2; ++pb) mbar_init(sbase + a.off_bar + 8u * (2 * kMaxSlots + pb), 1);
     }
     ring_init(a, S, dsm);  // (its thread 0 fences the barrier inits for the cluster)
     __syncthreads();
@@ -1781,7 +1811,7 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     Pipe pp{-1, 0, -1, 0, 1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
     cluster_body<MAXNT, DOTS>(a, io, S, dsm, pp);
-    ring_drain(a, S, dsm);
+    ring_drain(a, S, dsm, S.rns);
     __syncwarp();
     cluster_sync_all();  // no CTA leaves while its peer may still address it
 }
@@ -1856,7 +1886,7 @@ int g_prep_carveout[64] = {};
 
 struct Plan {
     int ns, st, off_bar, off_ax, off_ah, ah_bytes, off_red, smem;
-    int off_p, off_h, h_bytes;  // clustered kernel
+    int ring_bytes, off_h, h_bytes;  // clustered kernel
 };
 
 int al128(long long v) { return (int)((v + 127) & ~127ll); }
@@ -1885,40 +1915,42 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
     p->off_red = p->off_ah + 2 * (int)ah;
     p->off_ax = al128(p->off_red + 2 * kRedBytes);
     p->off_bar = al128(p->off_ax + ax);
-    p->smem = p->off_bar + 2 * kGroups * ns * 8;
+    p->smem = p->off_bar + 2 * kMaxSlots * 8;
     // the routing phase keeps all T x E logits and their order keys below
     // the codes of x
     return (long long)T * E * 8 <= p->off_ax;
 }
 
 // Shared-memory plan of the clustered layer kernel; false if it does not
-// fit (or T exceeds kClusterMaxT).  Layout: the two rings, the K-part
-// exchange buffers [2][workers][T][128] fp32, the groups' h buffers, the
-// codes of x, the barriers (rings, then the two exchange barriers).
+// fit (or T exceeds kClusterMaxT).  Layout: the rings and the K-part
+// exchange buffers [2][workers][cmax][128] fp32 (ring_bytes, laid out by the
+// kernel once the largest bucket cmax is known), the groups' h buffers, the
+// codes of x over the CTA's K part, the barriers (rings, then the two
+// exchange barriers).  ring_bytes must hold the exchange buffers of T tokens
+// and two two-tile slots a group.
 bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p) {
     (void)I;
     if (T < 1 || T > kClusterMaxT) return false;
     if ((H / kTileK) % kClusterCTAs) return false;
-    const long long ax = al128((long long)T * H + (long long)T * (H / kGroup) * 8);
-    const long long pbytes = al128(2ll * kUnitWorkers * T * kTileRows * 4);
+    const long long ax = al128((long long)T * (H / kClusterCTAs) + (long long)T * (H / kGroup / kClusterCTAs) * 8);
     const long long hbytes = al128((long long)T * kTileRows + (long long)T * 4 * 8);
-    const long long rest = budget - ax - pbytes - 2 * hbytes - (4ll * kMaxSlots + 2) * 8 - 256;
-    const int st = T >= 4 && rest >= (long long)kGroups * 3 * kSlotTiles * kTileBytes ? kSlotTiles : 2;
-    int ns = (int)(rest / ((long long)st * kTileBytes)) / kGroups;
-    ns = ns > kMaxSlots / kGroups ? kMaxSlots / kGroups : ns;
-    if (ns < 2) return false;
-    p->ns = ns;
-    p->st = st;
-    p->off_p = kGroups * ns * st * kTileBytes;
-    p->off_h = p->off_p + (int)pbytes;
+    const long long bars = (2ll * kMaxSlots + 2) * 8;
+    const long long rb = (budget - ax - 2 * hbytes - bars - 256) & ~127ll;
+    const long long pmax = al128(2ll * kUnitWorkers * T * kTileRows * 4);
+    const long long ring_min = (long long)kGroups * 2 * 2 * kTileBytes;
+    if (rb < pmax + ring_min) return false;
+    // the routing scratch (logits and keys) stays below the exchange
+    // buffers, which a peer may fill while this CTA still routes
+    if ((long long)T * E * 8 > ring_min) return false;
+    p->ns = p->st = 0;
+    p->ring_bytes = (int)rb;
+    p->off_h = (int)rb;
     p->h_bytes = (int)hbytes;
     p->off_ax = al128(p->off_h + 2 * hbytes);
     p->off_bar = al128(p->off_ax + ax);
-    p->smem = p->off_bar + (4 * ns + 2) * 8;
+    p->smem = p->off_bar + (int)bars;
     p->off_ah = p->off_red = p->ah_bytes = 0;
-    // the routing scratch (logits and keys) stays below the exchange
-    // buffers, which a peer may fill while this CTA still routes
-    return (long long)T * E * 8 <= p->off_p;
+    return true;
 }
 
 __global__ void coop_pdl_probe_kernel(int* p) {
@@ -2013,12 +2045,9 @@ int decode_sync_ints(int T, int H, int I, int E, int k) {
     return nslot * (I / kTileRows) + H / kTileRows;
 }
 
-int decode_y_parts(int T, int H, int I, int E, int k) {
-    int cap_g, cap_d, nsg, nsd;
-    decode_split_bounds(T, H, I, E, k, &cap_g, &cap_d, &nsg, &nsd);
+int decode_cluster_parts(int T, int H, int I, int E) {
     Plan p;
-    const int ncl = plan_cluster(T, H, I, E, kLayerSmemBudget, &p) ? I / kTileRows : 0;
-    return std::max(nsd, ncl);
+    return plan_cluster(T, H, I, E, kLayerSmemBudget, &p) ? I / kTileRows : 0;
 }
 
 namespace {
@@ -2214,15 +2243,16 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     const bool dots = dots_gu || dots_d;
     Plan cplan;
     if (g_cluster_mode[dev & 63] <= 2 && plan_cluster(T, H, I, E, kLayerSmemBudget, &cplan)) {
-        a.ns = cplan.ns;
-        a.st = cplan.st;
+        a.ns = a.st = 0;  // (the kernel lays out its rings)
         a.off_bar = cplan.off_bar;
         a.off_ax = cplan.off_ax;
-        a.off_p = cplan.off_p;
+        a.ring_bytes = cplan.ring_bytes;
         a.off_h = cplan.off_h;
         a.h_bytes = cplan.h_bytes;
-        void (*kern)(LayerArgs) = dots ? decode_cluster_kernel<kClusterMaxT, true>
-                                       : decode_cluster_kernel<kClusterMaxT, false>;
+        a.y_part = ws.y_unit;
+        void (*kern)(LayerArgs) =
+            T <= 8 ? (dots ? decode_cluster_kernel<8, true> : decode_cluster_kernel<8, false>)
+                   : (dots ? decode_cluster_kernel<kClusterMaxT, true> : decode_cluster_kernel<kClusterMaxT, false>);
         if ((err = launch_cluster(kern, a, num_sms, cplan.smem, dev, s)) != cudaSuccess) return err;
         for (int i = 2; i <= 5; ++i)
             if ((err = mark(i)) != cudaSuccess) return err;

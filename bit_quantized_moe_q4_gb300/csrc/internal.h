@@ -46,7 +46,9 @@ struct Workspace {
     float* gu_part;         // [nsg, T*k, 2I] K parts of the gate/up row sums, bucket order
     int8_t* q_h;            // [T*k, I]      (stage output)
     uint16_t* d_h;          // [T*k, I/32]
-    float* y_part;          // [parts, T*k, H] parts of the weighted expert outputs
+    float* y_part;          // [nsd, T*k, H] K parts of the weighted expert outputs (task kernel)
+    float* y_unit;          // [I/128, T*k, H] h-block parts (clustered kernel; shares memory
+                            // with gu_part and y_part)
     int32_t* sync;          // counters of the layer kernel, cleared by its prep kernel
     uint16_t* xbuf0;        // [T, H] decode stack: layer outputs inside the stack (ping-pong)
     uint16_t* xbuf1;
@@ -145,9 +147,9 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
                          int* nsd_max);
 // Counters the decode prep kernel clears.
 int decode_sync_ints(int T, int H, int I, int E, int k);
-// Parts of the weighted expert outputs the decode layer may store (the
-// y_part buffer holds that many [T*k, H] planes).
-int decode_y_parts(int T, int H, int I, int E, int k);
+// Parts of the weighted expert outputs the clustered decode kernel stores
+// (I/128 planes of [T*k, H]), or 0 when the shape never takes that kernel.
+int decode_cluster_parts(int T, int H, int I, int E);
 // xn[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), one warp per token.
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* xn,
                            cudaStream_t s);

@@ -247,7 +247,7 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
  * (programmatic dependent launch): a prep kernel (router logits, int8 codes
  * of x, and the clearing of the counters the layer kernel synchronises on)
  * and a cooperative layer kernel (one CTA per SM: top-k, buckets, gate/up,
- * h, down and the combine).  For T <= 8 the layer kernel runs in clusters
+ * h, down and the combine).  For T <= 16 the layer kernel runs in clusters
  * of two CTAs that share each (expert, 128-feature block of h) unit through
  * distributed shared memory; for larger T it splits the experts' rows and K
  * ranges over all CTAs.  The prep kernel reads `wr` before the work that
@@ -307,8 +307,8 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
  * cudaMalloc, cudaFree or allocating library routine is called.
  *   - Shapes whose workspace (moe_workspace_bytes(MOE_MODE_DECODE, ...)) is
  *     larger than the array are rejected with MOE_ERR_WORKSPACE; 8 MiB covers
- *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8 (6.2 MiB at most, at
- *     T = 8).
+ *     T <= 32 at H = 2048, I = 768, E <= 256, k = 8 (6.4 MiB at most, at
+ *     T = 16).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
