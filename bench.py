@@ -39,7 +39,7 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # current kernels
 NCU_TRAFFIC_DECODE_LAYER_T1 = None
 NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch at T=2048
-# kernels of one decode layer: prep (logits, x codes) and, for T <= 8, the
+# kernels of one decode layer: prep (logits, x codes) and, for T <= 16, the
 # clustered expert kernel and the combine kernel; else the task kernel (top-k,
 # buckets, experts, combine)
 
