@@ -20,7 +20,8 @@ __all__ = [
     "MoeError", "MoeDebug", "load_library", "build",
     "moe_version", "moe_q4_packed_bytes", "moe_q4_pack", "moe_q4_quantize", "moe_route_topk",
     "moe_workspace_bytes", "moe_q4_forward_prefill", "moe_w4a8_forward_decode",
-    "moe_w4a8_forward_decode_stack", "moe_get_device_status", "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
+    "moe_w4a8_forward_decode_stack", "moe_q4_forward_prefill_stack_streamed", "moe_get_device_status",
+    "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -39,13 +40,14 @@ MOE_OUT_FP32 = 1
 MOE_STACKED_PRENORM = 2
 MOE_MODE_PREFILL = 0
 MOE_MODE_DECODE = 1
+MOE_MODE_PREFILL_STREAMED = 2
 MOE_DECODE_MAX_T = 32
 
 EXPORTED_SYMBOLS = (
     "moe_version", "moe_last_error_string", "moe_get_device_status", "moe_clear_device_status",
     "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk", "moe_workspace_bytes",
     "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
-    "moe_q4_quantize", "moe_w4a8_forward_decode_stack",
+    "moe_q4_quantize", "moe_w4a8_forward_decode_stack", "moe_q4_forward_prefill_stack_streamed",
 )
 MOE_DECODE_MAX_LAYERS = 64
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -102,6 +104,8 @@ def load_library(path: str | None = None):
                                                  _vp]),
         "moe_w4a8_forward_decode_stack": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                                ctypes.c_uint, _vp, _vp, _sz, _vp]),
+        "moe_q4_forward_prefill_stack_streamed": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                                       ctypes.c_uint, _vp, _vp, _sz, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -115,6 +119,14 @@ def _check(rc: int) -> None:
     if rc != MOE_OK:
         msg = load_library().moe_last_error_string().decode(errors="replace")
         raise MoeError(rc, msg)
+
+
+def _host_ptr(t: torch.Tensor):
+    if t.is_cuda or not t.is_pinned():
+        raise MoeError(MOE_ERR_INVALID_ARG, "streamed expert weights must be pinned CPU tensors")
+    if not t.is_contiguous():
+        raise MoeError(MOE_ERR_INVALID_ARG, "tensor arguments must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _ptr(t: torch.Tensor | None):
@@ -291,6 +303,33 @@ def moe_w4a8_forward_decode_stack(x, layers, I: int, k: int, out=None, out_fp32:
             for j in range(3)]
     flags = (MOE_OUT_FP32 if out_fp32 else 0) | (MOE_STACKED_PRENORM if prenorm else 0)
     _check(load_library().moe_w4a8_forward_decode_stack(
+        _ptr(x), L, arrs[0], arrs[1], arrs[2], T, H, I, E, k, flags, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_q4_forward_prefill_stack_streamed(x, layers, I: int, k: int, out=None,
+                                          out_fp32: bool = True, workspace=None, stream=None,
+                                          prenorm: bool = True):
+    """L stacked prefill layers whose packed experts stay in pinned host memory
+    and are copied to the GPU layer by layer, overlapped with compute.
+    ``layers``: a sequence of (wr on the device, wgu_packed and wd_packed as
+    pinned CPU tensors) per layer; layer l + 1 reads layer l's output rounded
+    to bf16.  Returns the last layer's output [T, H]."""
+    T, H = x.shape
+    L = len(layers)
+    E = layers[0][0].shape[0] if L else 0
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(moe_workspace_bytes(MOE_MODE_PREFILL_STREAMED, T, H, I, E, k), 1),
+                                dtype=torch.uint8, device=x.device)
+    arrs = [(ctypes.c_void_p * max(L, 1))(*[(_ptr(layer[j]) if j == 0 else _host_ptr(layer[j])).value
+                                            for layer in layers])
+            for j in range(3)]
+    flags = (MOE_OUT_FP32 if out_fp32 else 0) | (MOE_STACKED_PRENORM if prenorm else 0)
+    _check(load_library().moe_q4_forward_prefill_stack_streamed(
         _ptr(x), L, arrs[0], arrs[1], arrs[2], T, H, I, E, k, flags, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

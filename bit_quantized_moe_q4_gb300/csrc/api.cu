@@ -33,6 +33,10 @@ struct DeviceInfo {
     bool supported = false;
     int num_sms = 0;
     int* status = nullptr;  // device address of g_device_status
+    // the streamed prefill stack: its copy stream and events (created on
+    // first use)
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_copied[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -448,10 +452,29 @@ int moe_route_topk(const uint16_t* x_bf16, const float* wr, int T, int H, int E,
                       "route");
 }
 
+// The streamed prefill stack's workspace: the prefill workspace, two staging
+// buffers of one layer's packed experts (gate/up, then down), two [T, H]
+// bf16 activations.
+struct StreamedPlan {
+    size_t prefill, gu, d, stage, act, total;
+};
+StreamedPlan streamed_plan(int T, int H, int I, int E, int k) {
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    StreamedPlan p{};
+    p.prefill = al(carve(MOE_MODE_PREFILL, T, H, I, E, k, nullptr, nullptr));
+    p.gu = moe_q4_packed_bytes(E, 2 * I, H);
+    p.d = moe_q4_packed_bytes(E, H, I);
+    p.stage = al(p.gu) + al(p.d);
+    p.act = al((size_t)T * H * 2);
+    p.total = p.prefill + 2 * p.stage + 2 * p.act;
+    return p;
+}
+
 size_t moe_workspace_bytes(int mode, int T, int H, int I, int E, int k) {
-    if ((mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE) || T < 0 || H <= 0 || I <= 0 ||
-        E <= 0 || k <= 0)
+    if ((mode != MOE_MODE_PREFILL && mode != MOE_MODE_DECODE && mode != MOE_MODE_PREFILL_STREAMED) ||
+        T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0)
         return 0;
+    if (mode == MOE_MODE_PREFILL_STREAMED) return streamed_plan(T, H, I, E, k).total;
     return carve(mode, T, H, I, E, k, nullptr, nullptr);
 }
 
@@ -469,6 +492,100 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void*
                             moe_debug* dbg, void* stream) {
     return forward(MOE_MODE_DECODE, x_bf16, wr, wgu_packed, wd_packed, T, H, I, E, k, flags, out,
                    workspace, ws_bytes, dbg, stream);
+}
+
+int moe_q4_forward_prefill_stack_streamed(const uint16_t* x_bf16, int L, const float* const* wr,
+                                          const void* const* wgu_host, const void* const* wd_host,
+                                          int T, int H, int I, int E, int k, unsigned flags,
+                                          void* out, void* workspace, size_t ws_bytes,
+                                          void* stream) {
+    int rc = check_layer_shape(MOE_MODE_PREFILL, T, H, I, E, k);
+    if (rc) return rc;
+    if (flags & ~(MOE_OUT_FP32 | MOE_STACKED_PRENORM))
+        return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (L < 1 || L > MOE_DECODE_MAX_LAYERS)
+        return set_err(MOE_ERR_SHAPE, "L=%d must satisfy 1 <= L <= %d", L, MOE_DECODE_MAX_LAYERS);
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !wr || !wgu_host || !wd_host || !out)
+        return set_err(MOE_ERR_INVALID_ARG, "null argument");
+    for (int l = 0; l < L; ++l) {
+        if (!wr[l] || !wgu_host[l] || !wd_host[l])
+            return set_err(MOE_ERR_INVALID_ARG, "null weight pointer of layer %d", l);
+        if (!aligned16(wr[l]) || !aligned16(wgu_host[l]) || !aligned16(wd_host[l]))
+            return set_err(MOE_ERR_ALIGN, "weights of layer %d must be 16-byte aligned", l);
+    }
+    if (!aligned16(x_bf16) || !aligned16(out) || !aligned16(workspace))
+        return set_err(MOE_ERR_ALIGN, "tensor arguments must be 16-byte aligned");
+    if (out == static_cast<const void*>(x_bf16))
+        return set_err(MOE_ERR_INVALID_ARG, "out may not alias x");
+    const StreamedPlan sp = streamed_plan(T, H, I, E, k);
+    if (!workspace || ws_bytes < sp.total)
+        return set_err(MOE_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", sp.total, ws_bytes);
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    // the expert weights must be page-locked host memory
+    for (int l = 0; l < L; ++l) {
+        for (const void* p : {wgu_host[l], wd_host[l]}) {
+            cudaPointerAttributes at{};
+            if (cudaPointerGetAttributes(&at, p) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+                cudaGetLastError();
+                return set_err(MOE_ERR_INVALID_ARG,
+                               "expert weights of layer %d must be pinned host memory", l);
+            }
+        }
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!dev->copy_stream) {
+            if ((rc = cuda_check(cudaStreamCreateWithFlags(&dev->copy_stream, cudaStreamNonBlocking),
+                                 "copy stream")))
+                return rc;
+            cudaEvent_t* evs[5] = {&dev->ev_fork, &dev->ev_copied[0], &dev->ev_copied[1], &dev->ev_done[0],
+                                   &dev->ev_done[1]};
+            for (cudaEvent_t* e : evs)
+                if ((rc = cuda_check(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "copy events")))
+                    return rc;
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream), cs = dev->copy_stream;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint8_t* stage[2] = {base + sp.prefill, base + sp.prefill + sp.stage};
+    uint16_t* act[2] = {reinterpret_cast<uint16_t*>(base + sp.prefill + 2 * sp.stage),
+                        reinterpret_cast<uint16_t*>(base + sp.prefill + 2 * sp.stage + sp.act)};
+    const size_t gu_off = 0, d_off = (sp.gu + 255) & ~(size_t)255;
+    // the copies start after the work the caller enqueued before this call
+    if ((rc = cuda_check(cudaEventRecord(dev->ev_fork, s), "fork"))) return rc;
+    if ((rc = cuda_check(cudaStreamWaitEvent(cs, dev->ev_fork, 0), "fork"))) return rc;
+    auto copy_layer = [&](int l) -> int {
+        uint8_t* st = stage[l & 1];
+        int r;
+        if ((r = cuda_check(cudaMemcpyAsync(st + gu_off, wgu_host[l], sp.gu, cudaMemcpyHostToDevice, cs),
+                            "expert copy")))
+            return r;
+        if ((r = cuda_check(cudaMemcpyAsync(st + d_off, wd_host[l], sp.d, cudaMemcpyHostToDevice, cs),
+                            "expert copy")))
+            return r;
+        return cuda_check(cudaEventRecord(dev->ev_copied[l & 1], cs), "copy event");
+    };
+    for (int l = 0; l < L && l < 2; ++l)
+        if ((rc = copy_layer(l))) return rc;
+    for (int l = 0; l < L; ++l) {
+        const bool last = l == L - 1;
+        if ((rc = cuda_check(cudaStreamWaitEvent(s, dev->ev_copied[l & 1], 0), "copy wait"))) return rc;
+        const uint16_t* xin = l == 0 ? x_bf16 : act[(l - 1) & 1];
+        void* dst = last ? out : static_cast<void*>(act[l & 1]);
+        const unsigned f = (flags & MOE_STACKED_PRENORM) | (last ? (flags & MOE_OUT_FP32) : 0u);
+        if ((rc = forward(MOE_MODE_PREFILL, xin, wr[l], stage[l & 1] + gu_off, stage[l & 1] + d_off, T, H,
+                          I, E, k, f, dst, workspace, sp.prefill, nullptr, stream)))
+            return rc;
+        if (l + 2 < L) {
+            // layer l + 2 refills the buffer once layer l has read it
+            if ((rc = cuda_check(cudaEventRecord(dev->ev_done[l & 1], s), "layer event"))) return rc;
+            if ((rc = cuda_check(cudaStreamWaitEvent(cs, dev->ev_done[l & 1], 0), "layer wait"))) return rc;
+            if ((rc = copy_layer(l + 2))) return rc;
+        }
+    }
+    return MOE_OK;
 }
 
 int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* const* wr,

@@ -90,6 +90,7 @@ extern "C" {
 /* ---- forward modes for moe_workspace_bytes ------------------------------- */
 #define MOE_MODE_PREFILL 0
 #define MOE_MODE_DECODE  1
+#define MOE_MODE_PREFILL_STREAMED 2  /* moe_q4_forward_prefill_stack_streamed */
 
 /*
  * Optional stage outputs of a forward call (all DEVICE pointers, each may be
@@ -291,6 +292,49 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
                                   const void* const* wgu_packed, const void* const* wd_packed,
                                   int T, int H, int I, int E, int k, unsigned flags, void* out,
                                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * moe_q4_forward_prefill_stack_streamed — L consecutive prefill layers whose
+ * packed expert weights stay in HOST memory and are streamed to the GPU layer
+ * by layer, overlapped with the layers' compute.  This is the pages' prefill
+ * mechanism (the page, Methodology 1 "Prefill (GPU)": the experts live in
+ * host RAM and move to the GPU one layer at a time) on the host-to-GPU link
+ * of this machine, for models whose experts do not fit in device memory.
+ *
+ * The call enqueues, on the caller's stream and a copy stream of the
+ * library, per layer l:
+ *   - one cudaMemcpyAsync for layer l's gate/up weights and one for its
+ *     down weights, into staging buffer l % 2 of the workspace;
+ *   - the layer itself (the kernels of moe_q4_forward_prefill) once that
+ *     copy is done.
+ * Layer l + 2's copies wait for layer l's kernels, which read the same
+ * buffer.  Events link the two streams, so the call can be captured into a
+ * CUDA graph.  Layer l + 1 reads layer l's output rounded to bf16 (kept in
+ * the workspace); the result equals, bit for bit, L moe_q4_forward_prefill
+ * calls chained through bf16 outputs with the same flags and the weights
+ * in device memory.  MOE_OUT_FP32 applies to the last layer only.
+ *   x_bf16     [T, H] DEVICE, input of layer 0 (not written)
+ *   L          1 <= L <= MOE_DECODE_MAX_LAYERS
+ *   wr         HOST array of L DEVICE pointers to the router weights
+ *   wgu_host, wd_host
+ *              HOST arrays of L HOST pointers to each layer's packed weights
+ *              (layouts as in moe_q4_forward_prefill).  They must be pinned
+ *              (page-locked: cudaHostAlloc or cudaHostRegister), else
+ *              MOE_ERR_INVALID_ARG.  They must not change until the work
+ *              the call enqueued has finished.
+ *   out        the last layer's output [T, H]; may not alias x
+ *   workspace  >= moe_workspace_bytes(MOE_MODE_PREFILL_STREAMED, T, H, I, E, k)
+ *              bytes: the prefill workspace, two staging buffers of one
+ *              layer's experts, and two [T, H] bf16 activations.
+ * Shapes as for moe_q4_forward_prefill.  The first call on a device creates
+ * the copy stream and its events; make that first call before any stream
+ * capture.
+ */
+int moe_q4_forward_prefill_stack_streamed(const uint16_t* x_bf16, int L, const float* const* wr,
+                                          const void* const* wgu_host, const void* const* wd_host,
+                                          int T, int H, int I, int E, int k, unsigned flags,
+                                          void* out, void* workspace, size_t ws_bytes,
+                                          void* stream);
 
 /*
  * moe_w4a8_forward_decode_noalloc — the same decode layer as

@@ -151,3 +151,36 @@ def test_quantize_argument_checks(lib):
     assert q(0, FAKE, 4, 64, 1, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG       # block18 + scales
     assert q(0, FAKE + 4, 4, 64, 0, FAKE, FAKE, None) == moe.MOE_ERR_ALIGN
     assert q(0, FAKE, 0, 64, 0, None, None, None) == moe.MOE_OK                     # nothing to do
+
+
+def _streamed(lib, L=2, T=4, H=256, I=128, E=8, k=2, flags=2, x=FAKE, layer=(FAKE, FAKE, FAKE),
+              bad_layer=None, out=FAKE * 2, ws=FAKE * 3, ws_bytes=1 << 40):
+    ptrs = [list(layer) for _ in range(max(L, 1))]
+    if bad_layer is not None:
+        ptrs[bad_layer[0]][bad_layer[1]] = bad_layer[2]
+    arrs = [(ctypes.c_void_p * len(ptrs))(*[p[j] for p in ptrs]) for j in range(3)]
+    return lib.moe_q4_forward_prefill_stack_streamed(x, L, arrs[0], arrs[1], arrs[2], T, H, I, E, k,
+                                                     flags, out, ws, ws_bytes, None)
+
+
+def test_prefill_stack_streamed_argument_checks(lib):
+    # every refusal here comes before the library touches the GPU
+    assert _streamed(lib, L=0) == moe.MOE_ERR_SHAPE
+    assert _streamed(lib, L=moe.MOE_DECODE_MAX_LAYERS + 1) == moe.MOE_ERR_SHAPE
+    assert _streamed(lib, H=200) == moe.MOE_ERR_SHAPE
+    assert _streamed(lib, flags=4) == moe.MOE_ERR_INVALID_ARG
+    assert _streamed(lib, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert _streamed(lib, bad_layer=(1, 1, None)) == moe.MOE_ERR_INVALID_ARG  # layer 1's gate/up
+    assert b"layer 1" in lib.moe_last_error_string()
+    assert _streamed(lib, bad_layer=(0, 2, FAKE + 8)) == moe.MOE_ERR_ALIGN
+    assert _streamed(lib, out=FAKE) == moe.MOE_ERR_INVALID_ARG               # out aliases x
+    assert _streamed(lib, ws_bytes=16) == moe.MOE_ERR_WORKSPACE
+    assert _streamed(lib, T=0) == moe.MOE_OK                                 # empty input: no-op
+
+
+def test_streamed_workspace_holds_two_layers_of_experts():
+    T, H, I, E, k = 2048, 2048, 768, 128, 8
+    pre = moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL, T, H, I, E, k)
+    experts = moe.moe_q4_packed_bytes(E, 2 * I, H) + moe.moe_q4_packed_bytes(E, H, I)
+    got = moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL_STREAMED, T, H, I, E, k)
+    assert pre + 2 * experts + 2 * T * H * 2 <= got <= pre + 2 * experts + 2 * T * H * 2 + 8 * 256
