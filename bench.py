@@ -28,6 +28,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "MoE-layer prefill tokens/s and decode µs/token; % of HBM / tensor roofline"
 DECODE_LAYERS = 16          # distinct weight copies per decode step
+STREAMED_LAYERS = 8         # layers of the stacked prefill timed with host-resident experts
 GU_BYTES_PER_EXPERT = 2 * 768 * 2048 * 18 // 32   # packed gate/up bytes of one expert
 D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one expert
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel as
@@ -376,7 +377,52 @@ def bench_prefill_stack(steps, warmup, torch, moe, device, barrier):
     res = {"workload": "stacked", "layers": L, "T": T, "E": E, "ms_per_stack": ms_stack,
            "ms_per_layer": ms_stack / L, "tokens_per_s": T / (ms_stack * 1e-3),
            "expert_tflops": flop * L / (ms_stack * 1e-3) / 1e12}
-    del layers, x0, bufs, ws
+    # NEXT-3: the first NS layers with their experts in pinned host memory,
+    # streamed to the GPU layer by layer (moe_q4_forward_prefill_stack_streamed)
+    NS = STREAMED_LAYERS
+    gu_b, d_b = layers[0][1].numel(), layers[0][2].numel()
+    pinned = torch.empty(NS * (gu_b + d_b), dtype=torch.uint8, pin_memory=True)
+    host = []
+    for l in range(NS):
+        o = l * (gu_b + d_b)
+        pinned[o:o + gu_b].copy_(layers[l][1])
+        pinned[o + gu_b:o + gu_b + d_b].copy_(layers[l][2])
+        host.append((layers[l][0], pinned[o:o + gu_b], pinned[o + gu_b:o + gu_b + d_b]))
+    sws = torch.empty(moe.moe_workspace_bytes(moe.MOE_MODE_PREFILL_STREAMED, T, H, I, E, k),
+                      dtype=torch.uint8, device=device)
+    sout = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+
+    def streamed():
+        moe.moe_q4_forward_prefill_stack_streamed(x0, host, I, k, out=sout, out_fp32=False,
+                                                  workspace=sws, prenorm=True)
+
+    streamed()
+    cur = x0  # the same layers on device-resident weights, for the bits check
+    for l in range(NS):
+        nxt = bufs[l % 2]
+        moe.moe_q4_forward_prefill(cur, layers[l][0], layers[l][1], layers[l][2], I, k, out=nxt,
+                                   out_fp32=False, workspace=ws, prenorm=True)
+        cur = nxt
+    torch.cuda.synchronize()
+    same = bool(torch.equal(sout.view(torch.int16), cur.view(torch.int16)))
+    barrier()
+    nst = max(2, steps // 4)
+    t0.record(stream)
+    for _ in range(nst):
+        streamed()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_str = t0.elapsed_time(t1) / nst
+    res["streamed"] = {
+        "entry": "moe_q4_forward_prefill_stack_streamed (experts in pinned host memory, copied "
+                 "layer by layer on a copy stream, overlapped with the layers' kernels)",
+        "layers": NS, "ms_per_layer": ms_str / NS,
+        "expert_bytes_per_layer": gu_b + d_b,
+        "h2d_gbs": (gu_b + d_b) * NS / (ms_str * 1e-3) / 1e9,
+        "device_resident_ms_per_layer": ms_stack / L,
+        "equals_device_chain_bits": same,
+    }
+    del layers, x0, bufs, ws, host, pinned, sws, sout
     torch.cuda.empty_cache()
     return res
 
