@@ -130,6 +130,36 @@ def q4_from_blocks18(blocks: np.ndarray):
     return codes.reshape(*lead, nb * GROUP), scales
 
 
+def q8_encode(w: np.ndarray):
+    """Encode float weights into 8-bit blocks (READING of a Q8_0-style rule).
+
+    The companion page (mlsanity.com 2607.14568, abstract) runs 8-bit weights
+    against 4-bit ones without printing the format; the plainest member of the
+    same family: per block of 32, d = fp16(amax / 127), amax the block's
+    largest magnitude; q_i = clamp(round_half_away_from_zero(x_i / d), -127,
+    127), taken against the stored (fp16-rounded) d; a block of zeros has
+    d = 0 and all q = 0.  Returns (codes int8, scales fp16)."""
+    w = np.asarray(w, dtype=np.float64)
+    *lead, K = w.shape
+    b = w.reshape(*lead, K // GROUP, GROUP)
+    amax = np.abs(b).max(axis=-1)
+    d16 = (amax / 127.0).astype(np.float16)
+    d = d16.astype(np.float64)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(d != 0, b / np.where(d != 0, d, 1.0), 0.0)
+    q = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    return q.reshape(*lead, K), d16
+
+
+def q8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Decode 8-bit weights: w = d * q (exact in float64)."""
+    codes = np.asarray(codes)
+    *lead, K = codes.shape
+    q = codes.astype(np.int64)
+    d = np.asarray(scales).astype(np.float64)
+    return (q.reshape(*lead, K // GROUP, GROUP) * d[..., None]).reshape(*lead, K)
+
+
 # --------------------------------------------------------------------------
 # Router (Methodology 1: tokens are routed to experts before the grouped GEMM)
 # --------------------------------------------------------------------------
@@ -259,6 +289,24 @@ def w4a8_rows(codes: np.ndarray, scales: np.ndarray, qa: np.ndarray, da: np.ndar
     return (dw * dA * G).sum(axis=-1), G
 
 
+def group_dots8(codes: np.ndarray, qa: np.ndarray) -> np.ndarray:
+    """W8A8 integer group dot products: G[..., r, g] = sum over i in block g
+    of codes[r, i] * qa[..., i], exact in int64.  ``codes`` int8 [R, K]."""
+    w = np.asarray(codes).astype(np.int64)
+    a = np.asarray(qa).astype(np.int64)
+    R, K = w.shape
+    prod = a[..., None, :] * w
+    return prod.reshape(*prod.shape[:-1], K // GROUP, GROUP).sum(axis=-1)
+
+
+def w8a8_rows(codes: np.ndarray, scales: np.ndarray, qa: np.ndarray, da: np.ndarray):
+    """Rows of a W8A8 projection: y_r = sum_g d_w[r, g] * d_a[g] * G[r, g]."""
+    G = group_dots8(codes, qa)
+    dw = np.asarray(scales).astype(np.float64)
+    dA = np.asarray(da).astype(np.float64)[..., None, :]
+    return (dw * dA * G).sum(axis=-1), G
+
+
 # --------------------------------------------------------------------------
 # The layer
 # --------------------------------------------------------------------------
@@ -320,8 +368,10 @@ def moe_dense_bruteforce(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k):
 
 
 def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=None,
-               keep_dots=False, prenorm=False):
-    """Decode layer with W4A8 arithmetic (Methodology 1, "Decode (CPU)").
+               keep_dots=False, prenorm=False, wbits=4):
+    """Decode layer with W4A8 arithmetic (Methodology 1, "Decode (CPU)"), or
+    with 8-bit weights (``wbits=8``: int8 codes, ``w8a8_rows``; the companion
+    page's 8-bit setting) and otherwise the same steps.
 
     The bf16 hidden state is quantised to int8 per 32 (``act_quant``); gate
     and up rows are exact integer group dots scaled by d_w * d_x; h =
@@ -340,6 +390,7 @@ def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=Non
     n, H = X64.shape
     I = gu_codes.shape[1] // 2
     logits, idx, w = route(X64, wr, k)
+    rows = w8a8_rows if wbits == 8 else w4a8_rows
     qx, dx = act_quant(X32)
     out = residual.copy()
     qh = np.zeros((n, k, I), np.int64)
@@ -350,11 +401,11 @@ def moe_decode(x_bits, wr, gu_codes, gu_scales, d_codes, d_scales, k, tokens=Non
     for t in range(n):
         for j in range(k):
             e = idx[t, j]
-            gu, G_gu = w4a8_rows(gu_codes[e], gu_scales[e], qx[t], dx[t])
+            gu, G_gu = rows(gu_codes[e], gu_scales[e], qx[t], dx[t])
             h = swiglu(gu[:I], gu[I:])
             hh[t, j] = h
             qh[t, j], dh[t, j] = act_quant(h.astype(np.float32))
-            y, G_d = w4a8_rows(d_codes[e], d_scales[e], qh[t, j], dh[t, j])
+            y, G_d = rows(d_codes[e], d_scales[e], qh[t, j], dh[t, j])
             out[t] += w[t, j] * y
             if keep_dots:
                 dots_gu[(t, j)] = G_gu
