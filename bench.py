@@ -134,7 +134,7 @@ def _device_layer(li, torch, moe, device):
     return x, wr, pack(li.gu_codes, li.gu_scales), pack(li.d_codes, li.d_scales)
 
 
-def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS):
+def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS, w8=True):
     """A chain of L pre-norm decode layers (distinct weight copies) in one CUDA
     graph: layer l + 1 decodes layer l's bf16 output."""
     import workloads
@@ -252,8 +252,70 @@ def bench_decode(T, steps, warmup, torch, moe, device, barrier, L=DECODE_LAYERS)
             "kernels_per_step": L * kernels_per_decode_layer(T),
         },
     }
+    if w8 and T <= moe.MOE_W8_DECODE_MAX_T:
+        res["w8"] = _decode_w8_chain(li, x, [l[0] for l in layers], outs[-1], distinct, ws, steps,
+                                     warmup, torch, moe, device, barrier)
     del layers, outs, ws, g, gs
     torch.cuda.empty_cache()
+    return res
+
+
+def _decode_w8_chain(li, x, wrs, ref_out, distinct, ws, steps, warmup, torch, moe, device, barrier):
+    """The same chain on the 8-bit weight path: each layer's 4-bit codes
+    written as int8 (q - 8) with the same scales, packed as 8-bit tiles, so
+    the layers move 34/18 of the 4-bit bytes and must return the 4-bit
+    chain's bits."""
+    T = li.T
+
+    def pack8(codes, scales):
+        E, N, K = codes.shape
+        c = torch.from_numpy((codes.astype(np.int16) - 8).astype(np.int8)).to(device)
+        s = torch.from_numpy(scales.view(np.int16)).to(device)
+        out = moe.moe_q8_pack(c, s, E, N, K)
+        del c, s
+        return out
+
+    wgu8, wd8 = pack8(li.gu_codes, li.gu_scales), pack8(li.d_codes, li.d_scales)
+    layers8 = [(wr, wgu8.clone(), wd8.clone()) for wr in wrs]
+    del wgu8, wd8
+    outs8 = [torch.empty((T, li.H), dtype=torch.bfloat16, device=device) for _ in wrs]
+
+    def run():
+        cur = x
+        for l, (wr_l, wgu_l, wd_l) in enumerate(layers8):
+            moe.moe_w8a8_forward_decode(cur, wr_l, wgu_l, wd_l, li.I, li.k, out=outs8[l],
+                                        out_fp32=False, workspace=ws, prenorm=True)
+            cur = outs8[l]
+
+    run()
+    torch.cuda.synchronize()
+    same = bool(torch.equal(outs8[-1].view(torch.int16), ref_out.view(torch.int16)))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        run()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    L = len(wrs)
+    expert_bytes8 = (GU_BYTES_PER_EXPERT + D_BYTES_PER_EXPERT) * 34 // 18
+    layer_bytes = [d * expert_bytes8 + li.E * li.H * 4 + T * li.H * (2 + 2) for d in distinct]
+    us_layer = ms * 1e3 / L
+    res = {
+        "entry": "moe_w8a8_forward_decode (8-bit tiles: 32 int8 codes + one fp16 scale per group)",
+        "equals_4bit_chain_bits": same, "ms_per_step": ms, "us_per_layer": us_layer,
+        "us_per_token": us_layer / T, "algorithmic_bytes_per_layer": statistics.mean(layer_bytes),
+        "layer_gbs": statistics.mean(layer_bytes) / (us_layer * 1e-6) / 1e9,
+    }
+    del layers8, outs8, g
     return res
 
 
@@ -593,6 +655,8 @@ def main():
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one workload only (short profiling runs)")
     ap.add_argument("--decode-tokens", type=str, default="1,4,16")
+    ap.add_argument("--no-w8", action="store_true",
+                    help="leave the 8-bit-weight decode chain out")
     ap.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
                     help="layers in the decode chain (fewer: smaller profiling runs)")
     ap.add_argument("--prefill-workload", choices=["prefill", "skewed", "stacked"],
@@ -630,7 +694,7 @@ def main():
     pre = skew = stack = None
     with ClockSampler(local) as clk:
         dec = {T: bench_decode(T, args.steps, warm, torch, moe, device, barrier,
-                               L=args.decode_layers) for T in dec_T}
+                               L=args.decode_layers, w8=not args.no_w8) for T in dec_T}
         if args.only == "prefill":
             if args.prefill_workload == "stacked":
                 pre = bench_prefill_stack(min(args.steps, 10), warm, torch, moe, device, barrier)

@@ -20,7 +20,8 @@ __all__ = [
     "MoeError", "MoeDebug", "load_library", "build",
     "moe_version", "moe_q4_packed_bytes", "moe_q4_pack", "moe_q4_quantize", "moe_route_topk",
     "moe_workspace_bytes", "moe_q4_forward_prefill", "moe_w4a8_forward_decode",
-    "moe_w4a8_forward_decode_stack", "moe_q4_forward_prefill_stack_streamed", "moe_get_device_status",
+    "moe_w4a8_forward_decode_stack", "moe_q4_forward_prefill_stack_streamed", "moe_q8_packed_bytes",
+    "moe_q8_pack", "moe_w8a8_forward_decode", "moe_get_device_status",
     "moe_clear_device_status", "make_debug", "EXPORTED_SYMBOLS",
 ]
 
@@ -42,12 +43,14 @@ MOE_MODE_PREFILL = 0
 MOE_MODE_DECODE = 1
 MOE_MODE_PREFILL_STREAMED = 2
 MOE_DECODE_MAX_T = 32
+MOE_W8_DECODE_MAX_T = 16
 
 EXPORTED_SYMBOLS = (
     "moe_version", "moe_last_error_string", "moe_get_device_status", "moe_clear_device_status",
     "moe_q4_packed_bytes", "moe_q4_pack", "moe_route_topk", "moe_workspace_bytes",
     "moe_q4_forward_prefill", "moe_w4a8_forward_decode", "moe_w4a8_forward_decode_noalloc",
     "moe_q4_quantize", "moe_w4a8_forward_decode_stack", "moe_q4_forward_prefill_stack_streamed",
+    "moe_q8_packed_bytes", "moe_q8_pack", "moe_w8a8_forward_decode",
 )
 MOE_DECODE_MAX_LAYERS = 64
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -92,6 +95,10 @@ def load_library(path: str | None = None):
         "moe_clear_device_status": (_i, [_vp]),
         "moe_q4_packed_bytes": (_sz, [_i, _i, _i]),
         "moe_q4_pack": (_i, [_i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+        "moe_q8_packed_bytes": (_sz, [_i, _i, _i]),
+        "moe_q8_pack": (_i, [_vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+        "moe_w8a8_forward_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_uint,
+                                         _vp, _vp, _sz, ctypes.POINTER(MoeDebug), _vp]),
         "moe_q4_quantize": (_i, [_i, _vp, ctypes.c_longlong, _i, _i, _vp, _vp, _vp]),
         "moe_route_topk": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
         "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -174,6 +181,22 @@ def moe_q4_pack(src: torch.Tensor, src_scales: torch.Tensor | None, E: int, N: i
     if out is None:
         out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=src.device)
     _check(load_library().moe_q4_pack(fmt, _ptr(src), _ptr(src_scales), E, N, K, _ptr(out),
+                                      out.numel() * out.element_size(), _stream(stream)))
+    return out
+
+
+def moe_q8_packed_bytes(E: int, N: int, K: int) -> int:
+    return int(load_library().moe_q8_packed_bytes(E, N, K))
+
+
+def moe_q8_pack(codes: torch.Tensor, scales: torch.Tensor, E: int, N: int, K: int,
+                out: torch.Tensor | None = None, stream=None):
+    """Packs 8-bit weights (int8 codes [E,N,K] + fp16 scales [E,N,K/32] as
+    int16 bits) into 8-bit tiles; returns the packed uint8 tensor."""
+    nbytes = moe_q8_packed_bytes(E, N, K)
+    if out is None:
+        out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=codes.device)
+    _check(load_library().moe_q8_pack(_ptr(codes), _ptr(scales), E, N, K, _ptr(out),
                                       out.numel() * out.element_size(), _stream(stream)))
     return out
 
@@ -265,6 +288,14 @@ def _forward(fn_name, x, wr, wgu_packed, wd_packed, I, k, out, out_fp32, workspa
               _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
               ctypes.byref(debug) if debug is not None else None, _stream(stream)))
     return out
+
+
+def moe_w8a8_forward_decode(x, wr, wgu_q8, wd_q8, I: int, k: int, out=None, out_fp32: bool = True,
+                            workspace=None, debug: MoeDebug | None = None, stream=None,
+                            prenorm: bool = False):
+    """One decode MoE layer with 8-bit expert weights (packed by moe_q8_pack)."""
+    return _forward("moe_w8a8_forward_decode", x, wr, wgu_q8, wd_q8, I, k, out, out_fp32,
+                    workspace, debug, stream, prenorm)
 
 
 def moe_q4_forward_prefill(x, wr, wgu_packed, wd_packed, I: int, k: int, out=None,

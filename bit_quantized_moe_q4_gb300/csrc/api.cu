@@ -236,9 +236,13 @@ int copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t s) {
 
 int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const void* wd, int T,
             int H, int I, int E, int k, unsigned flags, void* out, void* workspace,
-            size_t ws_bytes, moe_debug* dbg, void* stream) {
+            size_t ws_bytes, moe_debug* dbg, void* stream, int wbits = 4) {
     int rc = check_layer_shape(mode, T, H, I, E, k);
     if (rc) return rc;
+    if (wbits == 8 && T > 0 && !decode_w8_fits(T, H, I, E))
+        return set_err(MOE_ERR_SHAPE,
+                       "8-bit decode takes at most %d tokens and must fit the on-chip staging "
+                       "(T=%d H=%d I=%d E=%d)", MOE_W8_DECODE_MAX_T, T, H, I, E);
     if (flags & ~(MOE_OUT_FP32 | MOE_STACKED_PRENORM))
         return set_err(MOE_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (T == 0) return MOE_OK;
@@ -282,7 +286,7 @@ int forward(int mode, const uint16_t* x, const float* wr, const void* wgu, const
                                            dbg ? dbg->dots_gu : nullptr,
                                            dbg ? dbg->dots_d : nullptr,
                                            dbg != nullptr && (dbg->q_h || dbg->d_h), dev->status,
-                                           dev->num_sms, ev, capturing, s),
+                                           dev->num_sms, ev, capturing, s, wbits),
                              "decode")))
             return rc;
     } else {
@@ -492,6 +496,36 @@ int moe_w4a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void*
                             moe_debug* dbg, void* stream) {
     return forward(MOE_MODE_DECODE, x_bf16, wr, wgu_packed, wd_packed, T, H, I, E, k, flags, out,
                    workspace, ws_bytes, dbg, stream);
+}
+
+int moe_w8a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void* wgu_q8,
+                            const void* wd_q8, int T, int H, int I, int E, int k, unsigned flags,
+                            void* out, void* workspace, size_t ws_bytes, moe_debug* dbg,
+                            void* stream) {
+    return forward(MOE_MODE_DECODE, x_bf16, wr, wgu_q8, wd_q8, T, H, I, E, k, flags, out, workspace,
+                   ws_bytes, dbg, stream, 8);
+}
+
+size_t moe_q8_packed_bytes(int E, int N, int K) {
+    if (E <= 0 || N <= 0 || K <= 0 || N % kTileRows || K % kTileK) return 0;
+    return (size_t)E * (N / kTileRows) * (K / kTileK) * kTileBytes8;
+}
+
+int moe_q8_pack(const void* codes, const void* scales, int E, int N, int K, void* dst,
+                size_t dst_bytes, void* stream) {
+    if (!codes || !scales || !dst) return set_err(MOE_ERR_INVALID_ARG, "null argument");
+    if (E <= 0 || N <= 0 || K <= 0 || N % kTileRows || K % kTileK)
+        return set_err(MOE_ERR_SHAPE, "E=%d N=%d K=%d: N must be a multiple of %d and K of %d", E, N, K,
+                       kTileRows, kTileK);
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(dst))
+        return set_err(MOE_ERR_ALIGN, "pointers must be 16-byte aligned");
+    const size_t need = moe_q8_packed_bytes(E, N, K);
+    if (dst_bytes < need)
+        return set_err(MOE_ERR_INVALID_ARG, "dst holds %zu bytes, %zu needed", dst_bytes, need);
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    return cuda_check(launch_pack8(codes, scales, E, N, K, dst, static_cast<cudaStream_t>(stream)), "pack8");
 }
 
 int moe_q4_forward_prefill_stack_streamed(const uint16_t* x_bf16, int L, const float* const* wr,

@@ -18,6 +18,10 @@ constexpr int kTileRows = 128;        // rows per packed tile
 constexpr int kTileK = 64;            // columns per packed tile
 constexpr int kTileCodeBytes = 4096;  // 128 rows x 32 bytes
 constexpr int kTileBytes = 4608;      // codes + 128 rows x 2 fp16 scales
+// 8-bit weight tiles (the decode path's 8-bit variant): 128 rows x 64 int8
+// codes, then the same 128 x 2 fp16 scales
+constexpr int kTileCodeBytes8 = 8192;
+constexpr int kTileBytes8 = 8704;
 constexpr int kMaxExperts = 256;
 
 // ---- device status word: kernels record a timed-out wait here -------------

@@ -189,6 +189,56 @@ __device__ __forceinline__ int group_dot(const uint32_t (&wl)[4], const uint32_t
     return p + q;
 }
 
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// A lane's 32 codes of a tile row as words that pair with the activation
+// words of group_dot: WB = 4, the low and the high nibbles of its four code
+// words; WB = 8, the first and the second word of each of its four 8-code
+// chunks (stored in the activations' order).
+template <int WB>
+__device__ __forceinline__ void unpack_codes(const uint8_t* p, uint32_t (&wl)[4], uint32_t (&wh)[4]) {
+    if constexpr (WB == 8) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(p);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(p + 16);
+        wl[0] = v0.x; wh[0] = v0.y; wl[1] = v0.z; wh[1] = v0.w;
+        wl[2] = v1.x; wh[2] = v1.y; wl[3] = v1.z; wh[3] = v1.w;
+    } else {
+        const uint4 wv = *reinterpret_cast<const uint4*>(p);
+        wl[0] = wv.x & 0x0F0F0F0Fu; wl[1] = wv.y & 0x0F0F0F0Fu;
+        wl[2] = wv.z & 0x0F0F0F0Fu; wl[3] = wv.w & 0x0F0F0F0Fu;
+        wh[0] = (wv.x >> 4) & 0x0F0F0F0Fu; wh[1] = (wv.y >> 4) & 0x0F0F0F0Fu;
+        wh[2] = (wv.z >> 4) & 0x0F0F0F0Fu; wh[3] = (wv.w >> 4) & 0x0F0F0F0Fu;
+    }
+}
+
+// Group dot of WB-bit codes with one activation group: WB = 4 as group_dot
+// (codes 0..15, `init` = -8 * sum of the activations); WB = 8, signed codes
+// times signed activations from 0.
+template <int WB>
+__device__ __forceinline__ int group_dot_w(const uint32_t (&wl)[4], const uint32_t (&wh)[4],
+                                           const uint8_t* act, int init) {
+    if constexpr (WB == 8) {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(act);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(act + 16);
+        int p = 0, q = 0;
+        p = dp4a_ss(wl[0], a0.x, p);
+        q = dp4a_ss(wh[0], a0.y, q);
+        p = dp4a_ss(wl[1], a0.z, p);
+        q = dp4a_ss(wh[1], a0.w, q);
+        p = dp4a_ss(wl[2], a1.x, p);
+        q = dp4a_ss(wh[2], a1.y, q);
+        p = dp4a_ss(wl[3], a1.z, p);
+        q = dp4a_ss(wh[3], a1.w, q);
+        return p + q;
+    } else {
+        return group_dot(wl, wh, act, init);
+    }
+}
+
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -1442,9 +1492,13 @@ __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, in
     return i * RBh + (int)(j < (u64)RBh ? j : (u64)RBh);
 }
 
-template <int MAXNT, bool DOTS>
+template <int MAXNT, bool DOTS, int WB>
 __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& io, LayerShared& S,
                                              uint8_t* dsm, Pipe& pp) {
+    // WB: weight bits (4: Q4_0 tiles; 8: 8-bit tiles, same layout of rows and
+    // scales, one byte a code)
+    constexpr int TB = WB == 8 ? kTileBytes8 : kTileBytes;
+    constexpr int TCB = WB == 8 ? kTileCodeBytes8 : kTileCodeBytes;
     volatile int& s_abort = S.abort;
     const int T = a.T, H = a.H, I = a.I, k = a.k;
     const int KBg = H / kTileK, KBd = I / kTileK;
@@ -1495,13 +1549,13 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     const int cmax = S.cmax;
     const int pbytes = (2 * kUnitWorkers * cmax * kTileRows * 4 + 127) & ~127;
     const int rbytes = a.ring_bytes - pbytes;
-    const int st = T >= 4 && rbytes >= kGroups * 3 * kSlotTiles * kTileBytes ? kSlotTiles : 2;
-    const int ns = min(kRingStride, rbytes / (st * kTileBytes) / kGroups);
-    const int off_p = kGroups * ns * st * kTileBytes;
+    const int st = T >= 4 && rbytes >= kGroups * 3 * kSlotTiles * TB ? kSlotTiles : 2;
+    const int ns = min(kRingStride, rbytes / (st * TB) / kGroups);
+    const int off_p = kGroups * ns * st * TB;
     S.rns = ns;  // (every thread stores the same value)
     auto full_bar = [&](int g, int s) { return ring_bar(a, sbase, true, g, s); };
     auto empty_bar = [&](int g, int s) { return ring_bar(a, sbase, false, g, s); };
-    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * kTileBytes); };
+    auto slot_addr = [&](int g, int s) { return (uint32_t)((g * ns + s) * st * TB); };
     auto pbar = [&](int pb) { return sbase + a.off_bar + 8u * (2 * kMaxSlots + pb); };
     const int KCg = KBg / kClusterCTAs, kb0 = rank * KCg;  // this CTA's K part of gate/up
     const int cptg = (KCg + st - 1) / st;                    // gate/up chunks of a unit
@@ -1525,11 +1579,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                 int n;
                 if (j < cptg) {
                     const int rb = g ? RBh + hb : hb, u0 = j * st;
-                    src = io.wgu + ((e * RBg + rb) * KBg + kb0 + u0) * kTileBytes;
+                    src = io.wgu + ((e * RBg + rb) * KBg + kb0 + u0) * TB;
                     n = KCg - u0 < st ? KCg - u0 : st;
                 } else {
                     const int rbd = w + (j - cptg) * kUnitWorkers;
-                    src = io.wd + ((e * RBd + rbd) * KBd + 2 * hb) * kTileBytes;
+                    src = io.wd + ((e * RBd + rbd) * KBd + 2 * hb) * TB;
                     n = 2;
                 }
                 S.ctab_p[g][lane] = src;
@@ -1552,7 +1606,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                         ok = false;
                         break;
                     }
-                    const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * kTileBytes);
+                    const uint32_t bytes = (uint32_t)(S.ctab_n[g][j] * TB);
                     S.slot_chunk[g * kRingStride + slot] = cidx;
                     mbar_arrive_expect_tx(full_bar(g, slot), bytes);
                     bulk_g2s(sbase + slot_addr(g, slot), S.ctab_p[g][j], bytes, full_bar(g, slot));
@@ -1585,8 +1639,8 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     int& phase = pp.phase;
     const int r_lane = lane >> 1, h_lane = lane & 1;
     const int lrow = w8 * 16 + r_lane;
-    const int code_off = w8 * 512 + lane * 16;
-    const int scale_off = kTileCodeBytes + w8 * 64 + lane * 2;
+    const int code_off = WB == 8 ? w8 * 1024 + lane * 32 : w8 * 512 + lane * 16;
+    const int scale_off = TCB + w8 * 64 + lane * 2;
     auto next_chunk = [&]() -> const uint8_t* {
         if (++slot == ns) {
             slot = 0;
@@ -1631,13 +1685,10 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             const uint8_t* chunk = next_chunk();
             if (live) {
                 for (int uu = 0; uu < nuj; ++uu) {
-                    const uint8_t* tile = chunk + uu * kTileBytes;
-                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                    const uint8_t* tile = chunk + uu * TB;
                     const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
-                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
-                                            wv.w & 0x0F0F0F0Fu};
-                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
-                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                    uint32_t wl[4], wh[4];
+                    unpack_codes<WB>(tile + code_off, wl, wh);
                     const int gl = 2 * (u0 + uu) + h_lane, g = 2 * kb0 + gl;  // (local, absolute)
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
@@ -1652,7 +1703,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                                 so = ar * Gxh;
                             }
                             const int2 sc = ax_s[so + gl];
-                            const int dot = group_dot(wl, wh, ax_q + ao + gl * kGroup, sc.y);
+                            const int dot = group_dot_w<WB>(wl, wh, ax_q + ao + gl * kGroup, sc.y);
                             acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
                             if (DOTS) a.dots_gu[((size_t)(off + n) * 2 * I + row) * Gx + g] = dot;
                         }
@@ -1742,19 +1793,16 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             if (live) {
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
-                    const uint8_t* tile = chunk + kt * kTileBytes;
-                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + code_off);
+                    const uint8_t* tile = chunk + kt * TB;
                     const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(tile + scale_off));
-                    const uint32_t wl[4] = {wv.x & 0x0F0F0F0Fu, wv.y & 0x0F0F0F0Fu, wv.z & 0x0F0F0F0Fu,
-                                            wv.w & 0x0F0F0F0Fu};
-                    const uint32_t wh[4] = {(wv.x >> 4) & 0x0F0F0F0Fu, (wv.y >> 4) & 0x0F0F0F0Fu,
-                                            (wv.z >> 4) & 0x0F0F0F0Fu, (wv.w >> 4) & 0x0F0F0F0Fu};
+                    uint32_t wl[4], wh[4];
+                    unpack_codes<WB>(tile + code_off, wl, wh);
                     const int gl = 2 * kt + h_lane;
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         if (n < c) {
                             const int2 sc = hs[n * 4 + gl];
-                            const int dot = group_dot(wl, wh, hq + n * kTileRows + gl * kGroup, sc.y);
+                            const int dot = group_dot_w<WB>(wl, wh, hq + n * kTileRows + gl * kGroup, sc.y);
                             accd[n] = fmaf((float)dot, dw * __int_as_float(sc.x), accd[n]);
                             if (DOTS)
                                 a.dots_d[((size_t)(off + n) * H + rbd * kTileRows + lrow) * Gh + hb * 4 + gl] = dot;
@@ -1795,7 +1843,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 
 // The experts of one decode layer by clusters of kClusterCTAs CTAs, one CTA
 // per SM.  MAXNT: the most tokens a bucket may hold (T <= MAXNT).
-template <int MAXNT, bool DOTS>
+template <int MAXNT, bool DOTS, int WB>
 __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ LayerShared S;
@@ -1810,7 +1858,7 @@ __global__ void __maxnreg__(96) decode_cluster_kernel(const LayerArgs a) {
     pdl_trigger();
     Pipe pp{-1, 0, -1, 0, 1};
     const LayerIO io{a.x_res, a.wgu, a.wd, a.out, a.out_fp32};
-    cluster_body<MAXNT, DOTS>(a, io, S, dsm, pp);
+    cluster_body<MAXNT, DOTS, WB>(a, io, S, dsm, pp);
     ring_drain(a, S, dsm, S.rns);
     __syncwarp();
     cluster_sync_all();  // no CTA leaves while its peer may still address it
@@ -1928,8 +1976,9 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
 // codes of x over the CTA's K part, the barriers (rings, then the two
 // exchange barriers).  ring_bytes must hold the exchange buffers of T tokens
 // and two two-tile slots a group.
-bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p) {
+bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p, int wbits = 4) {
     (void)I;
+    const int tile_bytes = wbits == 8 ? kTileBytes8 : kTileBytes;
     if (T < 1 || T > kClusterMaxT) return false;
     if ((H / kTileK) % kClusterCTAs) return false;
     const long long ax = al128((long long)T * (H / kClusterCTAs) + (long long)T * (H / kGroup / kClusterCTAs) * 8);
@@ -1937,7 +1986,7 @@ bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p) {
     const long long bars = (2ll * kMaxSlots + 2) * 8;
     const long long rb = (budget - ax - 2 * hbytes - bars - 256) & ~127ll;
     const long long pmax = al128(2ll * kUnitWorkers * T * kTileRows * 4);
-    const long long ring_min = (long long)kGroups * 2 * 2 * kTileBytes;
+    const long long ring_min = (long long)kGroups * 2 * 2 * tile_bytes;
     if (rb < pmax + ring_min) return false;
     // the routing scratch (logits and keys) stays below the exchange
     // buffers, which a peer may fill while this CTA still routes
@@ -2043,6 +2092,11 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
 int decode_sync_ints(int T, int H, int I, int E, int k) {
     const int nslot = std::min(E, T * k);
     return nslot * (I / kTileRows) + H / kTileRows;
+}
+
+bool decode_w8_fits(int T, int H, int I, int E) {
+    Plan p;
+    return T <= MOE_W8_DECODE_MAX_T && plan_cluster(T, H, I, E, kLayerSmemBudget, &p, 8);
 }
 
 int decode_cluster_parts(int T, int H, int I, int E) {
@@ -2195,7 +2249,7 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
                           int T, int H, int I, int E, int k, bool prenorm, bool out_fp32,
                           void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
                           bool write_qh, int* status, int num_sms, void** ev, bool capturing,
-                          cudaStream_t s) {
+                          cudaStream_t s, int wbits) {
     if (T == 0) return cudaSuccess;
     Plan plan;
     if (!plan_layer(T, H, I, E, kLayerSmemBudget, &plan)) return cudaErrorInvalidValue;
@@ -2242,7 +2296,9 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
     a.write_qh = write_qh ? 1 : 0;
     const bool dots = dots_gu || dots_d;
     Plan cplan;
-    if (g_cluster_mode[dev & 63] <= 2 && plan_cluster(T, H, I, E, kLayerSmemBudget, &cplan)) {
+    const bool clustered = g_cluster_mode[dev & 63] <= 2 && plan_cluster(T, H, I, E, kLayerSmemBudget, &cplan, wbits);
+    if (wbits == 8 && !clustered) return cudaErrorNotSupported;  // (8-bit weights: the clustered kernel only)
+    if (clustered) {
         a.ns = a.st = 0;  // (the kernel lays out its rings)
         a.off_bar = cplan.off_bar;
         a.off_ax = cplan.off_ax;
@@ -2250,9 +2306,15 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
         a.off_h = cplan.off_h;
         a.h_bytes = cplan.h_bytes;
         a.y_part = ws.y_unit;
-        void (*kern)(LayerArgs) =
-            T <= 8 ? (dots ? decode_cluster_kernel<8, true> : decode_cluster_kernel<8, false>)
-                   : (dots ? decode_cluster_kernel<kClusterMaxT, true> : decode_cluster_kernel<kClusterMaxT, false>);
+        void (*kern)(LayerArgs);
+        if (wbits == 8)
+            kern = T <= 8 ? (dots ? decode_cluster_kernel<8, true, 8> : decode_cluster_kernel<8, false, 8>)
+                          : (dots ? decode_cluster_kernel<kClusterMaxT, true, 8>
+                                  : decode_cluster_kernel<kClusterMaxT, false, 8>);
+        else
+            kern = T <= 8 ? (dots ? decode_cluster_kernel<8, true, 4> : decode_cluster_kernel<8, false, 4>)
+                          : (dots ? decode_cluster_kernel<kClusterMaxT, true, 4>
+                                  : decode_cluster_kernel<kClusterMaxT, false, 4>);
         if ((err = launch_cluster(kern, a, num_sms, cplan.smem, dev, s)) != cudaSuccess) return err;
         for (int i = 2; i <= 5; ++i)
             if ((err = mark(i)) != cudaSuccess) return err;
@@ -2288,7 +2350,7 @@ cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr
         const bool last = l == L - 1;
         void* dst = last ? out : static_cast<void*>(l % 2 ? ws.xbuf1 : ws.xbuf0);
         cudaError_t err = launch_decode(cur, wr[l], wgu[l], wd[l], T, H, I, E, k, prenorm, last && out_fp32,
-                                        dst, ws, nullptr, nullptr, false, status, num_sms, nullptr, false, s);
+                                        dst, ws, nullptr, nullptr, false, status, num_sms, nullptr, false, s, 4);
         if (err != cudaSuccess) return err;
         cur = static_cast<const uint16_t*>(dst);
     }

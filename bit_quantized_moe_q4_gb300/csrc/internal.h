@@ -90,6 +90,9 @@ int nchunks(int T);
 int record_error(int code, const char* msg);
 
 // launchers; each returns cudaGetLastError() of its launch
+// 8-bit codes int8 [E, N, K] and fp16 scales [E, N, K/32] -> 8-bit tiles.
+cudaError_t launch_pack8(const void* codes, const void* scales, int E, int N, int K, void* dst,
+                         cudaStream_t s);
 cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
                         void* dst, cudaStream_t s);
 cudaError_t launch_quantize(int src_type, const void* src, long long rows, int K, int fmt,
@@ -127,7 +130,7 @@ cudaError_t launch_decode(const uint16_t* x, const float* wr, const void* wgu, c
                           int T, int H, int I, int E, int k, bool prenorm, bool out_fp32,
                           void* out, const Workspace& ws, int32_t* dots_gu, int32_t* dots_d,
                           bool write_qh, int* status, int num_sms, void** events, bool capturing,
-                          cudaStream_t s);
+                          cudaStream_t s, int wbits = 4);
 // L chained decode layers: per layer the prep and layer kernels, linked by
 // programmatic dependent launch; layer l + 1 reads layer l's bf16 output.
 cudaError_t launch_decode_stack(const uint16_t* x, int L, const float* const* wr,
@@ -147,6 +150,8 @@ void decode_split_bounds(int T, int H, int I, int E, int k, int* cap_g, int* cap
                          int* nsd_max);
 // Counters the decode prep kernel clears.
 int decode_sync_ints(int T, int H, int I, int E, int k);
+// Whether the clustered decode kernel takes this shape with 8-bit weights.
+bool decode_w8_fits(int T, int H, int I, int E);
 // Parts of the weighted expert outputs the clustered decode kernel stores
 // (I/128 planes of [T*k, H]), or 0 when the shape never takes that kernel.
 int decode_cluster_parts(int T, int H, int I, int E);

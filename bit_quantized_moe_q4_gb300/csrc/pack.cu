@@ -84,7 +84,53 @@ __global__ void pack_scales_kernel(CodeSource cs, const uint16_t* scales, int E,
     }
 }
 
+// 8-bit tiles: one thread per 8 codes of a row.  Row r's 64 codes take bytes
+// r*64 .. r*64 + 63 of the tile; each 8-code chunk is stored in the order the
+// int8 activations are (columns 0, 4, 1, 5, 2, 6, 3, 7), so that two dp4a
+// of its two words with the activation chunk's two words give its dot.
+__global__ void pack8_codes_kernel(const int8_t* src, int E, int N, int K, uint8_t* dst) {
+    const int chunks_per_row = K / 8;
+    const size_t total = (size_t)E * N * chunks_per_row;
+    const int kb_per_row = K / kTileK;
+    const int rb_per_e = N / kTileRows;
+    for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total;
+         w += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = w / chunks_per_row;
+        const int c = (int)(w % chunks_per_row);
+        const int e = (int)(row / N), n = (int)(row % N);
+        const uint2 v = *reinterpret_cast<const uint2*>(src + row * (size_t)K + c * 8);
+        const uint2 o = make_uint2(__byte_perm(v.x, v.y, 0x5140), __byte_perm(v.x, v.y, 0x7362));
+        const size_t tile = ((size_t)e * rb_per_e + n / kTileRows) * kb_per_row + c / 8;
+        *reinterpret_cast<uint2*>(dst + tile * kTileBytes8 + (n % kTileRows) * 64 + (c % 8) * 8) = o;
+    }
+}
+
+__global__ void pack8_scales_kernel(const uint16_t* scales, int E, int N, int K, uint8_t* dst) {
+    const int kb_per_row = K / kTileK;
+    const int rb_per_e = N / kTileRows;
+    const size_t total = (size_t)E * N * kb_per_row;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / kb_per_row;
+        const int kb = (int)(i % kb_per_row);
+        const int e = (int)(row / N), n = (int)(row % N);
+        const size_t tile = ((size_t)e * rb_per_e + n / kTileRows) * kb_per_row + kb;
+        uint16_t* t = reinterpret_cast<uint16_t*>(dst + tile * kTileBytes8 + kTileCodeBytes8);
+        t[(n % kTileRows) * 2 + 0] = scales[row * (size_t)(K / kGroup) + 2 * kb];
+        t[(n % kTileRows) * 2 + 1] = scales[row * (size_t)(K / kGroup) + 2 * kb + 1];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack8(const void* codes, const void* scales, int E, int N, int K, void* dst,
+                         cudaStream_t s) {
+    pack8_codes_kernel<<<1184, 256, 0, s>>>(static_cast<const int8_t*>(codes), E, N, K,
+                                            static_cast<uint8_t*>(dst));
+    pack8_scales_kernel<<<592, 256, 0, s>>>(static_cast<const uint16_t*>(scales), E, N, K,
+                                            static_cast<uint8_t*>(dst));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(int fmt, const void* src, const void* src_scales, int E, int N, int K,
                         void* dst, cudaStream_t s) {

@@ -64,6 +64,7 @@ extern "C" {
 #define MOE_MAX_EXPERTS   256
 #define MOE_MAX_TOPK      16
 #define MOE_DECODE_MAX_T  32     /* decode path: tokens per call            */
+#define MOE_W8_DECODE_MAX_T 16   /* 8-bit-weight decode: tokens per call    */
 #define MOE_DECODE_MAX_LAYERS 64 /* decode stack: layers per call           */
 
 /* ---- moe_q4_pack formats ------------------------------------------------- */
@@ -292,6 +293,33 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
                                   const void* const* wgu_packed, const void* const* wd_packed,
                                   int T, int H, int I, int E, int k, unsigned flags, void* out,
                                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * 8-bit expert weights (NEXT-4: the companion page, mlsanity.com 2607.14568,
+ * runs 8-bit weights against 4-bit ones; its format is not printed, this
+ * library takes the Q8_0-style reading): blocks of 32 int8 codes q in
+ * -127..127 along a row share one fp16 scale d, w = d * q.
+ *
+ * moe_q8_packed_bytes / moe_q8_pack — int8 codes [E, N, K] and fp16 scales
+ * [E, N, K/32] (DEVICE) to 8-bit tiles: 128 rows x 64 columns, 8704 bytes
+ * (each row's 64 codes, 8-code chunks in the order 0,4,1,5,2,6,3,7, then the
+ * 128 x 2 fp16 scales), tiles ordered as the Q4_0 ones.  N % 128 == 0,
+ * K % 64 == 0.
+ *
+ * moe_w8a8_forward_decode — the decode layer of moe_w4a8_forward_decode with
+ * 8-bit expert weights (both packed by moe_q8_pack): the same routing,
+ * activation quantiser and combine; group dots sum q_w * q_a exactly.
+ * T <= MOE_W8_DECODE_MAX_T (the clustered layer kernel); workspace as for
+ * moe_w4a8_forward_decode (moe_workspace_bytes(MOE_MODE_DECODE, ...)).
+ * Stage outputs as for the 4-bit call.
+ */
+size_t moe_q8_packed_bytes(int E, int N, int K);
+int moe_q8_pack(const void* codes, const void* scales, int E, int N, int K, void* dst,
+                size_t dst_bytes, void* stream);
+int moe_w8a8_forward_decode(const uint16_t* x_bf16, const float* wr, const void* wgu_q8,
+                            const void* wd_q8, int T, int H, int I, int E, int k, unsigned flags,
+                            void* out, void* workspace, size_t ws_bytes, moe_debug* dbg,
+                            void* stream);
 
 /*
  * moe_q4_forward_prefill_stack_streamed — L consecutive prefill layers whose

@@ -66,7 +66,8 @@ def _prefill(lib, T=4, H=256, I=128, E=8, k=2, flags=1, x=FAKE, wr=FAKE, wgu=FAK
     return getattr(lib, fn)(x, wr, wgu, wd, T, H, I, E, k, flags, out, ws, ws_bytes, None, None)
 
 
-@pytest.mark.parametrize("fn", ["moe_q4_forward_prefill", "moe_w4a8_forward_decode"])
+@pytest.mark.parametrize("fn", ["moe_q4_forward_prefill", "moe_w4a8_forward_decode",
+                                "moe_w8a8_forward_decode"])
 def test_forward_argument_checks(lib, fn):
     assert _prefill(lib, fn=fn, H=200) == moe.MOE_ERR_SHAPE          # H % 128
     assert _prefill(lib, fn=fn, I=96) == moe.MOE_ERR_SHAPE           # I % 128
@@ -86,6 +87,11 @@ def test_forward_argument_checks(lib, fn):
     assert b"workspace" in lib.moe_last_error_string() or True
     if fn == "moe_w4a8_forward_decode":
         assert _prefill(lib, fn=fn, T=33) == moe.MOE_ERR_SHAPE       # decode takes <= 32 tokens
+    if fn == "moe_w8a8_forward_decode":
+        assert _prefill(lib, fn=fn, T=moe.MOE_W8_DECODE_MAX_T + 1) == moe.MOE_ERR_SHAPE
+        assert b"8-bit" in lib.moe_last_error_string()
+        # the full decode shape fits the on-chip staging at 16 tokens
+        assert _prefill(lib, fn=fn, T=16, H=2048, I=768, E=128, k=8, x=None) == moe.MOE_ERR_INVALID_ARG
 
 
 def _stack(lib, L=2, T=1, H=256, I=128, E=8, k=2, flags=1, x=FAKE, layer=(FAKE, FAKE, FAKE),
@@ -128,6 +134,19 @@ def test_pack_argument_checks(lib):
     assert f(1, FAKE, FAKE, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_INVALID_ARG
     assert f(0, FAKE + 4, FAKE, 1, 128, 64, FAKE, 4608, None) == moe.MOE_ERR_ALIGN
     assert f(0, FAKE, FAKE, 1, 128, 64, FAKE, 4607, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_q8_pack_argument_checks(lib):
+    assert moe.moe_q8_packed_bytes(128, 1536, 2048) == 128 * 1536 * 2048 * 34 // 32
+    assert moe.moe_q8_packed_bytes(1, 128, 64) == 8704
+    assert moe.moe_q8_packed_bytes(1, 100, 64) == 0
+    assert moe.moe_q8_packed_bytes(1, 128, 32) == 0
+    f = lib.moe_q8_pack
+    assert f(FAKE, FAKE, 1, 100, 64, FAKE, 8704, None) == moe.MOE_ERR_SHAPE
+    assert f(FAKE, FAKE, 1, 128, 96, FAKE, 8704, None) == moe.MOE_ERR_SHAPE
+    assert f(FAKE, None, 1, 128, 64, FAKE, 8704, None) == moe.MOE_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, 1, 128, 64, FAKE, 8704, None) == moe.MOE_ERR_ALIGN
+    assert f(FAKE, FAKE, 1, 128, 64, FAKE, 8703, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_route_argument_checks(lib):
