@@ -86,6 +86,11 @@ constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 
 constexpr int kLayerSmemBudget = 200 * 1024;
 constexpr int kPrepThreads = 128;
 constexpr int kMaxTk = MOE_DECODE_MAX_T * MOE_MAX_TOPK;
+// Bucket rows of a unit of the clustered kernel: a larger bucket is cut into
+// near-equal slices of at most this many rows, so that the work split can
+// spread one expert's tokens over several clusters.
+constexpr int kSliceRows = 4;
+constexpr int kMaxSlices = 16 * MOE_MAX_TOPK;  // slices of a launch (T <= 16)
 // Tasks the K split aims for (gate/up and down alike): the split depends only
 // on the number of touched experts and the shape, so results are
 // reproducible.  A task keeps at least two tiles.
@@ -539,7 +544,9 @@ struct LayerShared {
     int nt, nsg, nsd;
     int eqc;                    // every touched slot has the same bucket size
     int bnd[kGroups][4];        // group g: gate/up tasks [0], [1]; down tasks [2], [3]
-    int cmax;                   // clustered kernel: the largest bucket
+    int cmax;                   // clustered kernel: the largest slice
+    int sto[kMaxSlices + 1];    // clustered kernel: slice -> its first bucket row (+ total)
+    uint8_t sslot[kMaxSlices];  // clustered kernel: slice -> its touched slot
     int rns;                    // clustered kernel: slots of each group's ring
     volatile int abort;
     volatile int flag[kGroups];
@@ -731,10 +738,11 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     }
     for (int e = tid; e < E; e += kLayerThreads) s_mask[e] = 0u;
     __syncthreads();
-    if ((long long)T * E * E <= (long long)kLayerThreads * kRankCompares) {
+    if (T * E <= kLayerThreads && (long long)T * E * E <= (long long)kLayerThreads * kRankCompares) {
         // few tokens: every thread ranks (t, e) against a share of the
-        // token's keys (nsub threads an element, interleaved), the shares
-        // are added; rank < k places e in t's choices
+        // token's keys (nsub threads an element, interleaved; every element
+        // has a thread), the shares are added; rank < k places e in t's
+        // choices
         int nsub = 1;
         while (nsub < 32 && T * E * 2 * nsub <= kLayerThreads) nsub *= 2;
         const int el = tid / nsub, sub = tid % nsub;
@@ -1458,38 +1466,52 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 //            y (one per h block)
 // and a third kernel (decode_combine_kernel) adds, per output element, the
 // residual and the k * I/128 parts (slot order, then block order).
-// Units go to clusters in contiguous ranges of equal cost (a unit of slot i
-// weighs kTileCost + c_i per tile, all units have the same tiles).  No CTA
+// A unit is (slice, h block): each touched expert's bucket is cut into
+// ceil(c / kSliceRows) slices of near-equal size (rows floor(s c / n) ..
+// floor((s + 1) c / n) - 1 of slice s of n), so that no unit holds more than
+// kSliceRows tokens.  The slices of one expert read the same weights; they
+// sit next to each other in the unit order, so their clusters run at about
+// the same time and the later reads find the weights in L2.  Units go to
+// clusters in contiguous ranges of equal cost (a unit of slice i weighs
+// kTileCost + c_i per tile, all units have the same tiles).  No CTA
 // waits for a CTA outside its cluster, so the launch need not be
 // cooperative (a cooperative launch would not start before the prep kernel
 // has drained, and costs ~3 us a layer).
 constexpr int kClusterCTAs = 2;
 constexpr int kUnitWorkers = kClusterCTAs * kGroups;
 constexpr int kClusterMaxT = 16;  // tokens per call of the clustered kernel
+static_assert(kClusterMaxT * MOE_MAX_TOPK <= kMaxSlices, "a slice holds at least one bucket row");
 
 // The first unit of cluster q of NC: the unit whose cost range holds the
-// position q * total / NC (units of touched slot i, RBh of them, weigh
+// position q * total / NC (units of slice i, RBh of them, weigh
 // kTileCost + c_i each, c_i = toff[i + 1] - toff[i]).  Monotone in q;
-// bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp calls it.
+// bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp calls it.  Every
+// product stays below 2^31 (NC * RBh * (kTileCost * nt + Tk), checked by the
+// host plan), so the arithmetic is 32-bit.
 __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
                                                int lane, bool equal) {
-    if (equal) return (int)(((long long)q * nt * RBh + NC - 1) / NC);  // (all units weigh the same)
-    using u64 = unsigned long long;
-    const u64 tot = (u64)RBh * ((u64)kTileCost * nt + Tk);
-    const u64 qt = (u64)q * tot;  // NC times the position
-    int cnt = 0;                  // slots whose first unit starts before it
+    if (equal) return (q * nt * RBh + NC - 1) / NC;  // (all units weigh the same)
+    const unsigned tot = (unsigned)RBh * (unsigned)(kTileCost * nt + Tk);
+    const unsigned qt = (unsigned)q * tot;  // NC times the position
+    const unsigned ncr = (unsigned)(NC * RBh);
+    int cnt = 0;  // slices whose first unit starts before it
     for (int i0 = 0; i0 <= nt; i0 += 32) {
         const int i = i0 + lane;
-        const bool lt = i <= nt && (u64)NC * RBh * ((u64)kTileCost * i + toff[i]) < qt;
+        const bool lt = i <= nt && ncr * (unsigned)(kTileCost * i + toff[i]) < qt;
         cnt += __popc(__ballot_sync(0xffffffffu, lt));
     }
     if (cnt == 0) return 0;
     const int i = cnt - 1;
     if (i >= nt) return nt * RBh;
-    const u64 base = (u64)NC * RBh * ((u64)kTileCost * i + toff[i]);
-    const u64 wn = (u64)NC * (kTileCost + toff[i + 1] - toff[i]);
-    const u64 j = (qt - base + wn - 1) / wn;
-    return i * RBh + (int)(j < (u64)RBh ? j : (u64)RBh);
+    const unsigned base = ncr * (unsigned)(kTileCost * i + toff[i]);
+    const unsigned wn = (unsigned)NC * (unsigned)(kTileCost + toff[i + 1] - toff[i]);
+    const unsigned j = (qt - base + wn - 1) / wn;
+    return i * RBh + (int)(j < (unsigned)RBh ? j : (unsigned)RBh);
+}
+
+// floor(x / n) for n = 1 .. 4 and x <= 64 (slice bounds)
+__device__ __forceinline__ int div_small(int x, int n) {
+    return n == 3 ? (x * 21846) >> 16 : x >> (n >> 1);
 }
 
 template <int MAXNT, bool DOTS, int WB>
@@ -1529,12 +1551,46 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     }
     route_layer<MAXNT == 1 ? kRouteOneTokenOnly : kRouteOneTokenFast>(a, S, dsm, [&](int warp, int lane) {
         if (warp == 0) {
+            // the slices of the touched slots' buckets (a warp scan of their
+            // counts), the largest and the smallest slice
             const int nt = S.nt;
-            const int u0 = unit_bound_warp(cq, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
-            const int u1 = unit_bound_warp(cq + 1, NC, nt, Tk, RBh, S.toff, lane, S.eqc != 0);
-            int cm = 0;  // the largest bucket
-            for (int i = lane; i < nt; i += 32) cm = max(cm, S.toff[i + 1] - S.toff[i]);
+            int nsl = 0, cm = 0, cmin = kSliceRows;
+            if (T <= kSliceRows) {  // no bucket is larger: a slice per slot
+                for (int i = lane; i < nt; i += 32) {
+                    const int c = S.toff[i + 1] - S.toff[i];
+                    S.sto[i] = S.toff[i];
+                    S.sslot[i] = (uint8_t)i;
+                    cm = max(cm, c);
+                    cmin = min(cmin, c);
+                }
+                nsl = nt;
+            }
+            for (int i0 = 0; i0 < nt && T > kSliceRows; i0 += 32) {
+                const int i = i0 + lane;
+                const int c = i < nt ? S.toff[i + 1] - S.toff[i] : 0;
+                const int n = (c + kSliceRows - 1) / kSliceRows;
+                int incl = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const int first = nsl + incl - n;
+                for (int q = 0; q < n; ++q) {
+                    const int r0 = div_small(q * c, n), r1 = div_small((q + 1) * c, n);
+                    S.sto[first + q] = S.toff[i] + r0;
+                    S.sslot[first + q] = (uint8_t)i;
+                    cm = max(cm, r1 - r0);
+                    cmin = min(cmin, r1 - r0);
+                }
+                nsl += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) S.sto[nsl] = Tk;
+            __syncwarp();
             cm = __reduce_max_sync(0xffffffffu, cm);
+            const bool equal = __reduce_min_sync(0xffffffffu, cmin) == cm;
+            const int u0 = unit_bound_warp(cq, NC, nsl, Tk, RBh, S.sto, lane, equal);
+            const int u1 = unit_bound_warp(cq + 1, NC, nsl, Tk, RBh, S.sto, lane, equal);
             if (lane == 0) {
                 S.bnd[0][0] = u0;
                 S.bnd[0][1] = u1;
@@ -1574,7 +1630,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             if (c < nch) {
                 const int ul = c / cpu, j = c - ul * cpu;
                 const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;
-                const size_t e = (size_t)S.touched[i];
+                const size_t e = (size_t)S.touched[S.sslot[i]];
                 const uint8_t* src;
                 int n;
                 if (j < cptg) {
@@ -1659,8 +1715,8 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
 
     auto unit = [&](auto ntc, int ul) {
         constexpr int NT = decltype(ntc)::value;
-        const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;
-        const int e = S.touched[i], off = S.off[e], c = S.off[e + 1] - off;
+        const int u = ub0 + ul, i = u / RBh, hb = u - i * RBh;  // (slice, h block)
+        const int off = S.sto[i], c = S.sto[i + 1] - off;         // its bucket rows
         const int ux = pp.units + ul;  // the exchange's ordinal in the launch
         const int pb = ux & 1;
         const uint32_t ppar = (uint32_t)((ux >> 1) & 1);
@@ -1670,6 +1726,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
         const int rb = grp ? RBh + hb : hb;
         const int row = rb * kTileRows + lrow;
         constexpr int NH = NT <= 4 ? NT : 1;
+        constexpr int NB = NT < 4 ? NT : 4;  // bucket rows per block of dot chains
         int arow[NH], srow[NH];
 #pragma unroll
         for (int n = 0; n < NH; ++n) {
@@ -1690,22 +1747,34 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                     uint32_t wl[4], wh[4];
                     unpack_codes<WB>(tile + code_off, wl, wh);
                     const int gl = 2 * (u0 + uu) + h_lane, g = 2 * kb0 + gl;  // (local, absolute)
+                    // blocks of NB bucket rows as independent dot chains; rows
+                    // past c repeat an earlier row (in bounds) and their sums
+                    // are never sent
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        if (n < c) {
-                            int ao, so;
-                            if constexpr (NT <= 4) {
-                                ao = arow[n];
-                                so = srow[n];
-                            } else {
-                                const int ar = S.btok[off + n];
-                                ao = ar * Hh;
-                                so = ar * Gxh;
+                    for (int n0 = 0; n0 < NT; n0 += NB) {
+                        if (n0 < c) {
+                            int2 sc[NB];
+                            int dot[NB];
+#pragma unroll
+                            for (int j = 0; j < NB; ++j) {
+                                int ao, so;
+                                if constexpr (NT <= 4) {
+                                    ao = arow[n0 + j];
+                                    so = srow[n0 + j];
+                                } else {
+                                    const int ar = S.btok[off + (n0 + j < c ? n0 + j : c - 1)];
+                                    ao = ar * Hh;
+                                    so = ar * Gxh;
+                                }
+                                sc[j] = ax_s[so + gl];
+                                dot[j] = group_dot_w<WB>(wl, wh, ax_q + ao + gl * kGroup, sc[j].y);
                             }
-                            const int2 sc = ax_s[so + gl];
-                            const int dot = group_dot_w<WB>(wl, wh, ax_q + ao + gl * kGroup, sc.y);
-                            acc[n] = fmaf((float)dot, dw * __int_as_float(sc.x), acc[n]);
-                            if (DOTS) a.dots_gu[((size_t)(off + n) * 2 * I + row) * Gx + g] = dot;
+#pragma unroll
+                            for (int j = 0; j < NB; ++j) {
+                                acc[n0 + j] = fmaf((float)dot[j], dw * __int_as_float(sc[j].x), acc[n0 + j]);
+                                if (DOTS && n0 + j < c)
+                                    a.dots_gu[((size_t)(off + n0 + j) * 2 * I + row) * Gx + g] = dot[j];
+                            }
                         }
                     }
                 }
@@ -1799,24 +1868,40 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                     unpack_codes<WB>(tile + code_off, wl, wh);
                     const int gl = 2 * kt + h_lane;
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        if (n < c) {
-                            const int2 sc = hs[n * 4 + gl];
-                            const int dot = group_dot_w<WB>(wl, wh, hq + n * kTileRows + gl * kGroup, sc.y);
-                            accd[n] = fmaf((float)dot, dw * __int_as_float(sc.x), accd[n]);
-                            if (DOTS)
-                                a.dots_d[((size_t)(off + n) * H + rbd * kTileRows + lrow) * Gh + hb * 4 + gl] = dot;
+                    for (int n0 = 0; n0 < NT; n0 += NB) {
+                        if (n0 < c) {
+                            int2 sc[NB];
+                            int dot[NB];
+#pragma unroll
+                            for (int j = 0; j < NB; ++j) {
+                                const int n = n0 + j < c ? n0 + j : c - 1;  // rows past c: in bounds, unused
+                                sc[j] = hs[n * 4 + gl];
+                                dot[j] = group_dot_w<WB>(wl, wh, hq + n * kTileRows + gl * kGroup, sc[j].y);
+                            }
+#pragma unroll
+                            for (int j = 0; j < NB; ++j) {
+                                accd[n0 + j] = fmaf((float)dot[j], dw * __int_as_float(sc[j].x), accd[n0 + j]);
+                                if (DOTS && n0 + j < c)
+                                    a.dots_d[((size_t)(off + n0 + j) * H + rbd * kTileRows + lrow) * Gh +
+                                             hb * 4 + gl] = dot[j];
+                            }
                         }
                     }
                 }
             }
             free_chunk();
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const float v = accd[n] + __shfl_xor_sync(0xffffffffu, accd[n], 1);
-                if (n < c && h_lane == 0 && live) {
-                    const int tj = S.btok[off + n] * k + S.bslot[off + n];  // (token, choice)
-                    a.y_part[((size_t)hb * Tk + tj) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
+            for (int n0 = 0; n0 < NT; n0 += NB) {
+                if (n0 < c) {  // warp-uniform: every lane takes the shuffles
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const int n = n0 + j;
+                        const float v = accd[n] + __shfl_xor_sync(0xffffffffu, accd[n], 1);
+                        if (n < c && h_lane == 0 && live) {
+                            const int tj = S.btok[off + n] * k + S.bslot[off + n];  // (token, choice)
+                            a.y_part[((size_t)hb * Tk + tj) * H + rbd * kTileRows + lrow] = v * S.bsw[off + n];
+                        }
+                    }
                 }
             }
         }
@@ -1824,15 +1909,14 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
     };
 
     for (int ul = 0; ul < nu; ++ul) {
+        static_assert(kSliceRows == 4, "units hold at most 4 bucket rows");
         if constexpr (MAXNT == 1) {
             unit(IntC<1>{}, ul);
         } else {
-            const int u = ub0 + ul, i = u / RBh;
-            const int e = S.touched[i], c = S.off[e + 1] - S.off[e];
+            const int i = (ub0 + ul) / RBh, c = S.sto[i + 1] - S.sto[i];
             if (c <= 1) unit(IntC<1>{}, ul);
             else if (c <= 2) unit(IntC<2>{}, ul);
-            else if (c <= 4 || MAXNT <= 4) unit(IntC<4 < MAXNT ? 4 : MAXNT>{}, ul);
-            else unit(IntC<MAXNT>{}, ul);
+            else unit(IntC<4>{}, ul);
         }
     }
     pp.units += nu;
@@ -1977,9 +2061,11 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
 // exchange barriers).  ring_bytes must hold the exchange buffers of T tokens
 // and two two-tile slots a group.
 bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p, int wbits = 4) {
-    (void)I;
     const int tile_bytes = wbits == 8 ? kTileBytes8 : kTileBytes;
     if (T < 1 || T > kClusterMaxT) return false;
+    // the unit split's 32-bit products: NC * RBh * (kTileCost * slices + Tk)
+    // with at most 1024 clusters and kMaxSlices slices
+    if ((long long)(I / kTileRows) * 1024 * (kTileCost + 1) * kMaxSlices >= (1ll << 31)) return false;
     if ((H / kTileK) % kClusterCTAs) return false;
     const long long ax = al128((long long)T * (H / kClusterCTAs) + (long long)T * (H / kGroup / kClusterCTAs) * 8);
     const long long hbytes = al128((long long)T * kTileRows + (long long)T * 4 * 8);
@@ -2232,7 +2318,7 @@ cudaError_t launch_cluster(void (*kern)(LayerArgs), const LayerArgs& args, int n
             mx = ncl;
         }
     }
-    ncl = std::min(ncl, mx);
+    ncl = std::min(std::min(ncl, mx), 1024);  // (the unit split's 32-bit bound)
     if (ncl < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(ncl * kClusterCTAs);
     cfg.numAttrs = g_cluster_mode[dev & 63] == 1 ? 2 : 1;

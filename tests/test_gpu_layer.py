@@ -173,9 +173,27 @@ def test_decode_full_size(T):
     (3, 256, 128, 6, 6),      # k = E
     (1, 384, 256, 1, 1),      # one expert: a dense SwiGLU FFN, 3 row blocks
     (5, 128, 128, 3, 2),      # smallest hidden size
+    (16, 256, 128, 64, 4),    # more (token, expert) logits than threads of a CTA, E < 128
+    (32, 256, 128, 32, 2),    # the same on the task kernel (T > 16)
 ])
 def test_decode_edge_shapes(T, H, I, E, k):
     _decode_check(workloads.make_layer("dedge", T, H, I, E, k, seed=7 * T + H + E, wr_std=0.1))
+
+
+@pytest.mark.parametrize("T,groups", [
+    (16, 1),   # all 16 tokens alike: 8 buckets of 16 rows, four slices each
+    (12, 2),   # two kinds of token: buckets of 6 (two slices) or 12 (three)
+    (9, 3),    # buckets of 3, 6 or 9 rows
+    (5, 1),    # buckets of 5: slices of 2 and 3
+])
+def test_decode_concentrated_buckets(T, groups):
+    # tokens repeated so that many choose the same experts: the clustered
+    # kernel cuts each bucket into slices of at most four rows
+    li = workloads.decode(16)
+    rows = np.arange(T) % groups
+    li.T = T
+    li.x = li.x[rows].copy()
+    _decode_check(li)
 
 
 def test_decode_tiny_32_tokens():
