@@ -416,56 +416,68 @@ __device__ __forceinline__ uint32_t float_order_key(float v) {
 // first; equal logits -> lower expert index first.
 //
 // Lane l owns the contiguous experts [l*P, l*P + P), P = ceil(E/32) <= 8, and
-// keeps its best remaining one ("head": largest key, lowest index on a tie).
-// Each of the k rounds takes the warp maximum of the heads (redux.sync), and
-// among the lanes holding it the lowest one, which owns the lowest index
-// because lanes own ascending index ranges.  That lane drops its head and
-// finds the next.  The weights are a softmax over the k chosen logits.
-__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int& sel_i,
-                                          float& weight) {
+// sorts them once (a sorting network on (key descending, index ascending), in
+// PM >= P registers).  Each of the k rounds takes the warp maximum of the
+// lanes' heads (redux.sync), and among the lanes holding it the lowest one,
+// which owns the lowest index because lanes own ascending index ranges.  That
+// lane drops its head by shifting its list (predicated moves, no branch).
+// The weights are a softmax over the k chosen logits.
+template <int PM>
+__device__ __forceinline__ void warp_topk_sorted(const float* row, int E, int k, int& sel_i, float& weight) {
     const int lane = threadIdx.x % 32;
-    constexpr int PMAX = kMaxExperts / 32;
     const int P = (E + 31) / 32;
-    uint32_t key[PMAX];
+    uint32_t kk[PM];
+    int ii[PM];
 #pragma unroll
-    for (int i = 0; i < PMAX; ++i) {
+    for (int i = 0; i < PM; ++i) {
         const int e = lane * P + i;
-        key[i] = (i < P && e < E) ? float_order_key(row[e]) : 0u;
+        const bool have = i < P && e < E;
+        kk[i] = have ? float_order_key(row[e]) : 0u;  // key 0: absent
+        ii[i] = have ? e : 0;
     }
-    // key 0 marks "taken or absent"; a real logit has key >= 1 unless it is a
-    // NaN with every bit set, which is treated as absent.
-    auto head_of = [&](int& hi) {
-        uint32_t hk = 0u;
-        hi = -1;
-#pragma unroll
-        for (int i = 0; i < PMAX; ++i)
-            if (key[i] > hk) {
-                hk = key[i];
-                hi = i;
-            }
-        return hk;
+    auto cs = [&](int a, int b) {  // (a, b) into order: a first
+        const bool sw = kk[b] > kk[a] || (kk[b] == kk[a] && ii[b] < ii[a]);
+        const uint32_t ka = kk[a];
+        const int ia = ii[a];
+        kk[a] = sw ? kk[b] : ka;
+        ii[a] = sw ? ii[b] : ia;
+        kk[b] = sw ? ka : kk[b];
+        ii[b] = sw ? ia : ii[b];
     };
-    int hi;
-    uint32_t hk = head_of(hi);
+    if constexpr (PM == 2) {
+        cs(0, 1);
+    } else if constexpr (PM == 4) {
+        cs(0, 1); cs(2, 3); cs(0, 2); cs(1, 3); cs(1, 2);
+    } else if constexpr (PM == 8) {
+        cs(0, 2); cs(1, 3); cs(4, 6); cs(5, 7); cs(0, 4); cs(1, 5); cs(2, 6); cs(3, 7); cs(0, 1); cs(2, 3);
+        cs(4, 5); cs(6, 7); cs(2, 4); cs(3, 5); cs(1, 4); cs(3, 6); cs(1, 2); cs(3, 4); cs(5, 6);
+    }
     sel_i = 0;
     for (int r = 0; r < k; ++r) {
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk);
-        const uint32_t ball = __ballot_sync(0xffffffffu, hk == kmax && hi >= 0);
-        const int wl = __ffs(ball) - 1;
-        const int e = __shfl_sync(0xffffffffu, lane * P + hi, wl);
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, kk[0]);
+        const int wl = __ffs(__ballot_sync(0xffffffffu, kk[0] == kmax)) - 1;
+        const int e = __shfl_sync(0xffffffffu, ii[0], wl);
         if (lane == r) sel_i = e;
-        if (lane == wl) {
+        const bool win = lane == wl;
 #pragma unroll
-            for (int i = 0; i < PMAX; ++i)
-                if (i == hi) key[i] = 0u;
-            hk = head_of(hi);
+        for (int i = 0; i + 1 < PM; ++i) {
+            kk[i] = win ? kk[i + 1] : kk[i];
+            ii[i] = win ? ii[i + 1] : ii[i];
         }
+        kk[PM - 1] = win ? 0u : kk[PM - 1];
     }
     const float sel_v = (lane < k) ? row[sel_i] : 0.f;
     const float m = __shfl_sync(0xffffffffu, sel_v, 0);  // the largest
     const float z = (lane < k) ? expf(sel_v - m) : 0.f;
     const float s = warp_sum(z);
     weight = z / s;
+}
+
+__device__ __forceinline__ void warp_topk(const float* row, int E, int k, int& sel_i, float& weight) {
+    if (E <= 32) warp_topk_sorted<1>(row, E, k, sel_i, weight);
+    else if (E <= 64) warp_topk_sorted<2>(row, E, k, sel_i, weight);
+    else if (E <= 128) warp_topk_sorted<4>(row, E, k, sel_i, weight);
+    else warp_topk_sorted<8>(row, E, k, sel_i, weight);
 }
 
 // Activation quantiser decision, taken in fp32 (see act-quant kernels):

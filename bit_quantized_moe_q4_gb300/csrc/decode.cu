@@ -637,7 +637,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     const int RBg = 2 * I / kTileRows, RBd = H / kTileRows;
     const int Tk = T * k;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int b = blockIdx.x;
+    const bool b0 = blockIdx.x == 0;  // CTA 0 stores the routing results
     if (ROUTE == kRouteOneTokenOnly || (ONE_TOKEN_PATH && T == 1)) {
         // One token: warps 0..3 (expert e on thread e % 128) rank every
         // expert's logit against all E (larger first, the lower index on a
@@ -696,7 +696,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
                     s_bsw[pos] = sw;
                     s_touched[pos] = si;
                     s_toff[pos] = pos;
-                    if (b == 0) {
+                    if (b0) {
                         a.topk_idx[lane] = si;
                         a.topk_w[lane] = sw;
                         a.bucket_token[pos] = 0;
@@ -709,7 +709,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
                     s_toff[k] = k;
                     s_nt = k;
                     s_eqc = 1;
-                    if (b == 0) {
+                    if (b0) {
                         a.offsets[E] = k;
                         a.counters[kCntTouched] = k;
                     }
@@ -719,7 +719,7 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
                 int c = 0;
                 for (int q = 0; q < k; ++q) c += s_idx[q] < e ? 1 : 0;
                 s_off[e] = c;
-                if (b == 0) a.offsets[e] = c;
+                if (b0) a.offsets[e] = c;
             }
         }
         __syncthreads();
@@ -738,11 +738,14 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
     }
     for (int e = tid; e < E; e += kLayerThreads) s_mask[e] = 0u;
     __syncthreads();
-    if (T * E <= kLayerThreads && (long long)T * E * E <= (long long)kLayerThreads * kRankCompares) {
-        // few tokens: every thread ranks (t, e) against a share of the
-        // token's keys (nsub threads an element, interleaved; every element
-        // has a thread), the shares are added; rank < k places e in t's
-        // choices
+    // a warp a token (warp_topk) while every token has its warp; beyond
+    // that, few experts: every thread ranks elements
+    const bool rank_path = T > kConsumerWarps && T * E <= kLayerThreads &&
+                           (long long)T * E * E <= (long long)kLayerThreads * kRankCompares;
+    if (rank_path) {
+        // every thread ranks (t, e) against a share of the token's keys
+        // (nsub threads an element, interleaved; every element has a
+        // thread), the shares are added; rank < k places e in t's choices
         int nsub = 1;
         while (nsub < 32 && T * E * 2 * nsub <= kLayerThreads) nsub *= 2;
         const int el = tid / nsub, sub = tid % nsub;
@@ -762,23 +765,24 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
             s_idx[t * k + rank] = e;
             atomicOr(&s_mask[e], 1u << t);
         }
-    } else {
-        if (warp < kConsumerWarps) {
-            for (int t = warp; t < T; t += kConsumerWarps) {
-                int si;
-                float sw;
-                warp_topk(s_lg + t * E, E, k, si, sw);
-                if (lane < k) s_idx[t * k + lane] = si;
+    } else if (warp < kConsumerWarps) {
+        // the choices, their softmax weights and token t's bit in the mask
+        // of each expert it chose (T <= 32)
+        for (int t = warp; t < T; t += kConsumerWarps) {
+            int si;
+            float sw;
+            warp_topk(s_lg + t * E, E, k, si, sw);
+            if (lane < k) {
+                s_idx[t * k + lane] = si;
+                s_w[t * k + lane] = sw;
+                atomicOr(&s_mask[si], 1u << t);
             }
         }
-        __syncthreads();
-        // token t's bit in the mask of each expert it chose (T <= 32)
-        for (int p = tid; p < Tk; p += kLayerThreads) atomicOr(&s_mask[s_idx[p]], 1u << (p / k));
     }
     __syncthreads();
     if (warp < kConsumerWarps) {
-        // the softmax weights over each token's k choices
-        for (int t = warp; t < T; t += kConsumerWarps) {
+        // the softmax weights over each token's k choices (the rank path)
+        for (int t = warp; t < T && rank_path; t += kConsumerWarps) {
             const float v = lane < k ? s_lg[t * E + s_idx[t * k + lane]] : 0.f;
             const float m = __shfl_sync(0xffffffffu, v, 0);  // the largest
             const float z = lane < k ? expf(v - m) : 0.f;
@@ -855,14 +859,14 @@ __device__ __forceinline__ void route_layer(const LayerArgs& a, LayerShared& S, 
             S.bslot[pos] = p % k;
             s_bsw[pos] = s_w[p];
             s_slotpos[p] = pos;
-            if (b == 0) {
+            if (b0) {
                 a.topk_idx[p] = e;
                 a.topk_w[p] = s_w[p];
                 a.bucket_token[pos] = t;
                 a.bucket_slot[pos] = p % k;
             }
         }
-        if (b == 0) {
+        if (b0) {
             for (int i = tid2; i <= E; i += nthr2) a.offsets[i] = s_off[i];
             for (int i = tid2; i < nt; i += nthr2) a.touched[i] = s_touched[i];
             if (tid2 == 0) a.counters[kCntTouched] = nt;
