@@ -475,12 +475,30 @@ def bench_prefill_stack(steps, warmup, torch, moe, device, barrier):
     t1.record(stream)
     torch.cuda.synchronize()
     ms_str = t0.elapsed_time(t1) / nst
+    # the link's copy rate: one layer's experts copied alone from pinned
+    # host memory, the same bytes the streamed stack moves per layer
+    gd = torch.empty(gu_b + d_b, dtype=torch.uint8, device=device)
+    src = host[0][1]
+    dst = gd[: src.numel()]
+    for _ in range(2):
+        dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+        gd[src.numel(): src.numel() + host[0][2].numel()].copy_(host[0][2], non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    copy_gbs = 3 * (gu_b + d_b) / (t0.elapsed_time(t1) * 1e-3) / 1e9
+    del gd
     res["streamed"] = {
         "entry": "moe_q4_forward_prefill_stack_streamed (experts in pinned host memory, copied "
                  "layer by layer on a copy stream, overlapped with the layers' kernels)",
         "layers": NS, "ms_per_layer": ms_str / NS,
         "expert_bytes_per_layer": gu_b + d_b,
         "h2d_gbs": (gu_b + d_b) * NS / (ms_str * 1e-3) / 1e9,
+        "plain_copy_gbs": copy_gbs,
+        "copy_frac": (gu_b + d_b) * NS / (ms_str * 1e-3) / 1e9 / copy_gbs,
         "device_resident_ms_per_layer": ms_stack / L,
         "equals_device_chain_bits": same,
     }
