@@ -245,14 +245,17 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
  * E = 256 fits).  The int32 group dots are exact; the float sums run in fp32
  * in a fixed order, so repeated calls give the same bits.
  *
- * The call launches two kernels that let their successors start early
- * (programmatic dependent launch): a prep kernel (router logits, int8 codes
- * of x, and the clearing of the counters the layer kernel synchronises on)
- * and a cooperative layer kernel (one CTA per SM: top-k, buckets, gate/up,
- * h, down and the combine).  For T <= 16 the layer kernel runs in clusters
- * of two CTAs that share each (expert, 128-feature block of h) unit through
- * distributed shared memory; for larger T it splits the experts' rows and K
- * ranges over all CTAs.  The prep kernel reads `wr` before the work that
+ * The call launches kernels that let their successors start early
+ * (programmatic dependent launch), first a prep kernel (router logits, int8
+ * codes of x, and the clearing of the counters the layer kernel
+ * synchronises on).  For T <= 16 two follow: the experts kernel, in
+ * clusters of two CTAs (top-k and buckets in every CTA; each bucket cut into
+ * slices of at most 4 rows; units of (slice, 128-feature block of h) shared
+ * by the cluster's CTAs through distributed shared memory: gate/up, h,
+ * down), and a combine kernel (residual plus the parts of every output).
+ * For larger T one cooperative layer kernel (one CTA per SM: top-k,
+ * buckets, gate/up, h, down and the combine over all CTAs, the experts'
+ * rows and K ranges split into tasks) follows.  The prep kernel reads `wr` before the work that
  * precedes it on the stream has finished, so `wr` must not be written by the
  * kernel launched immediately before this call on the same stream; x, the
  * output and the workspace are touched only after that work has finished.

@@ -11,6 +11,7 @@ Cases:
   shape: routing and the int8 codes of x exact, the gate/up and down int32
   group dots bit-exact (down: the oracle's dots of the GPU's own h codes), h
   codes within one step, the output within 2e-2 of the output's RMS;
+* 12 tokens of two kinds (buckets of 6 and 12 rows, cut into slices);
 * a 4-bit layer written as 8-bit codes (q - 8, same scales): the 8-bit call
   gives the 4-bit call's output bit for bit;
 * the shape limit.
@@ -71,6 +72,23 @@ def test_w8_decode_against_the_oracle(T):
     qh_o = np.stack([st["qh"][tok[p], slot[p]] for p in range(li.T * li.k)])
     diff = np.abs(q_h - qh_o)
     assert diff.max() <= 1 and (diff > 0).mean() < 0.01
+    assert_within_tol(out, ref, tol=2e-2)
+
+
+def test_w8_concentrated_buckets():
+    # 12 tokens of two kinds: buckets of 6 or 12 rows, cut into slices
+    li = W.decode(16)
+    li.T = 12
+    li.x = li.x[np.arange(12) % 2].copy()
+    rng = np.random.default_rng(7)
+    gu8, gus8 = _to_q8(li.gu_codes, li.gu_scales, rng)
+    d8, ds8 = _to_q8(li.d_codes, li.d_scales, rng)
+    dl = DeviceLayer(li)
+    wgu, wd = _pack8(gu8, gus8), _pack8(d8, ds8)
+    out = out_to_f64(moe.moe_w8a8_forward_decode(dl.x, dl.wr, wgu, wd, li.I, li.k))
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+    ref, _ = O.moe_decode(li.x, li.wr, gu8, gus8, d8, ds8, li.k, wbits=8)
     assert_within_tol(out, ref, tol=2e-2)
 
 
