@@ -86,9 +86,10 @@ constexpr int kRedBytes = kGroupWarps * 32 * 32;        // per group: 8 warps x 
 constexpr int kLayerSmemBudget = 200 * 1024;
 constexpr int kPrepThreads = 128;
 constexpr int kMaxTk = MOE_DECODE_MAX_T * MOE_MAX_TOPK;
-// Bucket rows of a unit of the clustered kernel: a larger bucket is cut into
-// near-equal slices of at most this many rows, so that the work split can
-// spread one expert's tokens over several clusters.
+// Bucket rows of a unit of the clustered kernel, at most: a larger bucket is
+// cut into near-equal slices (of 1, 2 or 4 rows at most, by T and the weight
+// bits), so that the work split can spread one expert's tokens over several
+// clusters.
 constexpr int kSliceRows = 4;
 constexpr int kMaxSlices = 16 * MOE_MAX_TOPK;  // slices of a launch (T <= 16)
 // Tasks the K split aims for (gate/up and down alike): the split depends only
@@ -1471,9 +1472,12 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 // and a third kernel (decode_combine_kernel) adds, per output element, the
 // residual and the k * I/128 parts (slot order, then block order).
 // A unit is (slice, h block): each touched expert's bucket is cut into
-// ceil(c / kSliceRows) slices of near-equal size (rows floor(s c / n) ..
-// floor((s + 1) c / n) - 1 of slice s of n), so that no unit holds more than
-// kSliceRows tokens.  The slices of one expert read the same weights; they
+// n = ceil(c / cap) slices of near-equal size (rows floor(s c / n) ..
+// floor((s + 1) c / n) - 1 of slice s): cap = 1 row for T <= 4, else 2 rows
+// for 4-bit and 4 for 8-bit weights.  (Measured on the 16-layer decode
+// chain, 4-bit: cap 1 / 2 / 4 gave T=4 32.9 / 34.1 / 37.6 us and T=16
+// 92.2 / 78.4 / 79.7 us a layer; 8-bit at T=16: cap 2 94.1, cap 4 89.3 us,
+// the re-read slices cost more with weights 1.89 times as large.)  The slices of one expert read the same weights; they
 // sit next to each other in the unit order, so their clusters run at about
 // the same time and the later reads find the weights in L2.  Units go to
 // clusters in contiguous ranges of equal cost (a unit of slice i weighs
@@ -1511,11 +1515,6 @@ __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, in
     const unsigned wn = (unsigned)NC * (unsigned)(kTileCost + toff[i + 1] - toff[i]);
     const unsigned j = (qt - base + wn - 1) / wn;
     return i * RBh + (int)(j < (unsigned)RBh ? j : (unsigned)RBh);
-}
-
-// floor(x / n) for n = 1 .. 4 and x <= 64 (slice bounds)
-__device__ __forceinline__ int div_small(int x, int n) {
-    return n == 3 ? (x * 21846) >> 16 : x >> (n >> 1);
 }
 
 template <int MAXNT, bool DOTS, int WB>
@@ -1558,8 +1557,9 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             // the slices of the touched slots' buckets (a warp scan of their
             // counts), the largest and the smallest slice
             const int nt = S.nt;
+            const int cap = T <= 4 ? 1 : (WB == 8 ? 4 : 2);  // bucket rows a slice may hold
             int nsl = 0, cm = 0, cmin = kSliceRows;
-            if (T <= kSliceRows) {  // no bucket is larger: a slice per slot
+            if (T == 1) {  // every bucket holds one row: a slice per slot
                 for (int i = lane; i < nt; i += 32) {
                     const int c = S.toff[i + 1] - S.toff[i];
                     S.sto[i] = S.toff[i];
@@ -1569,10 +1569,10 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                 }
                 nsl = nt;
             }
-            for (int i0 = 0; i0 < nt && T > kSliceRows; i0 += 32) {
+            for (int i0 = 0; i0 < nt && T > 1; i0 += 32) {
                 const int i = i0 + lane;
                 const int c = i < nt ? S.toff[i + 1] - S.toff[i] : 0;
-                const int n = (c + kSliceRows - 1) / kSliceRows;
+                const int n = (c + cap - 1) / cap;
                 int incl = n;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -1581,7 +1581,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                 }
                 const int first = nsl + incl - n;
                 for (int q = 0; q < n; ++q) {
-                    const int r0 = div_small(q * c, n), r1 = div_small((q + 1) * c, n);
+                    const int r0 = q * c / n, r1 = (q + 1) * c / n;
                     S.sto[first + q] = S.toff[i] + r0;
                     S.sslot[first + q] = (uint8_t)i;
                     cm = max(cm, r1 - r0);
@@ -1920,7 +1920,7 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             const int i = (ub0 + ul) / RBh, c = S.sto[i + 1] - S.sto[i];
             if (c <= 1) unit(IntC<1>{}, ul);
             else if (c <= 2) unit(IntC<2>{}, ul);
-            else unit(IntC<4>{}, ul);
+            else if constexpr (WB == 8) unit(IntC<4>{}, ul);  // (4-bit units hold at most 2 rows)
         }
     }
     pp.units += nu;

@@ -247,18 +247,19 @@ int moe_q4_forward_prefill(const uint16_t* x_bf16, const float* wr,
  *
  * The call launches kernels that let their successors start early
  * (programmatic dependent launch), first a prep kernel (router logits, int8
- * codes of x, and the clearing of the counters the layer kernel
- * synchronises on).  For T <= 16 two follow: the experts kernel, in
- * clusters of two CTAs (top-k and buckets in every CTA; each bucket cut into
- * slices of at most 4 rows; units of (slice, 128-feature block of h) shared
- * by the cluster's CTAs through distributed shared memory: gate/up, h,
- * down), and a combine kernel (residual plus the parts of every output).
- * For larger T one cooperative layer kernel (one CTA per SM: top-k,
- * buckets, gate/up, h, down and the combine over all CTAs, the experts'
- * rows and K ranges split into tasks) follows.  The prep kernel reads `wr` before the work that
- * precedes it on the stream has finished, so `wr` must not be written by the
- * kernel launched immediately before this call on the same stream; x, the
- * output and the workspace are touched only after that work has finished.
+ * codes of x, and the clearing of the counters the layer kernel synchronises
+ * on). For T <= 16 two follow: the experts kernel, in clusters of two CTAs
+ * (top-k and buckets in every CTA; each bucket cut into slices of at most 2
+ * rows, 1 for T <= 4 (8-bit weights: 4 and 1); units of (slice, 128-feature
+ * block of h) shared by the cluster's CTAs through distributed shared
+ * memory: gate/up, h, down), and a combine kernel (residual plus the parts
+ * of every output). For larger T one cooperative layer kernel (one CTA per
+ * SM: top-k, buckets, gate/up, h, down and the combine over all CTAs, the
+ * experts' rows and K ranges split into tasks) follows. The prep kernel
+ * reads `wr` before the work that precedes it on the stream has finished, so
+ * `wr` must not be written by the kernel launched immediately before this
+ * call on the same stream; x, the output and the workspace are touched only
+ * after that work has finished.
  * Nothing in the workspace has to survive from one call to the next, and
  * any other call may use the same workspace in between.  Routing needs
  * E <= 256 (one prep CTA per expert).

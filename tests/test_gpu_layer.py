@@ -181,14 +181,15 @@ def test_decode_edge_shapes(T, H, I, E, k):
 
 
 @pytest.mark.parametrize("T,groups", [
-    (16, 1),   # all 16 tokens alike: 8 buckets of 16 rows, four slices each
-    (12, 2),   # two kinds of token: buckets of 6 (two slices) or 12 (three)
-    (9, 3),    # buckets of 3, 6 or 9 rows
-    (5, 1),    # buckets of 5: slices of 2 and 3
+    (16, 1),   # all 16 tokens alike: 8 buckets of 16 rows, eight slices each
+    (12, 2),   # two kinds of token: buckets of 6 (three slices) or 12 (six)
+    (9, 3),    # buckets of 3, 6 or 9 rows (slices of 1 and 2 rows)
+    (5, 1),    # buckets of 5: slices of 1, 2 and 2 rows
+    (4, 2),    # T <= 4: buckets of 2 or 4 rows, a slice per row
 ])
 def test_decode_concentrated_buckets(T, groups):
     # tokens repeated so that many choose the same experts: the clustered
-    # kernel cuts each bucket into slices of at most four rows
+    # kernel cuts each bucket into slices of at most two rows (one for T <= 4)
     li = workloads.decode(16)
     rows = np.arange(T) % groups
     li.T = T
