@@ -439,7 +439,7 @@ def bench_prefill_stack(steps, warmup, torch, moe, device, barrier):
     res = {"workload": "stacked", "layers": L, "T": T, "E": E, "ms_per_stack": ms_stack,
            "ms_per_layer": ms_stack / L, "tokens_per_s": T / (ms_stack * 1e-3),
            "expert_tflops": flop * L / (ms_stack * 1e-3) / 1e12}
-    # NEXT-3: the first NS layers with their experts in pinned host memory,
+    # the first NS layers with their experts in pinned host memory,
     # streamed to the GPU layer by layer (moe_q4_forward_prefill_stack_streamed)
     NS = STREAMED_LAYERS
     gu_b, d_b = layers[0][1].numel(), layers[0][2].numel()

@@ -299,9 +299,10 @@ int moe_w4a8_forward_decode_stack(const uint16_t* x_bf16, int L, const float* co
                                   void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * 8-bit expert weights (NEXT-4: the companion page, mlsanity.com 2607.14568,
- * runs 8-bit weights against 4-bit ones; its format is not printed, this
- * library takes the Q8_0-style reading): blocks of 32 int8 codes q in
+ * 8-bit expert weights (the companion page "A Modern Multimodal Assistant
+ * on a 6 GB 2011 GPU: Stage-Validated, All-GPU CUDA Inference for Fermi",
+ * Abstract, runs 8-bit weights against 4-bit ones; its format is not
+ * printed, this library takes the Q8_0-style reading): blocks of 32 int8 codes q in
  * -127..127 along a row share one fp16 scale d, w = d * q.
  *
  * moe_q8_packed_bytes / moe_q8_pack — int8 codes [E, N, K] and fp16 scales

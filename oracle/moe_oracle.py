@@ -133,8 +133,9 @@ def q4_from_blocks18(blocks: np.ndarray):
 def q8_encode(w: np.ndarray):
     """Encode float weights into 8-bit blocks (READING of a Q8_0-style rule).
 
-    The companion page (mlsanity.com 2607.14568, abstract) runs 8-bit weights
-    against 4-bit ones without printing the format; the plainest member of the
+    The companion page "A Modern Multimodal Assistant on a 6 GB 2011 GPU:
+    Stage-Validated, All-GPU CUDA Inference for Fermi" (Abstract) runs 8-bit
+    weights against 4-bit ones without printing the format; the plainest member of the
     same family: per block of 32, d = fp16(amax / 127), amax the block's
     largest magnitude; q_i = clamp(round_half_away_from_zero(x_i / d), -127,
     127), taken against the stored (fp16-rounded) d; a block of zeros has

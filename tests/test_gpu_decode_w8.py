@@ -1,10 +1,11 @@
-"""GPU: the 8-bit-weight decode layer (NEXT-4, moe_w8a8_forward_decode with
+"""GPU: the 8-bit-weight decode layer (moe_w8a8_forward_decode with
 weights packed by moe_q8_pack) through the C ABI, against the oracle's 8-bit
 path (moe_decode with wbits=8).
 
-The companion page (mlsanity.com 2607.14568, abstract) runs 8-bit weights
-against 4-bit ones at decode; the format is the Q8_0-style reading of the
-oracle (blocks of 32 int8 codes, one fp16 scale, w = d * q).
+The companion page "A Modern Multimodal Assistant on a 6 GB 2011 GPU:
+Stage-Validated, All-GPU CUDA Inference for Fermi" (Abstract) runs 8-bit
+weights against 4-bit ones at decode; the format is the Q8_0-style reading
+of the oracle (blocks of 32 int8 codes, one fp16 scale, w = d * q).
 
 Cases:
 * genuine 8-bit codes over the whole range at T = 1, 4 and 16 of the decode

@@ -1,5 +1,6 @@
-"""The oracle's 8-bit weight path (NEXT-4: the companion page's 8-bit setting,
-mlsanity.com 2607.14568, abstract), pinned to facts outside the oracle:
+"""The oracle's 8-bit weight path (the 8-bit setting of the companion page
+"A Modern Multimodal Assistant on a 6 GB 2011 GPU: Stage-Validated, All-GPU
+CUDA Inference for Fermi", Abstract), pinned to facts outside the oracle:
 
 * a block worked by hand: d = fp16(amax / 127) exact at 2^-7, codes rounded
   half away from zero (0.5 d -> 1, -0.5 d -> -1, 1.5 d -> 2);
