@@ -12,6 +12,8 @@ Cases:
   shape: routing and the int8 codes of x exact, the gate/up and down int32
   group dots bit-exact (down: the oracle's dots of the GPU's own h codes), h
   codes within one step, the output within 2e-2 of the output's RMS;
+* edge shapes: one token, k = E, one expert, the smallest hidden size, 16
+  tokens over 64 experts (routing, gate/up dots, output);
 * 12 tokens of two kinds (buckets of 6 and 12 rows, cut into slices);
 * a 4-bit layer written as 8-bit codes (q - 8, same scales): the 8-bit call
   gives the 4-bit call's output bit for bit;
@@ -73,6 +75,34 @@ def test_w8_decode_against_the_oracle(T):
     qh_o = np.stack([st["qh"][tok[p], slot[p]] for p in range(li.T * li.k)])
     diff = np.abs(q_h - qh_o)
     assert diff.max() <= 1 and (diff > 0).mean() < 0.01
+    assert_within_tol(out, ref, tol=2e-2)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 256, 128, 8, 2),      # one token, few experts
+    (3, 256, 128, 6, 6),      # k = E
+    (1, 384, 256, 1, 1),      # one expert: a dense SwiGLU FFN, 3 row blocks
+    (5, 128, 128, 3, 2),      # smallest hidden size
+    (16, 256, 128, 64, 4),    # 16 tokens over 64 experts
+])
+def test_w8_edge_shapes(T, H, I, E, k):
+    li = W.make_layer("w8edge", T, H, I, E, k, seed=11 * T + H + E, wr_std=0.1)
+    rng = np.random.default_rng(T + E)
+    gu8, gus8 = _to_q8(li.gu_codes, li.gu_scales, rng)
+    d8, ds8 = _to_q8(li.d_codes, li.d_scales, rng)
+    dl = DeviceLayer(li)
+    wgu, wd = _pack8(gu8, gus8), _pack8(d8, ds8)
+    d, dbg = moe.make_debug(moe.MOE_MODE_DECODE, li.T, li.H, li.I, li.E, li.k)
+    out = out_to_f64(moe.moe_w8a8_forward_decode(dl.x, dl.wr, wgu, wd, li.I, li.k, debug=dbg))
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status() == 0
+    ref, st = O.moe_decode(li.x, li.wr, gu8, gus8, d8, ds8, li.k, keep_dots=True, wbits=8)
+    assert np.array_equal(d["topk_idx"].cpu().numpy(), st["idx"])
+    tok = d["bucket_token"].cpu().numpy()
+    slot = d["bucket_slot"].cpu().numpy()
+    dots_gu = d["dots_gu"].cpu().numpy()
+    for p in range(li.T * li.k):
+        assert np.array_equal(dots_gu[p], st["dots_gu"][(tok[p], slot[p])]), f"gate/up dots at row {p}"
     assert_within_tol(out, ref, tol=2e-2)
 
 
