@@ -1481,38 +1481,44 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 // sit next to each other in the unit order, so their clusters run at about
 // the same time and the later reads find the weights in L2.  Units go to
 // clusters in contiguous ranges of equal cost (a unit of slice i weighs
-// kTileCost + c_i per tile, all units have the same tiles).  No CTA
+// kUnitTileCost + c_i, all units have the same tiles).  No CTA
 // waits for a CTA outside its cluster, so the launch need not be
 // cooperative (a cooperative launch would not start before the prep kernel
 // has drained, and costs ~3 us a layer).
 constexpr int kClusterCTAs = 2;
 constexpr int kUnitWorkers = kClusterCTAs * kGroups;
 constexpr int kClusterMaxT = 16;  // tokens per call of the clustered kernel
+// Weight of a unit in the clustered kernel's split: w0 + c for a slice of c
+// rows (all units have the same tiles).  4-bit weights: w0 = kUnitTileCost;
+// measured units take ~6.2 us with one row and ~7.2 us with two (T=16), a
+// ratio of 7/6: most of a unit's time does not grow with its rows.  8-bit
+// weights (slices of up to 4 rows): w0 = kTileCost, as measured best there.
+constexpr int kUnitTileCost = 5;
 static_assert(kClusterMaxT * MOE_MAX_TOPK <= kMaxSlices, "a slice holds at least one bucket row");
 
 // The first unit of cluster q of NC: the unit whose cost range holds the
-// position q * total / NC (units of slice i, RBh of them, weigh
-// kTileCost + c_i each, c_i = toff[i + 1] - toff[i]).  Monotone in q;
-// bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp calls it.  Every
-// product stays below 2^31 (NC * RBh * (kTileCost * nt + Tk), checked by the
-// host plan), so the arithmetic is 32-bit.
+// position q * total / NC (units of slice i, RBh of them, weigh w0 + c_i
+// each, c_i = toff[i + 1] - toff[i]).  Monotone in q; bound(0) = 0 and
+// bound(NC) = nt * RBh.  The whole warp calls it.  Every product stays below
+// 2^31 (NC * RBh * (w0 * nt + Tk), w0 <= kUnitTileCost, checked by the host
+// plan), so the arithmetic is 32-bit.
 __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
-                                               int lane, bool equal) {
+                                               int lane, bool equal, int w0) {
     if (equal) return (q * nt * RBh + NC - 1) / NC;  // (all units weigh the same)
-    const unsigned tot = (unsigned)RBh * (unsigned)(kTileCost * nt + Tk);
+    const unsigned tot = (unsigned)RBh * (unsigned)(w0 * nt + Tk);
     const unsigned qt = (unsigned)q * tot;  // NC times the position
     const unsigned ncr = (unsigned)(NC * RBh);
     int cnt = 0;  // slices whose first unit starts before it
     for (int i0 = 0; i0 <= nt; i0 += 32) {
         const int i = i0 + lane;
-        const bool lt = i <= nt && ncr * (unsigned)(kTileCost * i + toff[i]) < qt;
+        const bool lt = i <= nt && ncr * (unsigned)(w0 * i + toff[i]) < qt;
         cnt += __popc(__ballot_sync(0xffffffffu, lt));
     }
     if (cnt == 0) return 0;
     const int i = cnt - 1;
     if (i >= nt) return nt * RBh;
-    const unsigned base = ncr * (unsigned)(kTileCost * i + toff[i]);
-    const unsigned wn = (unsigned)NC * (unsigned)(kTileCost + toff[i + 1] - toff[i]);
+    const unsigned base = ncr * (unsigned)(w0 * i + toff[i]);
+    const unsigned wn = (unsigned)NC * (unsigned)(w0 + toff[i + 1] - toff[i]);
     const unsigned j = (qt - base + wn - 1) / wn;
     return i * RBh + (int)(j < (unsigned)RBh ? j : (unsigned)RBh);
 }
@@ -1593,8 +1599,10 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             __syncwarp();
             cm = __reduce_max_sync(0xffffffffu, cm);
             const bool equal = __reduce_min_sync(0xffffffffu, cmin) == cm;
-            const int u0 = unit_bound_warp(cq, NC, nsl, Tk, RBh, S.sto, lane, equal);
-            const int u1 = unit_bound_warp(cq + 1, NC, nsl, Tk, RBh, S.sto, lane, equal);
+            constexpr int w0 = WB == 8 ? kTileCost : kUnitTileCost;  // a unit's weight: w0 + rows
+            static_assert(w0 <= kUnitTileCost, "the host's 32-bit bound");
+            const int u0 = unit_bound_warp(cq, NC, nsl, Tk, RBh, S.sto, lane, equal, w0);
+            const int u1 = unit_bound_warp(cq + 1, NC, nsl, Tk, RBh, S.sto, lane, equal, w0);
             if (lane == 0) {
                 S.bnd[0][0] = u0;
                 S.bnd[0][1] = u1;
@@ -2067,9 +2075,9 @@ bool plan_layer(int T, int H, int I, int E, long long budget, Plan* p) {
 bool plan_cluster(int T, int H, int I, int E, long long budget, Plan* p, int wbits = 4) {
     const int tile_bytes = wbits == 8 ? kTileBytes8 : kTileBytes;
     if (T < 1 || T > kClusterMaxT) return false;
-    // the unit split's 32-bit products: NC * RBh * (kTileCost * slices + Tk)
-    // with at most 1024 clusters and kMaxSlices slices
-    if ((long long)(I / kTileRows) * 1024 * (kTileCost + 1) * kMaxSlices >= (1ll << 31)) return false;
+    // the unit split's 32-bit products: NC * RBh * (kUnitTileCost * slices +
+    // Tk) with at most 1024 clusters and kMaxSlices slices
+    if ((long long)(I / kTileRows) * 1024 * (kUnitTileCost + 1) * kMaxSlices >= (1ll << 31)) return false;
     if ((H / kTileK) % kClusterCTAs) return false;
     const long long ax = al128((long long)T * (H / kClusterCTAs) + (long long)T * (H / kGroup / kClusterCTAs) * 8);
     const long long hbytes = al128((long long)T * kTileRows + (long long)T * 4 * 8);
