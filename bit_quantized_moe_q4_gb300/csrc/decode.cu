@@ -87,9 +87,8 @@ constexpr int kLayerSmemBudget = 200 * 1024;
 constexpr int kPrepThreads = 128;
 constexpr int kMaxTk = MOE_DECODE_MAX_T * MOE_MAX_TOPK;
 // Bucket rows of a unit of the clustered kernel, at most: a larger bucket is
-// cut into near-equal slices (of 1, 2 or 4 rows at most, by T and the weight
-// bits), so that the work split can spread one expert's tokens over several
-// clusters.
+// cut into slices (of 1, 2 or 4 rows at most, by T and the weight bits), so
+// that the work split can spread one expert's tokens over several clusters.
 constexpr int kSliceRows = 4;
 constexpr int kMaxSlices = 16 * MOE_MAX_TOPK;  // slices of a launch (T <= 16)
 // Tasks the K split aims for (gate/up and down alike): the split depends only
@@ -1471,17 +1470,17 @@ __global__ void __maxnreg__(96) decode_layer_kernel(const LayerArgs a) {
 //            y (one per h block)
 // and a third kernel (decode_combine_kernel) adds, per output element, the
 // residual and the k * I/128 parts (slot order, then block order).
-// A unit is (slice, h block): each touched expert's bucket is cut into
-// n = ceil(c / cap) slices of near-equal size (rows floor(s c / n) ..
-// floor((s + 1) c / n) - 1 of slice s): cap = 1 row for T <= 4, else 2 rows
-// for 4-bit and 4 for 8-bit weights.  (Measured on the 16-layer decode
-// chain, 4-bit: cap 1 / 2 / 4 gave T=4 32.9 / 34.1 / 37.6 us and T=16
-// 92.2 / 78.4 / 79.7 us a layer; 8-bit at T=16: cap 2 94.1, cap 4 89.3 us,
-// the re-read slices cost more with weights 1.89 times as large.)  The slices of one expert read the same weights; they
-// sit next to each other in the unit order, so their clusters run at about
-// the same time and the later reads find the weights in L2.  Units go to
-// clusters in contiguous ranges of equal cost (a unit of slice i weighs
-// kUnitTileCost + c_i, all units have the same tiles).  No CTA
+// A unit is (slice, h block): each touched expert's bucket of c rows is cut
+// into n = ceil(c / cap) slices, rows s cap .. min(c, (s + 1) cap) - 1 of
+// slice s: cap = 1 row for T <= 4, else 2 rows for 4-bit and 4 for 8-bit
+// weights.  (Measured on the 16-layer decode chain, 4-bit: cap 1 / 2 / 4
+// gave T=4 32.9 / 34.1 / 37.6 us and T=16 92.2 / 78.4 / 79.7 us a layer;
+// 8-bit at T=16: cap 2 94.1, cap 4 89.3 us, the re-read slices cost more
+// with weights 1.89 times as large.)  The slices of one expert read the
+// same weights; they sit next to each other in the unit order, so their
+// clusters run at about the same time and the later reads find the weights
+// in L2.  Units go to clusters in contiguous ranges of equal cost (a unit of
+// slice i weighs w0 + c_i, all units have the same tiles).  No CTA
 // waits for a CTA outside its cluster, so the launch need not be
 // cooperative (a cooperative launch would not start before the prep kernel
 // has drained, and costs ~3 us a layer).
@@ -1496,24 +1495,8 @@ constexpr int kClusterMaxT = 16;  // tokens per call of the clustered kernel
 constexpr int kUnitTileCost = 5;
 static_assert(kClusterMaxT * MOE_MAX_TOPK <= kMaxSlices, "a slice holds at least one bucket row");
 
-// The first unit of cluster q of NC: the unit whose cost range holds the
-// position q * total / NC (units of slice i, RBh of them, weigh w0 + c_i
-// each, c_i = toff[i + 1] - toff[i]).  Monotone in q; bound(0) = 0 and
-// bound(NC) = nt * RBh.  The whole warp calls it.  Every product stays below
-// 2^31 (NC * RBh * (w0 * nt + Tk), w0 <= kUnitTileCost, checked by the host
-// plan), so the arithmetic is 32-bit.
-__device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
-                                               int lane, bool equal, int w0) {
-    if (equal) return (q * nt * RBh + NC - 1) / NC;  // (all units weigh the same)
-    const unsigned tot = (unsigned)RBh * (unsigned)(w0 * nt + Tk);
-    const unsigned qt = (unsigned)q * tot;  // NC times the position
-    const unsigned ncr = (unsigned)(NC * RBh);
-    int cnt = 0;  // slices whose first unit starts before it
-    for (int i0 = 0; i0 <= nt; i0 += 32) {
-        const int i = i0 + lane;
-        const bool lt = i <= nt && ncr * (unsigned)(w0 * i + toff[i]) < qt;
-        cnt += __popc(__ballot_sync(0xffffffffu, lt));
-    }
+__device__ __forceinline__ int unit_bound_at(unsigned qt, int cnt, int nt, int NC, int RBh, unsigned ncr,
+                                             const int* toff, int w0) {
     if (cnt == 0) return 0;
     const int i = cnt - 1;
     if (i >= nt) return nt * RBh;
@@ -1521,6 +1504,34 @@ __device__ __forceinline__ int unit_bound_warp(int q, int NC, int nt, int Tk, in
     const unsigned wn = (unsigned)NC * (unsigned)(w0 + toff[i + 1] - toff[i]);
     const unsigned j = (qt - base + wn - 1) / wn;
     return i * RBh + (int)(j < (unsigned)RBh ? j : (unsigned)RBh);
+}
+
+// The first units of clusters q and q + 1 of NC (their range [*u0, *u1)):
+// the unit whose cost range holds the position q * total / NC (units of
+// slice i, RBh of them, weigh w0 + c_i each, c_i = toff[i + 1] - toff[i]).
+// Monotone in q; bound(0) = 0 and bound(NC) = nt * RBh.  The whole warp
+// calls it.  Every product stays below 2^31 (NC * RBh * (w0 * nt + Tk),
+// w0 <= kUnitTileCost, checked by the host plan), so the arithmetic is
+// 32-bit.
+__device__ __forceinline__ void unit_bounds_warp(int q, int NC, int nt, int Tk, int RBh, const int* toff,
+                                                 int lane, bool equal, int w0, int* u0, int* u1) {
+    if (equal) {  // (all units weigh the same)
+        *u0 = (q * nt * RBh + NC - 1) / NC;
+        *u1 = ((q + 1) * nt * RBh + NC - 1) / NC;
+        return;
+    }
+    const unsigned tot = (unsigned)RBh * (unsigned)(w0 * nt + Tk);
+    const unsigned qt0 = (unsigned)q * tot, qt1 = qt0 + tot;  // NC times the positions
+    const unsigned ncr = (unsigned)(NC * RBh);
+    int cnt0 = 0, cnt1 = 0;  // slices whose first unit starts before each
+    for (int i0 = 0; i0 <= nt; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned pos = i <= nt ? ncr * (unsigned)(w0 * i + toff[i]) : 0xffffffffu;
+        cnt0 += __popc(__ballot_sync(0xffffffffu, pos < qt0));
+        cnt1 += __popc(__ballot_sync(0xffffffffu, pos < qt1));
+    }
+    *u0 = unit_bound_at(qt0, cnt0, nt, NC, RBh, ncr, toff, w0);
+    *u1 = unit_bound_at(qt1, cnt1, nt, NC, RBh, ncr, toff, w0);
 }
 
 template <int MAXNT, bool DOTS, int WB>
@@ -1578,7 +1589,8 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             for (int i0 = 0; i0 < nt && T > 1; i0 += 32) {
                 const int i = i0 + lane;
                 const int c = i < nt ? S.toff[i + 1] - S.toff[i] : 0;
-                const int n = (c + cap - 1) / cap;
+                const int lc = cap == 4 ? 2 : cap == 2 ? 1 : 0;  // log2(cap)
+                const int n = (c + cap - 1) >> lc;
                 int incl = n;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -1586,12 +1598,13 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
                     if (lane >= o) incl += v;
                 }
                 const int first = nsl + incl - n;
-                for (int q = 0; q < n; ++q) {
-                    const int r0 = q * c / n, r1 = (q + 1) * c / n;
-                    S.sto[first + q] = S.toff[i] + r0;
+                for (int q = 0; q < n; ++q) {  // runs of cap rows, the last one shorter
+                    S.sto[first + q] = S.toff[i] + (q << lc);
                     S.sslot[first + q] = (uint8_t)i;
-                    cm = max(cm, r1 - r0);
-                    cmin = min(cmin, r1 - r0);
+                }
+                if (n > 0) {
+                    cm = max(cm, min(c, cap));
+                    cmin = min(cmin, c - ((n - 1) << lc));
                 }
                 nsl += __shfl_sync(0xffffffffu, incl, 31);
             }
@@ -1601,8 +1614,8 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             const bool equal = __reduce_min_sync(0xffffffffu, cmin) == cm;
             constexpr int w0 = WB == 8 ? kTileCost : kUnitTileCost;  // a unit's weight: w0 + rows
             static_assert(w0 <= kUnitTileCost, "the host's 32-bit bound");
-            const int u0 = unit_bound_warp(cq, NC, nsl, Tk, RBh, S.sto, lane, equal, w0);
-            const int u1 = unit_bound_warp(cq + 1, NC, nsl, Tk, RBh, S.sto, lane, equal, w0);
+            int u0, u1;
+            unit_bounds_warp(cq, NC, nsl, Tk, RBh, S.sto, lane, equal, w0, &u0, &u1);
             if (lane == 0) {
                 S.bnd[0][0] = u0;
                 S.bnd[0][1] = u1;
