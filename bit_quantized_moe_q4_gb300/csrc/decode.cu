@@ -1578,13 +1578,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             int nsl = 0, cm = 0, cmin = kSliceRows;
             if (T == 1) {  // every bucket holds one row: a slice per slot
                 for (int i = lane; i < nt; i += 32) {
-                    const int c = S.toff[i + 1] - S.toff[i];
                     S.sto[i] = S.toff[i];
                     S.sslot[i] = (uint8_t)i;
-                    cm = max(cm, c);
-                    cmin = min(cmin, c);
                 }
                 nsl = nt;
+                cm = cmin = 1;
             }
             for (int i0 = 0; i0 < nt && T > 1; i0 += 32) {
                 const int i = i0 + lane;
@@ -1610,8 +1608,11 @@ __device__ __forceinline__ void cluster_body(const LayerArgs& a, const LayerIO& 
             }
             if (lane == 0) S.sto[nsl] = Tk;
             __syncwarp();
-            cm = __reduce_max_sync(0xffffffffu, cm);
-            const bool equal = __reduce_min_sync(0xffffffffu, cmin) == cm;
+            if (T > 1) {
+                cm = __reduce_max_sync(0xffffffffu, cm);
+                cmin = __reduce_min_sync(0xffffffffu, cmin);
+            }
+            const bool equal = cmin == cm;
             constexpr int w0 = WB == 8 ? kTileCost : kUnitTileCost;  // a unit's weight: w0 + rows
             static_assert(w0 <= kUnitTileCost, "the host's 32-bit bound");
             int u0, u1;
