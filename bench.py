@@ -36,8 +36,8 @@ D_BYTES_PER_EXPERT = 2048 * 768 * 18 // 32        # packed down bytes of one exp
 # expert GEMMs (T=2048).  Set to None when a kernel changes before a new
 # capture.
 # DRAM bytes (read + write) of one decode layer at T=1: the prep, clustered
-# and combine kernels, averages of 10 launches each under ncu (1.093 + 21.328 + 0.406 MB)
-NCU_TRAFFIC_DECODE_LAYER_T1 = 22_826_931
+# and combine kernels, averages of 10 launches each under ncu (1.093 + 21.330 + 0.406 MB)
+NCU_TRAFFIC_DECODE_LAYER_T1 = 22_828_262
 NCU_TRAFFIC_PREFILL_EXPERTS = 384_733_696  # dram read + write, ncu, one launch at T=2048
 # kernels of one decode layer: prep (logits, x codes) and, for T <= 16, the
 # clustered expert kernel and the combine kernel; else the task kernel (top-k,
